@@ -1,0 +1,89 @@
+"""Seeded synthetic inputs for the attention forward.
+
+This module holds no attention arithmetic: it only draws random tensors, so
+both the CUDA path and the CPU oracle can be fed the same bits.  Q, K and V
+are drawn in that order from one ``torch.Generator`` as float32 normals times
+a standard deviation, then rounded to bf16 (round-to-nearest-even); the bf16
+values convert to float64 exactly on the oracle side.
+
+The workloads are the five shapes the attention forward is measured and
+checked on; each is named by what it is.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    d: int
+    causal: bool
+    qk_std: float = 1.0
+    v_std: float = 1.0
+    seed: int = 0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / (self.d ** 0.5)
+
+    def flops(self) -> float:
+        """4*B*H*N^2*d multiply-adds counted as 2 flops each, halved when causal."""
+        f = 4.0 * self.B * self.H * self.N * self.N * self.d
+        return f / 2.0 if self.causal else f
+
+    def algorithmic_bytes(self) -> int:
+        """Q, K, V read once and O written once (bf16), LSE written once (fp32)."""
+        return 4 * self.B * self.H * self.N * self.d * 2 + self.B * self.H * self.N * 4
+
+
+WORKLOADS = {
+    w.name: w
+    for w in (
+        Workload("n128_d64", 1, 1, 128, 64, False, seed=20261),
+        Workload("n2048_d64", 4, 16, 2048, 64, False, seed=20262),
+        Workload("causal_n8192_d128", 2, 16, 8192, 128, True, seed=20263),
+        Workload("wide_scores_n1024_d128", 8, 32, 1024, 128, False, qk_std=3.0, seed=20264),
+        Workload("causal_n32768_d128", 1, 32, 32768, 128, True, seed=20265),
+    )
+}
+
+HEADLINE = "causal_n8192_d128"
+
+
+def make_qkv(B: int, H: int, N: int, d: int, seed: int, qk_std: float = 1.0,
+             v_std: float = 1.0):
+    """Return CPU bf16 tensors q, k, v of shape [B, H, N, d] (contiguous)."""
+    g = torch.Generator().manual_seed(int(seed))
+    shape = (B, H, N, d)
+    q = (torch.randn(shape, generator=g, dtype=torch.float32) * qk_std).to(torch.bfloat16)
+    k = (torch.randn(shape, generator=g, dtype=torch.float32) * qk_std).to(torch.bfloat16)
+    v = (torch.randn(shape, generator=g, dtype=torch.float32) * v_std).to(torch.bfloat16)
+    return q, k, v
+
+
+def make_workload(w: Workload):
+    return make_qkv(w.B, w.H, w.N, w.d, w.seed, w.qk_std, w.v_std)
+
+
+def sample_slices(B: int, H: int, count: int, seed: int):
+    """``count`` distinct (b, h) pairs drawn from Generator(seed)."""
+    g = torch.Generator().manual_seed(int(seed))
+    total = B * H
+    count = min(count, total)
+    idx = torch.randperm(total, generator=g)[:count].tolist()
+    return [(i // H, i % H) for i in sorted(idx)]
+
+
+def sample_rows(N: int, count: int, seed: int):
+    """``count`` distinct query rows of a length-N sequence, always including
+    row 0, the last row and the first/last row of the last 128-row tile."""
+    g = torch.Generator().manual_seed(int(seed))
+    fixed = {0, N - 1, max(0, (N - 1) // 128 * 128)}
+    rest = torch.randperm(N, generator=g)[:max(0, count - len(fixed))].tolist()
+    return sorted(fixed | set(rest))

@@ -1,0 +1,65 @@
+"""Plant plausible mistakes in a copy of the CPU oracle and check that the pins
+catch every one of them (no GPU).  A mutant is a text substitution in the
+oracle's source, loaded as a fresh module; the real oracle is never touched.
+"""
+import os
+import types
+
+import pytest
+
+from tests.oracle_pins import ALL_PINS
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                   "oracle", "attention.py")
+
+# (name, exact text in the oracle, replacement, how many occurrences to replace)
+MUTANTS = [
+    ("scale dropped", "s = scale * (q_rows @ k.T)", "s = (q_rows @ k.T)", 1),
+    ("K not transposed", "s = scale * (q_rows @ k.T)", "s = scale * (q_rows @ k)", 1),
+    ("mask off by one", "k_pos[None, :] > q_pos[:, None]", "k_pos[None, :] >= q_pos[:, None]", 1),
+    ("mask transposed", "k_pos[None, :] > q_pos[:, None]", "k_pos[None, :] < q_pos[:, None]", 1),
+    ("no max subtraction", "e = np.exp(s - m[:, None])\n        l = e.sum(axis=1)",
+     "e = np.exp(s)\n        l = e.sum(axis=1)", 1),
+    ("exp sign flipped", "e = np.exp(s - m[:, None])\n        l = e.sum(axis=1)",
+     "e = np.exp(m[:, None] - s)\n        l = e.sum(axis=1)", 1),
+    ("no division by l", "out[c0:c0 + row_chunk] = (e @ v) / l[:, None]",
+     "out[c0:c0 + row_chunk] = (e @ v)", 1),
+    ("LSE without m", "lse[c0:c0 + row_chunk] = m + np.log(l)", "lse[c0:c0 + row_chunk] = np.log(l)", 1),
+    ("LSE in log2", "lse[c0:c0 + row_chunk] = m + np.log(l)", "lse[c0:c0 + row_chunk] = m + np.log2(l)", 1),
+    ("P uses V", "return e / e.sum(axis=1)[:, None]", "return e / e.sum(axis=0)[None, :]", 1),
+    ("rescale with tile max", "r = np.where(seen, np.exp(m - m_new), 0.0)",
+     "r = np.where(seen, np.exp(m_ij - m_new), 0.0)", 1),
+    ("rescale dropped from l", "l = r * l + p_ij.sum(axis=1)", "l = l + p_ij.sum(axis=1)", 1),
+    ("rescale dropped from O~", "acc = r[:, None] * acc + p_ij @ v[a:b]", "acc = acc + p_ij @ v[a:b]", 1),
+    ("block exp against tile max", "np.exp(s_ij - m_new[:, None])", "np.exp(s_ij - m_ij[:, None])", 1),
+    ("running max not kept", "        m = m_new\n        if trace is not None:\n            with",
+     "        if trace is not None:\n            with", 1),
+    ("normalised: l factor dropped", "((a_old * ell)[:, None] * out", "((a_old)[:, None] * out", 1),
+    ("normalised: new-block weight dropped", "a_new[:, None] * (p_t @ v[a:b])", "(p_t @ v[a:b])", 1),
+    ("normalised: l~ not rescaled", "l_new = a_old * ell + a_new * l_t", "l_new = a_old * ell + l_t", 1),
+    ("brute force: wrong LSE", "lse[i] = m + math.log(denom)", "lse[i] = math.log(denom)", 1),
+    ("brute force: scale dropped", "s[j] = scale * dot", "s[j] = dot", 1),
+    ("brute force: causal off by one", "if not (causal and j > i)", "if not (causal and j >= i)", 1),
+]
+
+
+def _load_mutant(old, new, count):
+    src = open(SRC, encoding="utf-8").read()
+    assert src.count(old) >= count, f"mutation site not found: {old!r}"
+    mutated = src.replace(old, new, count)
+    mod = types.ModuleType("oracle_mutant")
+    exec(compile(mutated, "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")
+@pytest.mark.parametrize("name,old,new,count", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(name, old, new, count):
+    mod = _load_mutant(old, new, count)
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(mod)
+        except Exception:  # noqa: BLE001 -- any failure of a pin counts
+            caught.append(pin.__name__)
+    assert caught, f"mutant '{name}' passed every pin"

@@ -1,0 +1,346 @@
+"""Benchmark of the exact attention forward on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one fa_fwd call over the whole workload (every (b, h) and query
+tile), inputs resident in HBM.  The default workload is the causal
+B=2 H=16 N=8192 d=128 forward; the metric is forward TFLOP/s with
+4*B*H*N^2*d flops, halved for causal.  Prints one JSON line (rank 0).
+
+--impl reference times the fp64 CPU oracle on the host cores instead (each
+step: one 128-row query tile of one (b, h) slice of the same workload).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from exact_io_aware_02_gb300.inputs import HEADLINE, WORKLOADS, make_workload  # noqa: E402
+
+METRIC = "fwd attention TFLOP/s & % of GB300 bf16 tensor peak (B=2 H=16 N=8K d=128 causal)"
+UNIT = "TFLOP/s"
+L2_FLUSH_BYTES = 256 << 20
+KERNEL_FILES = [os.path.join(ROOT, "exact_io_aware_02_gb300", "csrc", f)
+                for f in ("fa_fwd_sm103.cu", "sm103_ptx.cuh")]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+
+
+def kernel_digest() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_FILES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source (same digest); else None."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    digest = kernel_digest()
+    for line in open(TRAFFIC_FILE, encoding="utf-8"):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == digest:
+            return float(parts[2])
+    return None
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["bf16_tflops"]), float(d["hbm_gbs"]), "measured"
+    return 1900.0, 6800.0, "fallback"
+
+
+def workload_config(w, l2_note):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+            "qk_std": w.qk_std, "v_std": w.v_std, "seed": w.seed, "l2": l2_note}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled in the background."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,utilization.gpu,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self):
+        return time.perf_counter()
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 8:
+                continue
+            rows.append((ts, parts))
+        inside = [r for r in rows if t0 <= r[0] <= t1 + 0.05]
+        if not inside and rows:  # region shorter than the sampling period: nearest sample
+            inside = [min(rows, key=lambda r: abs(r[0] - (t0 + t1) / 2))]
+        sm = [float(p[0]) for _, p in inside if p[0].replace(".", "").isdigit()]
+        busy = [float(p[0]) for _, p in inside if p[0].replace(".", "").isdigit()
+                and p[3].isdigit() and int(p[3]) > 0]
+        mx = [float(p[1]) for _, p in inside if p[1].replace(".", "").isdigit()]
+        reasons = sorted({name for _, p in inside for name, val in zip(self.NAMES, p[4:])
+                          if val.strip().lower() == "active"})
+        use = busy or sm
+        return {"sm_mhz": statistics.median(use) if use else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(inside)}
+
+
+def gpu_selector(dev) -> str:
+    """nvidia-smi -i argument for a torch device: its UUID when torch knows it."""
+    uuid = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    if uuid is not None:
+        text = str(uuid)
+        return text if text.startswith("GPU-") else "GPU-" + text
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if visible:
+        return visible.split(",")[dev.index or 0].strip()
+    return str(dev.index or 0)
+
+
+def cpu_baseline(w, budget_s=12.0, max_slices=8):
+    """The fp64 oracle as it stands, on whole (b, h) slices of the workload until
+    about ``budget_s`` seconds of CPU work; TFLOP/s counted like the GPU metric."""
+    import numpy as np
+    import oracle
+    from exact_io_aware_02_gb300.inputs import sample_slices
+
+    q, k, v = make_workload(w)
+    slices = sample_slices(w.B, w.H, max_slices, w.seed + 3)
+    per_slice = w.flops() / (w.B * w.H)
+    done, t_total = 0, 0.0
+    for (b, h) in slices:
+        qa, ka, va = (t[b, h].to(torch.float64).numpy() for t in (q, k, v))
+        t0 = time.perf_counter()
+        oracle.naive_attention(qa, ka, va, w.scale, w.causal)
+        t_total += time.perf_counter() - t0
+        done += 1
+        if t_total >= budget_s:
+            break
+    del np
+    return {"value": done * per_slice / t_total / 1e12, "unit": UNIT,
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{done} whole (b,h) slice(s) of {w.name} (N={w.N}, d={w.d}), fp64 NumPy, "
+                      f"{t_total:.1f} s; threads = NumPy BLAS default on the listed cores"}
+
+
+def run_reference(args, w, rank, world):
+    """Reference arm: the CPU oracle, rank 0 only."""
+    if rank != 0:
+        return
+    import oracle
+
+    q, k, v = make_workload(w)
+    n_tiles = (w.N + 127) // 128
+    total_flops, total_t = 0.0, 0.0
+
+    def step(s, timed):
+        nonlocal total_flops, total_t
+        idx = (s * 7919) % (w.B * w.H * n_tiles)
+        bh, tile = divmod(idx, n_tiles)
+        b, h = divmod(bh, w.H)
+        rows = list(range(tile * 128, min(w.N, tile * 128 + 128)))
+        qa, ka, va = (t[b, h].to(torch.float64).numpy() for t in (q, k, v))
+        t0 = time.perf_counter()
+        oracle.naive_attention(qa, ka, va, w.scale, w.causal, rows=rows)
+        dt = time.perf_counter() - t0
+        if timed:
+            keys = [(i + 1) if w.causal else w.N for i in rows]
+            total_flops += sum(4.0 * kk * w.d for kk in keys)
+            total_t += dt
+
+    for s in range(args.warmup):
+        step(s, False)
+    for s in range(args.steps):
+        step(args.warmup + s, True)
+    value = total_flops / total_t / 1e12
+    cores = len(os.sched_getaffinity(0))
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(w, "n/a (CPU)"),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} steps of one 128-row query tile of one (b,h) "
+                                       f"slice each, fp64 NumPy"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, rank, world, local_rank):
+    from exact_io_aware_02_gb300 import fa
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    qh, kh, vh = (t.pin_memory() for t in make_workload(w))
+    q, k, v = (t.to(dev, non_blocking=True) for t in (qh, kh, vh))
+    o = torch.empty_like(q)
+    lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        fa.fa_fwd(q, k, v, o, lse, scale=w.scale, causal=w.causal, stream=stream)
+    torch.cuda.synchronize()
+    if fa.fa_status(clear=True) != 0:
+        raise RuntimeError("device status word set during warm-up")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(gpu_selector(dev))
+    if rank == 0:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    launches = 0
+    for i in range(args.steps):
+        flush.zero_()  # write a buffer larger than L2 between timed launches
+        starts[i].record(stream)
+        fa.fa_fwd(q, k, v, o, lse, scale=w.scale, causal=w.causal, stream=stream)
+        ends[i].record(stream)
+        launches += 1
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t1 = time.perf_counter()
+    clocks = sampler.stop(t0, t1) if rank == 0 else None
+    kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(kernel_ms) / len(kernel_ms)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    if fa.fa_status(clear=True) != 0:
+        raise RuntimeError("device status word set during the timed region")
+
+    # end to end through the public API: pinned host -> device, forward, device -> host
+    o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    e2e_steps = max(1, min(args.steps, 10))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(e2e_steps + 1):
+        if i == 1:
+            e0.record(stream)
+        for dst, src in ((q, qh), (k, kh), (v, vh)):
+            dst.copy_(src, non_blocking=True)
+        fa.fa_fwd(q, k, v, o, lse, scale=w.scale, causal=w.causal, stream=stream)
+        o_h.copy_(o, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    if rank != 0:
+        return
+
+    flops = w.flops()
+    value = world * flops / (ms * 1e-3) / 1e12
+    peak_tf, _, peak_kind = peaks()
+    achieved = flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(w, "flushed between timed launches (256 MiB write); "
+                                     "per-launch CUDA events on the launch stream"),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": achieved / peak_tf, "traffic": measured_traffic(w.name),
+                     "peak_kind": f"bf16 dense burst, {peak_kind}",
+                     "algorithmic_flops": flops, "algorithmic_bytes": w.algorithmic_bytes()},
+        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
+                "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * lse.element_size()},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "kernel_ms": {"min": min(kernel_ms), "median": statistics.median(kernel_ms), "max": max(kernel_ms)},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, rank, world)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

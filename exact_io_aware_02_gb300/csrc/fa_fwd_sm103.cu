@@ -1,0 +1,601 @@
+// fa_fwd_sm103.cu -- exact attention forward (O and per-row LSE) for GB300, sm_103a.
+//
+// The method is FlashAttention's: S = scale*Q K^T and P = softmax(S) live only
+// on chip, and K/V tiles are merged with a running row max m and running
+// exp-sum l ("在线Softmax算法" on the aiqz.cc flash-attention-io-optimization
+// article: m_new = max(m, m_ij), r = e^(m - m_new), l_new = r l + sum e^(s-m_new),
+// O~_new = r O~ + sum e^(s-m_new) v, O = O~/l; the same merge as §5 of the
+// zzszmyf.github.io notes "FlashAttention 原理是什么？为什么又省显存又快").
+// The loop order is the one of FlashAttention-2 (§9 of the notes page): each
+// CTA owns query tiles and streams the K/V tiles of its (batch, head).  The
+// structure follows FlashAttention-3 (§10 there): a TMA producer warp fills
+// shared memory while the math warps consume it, and softmax work overlaps
+// the tensor-core work.
+//
+// GB300 design (one CTA per SM, 320 threads):
+//   * two 128-row query tiles per CTA (Q_0, Q_1) share every K/V tile that is
+//     loaded, halving K/V traffic per flop;
+//   * warp 8  -- TMA producer: Q_0, Q_1 once, then K_j and V_j into separate
+//                shared-memory rings gated by full/empty mbarriers;
+//   * warp 9  -- MMA issuer (one thread): S_t = Q_t K_j^T with tcgen05.mma
+//                (A and B from shared memory, fp32 accumulator in tensor memory),
+//                then O_t += P_t V_j with P_t read from tensor memory;
+//   * warps 0-3 / 4-7 -- softmax for tile 0 / tile 1, one row per thread:
+//                row max, exp2 with scale*log2(e) folded in, running (m, l),
+//                bf16 P written back into tensor memory over S_t, and the
+//                correction O_t *= r, which only runs when some row's max grew
+//                by more than 2^8 (the rescale is exact for any reference m,
+//                because l and O~ share it); epilogue O = O~/l -> bf16 ->
+//                shared memory -> TMA store, LSE = m*scale + ln l.
+//   * causal: query tile i visits K/V tiles 0..i only; the mask is applied on
+//     the diagonal tile (and on a ragged last tile) only; CTAs are scheduled
+//     longest first.
+// Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 and O_1 after
+// that (d columns each).  P_t overwrites the first 64 columns of S_t (bf16 pairs).
+//
+// Every mbarrier wait is bounded (globaltimer); on expiry the CTA raises a
+// status bit, waits for its own copies and MMAs in flight, frees its tensor
+// memory and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "fa_gb300.h"
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+__device__ unsigned int g_status;
+
+constexpr int kThreads = 320;
+constexpr float kRescaleLog2Threshold = 8.0f;  // skip the O correction unless max grows > 2^8
+
+template <int D>
+struct Cfg {
+  static constexpr int kChunks = D / 64;           // 128-byte swizzle atoms along d
+  static constexpr int kChunkBytes = 128 * 128;    // 128 rows x 64 bf16
+  static constexpr int kTileBytes = 128 * D * 2;   // one 128-row tile of Q, K, V or O
+  static constexpr int kSK = D == 128 ? 3 : 4;     // K ring depth
+  static constexpr int kSV = D == 128 ? 2 : 4;     // V ring depth
+  static constexpr int kOffQ = 0;                  // Q_0, Q_1 (reused for the O staging)
+  static constexpr int kOffK = 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kSK * kTileBytes;
+  static constexpr int kOffBar = kOffV + kSV * kTileBytes;
+  static constexpr int kBarQ = 0;
+  static constexpr int kBarKFull = 1;
+  static constexpr int kBarKEmpty = kBarKFull + kSK;
+  static constexpr int kBarVFull = kBarKEmpty + kSK;
+  static constexpr int kBarVEmpty = kBarVFull + kSV;
+  static constexpr int kBarSFull = kBarVEmpty + kSV;  // one per query tile
+  static constexpr int kBarPFull = kBarSFull + 2;
+  static constexpr int kBarOFinal = kBarPFull + 2;
+  static constexpr int kBarDrain = kBarOFinal + 2;
+  static constexpr int kNumBars = kBarDrain + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-B alignment
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kColS = 0;    // S_t at t*128
+  static constexpr uint32_t kColO = 256;  // O_t at 256 + t*D
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct Params {
+  float* lse;
+  int BH;
+  int N;
+  int n_qtiles;  // ceil(N / 128)
+  int n_cta_q;   // ceil(n_qtiles / 2)
+  float scale;
+  float scale_log2;  // scale * log2(e)
+  int causal;
+  int withhold_v0;   // test hook: never load V tile 0
+  unsigned long long timeout_ns;
+};
+
+// Bounded mbarrier waits.  `wait` gives up when the CTA's abort flag is set or
+// the deadline passes (then it sets the flag and the device status word);
+// `drain` ignores the abort flag (used to wait for in-flight work on the way out).
+struct Waiter {
+  volatile uint32_t* abort_flag;
+  unsigned long long timeout_ns;
+
+  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    return slow(bar, parity, true);
+  }
+  __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    return slow(bar, parity, false);
+  }
+  __device__ __forceinline__ bool slow(uint32_t bar, uint32_t parity, bool honour_abort) const {
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+      for (int i = 0; i < 16; ++i)
+        if (ptx::mbar_try_wait(bar, parity)) return true;
+      if (honour_abort && *abort_flag) return false;
+      if (ptx::globaltimer_ns() - t0 > timeout_ns) {
+        *abort_flag = 1u;
+        atomicOr(&g_status, FA_STATUS_TIMEOUT);
+        return false;
+      }
+    }
+  }
+};
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const Params p) {
+  using C = Cfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- which (batch*head, query-tile pair) this CTA owns
+  const int bid = blockIdx.x;
+  int bh, cta_q;
+  if (p.causal) {  // longest first: the last query tiles have the most K/V tiles
+    cta_q = p.n_cta_q - 1 - bid / p.BH;
+    bh = bid % p.BH;
+  } else {         // head-major: CTAs of one head run together and share K/V in L2
+    bh = bid / p.n_cta_q;
+    cta_q = bid % p.n_cta_q;
+  }
+  const int qt0 = 2 * cta_q;
+  const int qt1 = qt0 + 1;
+  const bool has1 = qt1 < p.n_qtiles;
+  const int n0 = p.causal ? qt0 + 1 : p.n_qtiles;  // K/V tiles visited by query tile 0
+  const int n1 = has1 ? (p.causal ? qt1 + 1 : p.n_qtiles) : 0;
+  const int nmax = n0 > n1 ? n0 : n1;
+
+  if (warp == 8 && lane == 0) {
+    ptx::mbar_init(bar(C::kBarQ), 1);
+    for (int s = 0; s < C::kSK; ++s) {
+      ptx::mbar_init(bar(C::kBarKFull + s), 1);
+      ptx::mbar_init(bar(C::kBarKEmpty + s), 1);
+    }
+    for (int s = 0; s < C::kSV; ++s) {
+      ptx::mbar_init(bar(C::kBarVFull + s), 1);
+      ptx::mbar_init(bar(C::kBarVEmpty + s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(bar(C::kBarSFull + t), 1);
+      ptx::mbar_init(bar(C::kBarPFull + t), 4);  // one arrive per softmax warp
+      ptx::mbar_init(bar(C::kBarOFinal + t), 1);
+    }
+    ptx::mbar_init(bar(C::kBarDrain), 1);
+    *abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 9) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Waiter w{abort_flag, p.timeout_ns};
+
+  if (warp == 8) {
+    // ================================================================ TMA producer
+    if (lane == 0) {
+      ptx::prefetch_tensormap(&tm_q);
+      ptx::prefetch_tensormap(&tm_k);
+      ptx::prefetch_tensormap(&tm_v);
+      ptx::prefetch_tensormap(&tm_o);
+      ptx::mbar_arrive_expect_tx(bar(C::kBarQ), (has1 ? 2 : 1) * C::kTileBytes);
+      for (int c = 0; c < C::kChunks; ++c)
+        ptx::tma_load_3d(sbase + C::kOffQ + c * C::kChunkBytes, &tm_q, bar(C::kBarQ), c * 64,
+                         qt0 * 128, bh);
+      if (has1)
+        for (int c = 0; c < C::kChunks; ++c)
+          ptx::tma_load_3d(sbase + C::kOffQ + C::kTileBytes + c * C::kChunkBytes, &tm_q,
+                           bar(C::kBarQ), c * 64, qt1 * 128, bh);
+      int nk = 0, nv = 0;  // K and V tiles issued so far (V: counting from v_first)
+      const int v_first = p.withhold_v0 ? 1 : 0;
+      bool ok = true;
+      for (int j = 0; j < nmax; ++j) {
+        const int sk = j % C::kSK, uk = j / C::kSK;
+        if (uk > 0 && !w.wait(bar(C::kBarKEmpty + sk), (uk - 1) & 1)) { ok = false; break; }
+        ptx::mbar_arrive_expect_tx(bar(C::kBarKFull + sk), C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          ptx::tma_load_3d(sbase + C::kOffK + sk * C::kTileBytes + c * C::kChunkBytes, &tm_k,
+                           bar(C::kBarKFull + sk), c * 64, j * 128, bh);
+        nk = j + 1;
+        const int sv = j % C::kSV, uv = j / C::kSV;
+        if (uv > 0 && !w.wait(bar(C::kBarVEmpty + sv), (uv - 1) & 1)) { ok = false; break; }
+        if (j >= v_first) {
+          ptx::mbar_arrive_expect_tx(bar(C::kBarVFull + sv), C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            ptx::tma_load_3d(sbase + C::kOffV + sv * C::kTileBytes + c * C::kChunkBytes, &tm_v,
+                             bar(C::kBarVFull + sv), c * 64, j * 128, bh);
+          nv = j + 1;
+        }
+      }
+      if (!ok) {  // let every copy already issued land before the CTA's memory is released
+        w.drain(bar(C::kBarQ), 0);
+        for (int s = 0; s < C::kSK; ++s)
+          if (s < nk) {
+            const int jl = s + C::kSK * ((nk - 1 - s) / C::kSK);
+            w.drain(bar(C::kBarKFull + s), (jl / C::kSK) & 1);
+          }
+        for (int s = 0; s < C::kSV; ++s) {
+          int jl = -1;
+          for (int j = v_first; j < nv; ++j)
+            if (j % C::kSV == s) jl = j;
+          if (jl >= 0) w.drain(bar(C::kBarVFull + s), (jl / C::kSV) & 1);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 9) {
+    // ================================================================ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 128, false);
+      constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, D, true);
+      bool ok = w.wait(bar(C::kBarQ), 0);
+      ptx::tc_fence_after();
+      for (int j = 0; ok && j <= nmax; ++j) {
+        if (j < nmax && !w.wait(bar(C::kBarKFull + j % C::kSK), (j / C::kSK) & 1)) { ok = false; break; }
+        if (j >= 1 && !w.wait(bar(C::kBarVFull + (j - 1) % C::kSV), ((j - 1) / C::kSV) & 1)) {
+          ok = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        for (int t = 0; t < 2; ++t) {
+          const int nt = t ? n1 : n0;
+          if (j >= 1 && j - 1 < nt) {
+            // O_t += P_t V_{j-1}: P from tensor memory, V (N-contiguous) from shared memory
+            if (!w.wait(bar(C::kBarPFull + t), (j - 1) & 1)) { ok = false; break; }
+            ptx::tc_fence_after();
+            const uint32_t vb = sbase + C::kOffV + ((j - 1) % C::kSV) * C::kTileBytes;
+            const uint32_t t_o = tmem + C::kColO + t * D;
+            const uint32_t t_p = tmem + C::kColS + t * 128;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              // 16 keys per step: 2 groups of 8 rows (SBO 1024 B); d beyond 64 at +16 KB (LBO)
+              const uint64_t bdesc = ptx::smem_desc_sw128(vb + kk * 2048, C::kChunkBytes, 1024);
+              ptx::mma_ts(t_o, t_p + kk * 8, bdesc, kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
+            }
+            if (j - 1 == nt - 1) ptx::tc_commit(bar(C::kBarOFinal + t));
+          }
+          if (j < nt) {
+            // S_t = Q_t K_j^T, both K-major (d contiguous), 16 d-columns per step
+            const uint32_t qb = sbase + C::kOffQ + t * C::kTileBytes;
+            const uint32_t kb = sbase + C::kOffK + (j % C::kSK) * C::kTileBytes;
+            const uint32_t t_s = tmem + C::kColS + t * 128;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
+              ptx::mma_ss(t_s, ptx::smem_desc_sw128(qb + off, 16, 1024),
+                          ptx::smem_desc_sw128(kb + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+            }
+            ptx::tc_commit(bar(C::kBarSFull + t));
+          }
+        }
+        if (!ok) break;
+        if (j < nmax) ptx::tc_commit(bar(C::kBarKEmpty + j % C::kSK));
+        if (j >= 1) ptx::tc_commit(bar(C::kBarVEmpty + (j - 1) % C::kSV));
+      }
+      // every MMA issued by this thread completes before tensor memory is freed
+      ptx::tc_commit(bar(C::kBarDrain));
+      w.drain(bar(C::kBarDrain), 0);
+    }
+    __syncwarp();
+  } else {
+    // ================================================================ softmax warpgroups
+    const int t = warp >> 2;
+    const int quarter = warp & 3;
+    const int nt = t ? n1 : n0;
+    const int qt = t ? qt1 : qt0;
+    const int row = quarter * 32 + lane;
+    const int qrow = qt * 128 + row;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + C::kColS + t * 128;
+    const uint32_t t_o = tmem + lane_off + C::kColO + t * D;
+    const float c2 = p.scale_log2;
+    float m_run = -INFINITY;  // running max of the raw scores q.k (scale > 0)
+    float l_run = 0.f;        // running sum of 2^((s - m_run) * c2)
+    bool ok = nt > 0;
+    for (int j = 0; ok && j < nt; ++j) {
+      ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarSFull + t), j & 1));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      float s[128];
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t r[32];
+        ptx::tmem_ld32(t_s + cc * 32, r);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(r[i]);
+      }
+      // mask: keys past the end of the sequence, and keys after the query when causal
+      const int col0 = j * 128;
+      int lim = p.N - col0;
+      if (p.causal && qrow - col0 + 1 < lim) lim = qrow - col0 + 1;
+      if (lim < 128) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) s[c] = -INFINITY;
+      }
+      float mx[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
+      const float tile_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      const float m_new = fmaxf(m_run, tile_max);
+      // Keep the old reference unless the max grew by more than 2^8: l and O~ share the
+      // reference, so O = O~/l is unchanged; only the size of the terms is bounded.
+      const bool rescale = (m_new - m_run) * c2 > kRescaleLog2Threshold;
+      const float m_ref = rescale ? m_new : m_run;
+      const float r_fac = rescale ? ptx::ex2_approx((m_run - m_new) * c2) : 1.f;
+      const float neg = -m_ref * c2;
+      float sum[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sum[i] = 0.f;
+#pragma unroll
+      for (int c = 0; c < 128; ++c) {
+        const float e = ptx::ex2_approx(fmaf(s[c], c2, neg));
+        s[c] = e;
+        sum[c & 7] += e;
+      }
+      l_run = l_run * r_fac + (((sum[0] + sum[1]) + (sum[2] + sum[3])) +
+                               ((sum[4] + sum[5]) + (sum[6] + sum[7])));
+      m_run = m_ref;
+      // correction O~ *= r (PV of tile j-1 has completed: S_t's commit covers it)
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t r[32];
+          ptx::tmem_ld32(t_o + cc * 32, r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
+          ptx::tmem_st32(t_o + cc * 32, r);
+        }
+      }
+      // P_t (bf16 pairs) over the first 64 columns of S_t
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) pk[i] = ptx::pack_bf16x2(s[h * 64 + 2 * i], s[h * 64 + 2 * i + 1]);
+        ptx::tmem_st32(t_s + h * 32, pk);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::kBarPFull + t));
+    }
+    // ---- epilogue: O = O~ / l -> bf16 -> shared (Q_t's buffer) -> TMA store; LSE
+    const uint32_t so = sbase + C::kOffQ + t * C::kTileBytes;
+    if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarOFinal + t), 0));
+    if (ok) {
+      ptx::tc_fence_after();
+      const float inv_l = 1.f / l_run;
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        ptx::tmem_ld32(t_o + cc * 32, r);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+        const uint32_t chunk_base = so + (cc >> 1) * C::kChunkBytes + row * 128;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const int gran = (cc & 1) * 4 + g;  // 16-byte granule within the 128-byte row
+          ptx::st_shared_v4(chunk_base + ((gran ^ (row & 7)) << 4), pk[4 * g], pk[4 * g + 1],
+                            pk[4 * g + 2], pk[4 * g + 3]);
+        }
+      }
+      if (qrow < p.N) p.lse[static_cast<size_t>(bh) * p.N + qrow] = m_run * p.scale + logf(l_run);
+      ptx::fence_proxy_async_smem();
+    }
+    ptx::named_barrier(1 + t, 128);
+    if (ok && row == 0) {
+      for (int c = 0; c < C::kChunks; ++c) ptx::tma_store_3d(&tm_o, so + c * C::kChunkBytes, c * 64, qt * 128, bh);
+      ptx::bulk_commit();
+      ptx::bulk_wait_all();
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// ==================================================================== host side
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// [B*H, N, d] bf16 viewed as 3-D; box = 64 columns (128 bytes) x 128 rows x 1 head.
+bool encode_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_dev_mutex;
+int g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, -1 wrong arch
+
+int prepare_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (g_dev_state[dev] == 1) return FA_OK;
+  if (g_dev_state[dev] == -1) return FA_ERR_ARCH;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return FA_ERR_CUDA;
+  if (major != 10 || minor != 3) {
+    g_dev_state[dev] = -1;
+    return FA_ERR_ARCH;
+  }
+  if (cudaFuncSetAttribute(fa_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<64>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(fa_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<128>::kSmemBytes) != cudaSuccess)
+    return FA_ERR_CUDA;
+  g_dev_state[dev] = 1;
+  return FA_OK;
+}
+
+bool is_device_pointer(const void* ptr) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+int validate(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
+             int H, int N, int d, float scale) {
+  if (!q || !k || !v || !o || !lse) return FA_ERR_ARG;
+  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return FA_ERR_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_ARG;
+  const long long rows = static_cast<long long>(B) * H * N;
+  if (rows > 2147483647LL) return FA_ERR_ARG;
+  for (const void* ptr : {q, k, v, o, static_cast<const void*>(lse)})
+    if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_ARG;
+  const size_t tb = static_cast<size_t>(rows) * d * 2, lb = static_cast<size_t>(rows) * 4;
+  for (const void* in : {q, k, v})
+    if (overlaps(o, tb, in, tb) || overlaps(lse, lb, in, tb)) return FA_ERR_ARG;
+  if (overlaps(o, tb, lse, lb)) return FA_ERR_ARG;
+  for (const void* ptr : {q, k, v, o, static_cast<const void*>(lse)})
+    if (!is_device_pointer(ptr)) return FA_ERR_ARG;
+  return FA_OK;
+}
+
+template <int D>
+int launch(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N, float scale,
+           int causal, int withhold_v0, unsigned long long timeout_ns, cudaStream_t stream) {
+  CUtensorMap mq, mk, mv, mo;
+  if (!encode_map(&mq, q, BH, N, D) || !encode_map(&mk, k, BH, N, D) || !encode_map(&mv, v, BH, N, D) ||
+      !encode_map(&mo, o, BH, N, D))
+    return FA_ERR_LAUNCH;
+  Params p{};
+  p.lse = lse;
+  p.BH = BH;
+  p.N = N;
+  p.n_qtiles = (N + 127) / 128;
+  p.n_cta_q = (p.n_qtiles + 1) / 2;
+  p.scale = scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  p.causal = causal ? 1 : 0;
+  p.withhold_v0 = withhold_v0;
+  p.timeout_ns = timeout_ns;
+  const long long grid = static_cast<long long>(BH) * p.n_cta_q;
+  if (grid > 2147483647LL) return FA_ERR_ARG;
+  fa_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(mq, mk, mv, mo, p);
+  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+}
+
+int forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+            float scale, int causal, int withhold_v0, unsigned long long timeout_ns, cudaStream_t stream) {
+  int rc = validate(q, k, v, o, lse, B, H, N, d, scale);
+  if (rc != FA_OK) return rc;
+  rc = prepare_device();
+  if (rc != FA_OK) return rc;
+  const int BH = B * H;
+  return d == 64 ? launch<64>(q, k, v, o, lse, BH, N, scale, causal, withhold_v0, timeout_ns, stream)
+                 : launch<128>(q, k, v, o, lse, BH, N, scale, causal, withhold_v0, timeout_ns, stream);
+}
+
+constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
+
+}  // namespace
+}  // namespace fa
+
+extern "C" {
+
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+           float scale, int causal, cudaStream_t stream) {
+  return fa::forward(q, k, v, o, lse, B, H, N, d, scale, causal, 0, fa::kDefaultTimeoutNs, stream);
+}
+
+int fa_fwd_withheld_tile(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                         int N, int d, float scale, int causal, double wait_timeout_ms,
+                         cudaStream_t stream) {
+  if (!(wait_timeout_ms >= 1.0 && wait_timeout_ms <= 10000.0)) return FA_ERR_ARG;
+  return fa::forward(q, k, v, o, lse, B, H, N, d, scale, causal, 1,
+                     static_cast<unsigned long long>(wait_timeout_ms * 1e6), stream);
+}
+
+int fa_status(int clear, cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, fa::g_status, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+  if (clear) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(fa::g_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return static_cast<int>(word & 0x7fffffffu);
+}
+
+const char* fa_strerror(int code) {
+  switch (code) {
+    case FA_OK: return "success";
+    case FA_ERR_ARG: return "invalid argument (pointer, alignment, size, d or scale)";
+    case FA_ERR_ARCH: return "device is not compute capability 10.3 (GB300)";
+    case FA_ERR_LAUNCH: return "kernel launch or TMA descriptor encoding failed";
+    case FA_ERR_TIMEOUT: return "a device-side barrier wait timed out";
+    case FA_ERR_CUDA: return "CUDA runtime call failed";
+    default: return "unknown error";
+  }
+}
+
+int fa_version(void) { return 1; }
+
+}  // extern "C"

@@ -1,0 +1,110 @@
+"""Python binding of the C-ABI library ``libfa_gb300.so`` (argument marshalling only).
+
+Every function here has the name of the C entry point it calls (declared in
+``include/fa_gb300.h``).  Tensors are PyTorch CUDA tensors; PyTorch provides
+device memory and the stream, the library does all the work.  Importing this
+module loads the library and raises ImportError when it has not been built:
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libfa_gb300.so")
+
+FA_OK = 0
+FA_ERR_ARG = -1
+FA_ERR_ARCH = -2
+FA_ERR_LAUNCH = -3
+FA_ERR_TIMEOUT = -4
+FA_ERR_CUDA = -5
+FA_STATUS_TIMEOUT = 0x1
+
+EXPORTED = ("fa_fwd", "fa_status", "fa_fwd_withheld_tile", "fa_strerror", "fa_version")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+
+lib = ctypes.CDLL(LIB_PATH)
+_vp, _i, _f, _d = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double
+lib.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]
+lib.fa_fwd.restype = _i
+lib.fa_fwd_withheld_tile.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _d, _vp]
+lib.fa_fwd_withheld_tile.restype = _i
+lib.fa_status.argtypes = [_i, _vp]
+lib.fa_status.restype = _i
+lib.fa_strerror.argtypes = [_i]
+lib.fa_strerror.restype = ctypes.c_char_p
+lib.fa_version.argtypes = []
+lib.fa_version.restype = _i
+
+
+class FAError(RuntimeError):
+    def __init__(self, code: int):
+        self.code = code
+        super().__init__(f"fa error {code}: {lib.fa_strerror(code).decode()}")
+
+
+def _stream_handle(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _prepare(q, k, v, o, lse):
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    B, H, N, d = q.shape
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    return B, H, N, d, o, lse
+
+
+def fa_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, stream=None):
+    """Exact attention forward.  q, k, v: CUDA bf16 [B, H, N, d] contiguous.
+
+    Returns (o, lse): o bf16 [B, H, N, d], lse fp32 [B, H, N] (natural log).
+    Preallocated ``o`` / ``lse`` are written in place.  Raises FAError on a
+    nonzero return code.  Shape, dtype and placement checks are the library's.
+    """
+    B, H, N, d, o, lse = _prepare(q, k, v, o, lse)
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    rc = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                    B, H, N, d, float(scale), int(bool(causal)), _stream_handle(stream, q.device))
+    if rc != FA_OK:
+        raise FAError(rc)
+    return o, lse
+
+
+def fa_fwd_withheld_tile(q, k, v, o=None, lse=None, scale=None, causal=False,
+                         wait_timeout_ms=50.0, stream=None) -> int:
+    """Test hook: run the kernel with V tile 0 never loaded; returns the C return code."""
+    B, H, N, d, o, lse = _prepare(q, k, v, o, lse)
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    return lib.fa_fwd_withheld_tile(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                    lse.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
+                                    float(wait_timeout_ms), _stream_handle(stream, q.device))
+
+
+def fa_status(clear=False, stream=None) -> int:
+    """Synchronise the stream and return the device status word (optionally clearing it)."""
+    dev = torch.cuda.current_device()
+    rc = lib.fa_status(int(bool(clear)), _stream_handle(stream, dev))
+    if rc < 0:
+        raise FAError(rc)
+    return rc
+
+
+def fa_strerror(code: int) -> str:
+    return lib.fa_strerror(int(code)).decode()
+
+
+def fa_version() -> int:
+    return lib.fa_version()

@@ -1,0 +1,110 @@
+/*
+ * fa_gb300.h -- C ABI of the exact attention forward for NVIDIA GB300 (sm_103a).
+ *
+ * The operation is the exact attention forward of FlashAttention: for every
+ * batch b and head h,
+ *
+ *     S = scale * Q K^T               (masked: key j > query i set to -inf when causal)
+ *     P = softmax(S) by rows,         O = P V,
+ *     LSE_i = ln sum_j exp(S_ij)      (natural log, over the unmasked j)
+ *
+ * as defined on the zzszmyf.github.io notes page "FlashAttention 原理是什么？
+ * 为什么又省显存又快" (§2 the three-step definition, §5 online softmax, §6 the
+ * per-row statistics kept for the backward recompute, §7.1 Algorithm 1) and on
+ * the aiqz.cc "flash-attention-io-optimization" article (section 在线Softmax算法:
+ * m_new, r = e^(m - m_new), l_new, O~_new, O = O~/l).  S and P never leave the
+ * chip: K/V tiles are merged with a running row max m and a running exp-sum l,
+ * so the result is exact up to floating-point rounding.  The per-row LSE is the
+ * statistic a backward pass needs to rebuild P without storing it.
+ *
+ * Precision: bf16 inputs and output, fp32 accumulation of S and O, P rounded to
+ * bf16 for the P V product, LSE in fp32.
+ *
+ * Threading: every entry point is reentrant.  Calls on different streams may
+ * run concurrently.  The library keeps no per-call state and allocates no
+ * device memory in fa_fwd; the only device-global state is the status word
+ * read by fa_status().
+ */
+#ifndef FA_GB300_H
+#define FA_GB300_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes: 0 on success, negative on error. */
+#define FA_OK            0
+#define FA_ERR_ARG      -1  /* a null or misaligned pointer, or an unsupported size        */
+#define FA_ERR_ARCH     -2  /* the current device is not compute capability 10.3 (GB300)   */
+#define FA_ERR_LAUNCH   -3  /* the CUDA launch (or the TMA descriptor encoding) failed     */
+#define FA_ERR_TIMEOUT  -4  /* a device-side barrier wait gave up (see fa_status)           */
+#define FA_ERR_CUDA     -5  /* another CUDA runtime call failed                             */
+
+/* Bits of the device status word (fa_status). */
+#define FA_STATUS_TIMEOUT 0x1u  /* some CTA's bounded mbarrier wait expired and it bailed out */
+
+/*
+ * fa_fwd -- exact attention forward, O and LSE.
+ *
+ * q, k, v : device pointers, bf16, contiguous [B, H, N, d] (row stride d).
+ *           Read only.  Each must be 16-byte aligned.
+ * o       : device pointer, bf16, contiguous [B, H, N, d].  Written.
+ * lse     : device pointer, fp32, contiguous [B, H, N].  Written.
+ *           o and lse must not overlap q, k, v or each other.
+ * B, H, N : batch, heads, sequence length; each >= 1.  Any N is accepted
+ *           (the last 128-row tile may be partial).  B*H*N <= 2^31 - 1.
+ * d       : head dimension, 64 or 128.
+ * scale   : multiplies Q K^T before the softmax (usually 1/sqrt(d)); finite.
+ * causal  : nonzero masks key j for query i when j > i (square, top-left
+ *           aligned: every row keeps at least key 0).
+ * stream  : the CUDA stream the kernel is enqueued on (0 = legacy default).
+ *
+ * Ownership: the caller allocates every buffer; the call allocates nothing.
+ * The call is asynchronous with respect to the host: it only enqueues one
+ * kernel.  The arguments are validated before anything is enqueued; on an
+ * error return nothing was written.  A device-side wait that gives up (never
+ * expected in correct operation) does not surface here: it sets
+ * FA_STATUS_TIMEOUT in the status word, which fa_status() reads.
+ *
+ * Returns FA_OK, FA_ERR_ARG, FA_ERR_ARCH or FA_ERR_LAUNCH.
+ */
+int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+           int B, int H, int N, int d, float scale, int causal, cudaStream_t stream);
+
+/*
+ * fa_status -- read the device status word of the current device.
+ *
+ * Synchronises `stream` first, then copies the word to the host.  If `clear`
+ * is nonzero the word is reset to 0 afterwards.  Returns the word (>= 0) or
+ * FA_ERR_CUDA.
+ */
+int fa_status(int clear, cudaStream_t stream);
+
+/*
+ * fa_fwd_withheld_tile -- test hook for the bounded device waits.
+ *
+ * Same arguments as fa_fwd, plus wait_timeout_ms.  The kernel's producer warp
+ * deliberately never loads V tile 0, so the MMA warp's wait for it cannot be
+ * satisfied; every wait in the kernel gives up after about wait_timeout_ms,
+ * each CTA waits for the copies it has in flight, frees its tensor memory and
+ * returns, and FA_STATUS_TIMEOUT is set.  No fault and no hang: the context
+ * stays usable.  The contents of o and lse are unspecified afterwards.
+ * wait_timeout_ms must lie in [1, 10000].
+ */
+int fa_fwd_withheld_tile(const void* q, const void* k, const void* v, void* o, float* lse,
+                         int B, int H, int N, int d, float scale, int causal,
+                         double wait_timeout_ms, cudaStream_t stream);
+
+/* fa_strerror -- a static, human-readable string for a return code. */
+const char* fa_strerror(int code);
+
+/* fa_version -- the library's interface version (currently 1). */
+int fa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_GB300_H */

@@ -1,0 +1,72 @@
+"""The C-ABI library builds, loads and exports every entry point the header
+declares; host-side argument checks that run before any CUDA call (no GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__ as entry
+
+HEADER = os.path.join(entry.ROOT, "include", "fa_gb300.h")
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(fa_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def fa():
+    entry.build()
+    from exact_io_aware_02_gb300 import fa as mod
+    return mod
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert "fa_fwd" in names and "fa_strerror" in names and "fa_status" in names
+
+
+def test_library_exports_every_declared_symbol(fa):
+    for name in declared_functions():
+        assert hasattr(fa.lib, name), name
+        assert isinstance(getattr(fa.lib, name), ctypes._CFuncPtr)
+    assert set(fa.EXPORTED) == set(declared_functions())
+
+
+def test_strerror_and_version(fa):
+    assert fa.fa_version() == 1
+    for code in (0, -1, -2, -3, -4, -5):
+        assert fa.fa_strerror(code) and fa.fa_strerror(code) != "unknown error"
+    assert fa.fa_strerror(-99) == "unknown error"
+
+
+FAKE = 0x7f0000000000  # 16-byte aligned, never dereferenced: rejected before any CUDA call
+
+
+def _call(fa, q=FAKE, k=FAKE + 2**30, v=FAKE + 2**31, o=FAKE + 3 * 2**30, lse=FAKE + 2**32,
+          B=1, H=1, N=128, d=128, scale=0.088, causal=0):
+    return fa.lib.fa_fwd(q, k, v, o, lse, B, H, N, d, scale, causal, None)
+
+
+@pytest.mark.parametrize("kw", [
+    {"q": 0}, {"k": 0}, {"v": 0}, {"o": 0}, {"lse": 0},
+    {"d": 96}, {"d": 256}, {"d": 0}, {"B": 0}, {"H": -1}, {"N": 0},
+    {"scale": 0.0}, {"scale": -1.0}, {"scale": float("inf")}, {"scale": float("nan")},
+    {"q": FAKE + 8}, {"o": FAKE + 3 * 2**30 + 4}, {"lse": FAKE + 2**32 + 4},
+    {"B": 65536, "H": 65536, "N": 2},
+    {"o": FAKE},                       # output overlaps an input
+    {"lse": FAKE + 3 * 2**30 + 64},    # LSE overlaps O
+])
+def test_argument_errors_before_launch(fa, kw):
+    assert _call(fa, **kw) == fa.FA_ERR_ARG
+
+
+def test_withheld_tile_timeout_range(fa):
+    f = fa.lib.fa_fwd_withheld_tile
+    assert f(FAKE, FAKE + 2**30, FAKE + 2**31, FAKE + 3 * 2**30, FAKE + 2**32, 1, 1, 128, 128,
+             0.088, 0, 0.5, None) == fa.FA_ERR_ARG
+    assert f(FAKE, FAKE + 2**30, FAKE + 2**31, FAKE + 3 * 2**30, FAKE + 2**32, 1, 1, 128, 128,
+             0.088, 0, 20000.0, None) == fa.FA_ERR_ARG

@@ -310,6 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c2 = p.scale_log2;
     float m_run = -INFINITY;  // running max of the raw scores q.k (scale > 0)
     float l_run = 0.f;        // running sum of 2^((s - m_run) * c2)
+    float lp_run = 0.f;       // the same sum over the bf16-rounded terms
     bool ok = nt > 0;
     for (int j = 0; ok && j < nt; ++j) {
       ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarSFull + t), j & 1));
@@ -346,19 +347,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_ref = rescale ? m_new : m_run;
       const float r_fac = rescale ? ptx::ex2_approx((m_run - m_new) * c2) : 1.f;
       const float neg = -m_ref * c2;
-      float sum[8];
+      // P = 2^(s*c2 - m_ref*c2), rounded to bf16 pairs for the P V product.  Two running
+      // sums: l_run over the fp32 values (for LSE) and lp_run over the rounded values the
+      // tensor core multiplies (for O = sum(P v) / sum(P), a convex combination of V rows).
+      uint32_t pk[64];
+      float sum[4], sum_p[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sum[i] = 0.f;
+      for (int i = 0; i < 4; ++i) sum[i] = sum_p[i] = 0.f;
 #pragma unroll
-      for (int c = 0; c < 128; ++c) {
-        const float e = ptx::ex2_approx(fmaf(s[c], c2, neg));
-        s[c] = e;
-        sum[c & 7] += e;
+      for (int i = 0; i < 64; ++i) {
+        const float e0 = ptx::ex2_approx(fmaf(s[2 * i], c2, neg));
+        const float e1 = ptx::ex2_approx(fmaf(s[2 * i + 1], c2, neg));
+        pk[i] = ptx::pack_bf16x2(e0, e1);
+        sum[i & 3] += e0 + e1;
+        sum_p[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
       }
-      l_run = l_run * r_fac + (((sum[0] + sum[1]) + (sum[2] + sum[3])) +
-                               ((sum[4] + sum[5]) + (sum[6] + sum[7])));
+      l_run = l_run * r_fac + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
+      lp_run = lp_run * r_fac + ((sum_p[0] + sum_p[1]) + (sum_p[2] + sum_p[3]));
       m_run = m_ref;
       // correction O~ *= r (PV of tile j-1 has completed: S_t's commit covers it)
+      __syncwarp();
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
@@ -370,12 +378,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // P_t (bf16 pairs) over the first 64 columns of S_t
+      __syncwarp();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        uint32_t pk[32];
+        uint32_t half[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) pk[i] = ptx::pack_bf16x2(s[h * 64 + 2 * i], s[h * 64 + 2 * i + 1]);
-        ptx::tmem_st32(t_s + h * 32, pk);
+        for (int i = 0; i < 32; ++i) half[i] = pk[h * 32 + i];
+        ptx::tmem_st32(t_s + h * 32, half);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -387,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarOFinal + t), 0));
     if (ok) {
       ptx::tc_fence_after();
-      const float inv_l = 1.f / l_run;
+      const float inv_l = 1.f / lp_run;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t r[32];

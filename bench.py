@@ -67,6 +67,20 @@ def peaks():
     return 1900.0, 6800.0, "fallback"
 
 
+def reduce_max(x: float, world: int, device=None) -> float:
+    """Max of a per-rank number over all ranks (identity on one rank)."""
+    if world <= 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_rank: float, ms: float, world: int) -> float:
+    """Whole-job throughput: the units every rank processed over the slowest rank's time."""
+    return world * flops_per_rank / (ms * 1e-3) / 1e12
+
+
 def workload_config(w, l2_note):
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
             "qk_std": w.qk_std, "v_std": w.v_std, "seed": w.seed, "l2": l2_note}
@@ -146,7 +160,7 @@ def gpu_selector(dev) -> str:
     return str(dev.index or 0)
 
 
-def cpu_baseline(w, budget_s=12.0, max_slices=8):
+def cpu_baseline(w, budget_s=12.0, max_slices=32):
     """The fp64 oracle as it stands, on whole (b, h) slices of the workload until
     about ``budget_s`` seconds of CPU work; TFLOP/s counted like the GPU metric."""
     import numpy as np
@@ -257,11 +271,7 @@ def run_ours(args, w, rank, world, local_rank):
     t1 = time.perf_counter()
     clocks = sampler.stop(t0, t1) if rank == 0 else None
     kernel_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    ms = sum(kernel_ms) / len(kernel_ms)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(sum(kernel_ms) / len(kernel_ms), world, dev)
     if fa.fa_status(clear=True) != 0:
         raise RuntimeError("device status word set during the timed region")
 
@@ -280,16 +290,12 @@ def run_ours(args, w, rank, world, local_rank):
         lse_h.copy_(lse, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world, dev)
     if rank != 0:
         return
 
     flops = w.flops()
-    value = world * flops / (ms * 1e-3) / 1e12
+    value = job_tflops(flops, ms, world)
     peak_tf, _, peak_kind = peaks()
     achieved = flops / (ms * 1e-3) / 1e12
     line = {
@@ -302,7 +308,7 @@ def run_ours(args, w, rank, world, local_rank):
                      "frac": achieved / peak_tf, "traffic": measured_traffic(w.name),
                      "peak_kind": f"bf16 dense burst, {peak_kind}",
                      "algorithmic_flops": flops, "algorithmic_bytes": w.algorithmic_bytes()},
-        "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+        "e2e": {"value": job_tflops(flops, e2e_ms, world), "unit": UNIT,
                 "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
                 "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * lse.element_size()},
         "gpu_launches": launches,

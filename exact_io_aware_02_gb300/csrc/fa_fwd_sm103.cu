@@ -12,9 +12,10 @@
 // shared memory while the math warps consume it, and softmax work overlaps
 // the tensor-core work.
 //
-// GB300 design (one CTA per SM, 320 threads):
+// GB300 design (one CTA per SM, 384 threads in three warpgroups):
 //   * two 128-row query tiles per CTA (Q_0, Q_1) share every K/V tile that is
 //     loaded, halving K/V traffic per flop;
+//   * warps 8-11 give registers to warps 0-7 (setmaxnreg); warps 10, 11 idle;
 //   * warp 8  -- TMA producer: Q_0, Q_1 once, then K_j and V_j into separate
 //                shared-memory rings gated by full/empty mbarriers;
 //   * warp 9  -- MMA issuer (one thread): S_t = Q_t K_j^T with tcgen05.mma
@@ -51,7 +52,9 @@ namespace fa {
 
 __device__ unsigned int g_status;
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 384;  // 3 warpgroups: softmax 0, softmax 1, producer + MMA
+constexpr uint32_t kSoftmaxRegs = 224;  // setmaxnreg split of the 384 x 168 launch budget:
+constexpr uint32_t kOtherRegs = 56;     //   2 x 128 x 224 + 128 x 56 = 384 x 168
 constexpr float kRescaleLog2Threshold = 8.0f;  // skip the O correction unless max grows > 2^8
 
 template <int D>
@@ -190,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Waiter w{abort_flag, p.timeout_ns};
 
+  if (warp >= 8) ptx::regs_decrease<kOtherRegs>();
   if (warp == 8) {
     // ================================================================ TMA producer
     if (lane == 0) {
@@ -296,8 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       w.drain(bar(C::kBarDrain), 0);
     }
     __syncwarp();
-  } else {
+  } else if (warp < 8) {
     // ================================================================ softmax warpgroups
+    ptx::regs_increase<kSoftmaxRegs>();
     const int t = warp >> 2;
     const int quarter = warp & 3;
     const int nt = t ? n1 : n0;
@@ -317,12 +322,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       ptx::tc_fence_after();
       float s[128];
+      {
+        uint32_t r[128];
+        ptx::tmem_ld128(t_s, r);
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t r[32];
-        ptx::tmem_ld32(t_s + cc * 32, r);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[cc * 32 + i] = __uint_as_float(r[i]);
+        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
       }
       // mask: keys past the end of the sequence, and keys after the query when causal
       const int col0 = j * 128;
@@ -333,13 +337,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 128; ++c)
           if (c >= lim) s[c] = -INFINITY;
       }
-      float mx[8];
+      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
-#pragma unroll
-      for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], s[c]);
-      const float tile_max = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      for (int c = 4; c < 124; c += 8) {
+        mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
+        mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
+        mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
+        mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
+      }
+      mx0 = ptx::fmax3(mx0, s[124], s[125]);
+      mx1 = ptx::fmax3(mx1, s[126], s[127]);
+      const float tile_max = fmaxf(ptx::fmax3(mx0, mx1, mx2), mx3);
       const float m_new = fmaxf(m_run, tile_max);
       // Keep the old reference unless the max grew by more than 2^8: l and O~ share the
       // reference, so O = O~/l is unchanged; only the size of the terms is bounded.
@@ -347,26 +355,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float m_ref = rescale ? m_new : m_run;
       const float r_fac = rescale ? ptx::ex2_approx((m_run - m_new) * c2) : 1.f;
       const float neg = -m_ref * c2;
-      // P = 2^(s*c2 - m_ref*c2), rounded to bf16 pairs for the P V product.  Two running
+      // P = 2^(s*c2 - m_ref*c2), rounded to bf16 pairs for the P V product and written over
+      // the first 64 columns of S_t (first half while the second is computed).  Two running
       // sums: l_run over the fp32 values (for LSE) and lp_run over the rounded values the
       // tensor core multiplies (for O = sum(P v) / sum(P), a convex combination of V rows).
-      uint32_t pk[64];
-      float sum[4], sum_p[4];
+      __syncwarp();  // reconverge after the per-row mask before the warp-wide TMEM stores
+      const float2 c2v = make_float2(c2, c2), negv = make_float2(neg, neg);
+      float2 se[4], sp[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) sum[i] = sum_p[i] = 0.f;
+      for (int i = 0; i < 4; ++i) se[i] = sp[i] = make_float2(0.f, 0.f);
+      uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float e0 = ptx::ex2_approx(fmaf(s[2 * i], c2, neg));
-        const float e1 = ptx::ex2_approx(fmaf(s[2 * i + 1], c2, neg));
+        const float2 x = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), c2v, negv);
+        const float e0 = ptx::ex2_approx(x.x);
+        const float e1 = ptx::ex2_approx(x.y);
         pk[i] = ptx::pack_bf16x2(e0, e1);
-        sum[i & 3] += e0 + e1;
-        sum_p[i & 3] += __uint_as_float(pk[i] << 16) + __uint_as_float(pk[i] & 0xffff0000u);
+        se[i & 3] = __fadd2_rn(se[i & 3], make_float2(e0, e1));
+        sp[i & 3] = __fadd2_rn(sp[i & 3], make_float2(__uint_as_float(pk[i] << 16),
+                                                      __uint_as_float(pk[i] & 0xffff0000u)));
+        if (i == 31 || i == 63) {
+          uint32_t half[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) half[k] = pk[i - 31 + k];
+          ptx::tmem_st32(t_s + (i - 31), half);  // columns [0,32) then [32,64)
+        }
       }
-      l_run = l_run * r_fac + ((sum[0] + sum[1]) + (sum[2] + sum[3]));
-      lp_run = lp_run * r_fac + ((sum_p[0] + sum_p[1]) + (sum_p[2] + sum_p[3]));
+      const float2 se01 = __fadd2_rn(se[0], se[1]), se23 = __fadd2_rn(se[2], se[3]);
+      const float2 sp01 = __fadd2_rn(sp[0], sp[1]), sp23 = __fadd2_rn(sp[2], sp[3]);
+      l_run = l_run * r_fac + ((se01.x + se01.y) + (se23.x + se23.y));
+      lp_run = lp_run * r_fac + ((sp01.x + sp01.y) + (sp23.x + sp23.y));
       m_run = m_ref;
       // correction O~ *= r (PV of tile j-1 has completed: S_t's commit covers it)
-      __syncwarp();
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
@@ -376,15 +396,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
           ptx::tmem_st32(t_o + cc * 32, r);
         }
-      }
-      // P_t (bf16 pairs) over the first 64 columns of S_t
-      __syncwarp();
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t half[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) half[i] = pk[h * 32 + i];
-        ptx::tmem_st32(t_s + h * 32, half);
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();

@@ -16,8 +16,9 @@
 //   * two 128-row query tiles per CTA (Q_0, Q_1) share every K/V tile that is
 //     loaded, halving K/V traffic per flop;
 //   * warps 8-11 give registers to warps 0-7 (setmaxnreg); warps 10, 11 idle;
-//   * warp 8  -- TMA producer: Q_0, Q_1 once, then K_j and V_j into separate
-//                shared-memory rings gated by full/empty mbarriers;
+//   * warp 8  -- TMA producer: Q_0, Q_1 once, then K_0, V_0, K_1, V_1, ... into one
+//                shared-memory ring gated by full/empty mbarriers (the MMA warp
+//                consumes and releases the tiles in that order);
 //   * warp 9  -- MMA issuer (one thread): S_t = Q_t K_j^T with tcgen05.mma
 //                (A and B from shared memory, fp32 accumulator in tensor memory),
 //                then O_t += P_t V_j with P_t read from tensor memory;
@@ -53,8 +54,8 @@ namespace fa {
 __device__ unsigned int g_status;
 
 constexpr int kThreads = 384;  // 3 warpgroups: softmax 0, softmax 1, producer + MMA
-constexpr uint32_t kSoftmaxRegs = 224;  // setmaxnreg split of the 384 x 168 launch budget:
-constexpr uint32_t kOtherRegs = 56;     //   2 x 128 x 224 + 128 x 56 = 384 x 168
+constexpr uint32_t kSoftmaxRegs = 216;  // setmaxnreg split of the 384 x 168 launch budget:
+constexpr uint32_t kOtherRegs = 72;     //   2 x 128 x 216 + 128 x 72 = 384 x 168
 constexpr float kRescaleLog2Threshold = 8.0f;  // skip the O correction unless max grows > 2^8
 
 template <int D>
@@ -62,18 +63,16 @@ struct Cfg {
   static constexpr int kChunks = D / 64;           // 128-byte swizzle atoms along d
   static constexpr int kChunkBytes = 128 * 128;    // 128 rows x 64 bf16
   static constexpr int kTileBytes = 128 * D * 2;   // one 128-row tile of Q, K, V or O
-  static constexpr int kSK = D == 128 ? 3 : 4;     // K ring depth
-  static constexpr int kSV = D == 128 ? 2 : 4;     // V ring depth
+  // One ring of K/V tiles in the order the MMA warp consumes and releases them:
+  // K_0, V_0, K_1, V_1, ...  (tile u is K_{u/2} for even u, V_{u/2} for odd u)
+  static constexpr int kSlots = D == 128 ? 5 : 12;
   static constexpr int kOffQ = 0;                  // Q_0, Q_1 (reused for the O staging)
-  static constexpr int kOffK = 2 * kTileBytes;
-  static constexpr int kOffV = kOffK + kSK * kTileBytes;
-  static constexpr int kOffBar = kOffV + kSV * kTileBytes;
+  static constexpr int kOffRing = 2 * kTileBytes;
+  static constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
   static constexpr int kBarQ = 0;
-  static constexpr int kBarKFull = 1;
-  static constexpr int kBarKEmpty = kBarKFull + kSK;
-  static constexpr int kBarVFull = kBarKEmpty + kSK;
-  static constexpr int kBarVEmpty = kBarVFull + kSV;
-  static constexpr int kBarSFull = kBarVEmpty + kSV;  // one per query tile
+  static constexpr int kBarFull = 1;
+  static constexpr int kBarEmpty = kBarFull + kSlots;
+  static constexpr int kBarSFull = kBarEmpty + kSlots;  // one per query tile
   static constexpr int kBarPFull = kBarSFull + 2;
   static constexpr int kBarOFinal = kBarPFull + 2;
   static constexpr int kBarDrain = kBarOFinal + 2;
@@ -166,13 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 8 && lane == 0) {
     ptx::mbar_init(bar(C::kBarQ), 1);
-    for (int s = 0; s < C::kSK; ++s) {
-      ptx::mbar_init(bar(C::kBarKFull + s), 1);
-      ptx::mbar_init(bar(C::kBarKEmpty + s), 1);
-    }
-    for (int s = 0; s < C::kSV; ++s) {
-      ptx::mbar_init(bar(C::kBarVFull + s), 1);
-      ptx::mbar_init(bar(C::kBarVEmpty + s), 1);
+    for (int s = 0; s < C::kSlots; ++s) {
+      ptx::mbar_init(bar(C::kBarFull + s), 1);
+      ptx::mbar_init(bar(C::kBarEmpty + s), 1);
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(bar(C::kBarSFull + t), 1);
@@ -209,96 +204,100 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < C::kChunks; ++c)
           ptx::tma_load_3d(sbase + C::kOffQ + C::kTileBytes + c * C::kChunkBytes, &tm_q,
                            bar(C::kBarQ), c * 64, qt1 * 128, bh);
-      int nk = 0, nv = 0;  // K and V tiles issued so far (V: counting from v_first)
-      const int v_first = p.withhold_v0 ? 1 : 0;
+      const int n_tiles = 2 * nmax;
+      const int skip = p.withhold_v0 ? 1 : -1;  // test hook: tile 1 (V_0) is never loaded
+      int issued = 0;
       bool ok = true;
-      for (int j = 0; j < nmax; ++j) {
-        const int sk = j % C::kSK, uk = j / C::kSK;
-        if (uk > 0 && !w.wait(bar(C::kBarKEmpty + sk), (uk - 1) & 1)) { ok = false; break; }
-        ptx::mbar_arrive_expect_tx(bar(C::kBarKFull + sk), C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          ptx::tma_load_3d(sbase + C::kOffK + sk * C::kTileBytes + c * C::kChunkBytes, &tm_k,
-                           bar(C::kBarKFull + sk), c * 64, j * 128, bh);
-        nk = j + 1;
-        const int sv = j % C::kSV, uv = j / C::kSV;
-        if (uv > 0 && !w.wait(bar(C::kBarVEmpty + sv), (uv - 1) & 1)) { ok = false; break; }
-        if (j >= v_first) {
-          ptx::mbar_arrive_expect_tx(bar(C::kBarVFull + sv), C::kTileBytes);
+      for (int u = 0; u < n_tiles; ++u) {
+        const int slot = u % C::kSlots, use = u / C::kSlots;
+        if (use > 0 && !w.wait(bar(C::kBarEmpty + slot), (use - 1) & 1)) { ok = false; break; }
+        if (u != skip) {
+          ptx::mbar_arrive_expect_tx(bar(C::kBarFull + slot), C::kTileBytes);
+          const CUtensorMap* m = (u & 1) ? &tm_v : &tm_k;
           for (int c = 0; c < C::kChunks; ++c)
-            ptx::tma_load_3d(sbase + C::kOffV + sv * C::kTileBytes + c * C::kChunkBytes, &tm_v,
-                             bar(C::kBarVFull + sv), c * 64, j * 128, bh);
-          nv = j + 1;
+            ptx::tma_load_3d(sbase + C::kOffRing + slot * C::kTileBytes + c * C::kChunkBytes, m,
+                             bar(C::kBarFull + slot), c * 64, (u >> 1) * 128, bh);
         }
+        issued = u + 1;
       }
       if (!ok) {  // let every copy already issued land before the CTA's memory is released
         w.drain(bar(C::kBarQ), 0);
-        for (int s = 0; s < C::kSK; ++s)
-          if (s < nk) {
-            const int jl = s + C::kSK * ((nk - 1 - s) / C::kSK);
-            w.drain(bar(C::kBarKFull + s), (jl / C::kSK) & 1);
-          }
-        for (int s = 0; s < C::kSV; ++s) {
-          int jl = -1;
-          for (int j = v_first; j < nv; ++j)
-            if (j % C::kSV == s) jl = j;
-          if (jl >= 0) w.drain(bar(C::kBarVFull + s), (jl / C::kSV) & 1);
-        }
+        for (int u = issued - C::kSlots > 0 ? issued - C::kSlots : 0; u < issued; ++u)
+          if (u != skip) w.drain(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1);
       }
     }
     __syncwarp();
   } else if (warp == 9) {
     // ================================================================ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 128, false);
-      constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, D, true);
-      bool ok = w.wait(bar(C::kBarQ), 0);
+    // The whole warp runs the loop (waits and descriptor arithmetic stay warp-uniform);
+    // one elected lane issues each MMA and commit.  Descriptors are formed once: a step
+    // along a tile is a constant added to the 16-byte-unit address field.
+    constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 128, false);
+    constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, D, true);
+    constexpr uint64_t kSlotStep = C::kTileBytes >> 4;
+    const uint64_t desc_q0 = ptx::smem_desc_sw128(sbase + C::kOffQ, 16, 1024);
+    const uint64_t desc_q1 = desc_q0 + kSlotStep;
+    const uint64_t desc_k_ring = ptx::smem_desc_sw128(sbase + C::kOffRing, 16, 1024);
+    // V: N-contiguous; next 64 d-columns at +16 KB (LBO), next 8 keys at +1 KB (SBO)
+    const uint64_t desc_v_ring = ptx::smem_desc_sw128(sbase + C::kOffRing, C::kChunkBytes, 1024);
+    bool ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarQ), 0));
+    ptx::tc_fence_after();
+    for (int j = 0; ok && j <= nmax; ++j) {
+      const int uk = 2 * j, uv = 2 * j - 1;  // ring tiles K_j and V_{j-1}
+      if (j < nmax) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + uk % C::kSlots), (uk / C::kSlots) & 1));
+      if (ok && j >= 1) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + uv % C::kSlots), (uv / C::kSlots) & 1));
+      if (!ok) break;
       ptx::tc_fence_after();
-      for (int j = 0; ok && j <= nmax; ++j) {
-        if (j < nmax && !w.wait(bar(C::kBarKFull + j % C::kSK), (j / C::kSK) & 1)) { ok = false; break; }
-        if (j >= 1 && !w.wait(bar(C::kBarVFull + (j - 1) % C::kSV), ((j - 1) / C::kSV) & 1)) {
-          ok = false;
-          break;
-        }
-        ptx::tc_fence_after();
-        for (int t = 0; t < 2; ++t) {
-          const int nt = t ? n1 : n0;
-          if (j >= 1 && j - 1 < nt) {
-            // O_t += P_t V_{j-1}: P from tensor memory, V (N-contiguous) from shared memory
-            if (!w.wait(bar(C::kBarPFull + t), (j - 1) & 1)) { ok = false; break; }
-            ptx::tc_fence_after();
-            const uint32_t vb = sbase + C::kOffV + ((j - 1) % C::kSV) * C::kTileBytes;
-            const uint32_t t_o = tmem + C::kColO + t * D;
-            const uint32_t t_p = tmem + C::kColS + t * 128;
+      const uint64_t dk = desc_k_ring + static_cast<uint64_t>(uk % C::kSlots) * kSlotStep;
+      const uint64_t dv = desc_v_ring + static_cast<uint64_t>((uv + C::kSlots) % C::kSlots) * kSlotStep;
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-              // 16 keys per step: 2 groups of 8 rows (SBO 1024 B); d beyond 64 at +16 KB (LBO)
-              const uint64_t bdesc = ptx::smem_desc_sw128(vb + kk * 2048, C::kChunkBytes, 1024);
-              ptx::mma_ts(t_o, t_p + kk * 8, bdesc, kIdescPV, (j > 1 || kk > 0) ? 1u : 0u);
-            }
+      for (int t = 0; t < 2; ++t) {
+        const int nt = t ? n1 : n0;
+        if (j >= 1 && j - 1 < nt) {
+          // O_t += P_t V_{j-1}: P from tensor memory (8 columns per 16 keys), V from the ring
+          ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarPFull + t), (j - 1) & 1));
+          if (!ok) break;
+          ptx::tc_fence_after();
+          const uint32_t t_o = tmem + C::kColO + t * D;
+          const uint32_t t_p = tmem + C::kColS + t * 128;
+          if (ptx::elect_one()) {
+            if (j > 1) ptx::mma_ts_i<1>(t_o, t_p, dv, kIdescPV);
+            else ptx::mma_ts_i<0>(t_o, t_p, dv, kIdescPV);
+#pragma unroll
+            for (int kk = 1; kk < 8; ++kk) ptx::mma_ts_i<1>(t_o, t_p + kk * 8, dv + kk * 128, kIdescPV);
             if (j - 1 == nt - 1) ptx::tc_commit(bar(C::kBarOFinal + t));
           }
-          if (j < nt) {
-            // S_t = Q_t K_j^T, both K-major (d contiguous), 16 d-columns per step
-            const uint32_t qb = sbase + C::kOffQ + t * C::kTileBytes;
-            const uint32_t kb = sbase + C::kOffK + (j % C::kSK) * C::kTileBytes;
-            const uint32_t t_s = tmem + C::kColS + t * 128;
+          __syncwarp();
+        }
+        if (j < nt) {
+          // S_t = Q_t K_j^T, both K-major: 16 d-columns per step, +32 B inside a 128-byte
+          // swizzle atom, next atom (d >= 64) at +16 KB
+          const uint32_t t_s = tmem + C::kColS + t * 128;
+          const uint64_t dq = t ? desc_q1 : desc_q0;
+          if (ptx::elect_one()) {
+            ptx::mma_ss_i<0>(t_s, dq, dk, kIdescQK);
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off = (kk >> 2) * C::kChunkBytes + (kk & 3) * 32;
-              ptx::mma_ss(t_s, ptx::smem_desc_sw128(qb + off, 16, 1024),
-                          ptx::smem_desc_sw128(kb + off, 16, 1024), kIdescQK, kk > 0 ? 1u : 0u);
+            for (int kk = 1; kk < D / 16; ++kk) {
+              const uint64_t o = (kk >> 2) * (C::kChunkBytes >> 4) + (kk & 3) * 2;
+              ptx::mma_ss_i<1>(t_s, dq + o, dk + o, kIdescQK);
             }
             ptx::tc_commit(bar(C::kBarSFull + t));
           }
+          __syncwarp();
         }
-        if (!ok) break;
-        if (j < nmax) ptx::tc_commit(bar(C::kBarKEmpty + j % C::kSK));
-        if (j >= 1) ptx::tc_commit(bar(C::kBarVEmpty + (j - 1) % C::kSV));
       }
-      // every MMA issued by this thread completes before tensor memory is freed
-      ptx::tc_commit(bar(C::kBarDrain));
-      w.drain(bar(C::kBarDrain), 0);
+      if (!ok) break;
+      // release in ring order: V_{j-1} (tile 2j-1), then K_j (tile 2j)
+      if (ptx::elect_one()) {
+        if (j >= 1) ptx::tc_commit(bar(C::kBarEmpty + uv % C::kSlots));
+        if (j < nmax) ptx::tc_commit(bar(C::kBarEmpty + uk % C::kSlots));
+      }
+      __syncwarp();
     }
+    // every MMA issued by this warp completes before tensor memory is freed
+    if (ptx::elect_one()) ptx::tc_commit(bar(C::kBarDrain));
+    __syncwarp();
+    w.drain(bar(C::kBarDrain), 0);
     __syncwarp();
   } else if (warp < 8) {
     // ================================================================ softmax warpgroups

@@ -66,6 +66,7 @@ struct Cfg {
   // One ring of K/V tiles in the order the MMA warp consumes and releases them:
   // K_0, V_0, K_1, V_1, ...  (tile u is K_{u/2} for even u, V_{u/2} for odd u)
   static constexpr int kSlots = D == 128 ? 5 : 12;
+  static constexpr int kPrefetchAhead = 8;  // ring tiles fetched into L2 ahead of their load
   static constexpr int kOffQ = 0;                  // Q_0, Q_1 (reused for the O staging)
   static constexpr int kOffRing = 2 * kTileBytes;
   static constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
@@ -206,9 +207,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                            bar(C::kBarQ), c * 64, qt1 * 128, bh);
       const int n_tiles = 2 * nmax;
       const int skip = p.withhold_v0 ? 1 : -1;  // test hook: tile 1 (V_0) is never loaded
+      // warm L2 with the first tiles; then each load prefetches the tile kPrefetchAhead later
+      for (int u = 0; u < n_tiles && u < C::kPrefetchAhead; ++u)
+        for (int c = 0; c < C::kChunks; ++c)
+          ptx::tma_prefetch_3d((u & 1) ? &tm_v : &tm_k, c * 64, (u >> 1) * 128, bh);
       int issued = 0;
       bool ok = true;
       for (int u = 0; u < n_tiles; ++u) {
+        const int up = u + C::kPrefetchAhead;
+        if (up < n_tiles)
+          for (int c = 0; c < C::kChunks; ++c)
+            ptx::tma_prefetch_3d((up & 1) ? &tm_v : &tm_k, c * 64, (up >> 1) * 128, bh);
         const int slot = u % C::kSlots, use = u / C::kSlots;
         if (use > 0 && !w.wait(bar(C::kBarEmpty + slot), (use - 1) & 1)) { ok = false; break; }
         if (u != skip) {
@@ -244,10 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     for (int j = 0; ok && j <= nmax; ++j) {
       const int uk = 2 * j, uv = 2 * j - 1;  // ring tiles K_j and V_{j-1}
-      if (j < nmax) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + uk % C::kSlots), (uk / C::kSlots) & 1));
-      if (ok && j >= 1) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + uv % C::kSlots), (uv / C::kSlots) & 1));
+      if (j >= 1) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + uv % C::kSlots), (uv / C::kSlots) & 1));
       if (!ok) break;
-      ptx::tc_fence_after();
+      bool k_ready = false;  // K_j is waited for only right before its first use
       const uint64_t dk = desc_k_ring + static_cast<uint64_t>(uk % C::kSlots) * kSlotStep;
       const uint64_t dv = desc_v_ring + static_cast<uint64_t>((uv + C::kSlots) % C::kSlots) * kSlotStep;
 #pragma unroll
@@ -270,6 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
         if (j < nt) {
+          if (!k_ready) {
+            ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + uk % C::kSlots), (uk / C::kSlots) & 1));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            k_ready = true;
+          }
           // S_t = Q_t K_j^T, both K-major: 16 d-columns per step, +32 B inside a 128-byte
           // swizzle atom, next atom (d >= 64) at +16 KB
           const uint32_t t_s = tmem + C::kColS + t * 128;
@@ -373,11 +387,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         se[i & 3] = __fadd2_rn(se[i & 3], make_float2(e0, e1));
         sp[i & 3] = __fadd2_rn(sp[i & 3], make_float2(__uint_as_float(pk[i] << 16),
                                                       __uint_as_float(pk[i] & 0xffff0000u)));
-        if (i == 31 || i == 63) {
+        if (i == 31 || i == 63) {  // P_t columns [0,32) (keys 0-63), then [32,64)
           uint32_t half[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) half[k] = pk[i - 31 + k];
-          ptx::tmem_st32(t_s + (i - 31), half);  // columns [0,32) then [32,64)
+          ptx::tmem_st32(t_s + (i - 31), half);
         }
       }
       const float2 se01 = __fadd2_rn(se[0], se[1]), se23 = __fadd2_rn(se[2], se[3]);
@@ -385,7 +399,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       l_run = l_run * r_fac + ((se01.x + se01.y) + (se23.x + se23.y));
       lp_run = lp_run * r_fac + ((sp01.x + sp01.y) + (sp23.x + sp23.y));
       m_run = m_ref;
-      // correction O~ *= r (PV of tile j-1 has completed: S_t's commit covers it)
+      // correction O~ *= r, before P_t(j) is handed over: PV_t(j-1) has completed (the commit
+      // behind S_t(j) covers it) and PV_t(j) waits for the arrive below
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {

@@ -12,4 +12,5 @@ from .attention import (  # noqa: F401
     brute_force_attention,
     naive_attention,
     naive_attention_bhnd,
+    split_kv_attention,
 )

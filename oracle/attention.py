@@ -24,7 +24,12 @@ Readings taken where the pages are silent:
   [P1] demo is the special case scale = 1.
 * LSE: natural log, LSE_i = m_i + ln(l_i) = ln sum_j exp(scale * q_i . k_j)
   over the unmasked j.
-* causal: top-left aligned square mask, key j is masked for query i when j > i.
+* causal: key j is masked for query i when its position k_offset + j exceeds the query's
+  position q_offset + i.  With q_offset = k_offset = 0 this is the square, top-left
+  aligned mask (j > i); decoding appends the Nq new queries after the Nk - Nq cached
+  keys, i.e. q_offset = Nk - Nq (bottom-right alignment).
+* a query row that sees no key at all (possible only with offsets) has O = 0 and
+  LSE = -inf: the empty sum.
 * m starts at -inf; the one undefined case, (-inf) - (-inf) when a row has seen
   no unmasked key yet, is guarded explicitly (r = 0, block weights 0).
 
@@ -55,6 +60,16 @@ def _query_positions(n_queries: int, rows) -> np.ndarray:
     return np.asarray(rows, dtype=np.int64)
 
 
+def _finish(acc_or_e_v, l, m):
+    """O = acc / l and LSE = m + ln l, with the empty-row convention (l = 0):
+    O = 0 and LSE = -inf."""
+    empty = ~(l > 0)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        out = np.where(empty[:, None], 0.0, acc_or_e_v / np.where(empty, 1.0, l)[:, None])
+        lse = np.where(empty, -np.inf, m + np.log(np.where(empty, 1.0, l)))
+    return out.astype(acc_or_e_v.dtype), lse.astype(acc_or_e_v.dtype)
+
+
 def _scores(q_rows: np.ndarray, k: np.ndarray, scale: float, causal: bool,
             q_pos: np.ndarray, k_pos: np.ndarray) -> np.ndarray:
     """S = scale * Q K^T for the given query rows and key columns, causal mask
@@ -66,30 +81,33 @@ def _scores(q_rows: np.ndarray, k: np.ndarray, scale: float, causal: bool,
 
 
 def naive_attention(q, k, v, scale: float, causal: bool = False, rows=None,
-                    row_chunk: int = 256, dtype=np.float64):
+                    row_chunk: int = 256, dtype=np.float64, q_offset: int = 0,
+                    k_offset: int = 0):
     """The plain definition, row chunk by row chunk.
 
     [P2] §2 / [P3] §2.1: S = Q K^T, P = softmax(S) by rows, O = P V, with the
     safe softmax of [P3] §3.1 (m = row max, l = sum exp(s - m), P = exp(s-m)/l).
     LSE = m + ln l.  Row chunking is exact: rows are independent.
 
-    Returns (O [len(rows), d], LSE [len(rows)]) in ``dtype``.
+    ``q_offset`` / ``k_offset`` are the sequence positions of q's row 0 and k's row 0
+    for the causal mask.  Returns (O [len(rows), d], LSE [len(rows)]) in ``dtype``.
     """
     q = np.asarray(q, dtype=dtype)
     k = np.asarray(k, dtype=dtype)
     v = np.asarray(v, dtype=dtype)
-    q_pos = _query_positions(q.shape[0], rows)
-    k_pos = np.arange(k.shape[0], dtype=np.int64)
-    out = np.empty((q_pos.shape[0], v.shape[1]), dtype=dtype)
-    lse = np.empty((q_pos.shape[0],), dtype=dtype)
-    for c0 in range(0, q_pos.shape[0], row_chunk):
-        pos = q_pos[c0:c0 + row_chunk]
-        s = _scores(q[pos], k, dtype(scale), causal, pos, k_pos)
+    q_rows = _query_positions(q.shape[0], rows)
+    k_pos = k_offset + np.arange(k.shape[0], dtype=np.int64)
+    out = np.empty((q_rows.shape[0], v.shape[1]), dtype=dtype)
+    lse = np.empty((q_rows.shape[0],), dtype=dtype)
+    for c0 in range(0, q_rows.shape[0], row_chunk):
+        idx = q_rows[c0:c0 + row_chunk]
+        s = _scores(q[idx], k, dtype(scale), causal, q_offset + idx, k_pos)
         m = s.max(axis=1)
-        e = np.exp(s - m[:, None])
+        seen = m > NEG_INF
+        with np.errstate(invalid="ignore"):
+            e = np.where(seen[:, None], np.exp(s - m[:, None]), 0.0).astype(dtype)
         l = e.sum(axis=1)
-        out[c0:c0 + row_chunk] = (e @ v) / l[:, None]
-        lse[c0:c0 + row_chunk] = m + np.log(l)
+        out[c0:c0 + row_chunk], lse[c0:c0 + row_chunk] = _finish(e @ v, l, m)
     return out, lse
 
 
@@ -124,7 +142,8 @@ def _block_bounds(n_keys: int, block_sizes: Sequence[int] | int) -> list:
 
 def blocked_online_attention(q, k, v, scale: float, causal: bool = False,
                              block_sizes: Sequence[int] | int = 128, rows=None,
-                             dtype=np.float64, trace: list | None = None):
+                             dtype=np.float64, trace: list | None = None,
+                             q_offset: int = 0, k_offset: int = 0):
     """Online softmax over K/V blocks, unnormalised accumulator form.
 
     [P1] "在线Softmax算法" and [P3] §3.2: for each block,
@@ -140,13 +159,14 @@ def blocked_online_attention(q, k, v, scale: float, causal: bool = False,
     q = np.asarray(q, dtype=dtype)
     k = np.asarray(k, dtype=dtype)
     v = np.asarray(v, dtype=dtype)
-    q_pos = _query_positions(q.shape[0], rows)
-    qr = q[q_pos]
-    m = np.full(q_pos.shape[0], NEG_INF, dtype=dtype)
-    l = np.zeros(q_pos.shape[0], dtype=dtype)
-    acc = np.zeros((q_pos.shape[0], v.shape[1]), dtype=dtype)
+    q_rows = _query_positions(q.shape[0], rows)
+    q_pos = q_offset + q_rows
+    qr = q[q_rows]
+    m = np.full(q_rows.shape[0], NEG_INF, dtype=dtype)
+    l = np.zeros(q_rows.shape[0], dtype=dtype)
+    acc = np.zeros((q_rows.shape[0], v.shape[1]), dtype=dtype)
     for a, b in _block_bounds(k.shape[0], block_sizes):
-        k_pos = np.arange(a, b, dtype=np.int64)
+        k_pos = k_offset + np.arange(a, b, dtype=np.int64)
         s_ij = _scores(qr, k[a:b], dtype(scale), causal, q_pos, k_pos)
         m_ij = s_ij.max(axis=1)
         m_new = np.maximum(m, m_ij)
@@ -160,9 +180,7 @@ def blocked_online_attention(q, k, v, scale: float, causal: bool = False,
         if trace is not None:
             with np.errstate(invalid="ignore", divide="ignore"):
                 trace.append((m.copy(), l.copy(), acc / l[:, None]))
-    out = acc / l[:, None]
-    lse = m + np.log(l)
-    return out, lse
+    return _finish(acc, l, m)
 
 
 def blocked_normalised_attention(q, k, v, scale: float, causal: bool = False,
@@ -213,7 +231,8 @@ def blocked_normalised_attention(q, k, v, scale: float, causal: bool = False,
     return out, lse
 
 
-def brute_force_attention(q, k, v, scale: float, causal: bool = False):
+def brute_force_attention(q, k, v, scale: float, causal: bool = False, q_offset: int = 0,
+                          k_offset: int = 0):
     """A third, scalar implementation for tiny inputs (N <= 16): explicit loops
     over i, j and the head dimension with math.exp, straight from the
     definition softmax(s)_j = exp(s_j - m) / sum_k exp(s_k - m) ([P3] §3.1)."""
@@ -224,7 +243,10 @@ def brute_force_attention(q, k, v, scale: float, causal: bool = False):
     out = [[0.0] * d_v for _ in range(n_q)]
     lse = [0.0] * n_q
     for i in range(n_q):
-        allowed = [j for j in range(n_k) if not (causal and j > i)]
+        allowed = [j for j in range(n_k) if not (causal and k_offset + j > q_offset + i)]
+        if not allowed:  # empty sum: O = 0, LSE = -inf
+            lse[i] = -math.inf
+            continue
         s = {}
         for j in allowed:
             dot = 0.0
@@ -242,6 +264,32 @@ def brute_force_attention(q, k, v, scale: float, causal: bool = False):
             out[i][c] = num / denom
         lse[i] = m + math.log(denom)
     return np.array(out), np.array(lse)
+
+
+def split_kv_attention(q, k, v, scale: float, causal: bool = False,
+                       split_sizes: Sequence[int] | int = 128, rows=None,
+                       q_offset: int = 0):
+    """Split-KV attention as in FlashDecoding ([P2] §12.1): each split of the keys
+    gives a partial result (O_s, LSE_s) computed on its own (``naive_attention`` on the
+    split, with the split's key positions), and the partials merge exactly:
+        LSE = ln sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s.
+    Splits with no visible key (LSE_s = -inf) contribute nothing.
+    """
+    parts = []
+    for a, b in _block_bounds(np.asarray(k).shape[0], split_sizes):
+        parts.append(naive_attention(q, np.asarray(k)[a:b], np.asarray(v)[a:b], scale, causal,
+                                     rows=rows, q_offset=q_offset, k_offset=a))
+    lse_s = np.stack([p[1] for p in parts])            # [S, rows]
+    o_s = np.stack([p[0] for p in parts])              # [S, rows, d]
+    top = lse_s.max(axis=0)
+    seen = top > NEG_INF
+    with np.errstate(invalid="ignore"):
+        w = np.where(seen[None, :], np.exp(lse_s - np.where(seen, top, 0.0)[None, :]), 0.0)
+    total = w.sum(axis=0)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        out = np.where(seen[:, None], (w[:, :, None] * o_s).sum(axis=0) / np.where(seen, total, 1.0)[:, None], 0.0)
+        lse = np.where(seen, top + np.log(np.where(seen, total, 1.0)), NEG_INF)
+    return out, lse
 
 
 def naive_attention_bhnd(q, k, v, scale: float, causal: bool = False,

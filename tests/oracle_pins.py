@@ -252,6 +252,63 @@ def pin_rows_subset(mod):
         assert np.max(np.abs(o[rows] - o3)) < 1e-12 and np.max(np.abs(l[rows] - l3)) < 1e-12
 
 
+def pin_offsets_and_empty_rows(mod):
+    """Causal masks with sequence offsets against the brute-force loop; rows that
+    see no key give O = 0 and LSE = -inf (the empty sum)."""
+    rng = _rng(11)
+    q, k, v = rng.standard_normal((6, 4)), rng.standard_normal((9, 4)), rng.standard_normal((9, 3))
+    for q_off, k_off in ((3, 0), (0, 2), (-2, 0), (5, 5), (8, 0)):
+        o_b, l_b = mod.brute_force_attention(q, k, v, 0.7, True, q_offset=q_off, k_offset=k_off)
+        for o, l in (mod.naive_attention(q, k, v, 0.7, True, q_offset=q_off, k_offset=k_off, row_chunk=4),
+                     mod.blocked_online_attention(q, k, v, 0.7, True, 4, q_offset=q_off, k_offset=k_off)):
+            assert np.array_equal(np.isinf(l), np.isinf(l_b))
+            fin = np.isfinite(l_b)
+            assert np.max(np.abs(o - o_b)) < 1e-12 and np.max(np.abs(l[fin] - l_b[fin])) < 1e-12
+        empty = [i for i in range(6) if q_off + i < k_off]
+        for i in empty:
+            assert np.all(o_b[i] == 0.0) and l_b[i] == -np.inf
+    # hand check: q_offset = -1 leaves row 0 empty, row 1 sees key 0 only
+    o, l = mod.naive_attention(q[:2], k, v, 1.0, True, q_offset=-1)
+    assert np.all(o[0] == 0.0) and l[0] == -np.inf
+    assert np.allclose(o[1], v[0]) and abs(l[1] - q[1] @ k[0]) < 1e-14
+
+
+def pin_decode_alignment(mod):
+    """Bottom-right causal decode: one new query at position Nk - 1 sees every key
+    (equals non-causal); Nq = Nk with offset 0 is the square mask."""
+    rng = _rng(12)
+    q, k, v = rng.standard_normal((1, 8)), rng.standard_normal((40, 8)), rng.standard_normal((40, 8))
+    o_c, l_c = mod.naive_attention(q, k, v, 0.3, True, q_offset=39)
+    o_n, l_n = mod.naive_attention(q, k, v, 0.3, False)
+    assert np.max(np.abs(o_c - o_n)) < 1e-14 and np.max(np.abs(l_c - l_n)) < 1e-14
+    q4 = rng.standard_normal((4, 8))
+    o4, l4 = mod.naive_attention(q4, k, v, 0.3, True, q_offset=36)   # last 4 positions
+    for i in range(4):
+        oi, li = mod.naive_attention(q4[i:i + 1], k[:37 + i], v[:37 + i], 0.3, False)
+        assert np.max(np.abs(o4[i] - oi[0])) < 1e-13 and abs(l4[i] - li[0]) < 1e-13
+
+
+def pin_split_kv(mod):
+    """FlashDecoding merge ([P2] §12.1): split-KV partials merge to the full
+    result for every split; the §8 worked example as a 2+1 split gives 0.752."""
+    g = json.load(open(GOLDEN, encoding="utf-8"))
+    q = np.array([[1.0]])
+    k = np.array(g["scores"])[:, None]
+    v = np.array(g["v"])[:, None]
+    o, lse = mod.split_kv_attention(q, k, v, 1.0, False, [2, 1])
+    assert abs(o[0, 0] - g["split_2_1"]["block2"]["O"]) < g["tolerance"]["three_decimals"]
+    assert abs(lse[0] - (g["split_2_1"]["block2"]["m"] + math.log(g["split_2_1"]["block2"]["l"]))) < 1e-3
+    rng = _rng(13)
+    q, k, v = rng.standard_normal((5, 8)), rng.standard_normal((70, 8)), rng.standard_normal((70, 6))
+    for causal, q_off in ((False, 0), (True, 65), (True, 30)):
+        o_ref, l_ref = mod.naive_attention(q, k, v, 0.4, causal, q_offset=q_off)
+        for sp in (1, 7, 16, 70, [3, 60, 7], [69, 1]):
+            o, l = mod.split_kv_attention(q, k, v, 0.4, causal, sp, q_offset=q_off)
+            fin = np.isfinite(l_ref)
+            assert np.array_equal(np.isinf(l), np.isinf(l_ref))
+            assert np.max(np.abs(o - o_ref)) < 1e-12 and np.max(np.abs(l[fin] - l_ref[fin])) < 1e-12
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_worked_example_exact,
@@ -266,4 +323,7 @@ ALL_PINS = [
     pin_convex_hull,
     pin_shift_and_permutation,
     pin_rows_subset,
+    pin_offsets_and_empty_rows,
+    pin_decode_alignment,
+    pin_split_kv,
 ]

@@ -18,14 +18,23 @@ MUTANTS = [
     ("K not transposed", "s = scale * (q_rows @ k.T)", "s = scale * (q_rows @ k)", 1),
     ("mask off by one", "k_pos[None, :] > q_pos[:, None]", "k_pos[None, :] >= q_pos[:, None]", 1),
     ("mask transposed", "k_pos[None, :] > q_pos[:, None]", "k_pos[None, :] < q_pos[:, None]", 1),
-    ("no max subtraction", "e = np.exp(s - m[:, None])\n        l = e.sum(axis=1)",
-     "e = np.exp(s)\n        l = e.sum(axis=1)", 1),
-    ("exp sign flipped", "e = np.exp(s - m[:, None])\n        l = e.sum(axis=1)",
-     "e = np.exp(m[:, None] - s)\n        l = e.sum(axis=1)", 1),
-    ("no division by l", "out[c0:c0 + row_chunk] = (e @ v) / l[:, None]",
-     "out[c0:c0 + row_chunk] = (e @ v)", 1),
-    ("LSE without m", "lse[c0:c0 + row_chunk] = m + np.log(l)", "lse[c0:c0 + row_chunk] = np.log(l)", 1),
-    ("LSE in log2", "lse[c0:c0 + row_chunk] = m + np.log(l)", "lse[c0:c0 + row_chunk] = m + np.log2(l)", 1),
+    ("no max subtraction", "np.exp(s - m[:, None]), 0.0).astype(dtype)", "np.exp(s), 0.0).astype(dtype)", 1),
+    ("exp sign flipped", "np.exp(s - m[:, None]), 0.0).astype(dtype)",
+     "np.exp(m[:, None] - s), 0.0).astype(dtype)", 1),
+    ("no division by l", "acc_or_e_v / np.where(empty, 1.0, l)[:, None]", "acc_or_e_v", 1),
+    ("LSE without m", "m + np.log(np.where(empty, 1.0, l))", "np.log(np.where(empty, 1.0, l))", 1),
+    ("LSE in log2", "m + np.log(np.where(empty, 1.0, l))", "m + np.log2(np.where(empty, 1.0, l))", 1),
+    ("empty row gets NaN", "np.where(empty[:, None], 0.0, acc_or_e_v", "np.where(empty[:, None], np.nan, acc_or_e_v", 1),
+    ("query offset ignored", "causal, q_offset + idx, k_pos)", "causal, idx, k_pos)", 1),
+    ("key offset ignored", "k_pos = k_offset + np.arange(k.shape[0], dtype=np.int64)",
+     "k_pos = np.arange(k.shape[0], dtype=np.int64)", 1),
+    ("split merge weight sign", "np.exp(lse_s - np.where(seen, top, 0.0)[None, :])",
+     "np.exp(np.where(seen, top, 0.0)[None, :] - lse_s)", 1),
+    ("split merge ignores LSE_s", "np.exp(lse_s - np.where(seen, top, 0.0)[None, :])",
+     "np.exp(0.0 * lse_s)", 1),
+    ("split LSE drops total", "top + np.log(np.where(seen, total, 1.0))", "top + 0.0 * total", 1),
+    ("split key offsets ignored", "rows=rows, q_offset=q_offset, k_offset=a))",
+     "rows=rows, q_offset=q_offset, k_offset=0))", 1),
     ("P uses V", "return e / e.sum(axis=1)[:, None]", "return e / e.sum(axis=0)[None, :]", 1),
     ("rescale with tile max", "r = np.where(seen, np.exp(m - m_new), 0.0)",
      "r = np.where(seen, np.exp(m_ij - m_new), 0.0)", 1),
@@ -39,7 +48,8 @@ MUTANTS = [
     ("normalised: l~ not rescaled", "l_new = a_old * ell + a_new * l_t", "l_new = a_old * ell + l_t", 1),
     ("brute force: wrong LSE", "lse[i] = m + math.log(denom)", "lse[i] = math.log(denom)", 1),
     ("brute force: scale dropped", "s[j] = scale * dot", "s[j] = dot", 1),
-    ("brute force: causal off by one", "if not (causal and j > i)", "if not (causal and j >= i)", 1),
+    ("brute force: causal off by one", "if not (causal and k_offset + j > q_offset + i)",
+     "if not (causal and k_offset + j >= q_offset + i)", 1),
 ]
 
 

@@ -86,18 +86,38 @@ struct Cfg {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
+// A "group" is the set of query rows that share one K/V head: the G = Hq / Hkv query
+// heads of that K/V head, Nq rows each, contiguous in [B, Hq, Nq, d] (R = G * Nq rows).
+// Plain multi-head attention is G = 1, Nq = Nk.
 struct Params {
-  float* lse;
-  int BH;
-  int N;
-  int n_qtiles;  // ceil(N / 128)
-  int n_cta_q;   // ceil(n_qtiles / 2)
+  float* lse;        // [groups * R] final LSE (n_splits == 1)
+  void* o_bf16;      // [groups * R, D] bf16 final O (n_splits == 1; plain stores for empty tiles)
+  float* o_part;     // [n_splits, groups * R, D] fp32 partial O (n_splits > 1)
+  float* lse_part;   // [n_splits, groups * R] partial LSE (n_splits > 1)
+  int groups;        // B * Hkv
+  int R;             // query rows per group
+  int Nq;            // query rows per head
+  int Nk;            // keys per head
+  int q_offset;      // sequence position of each head's query row 0 (causal): Nk - Nq
+  int n_qtiles;      // ceil(R / 128)
+  int n_cta_q;       // ceil(n_qtiles / 2)
+  int n_kv_tiles;    // ceil(Nk / 128)
+  int n_splits;      // K/V splits (FlashDecoding); 1 = write the final O and LSE
+  int split_tiles;   // K/V tiles per split
   float scale;
   float scale_log2;  // scale * log2(e)
   int causal;
   int withhold_v0;   // test hook: never load V tile 0
   unsigned long long timeout_ns;
 };
+
+// Last key position (+1 in tiles) any row of query tile qt may see, causal case.
+__device__ __forceinline__ int causal_tile_limit(const Params& p, int qt) {
+  const int r0 = qt * 128;
+  const int r1 = min(r0 + 127, p.R - 1);
+  const int max_pos = (r1 / p.Nq != r0 / p.Nq) ? p.q_offset + p.Nq - 1 : p.q_offset + r1 % p.Nq;
+  return max_pos < 0 ? 0 : max_pos / 128 + 1;
+}
 
 // Bounded mbarrier waits.  `wait` gives up when the CTA's abort flag is set or
 // the deadline passes (then it sets the flag and the device status word);
@@ -147,21 +167,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- which (batch*head, query-tile pair) this CTA owns
-  const int bid = blockIdx.x;
-  int bh, cta_q;
-  if (p.causal) {  // longest first: the last query tiles have the most K/V tiles
-    cta_q = p.n_cta_q - 1 - bid / p.BH;
-    bh = bid % p.BH;
-  } else {         // head-major: CTAs of one head run together and share K/V in L2
+  // ---- which (group, query-tile pair, K/V split) this CTA owns
+  int bid = blockIdx.x;
+  int bh, cta_q, split = 0;
+  if (p.n_splits == 1 && p.causal) {  // longest first: the last query tiles have the most K/V tiles
+    cta_q = p.n_cta_q - 1 - bid / p.groups;
+    bh = bid % p.groups;
+  } else {  // group-major: CTAs of one K/V head run together and share K/V in L2
+    split = bid % p.n_splits;
+    bid /= p.n_splits;
     bh = bid / p.n_cta_q;
     cta_q = bid % p.n_cta_q;
   }
   const int qt0 = 2 * cta_q;
   const int qt1 = qt0 + 1;
   const bool has1 = qt1 < p.n_qtiles;
-  const int n0 = p.causal ? qt0 + 1 : p.n_qtiles;  // K/V tiles visited by query tile 0
-  const int n1 = has1 ? (p.causal ? qt1 + 1 : p.n_qtiles) : 0;
+  // K/V tiles [t_lo, t_hi) of this split; causal tiles end at the last visible key
+  const int t_lo = split * p.split_tiles;
+  const int t_hi = min(t_lo + p.split_tiles, p.n_kv_tiles);
+  auto tiles_for = [&](int qt) {
+    const int hi = p.causal ? min(t_hi, causal_tile_limit(p, qt)) : t_hi;
+    return hi > t_lo ? hi - t_lo : 0;
+  };
+  const int n0 = tiles_for(qt0);  // K/V tiles visited by query tile 0
+  const int n1 = has1 ? tiles_for(qt1) : 0;
   const int nmax = n0 > n1 ? n0 : n1;
 
   if (warp == 8 && lane == 0) {
@@ -210,14 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // warm L2 with the first tiles; then each load prefetches the tile kPrefetchAhead later
       for (int u = 0; u < n_tiles && u < C::kPrefetchAhead; ++u)
         for (int c = 0; c < C::kChunks; ++c)
-          ptx::tma_prefetch_3d((u & 1) ? &tm_v : &tm_k, c * 64, (u >> 1) * 128, bh);
+          ptx::tma_prefetch_3d((u & 1) ? &tm_v : &tm_k, c * 64, (t_lo + (u >> 1)) * 128, bh);
       int issued = 0;
       bool ok = true;
       for (int u = 0; u < n_tiles; ++u) {
         const int up = u + C::kPrefetchAhead;
         if (up < n_tiles)
           for (int c = 0; c < C::kChunks; ++c)
-            ptx::tma_prefetch_3d((up & 1) ? &tm_v : &tm_k, c * 64, (up >> 1) * 128, bh);
+            ptx::tma_prefetch_3d((up & 1) ? &tm_v : &tm_k, c * 64, (t_lo + (up >> 1)) * 128, bh);
         const int slot = u % C::kSlots, use = u / C::kSlots;
         if (use > 0 && !w.wait(bar(C::kBarEmpty + slot), (use - 1) & 1)) { ok = false; break; }
         if (u != skip) {
@@ -225,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const CUtensorMap* m = (u & 1) ? &tm_v : &tm_k;
           for (int c = 0; c < C::kChunks; ++c)
             ptx::tma_load_3d(sbase + C::kOffRing + slot * C::kTileBytes + c * C::kChunkBytes, m,
-                             bar(C::kBarFull + slot), c * 64, (u >> 1) * 128, bh);
+                             bar(C::kBarFull + slot), c * 64, (t_lo + (u >> 1)) * 128, bh);
         }
         issued = u + 1;
       }
@@ -321,7 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nt = t ? n1 : n0;
     const int qt = t ? qt1 : qt0;
     const int row = quarter * 32 + lane;
-    const int qrow = qt * 128 + row;
+    const int qrow = qt * 128 + row;              // row within the group
+    const int qpos = p.q_offset + qrow % p.Nq;    // its sequence position (causal mask)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + lane_off + C::kColS + t * 128;
     const uint32_t t_o = tmem + lane_off + C::kColO + t * D;
@@ -342,9 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
       }
       // mask: keys past the end of the sequence, and keys after the query when causal
-      const int col0 = j * 128;
-      int lim = p.N - col0;
-      if (p.causal && qrow - col0 + 1 < lim) lim = qrow - col0 + 1;
+      const int col0 = (t_lo + j) * 128;
+      int lim = p.Nk - col0;
+      if (p.causal && qpos - col0 + 1 < lim) lim = qpos - col0 + 1;
       if (lim < 128) {
 #pragma unroll
         for (int c = 0; c < 128; ++c)
@@ -367,7 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool rescale = (m_new - m_run) * c2 > kRescaleLog2Threshold;
       const float m_ref = rescale ? m_new : m_run;
       const float r_fac = rescale ? ptx::ex2_approx((m_run - m_new) * c2) : 1.f;
-      const float neg = -m_ref * c2;
+      // a row that has seen no unmasked key yet keeps m = -inf: its terms are all 0
+      const float neg = m_ref == -INFINITY ? 0.f : -m_ref * c2;
       // P = 2^(s*c2 - m_ref*c2), rounded to bf16 pairs for the P V product and written over
       // the first 64 columns of S_t (first half while the second is computed).  Two running
       // sums: l_run over the fp32 values (for LSE) and lp_run over the rounded values the
@@ -416,12 +447,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(C::kBarPFull + t));
     }
-    // ---- epilogue: O = O~ / l -> bf16 -> shared (Q_t's buffer) -> TMA store; LSE
+    // ---- epilogue: O = O~ / l, LSE = m*scale + ln l; a row that saw no key gets O = 0 and
+    // LSE = -inf.  One split: O -> bf16 -> shared (Q_t's buffer) -> TMA store.  Several
+    // splits: fp32 partial O and partial LSE straight to the workspace for the combine.
+    const bool tile_exists = t == 0 || has1;
+    const size_t grow = static_cast<size_t>(bh) * p.R + qrow;  // row in [B*Hq*Nq]
+    const bool row_valid = qrow < p.R;
     const uint32_t so = sbase + C::kOffQ + t * C::kTileBytes;
     if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarOFinal + t), 0));
-    if (ok) {
+    const bool have = l_run > 0.f;
+    const float inv_l = have ? 1.f / lp_run : 0.f;
+    const float lse_row = have ? m_run * p.scale + logf(l_run) : -INFINITY;
+    if (ok && p.n_splits == 1) {
       ptx::tc_fence_after();
-      const float inv_l = 1.f / lp_run;
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t r[32];
@@ -438,11 +476,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                             pk[4 * g + 2], pk[4 * g + 3]);
         }
       }
-      if (qrow < p.N) p.lse[static_cast<size_t>(bh) * p.N + qrow] = m_run * p.scale + logf(l_run);
+      if (row_valid) p.lse[grow] = lse_row;
       ptx::fence_proxy_async_smem();
+    } else if (ok && p.n_splits > 1) {
+      ptx::tc_fence_after();
+      float4* dst = reinterpret_cast<float4*>(p.o_part + (static_cast<size_t>(split) * p.groups * p.R + grow) * D);
+#pragma unroll 1
+      for (int cc = 0; cc < D / 32; ++cc) {
+        uint32_t r[32];
+        ptx::tmem_ld32(t_o + cc * 32, r);
+        if (row_valid) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i)
+            dst[cc * 8 + i] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
+                                          __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
+        }
+      }
+      if (row_valid) p.lse_part[static_cast<size_t>(split) * p.groups * p.R + grow] = lse_row;
+    } else if (tile_exists && nt == 0 && row_valid) {
+      // no K/V tile of this split is visible to the tile: the empty result
+      if (p.n_splits == 1) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.o_bf16) + grow * D * 2);
+        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+        p.lse[grow] = -INFINITY;
+      } else {
+        float4* dst = reinterpret_cast<float4*>(p.o_part + (static_cast<size_t>(split) * p.groups * p.R + grow) * D);
+        for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p.lse_part[static_cast<size_t>(split) * p.groups * p.R + grow] = -INFINITY;
+      }
     }
     ptx::named_barrier(1 + t, 128);
-    if (ok && row == 0) {
+    if (ok && p.n_splits == 1 && row == 0) {
       for (int c = 0; c < C::kChunks; ++c) ptx::tma_store_3d(&tm_o, so + c * C::kChunkBytes, c * 64, qt * 128, bh);
       ptx::bulk_commit();
       ptx::bulk_wait_all();
@@ -455,6 +519,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, C::kTmemCols);
   }
+}
+
+// ==================================================================== split-K/V combine
+// FlashDecoding's merge of K/V-split partials (one warp per query row):
+//   LSE = ln sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s,
+// splits that saw no key (LSE_s = -inf) weigh 0; a row with none at all gets O = 0,
+// LSE = -inf.
+template <int D>
+__global__ void __launch_bounds__(256)
+    fa_combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
+                      uint16_t* __restrict__ o, float* __restrict__ lse, int rows, int n_splits) {
+  constexpr int E = D / 32;  // elements per lane
+  const int row = static_cast<int>((static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float m = -INFINITY;
+  for (int s = 0; s < n_splits; ++s) m = fmaxf(m, lse_part[static_cast<size_t>(s) * rows + row]);
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+  float tot = 0.f;
+  if (m != -INFINITY) {
+    for (int s = 0; s < n_splits; ++s) {
+      const float w = expf(lse_part[static_cast<size_t>(s) * rows + row] - m);
+      tot += w;
+      const float* src = o_part + (static_cast<size_t>(s) * rows + row) * D + lane * E;
+      if constexpr (E == 4) {
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        acc[0] += w * x.x;
+        acc[1] += w * x.y;
+        acc[2] += w * x.z;
+        acc[3] += w * x.w;
+      } else {
+        const float2 x = *reinterpret_cast<const float2*>(src);
+        acc[0] += w * x.x;
+        acc[1] += w * x.y;
+      }
+    }
+  }
+  const float inv = tot > 0.f ? 1.f / tot : 0.f;
+  uint32_t packed[E / 2];
+#pragma unroll
+  for (int e = 0; e < E / 2; ++e) packed[e] = ptx::pack_bf16x2(acc[2 * e] * inv, acc[2 * e + 1] * inv);
+  uint16_t* dst = o + static_cast<size_t>(row) * D + lane * E;
+  if constexpr (E == 4)
+    *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+  else
+    *reinterpret_cast<uint32_t*>(dst) = packed[0];
+  if (lane == 0) lse[row] = tot > 0.f ? m + logf(tot) : -INFINITY;
 }
 
 // ==================================================================== host side
@@ -479,13 +592,13 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [B*H, N, d] bf16 viewed as 3-D; box = 64 columns (128 bytes) x 128 rows x 1 head.
-bool encode_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
+// [heads, rows, d] bf16 viewed as 3-D; box = 64 columns (128 bytes) x 128 rows x 1 head.
+bool encode_map(CUtensorMap* m, const void* base, int heads, int rows, int d) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                              static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(N) * d * 2};
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(heads)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
   const cuuint32_t box[3] = {64, 128, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
@@ -494,6 +607,7 @@ bool encode_map(CUtensorMap* m, const void* base, int BH, int N, int d) {
 }
 
 constexpr int kMaxDevices = 64;
+constexpr int kMaxSplits = 1024;
 std::mutex g_dev_mutex;
 int g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, -1 wrong arch
 
@@ -531,60 +645,118 @@ bool is_device_pointer(const void* ptr) {
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-  return x < y + nb && y < x + na;
+  return na > 0 && nb > 0 && x < y + nb && y < x + na;
 }
 
-int validate(const void* q, const void* k, const void* v, const void* o, const float* lse, int B,
-             int H, int N, int d, float scale) {
-  if (!q || !k || !v || !o || !lse) return FA_ERR_ARG;
-  if (B < 1 || H < 1 || N < 1 || (d != 64 && d != 128)) return FA_ERR_ARG;
-  if (!(scale > 0.f) || !std::isfinite(scale)) return FA_ERR_ARG;
-  const long long rows = static_cast<long long>(B) * H * N;
-  if (rows > 2147483647LL) return FA_ERR_ARG;
-  for (const void* ptr : {q, k, v, o, static_cast<const void*>(lse)})
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+  int B, Hq, Hkv, Nq, Nk, d;
+  float scale;
+  int causal;
+  int n_splits;
+  void* workspace;
+  size_t workspace_bytes;
+};
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// bytes of workspace for n_splits > 1: fp32 partial O, then partial LSE
+size_t workspace_needed(long long rows, int d, int n_splits) {
+  if (n_splits <= 1) return 0;
+  return align256(static_cast<size_t>(n_splits) * rows * d * 4) + align256(static_cast<size_t>(n_splits) * rows * 4);
+}
+
+int validate(const Problem& pr) {
+  if (!pr.q || !pr.k || !pr.v || !pr.o || !pr.lse) return FA_ERR_ARG;
+  if (pr.B < 1 || pr.Hq < 1 || pr.Hkv < 1 || pr.Nq < 1 || pr.Nk < 1 || (pr.d != 64 && pr.d != 128))
+    return FA_ERR_ARG;
+  if (pr.Hq % pr.Hkv != 0) return FA_ERR_ARG;
+  if (!(pr.scale > 0.f) || !std::isfinite(pr.scale)) return FA_ERR_ARG;
+  if (pr.n_splits < 1 || pr.n_splits > kMaxSplits) return FA_ERR_ARG;
+  const long long q_rows = static_cast<long long>(pr.B) * pr.Hq * pr.Nq;
+  const long long kv_rows = static_cast<long long>(pr.B) * pr.Hkv * pr.Nk;
+  if (q_rows > 2147483647LL || kv_rows > 2147483647LL) return FA_ERR_ARG;
+  const size_t ws = workspace_needed(q_rows, pr.d, pr.n_splits);
+  if (ws > 0 && (!pr.workspace || pr.workspace_bytes < ws || (reinterpret_cast<uintptr_t>(pr.workspace) & 255u)))
+    return FA_ERR_ARG;
+  for (const void* ptr : {pr.q, pr.k, pr.v, static_cast<const void*>(pr.o), static_cast<const void*>(pr.lse)})
     if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_ARG;
-  const size_t tb = static_cast<size_t>(rows) * d * 2, lb = static_cast<size_t>(rows) * 4;
-  for (const void* in : {q, k, v})
-    if (overlaps(o, tb, in, tb) || overlaps(lse, lb, in, tb)) return FA_ERR_ARG;
-  if (overlaps(o, tb, lse, lb)) return FA_ERR_ARG;
-  for (const void* ptr : {q, k, v, o, static_cast<const void*>(lse)})
+  const size_t qb = static_cast<size_t>(q_rows) * pr.d * 2, kb = static_cast<size_t>(kv_rows) * pr.d * 2;
+  const size_t lb = static_cast<size_t>(q_rows) * 4;
+  const struct { const void* p; size_t n; } in[3] = {{pr.q, qb}, {pr.k, kb}, {pr.v, kb}};
+  for (const auto& x : in) {
+    if (overlaps(pr.o, qb, x.p, x.n) || overlaps(pr.lse, lb, x.p, x.n)) return FA_ERR_ARG;
+    if (ws > 0 && overlaps(pr.workspace, ws, x.p, x.n)) return FA_ERR_ARG;
+  }
+  if (overlaps(pr.o, qb, pr.lse, lb)) return FA_ERR_ARG;
+  if (ws > 0 && (overlaps(pr.workspace, ws, pr.o, qb) || overlaps(pr.workspace, ws, pr.lse, lb))) return FA_ERR_ARG;
+  for (const void* ptr : {pr.q, pr.k, pr.v, static_cast<const void*>(pr.o), static_cast<const void*>(pr.lse)})
     if (!is_device_pointer(ptr)) return FA_ERR_ARG;
+  if (ws > 0 && !is_device_pointer(pr.workspace)) return FA_ERR_ARG;
   return FA_OK;
 }
 
 template <int D>
-int launch(const void* q, const void* k, const void* v, void* o, float* lse, int BH, int N, float scale,
-           int causal, int withhold_v0, unsigned long long timeout_ns, cudaStream_t stream) {
+int launch(const Problem& pr, int withhold_v0, unsigned long long timeout_ns, cudaStream_t stream) {
+  const int G = pr.Hq / pr.Hkv;
+  const int groups = pr.B * pr.Hkv;
+  const int R = G * pr.Nq;  // query rows per K/V head (contiguous in [B, Hq, Nq, d])
   CUtensorMap mq, mk, mv, mo;
-  if (!encode_map(&mq, q, BH, N, D) || !encode_map(&mk, k, BH, N, D) || !encode_map(&mv, v, BH, N, D) ||
-      !encode_map(&mo, o, BH, N, D))
+  if (!encode_map(&mq, pr.q, groups, R, D) || !encode_map(&mk, pr.k, groups, pr.Nk, D) ||
+      !encode_map(&mv, pr.v, groups, pr.Nk, D) || !encode_map(&mo, pr.o, groups, R, D))
     return FA_ERR_LAUNCH;
   Params p{};
-  p.lse = lse;
-  p.BH = BH;
-  p.N = N;
-  p.n_qtiles = (N + 127) / 128;
+  p.lse = pr.lse;
+  p.o_bf16 = pr.o;
+  p.groups = groups;
+  p.R = R;
+  p.Nq = pr.Nq;
+  p.Nk = pr.Nk;
+  p.q_offset = pr.Nk - pr.Nq;  // bottom-right causal alignment (square: 0)
+  p.n_qtiles = (R + 127) / 128;
   p.n_cta_q = (p.n_qtiles + 1) / 2;
-  p.scale = scale;
-  p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  p.causal = causal ? 1 : 0;
+  p.n_kv_tiles = (pr.Nk + 127) / 128;
+  p.n_splits = pr.n_splits;
+  p.split_tiles = (p.n_kv_tiles + pr.n_splits - 1) / pr.n_splits;
+  const long long rows = static_cast<long long>(groups) * R;
+  if (pr.n_splits > 1) {
+    uint8_t* ws = static_cast<uint8_t*>(pr.workspace);
+    p.o_part = reinterpret_cast<float*>(ws);
+    p.lse_part = reinterpret_cast<float*>(ws + align256(static_cast<size_t>(pr.n_splits) * rows * D * 4));
+  }
+  p.scale = pr.scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(pr.scale) * 1.4426950408889634);
+  p.causal = pr.causal ? 1 : 0;
   p.withhold_v0 = withhold_v0;
   p.timeout_ns = timeout_ns;
-  const long long grid = static_cast<long long>(BH) * p.n_cta_q;
+  const long long grid = static_cast<long long>(groups) * p.n_cta_q * pr.n_splits;
   if (grid > 2147483647LL) return FA_ERR_ARG;
   fa_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(mq, mk, mv, mo, p);
-  return cudaGetLastError() == cudaSuccess ? FA_OK : FA_ERR_LAUNCH;
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  if (pr.n_splits > 1) {
+    const long long blocks = (rows * 32 + 255) / 256;
+    fa_combine_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        p.o_part, p.lse_part, static_cast<uint16_t*>(pr.o), pr.lse, static_cast<int>(rows), pr.n_splits);
+    if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  }
+  return FA_OK;
 }
 
-int forward(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
-            float scale, int causal, int withhold_v0, unsigned long long timeout_ns, cudaStream_t stream) {
-  int rc = validate(q, k, v, o, lse, B, H, N, d, scale);
+int run(const Problem& pr, int withhold_v0, unsigned long long timeout_ns, cudaStream_t stream) {
+  int rc = validate(pr);
   if (rc != FA_OK) return rc;
   rc = prepare_device();
   if (rc != FA_OK) return rc;
-  const int BH = B * H;
-  return d == 64 ? launch<64>(q, k, v, o, lse, BH, N, scale, causal, withhold_v0, timeout_ns, stream)
-                 : launch<128>(q, k, v, o, lse, BH, N, scale, causal, withhold_v0, timeout_ns, stream);
+  return pr.d == 64 ? launch<64>(pr, withhold_v0, timeout_ns, stream) : launch<128>(pr, withhold_v0, timeout_ns, stream);
+}
+
+Problem mha(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
+            float scale, int causal) {
+  return Problem{q, k, v, o, lse, B, H, H, N, N, d, scale, causal, 1, nullptr, 0};
 }
 
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
@@ -596,15 +768,27 @@ extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            float scale, int causal, cudaStream_t stream) {
-  return fa::forward(q, k, v, o, lse, B, H, N, d, scale, causal, 0, fa::kDefaultTimeoutNs, stream);
+  return fa::run(fa::mha(q, k, v, o, lse, B, H, N, d, scale, causal), 0, fa::kDefaultTimeoutNs, stream);
+}
+
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
+               int Nq, int Nk, int d, float scale, int causal, int n_splits, void* workspace,
+               size_t workspace_bytes, cudaStream_t stream) {
+  const fa::Problem pr{q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, n_splits, workspace, workspace_bytes};
+  return fa::run(pr, 0, fa::kDefaultTimeoutNs, stream);
+}
+
+size_t fa_fwd_gqa_workspace_bytes(int B, int Hq, int Nq, int d, int n_splits) {
+  if (B < 1 || Hq < 1 || Nq < 1 || (d != 64 && d != 128) || n_splits < 1 || n_splits > fa::kMaxSplits) return 0;
+  return fa::workspace_needed(static_cast<long long>(B) * Hq * Nq, d, n_splits);
 }
 
 int fa_fwd_withheld_tile(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                          int N, int d, float scale, int causal, double wait_timeout_ms,
                          cudaStream_t stream) {
   if (!(wait_timeout_ms >= 1.0 && wait_timeout_ms <= 10000.0)) return FA_ERR_ARG;
-  return fa::forward(q, k, v, o, lse, B, H, N, d, scale, causal, 1,
-                     static_cast<unsigned long long>(wait_timeout_ms * 1e6), stream);
+  return fa::run(fa::mha(q, k, v, o, lse, B, H, N, d, scale, causal), 1,
+                 static_cast<unsigned long long>(wait_timeout_ms * 1e6), stream);
 }
 
 int fa_status(int clear, cudaStream_t stream) {
@@ -621,7 +805,7 @@ int fa_status(int clear, cudaStream_t stream) {
 const char* fa_strerror(int code) {
   switch (code) {
     case FA_OK: return "success";
-    case FA_ERR_ARG: return "invalid argument (pointer, alignment, size, d or scale)";
+    case FA_ERR_ARG: return "invalid argument (pointer, alignment, size, d, scale, heads or workspace)";
     case FA_ERR_ARCH: return "device is not compute capability 10.3 (GB300)";
     case FA_ERR_LAUNCH: return "kernel launch or TMA descriptor encoding failed";
     case FA_ERR_TIMEOUT: return "a device-side barrier wait timed out";
@@ -630,6 +814,6 @@ const char* fa_strerror(int code) {
   }
 }
 
-int fa_version(void) { return 1; }
+int fa_version(void) { return 2; }
 
 }  // extern "C"

@@ -23,7 +23,8 @@ FA_ERR_TIMEOUT = -4
 FA_ERR_CUDA = -5
 FA_STATUS_TIMEOUT = 0x1
 
-EXPORTED = ("fa_fwd", "fa_status", "fa_fwd_withheld_tile", "fa_strerror", "fa_version")
+EXPORTED = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_gqa_workspace_bytes", "fa_status",
+            "fa_fwd_withheld_tile", "fa_strerror", "fa_version")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
@@ -32,6 +33,11 @@ lib = ctypes.CDLL(LIB_PATH)
 _vp, _i, _f, _d = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double
 lib.fa_fwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]
 lib.fa_fwd.restype = _i
+lib.fa_fwd_gqa.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp,
+                           ctypes.c_size_t, _vp]
+lib.fa_fwd_gqa.restype = _i
+lib.fa_fwd_gqa_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
+lib.fa_fwd_gqa_workspace_bytes.restype = ctypes.c_size_t
 lib.fa_fwd_withheld_tile.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _d, _vp]
 lib.fa_fwd_withheld_tile.restype = _i
 lib.fa_status.argtypes = [_i, _vp]
@@ -77,6 +83,39 @@ def fa_fwd(q, k, v, o=None, lse=None, scale=None, causal=False, stream=None):
         scale = 1.0 / (d ** 0.5)
     rc = lib.fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                     B, H, N, d, float(scale), int(bool(causal)), _stream_handle(stream, q.device))
+    if rc != FA_OK:
+        raise FAError(rc)
+    return o, lse
+
+
+def fa_fwd_gqa_workspace_bytes(B, Hq, Nq, d, n_splits) -> int:
+    return int(lib.fa_fwd_gqa_workspace_bytes(B, Hq, Nq, d, n_splits))
+
+
+def fa_fwd_gqa(q, k, v, o=None, lse=None, scale=None, causal=False, n_splits=1,
+               workspace=None, stream=None):
+    """Grouped-K/V, split-K/V forward.  q: [B, Hq, Nq, d]; k, v: [B, Hkv, Nk, d]
+    (CUDA bf16, contiguous).  Returns (o, lse).  ``workspace`` (a CUDA tensor of at
+    least fa_fwd_gqa_workspace_bytes bytes, 256-byte aligned) is allocated here when
+    omitted and n_splits > 1."""
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape:
+        raise ValueError("q must be [B, Hq, Nq, d] and k, v [B, Hkv, Nk, d]")
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    ws_bytes = fa_fwd_gqa_workspace_bytes(B, Hq, Nq, d, n_splits)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=q.device)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib.fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                        B, Hq, Hkv, Nq, Nk, d, float(scale), int(bool(causal)), int(n_splits),
+                        ws_ptr, ws_len, _stream_handle(stream, q.device))
     if rc != FA_OK:
         raise FAError(rc)
     return o, lse

@@ -18,6 +18,8 @@ import torch
 
 @dataclass(frozen=True)
 class Workload:
+    """B batches; H query heads of N rows each; Hkv key/value heads of Nk rows each
+    (defaults: Hkv = H, Nk = N); d the head dimension; n_splits key ranges."""
     name: str
     B: int
     H: int
@@ -27,19 +29,34 @@ class Workload:
     qk_std: float = 1.0
     v_std: float = 1.0
     seed: int = 0
+    Hkv: int | None = None
+    Nk: int | None = None
+    n_splits: int = 1
+    bound: str = "tensor"   # the roofline that bounds it: "tensor" or "hbm"
+
+    @property
+    def hkv(self) -> int:
+        return self.H if self.Hkv is None else self.Hkv
+
+    @property
+    def nk(self) -> int:
+        return self.N if self.Nk is None else self.Nk
 
     @property
     def scale(self) -> float:
         return 1.0 / (self.d ** 0.5)
 
     def flops(self) -> float:
-        """4*B*H*N^2*d multiply-adds counted as 2 flops each, halved when causal."""
-        f = 4.0 * self.B * self.H * self.N * self.N * self.d
-        return f / 2.0 if self.causal else f
+        """4*B*H*Nq*Nk*d (two multiply-adds per query-key pair per dimension); the
+        square causal case counts half."""
+        f = 4.0 * self.B * self.H * self.N * self.nk * self.d
+        return f / 2.0 if (self.causal and self.N == self.nk) else f
 
     def algorithmic_bytes(self) -> int:
         """Q, K, V read once and O written once (bf16), LSE written once (fp32)."""
-        return 4 * self.B * self.H * self.N * self.d * 2 + self.B * self.H * self.N * 4
+        q_o = 2 * self.B * self.H * self.N * self.d * 2
+        kv = 2 * self.B * self.hkv * self.nk * self.d * 2
+        return q_o + kv + self.B * self.H * self.N * 4
 
 
 WORKLOADS = {
@@ -50,6 +67,12 @@ WORKLOADS = {
         Workload("causal_n8192_d128", 2, 16, 8192, 128, True, seed=20263),
         Workload("wide_scores_n1024_d128", 8, 32, 1024, 128, False, qk_std=3.0, seed=20264),
         Workload("causal_n32768_d128", 1, 32, 32768, 128, True, seed=20265),
+        # grouped K/V heads (8 query heads per K/V head), causal prefill
+        Workload("gqa_causal_n8192_d128", 1, 32, 8192, 128, True, seed=20266, Hkv=4),
+        # decoding: one new query per head against a 32K-key cache, 4 query heads
+        # per K/V head, the keys split 16 ways (memory-bound: reads K and V once)
+        Workload("gqa_decode_nk32768_d128", 8, 32, 1, 128, False, seed=20267, Hkv=8,
+                 Nk=32768, n_splits=16, bound="hbm"),
     )
 }
 
@@ -67,8 +90,20 @@ def make_qkv(B: int, H: int, N: int, d: int, seed: int, qk_std: float = 1.0,
     return q, k, v
 
 
+def make_qkv_gqa(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int, seed: int,
+                 qk_std: float = 1.0, v_std: float = 1.0):
+    """q [B, Hq, Nq, d], k and v [B, Hkv, Nk, d]: CPU bf16, drawn in that order."""
+    g = torch.Generator().manual_seed(int(seed))
+    q = (torch.randn((B, Hq, Nq, d), generator=g, dtype=torch.float32) * qk_std).to(torch.bfloat16)
+    k = (torch.randn((B, Hkv, Nk, d), generator=g, dtype=torch.float32) * qk_std).to(torch.bfloat16)
+    v = (torch.randn((B, Hkv, Nk, d), generator=g, dtype=torch.float32) * v_std).to(torch.bfloat16)
+    return q, k, v
+
+
 def make_workload(w: Workload):
-    return make_qkv(w.B, w.H, w.N, w.d, w.seed, w.qk_std, w.v_std)
+    if w.Hkv is None and w.Nk is None:
+        return make_qkv(w.B, w.H, w.N, w.d, w.seed, w.qk_std, w.v_std)
+    return make_qkv_gqa(w.B, w.H, w.hkv, w.N, w.nk, w.d, w.seed, w.qk_std, w.v_std)
 
 
 def sample_slices(B: int, H: int, count: int, seed: int):

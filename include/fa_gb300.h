@@ -28,6 +28,7 @@
 #ifndef FA_GB300_H
 #define FA_GB300_H
 
+#include <stddef.h>
 #include <cuda_runtime_api.h>
 
 #ifdef __cplusplus
@@ -74,6 +75,46 @@ int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
            int B, int H, int N, int d, float scale, int causal, cudaStream_t stream);
 
 /*
+ * fa_fwd_gqa -- exact attention forward with grouped K/V heads, different query and
+ * key lengths, and split-K/V (FlashDecoding) parallelism.
+ *
+ * Grouped-query attention (GQA; MQA when Hkv = 1) lets G = Hq / Hkv query heads share
+ * one K/V head, so fewer K/V bytes are read (the aiqz.cc article, section 性能调优经验,
+ * on MQA/GQA).  Query head h uses K/V head h / G.  Split-K/V is the FlashDecoding
+ * scheme of the notes page, §12.1: the keys are cut into n_splits ranges computed in
+ * parallel, each giving a partial (O_s, LSE_s), merged exactly by
+ *     LSE = ln sum_s exp(LSE_s),   O = sum_s exp(LSE_s - LSE) O_s.
+ *
+ * q       : device bf16 [B, Hq, Nq, d], contiguous.      Read only, 16-byte aligned.
+ * k, v    : device bf16 [B, Hkv, Nk, d], contiguous.     Read only, 16-byte aligned.
+ * o       : device bf16 [B, Hq, Nq, d].                  Written.
+ * lse     : device fp32 [B, Hq, Nq].                     Written.
+ * B, Hq, Hkv, Nq, Nk >= 1; Hq a multiple of Hkv; B*Hq*Nq and B*Hkv*Nk <= 2^31 - 1.
+ * d       : 64 or 128.   scale > 0 and finite.
+ * causal  : nonzero masks keys after each query's position, with the queries aligned
+ *           to the END of the keys (query i sits at position Nk - Nq + i): decoding
+ *           appends Nq new queries after Nk - Nq cached keys.  Nq = Nk is the square
+ *           mask of fa_fwd.  A query that sees no key (only if Nq > Nk) gets O = 0 and
+ *           LSE = -inf.
+ * n_splits: 1..1024 key ranges.  1 writes O and LSE directly; more write fp32
+ *           partials into the workspace and a second kernel merges them.
+ * workspace, workspace_bytes: device scratch for n_splits > 1, 256-byte aligned, at
+ *           least fa_fwd_gqa_workspace_bytes(B, Hq, Nq, d, n_splits) bytes, not
+ *           overlapping any other argument; ignored (may be NULL) for n_splits = 1.
+ *           Its contents on entry do not matter; it is clobbered.
+ * stream  : CUDA stream; one or two kernels are enqueued, nothing is synchronised.
+ *
+ * Ownership, validation and errors as for fa_fwd.  fa_fwd(q,k,v,o,lse,B,H,N,...) is
+ * fa_fwd_gqa with Hq = Hkv = H, Nq = Nk = N, n_splits = 1.
+ */
+int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
+               int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+               int n_splits, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Workspace bytes fa_fwd_gqa needs for these sizes (0 for n_splits = 1 or bad sizes). */
+size_t fa_fwd_gqa_workspace_bytes(int B, int Hq, int Nq, int d, int n_splits);
+
+/*
  * fa_status -- read the device status word of the current device.
  *
  * Synchronises `stream` first, then copies the word to the host.  If `clear`
@@ -100,7 +141,7 @@ int fa_fwd_withheld_tile(const void* q, const void* k, const void* v, void* o, f
 /* fa_strerror -- a static, human-readable string for a return code. */
 const char* fa_strerror(int code);
 
-/* fa_version -- the library's interface version (currently 1). */
+/* fa_version -- the library's interface version (currently 2). */
 int fa_version(void);
 
 #ifdef __cplusplus

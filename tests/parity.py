@@ -25,19 +25,23 @@ def bf16_half_ulp(x: np.ndarray) -> np.ndarray:
 
 
 def compare(o_gpu, lse_gpu, o_ref, lse_ref) -> dict:
+    """Error statistics of one result against the oracle.  Rows the oracle marks
+    empty (LSE = -inf, O = 0) must be empty on the GPU too."""
     o_gpu = np.asarray(o_gpu, dtype=np.float64)
     o_ref = np.asarray(o_ref, dtype=np.float64)
     lse_gpu = np.asarray(lse_gpu, dtype=np.float64)
     lse_ref = np.asarray(lse_ref, dtype=np.float64)
     d_o = np.abs(o_gpu - o_ref)
     excess = np.maximum(d_o - bf16_half_ulp(o_ref), 0.0)
-    d_l = np.abs(lse_gpu - lse_ref) / np.maximum(1.0, np.abs(lse_ref))
+    fin = np.isfinite(lse_ref)
+    same_empty = bool(np.array_equal(np.isneginf(lse_gpu), np.isneginf(lse_ref)))
+    d_l = np.abs(lse_gpu[fin] - lse_ref[fin]) / np.maximum(1.0, np.abs(lse_ref[fin]))
     return {
         "max_abs_o": float(d_o.max()) if d_o.size else 0.0,
         "max_abs_o_beyond_output_rounding": float(excess.max()) if excess.size else 0.0,
         "mean_abs_o": float(d_o.mean()) if d_o.size else 0.0,
         "max_rel_lse": float(d_l.max()) if d_l.size else 0.0,
-        "finite": bool(np.all(np.isfinite(o_gpu)) and np.all(np.isfinite(lse_gpu))),
+        "finite": bool(np.all(np.isfinite(o_gpu)) and np.all(np.isfinite(lse_gpu[fin]))) and same_empty,
         "count": int(d_o.size),
     }
 

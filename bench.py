@@ -81,9 +81,38 @@ def job_tflops(flops_per_rank: float, ms: float, world: int) -> float:
     return world * flops_per_rank / (ms * 1e-3) / 1e12
 
 
+def job_rate(units_per_rank: float, ms: float, world: int) -> float:
+    """Whole-job rate in units per second (units: TFLOP or GB per step)."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def workload_config(w, l2_note):
-    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
-            "qk_std": w.qk_std, "v_std": w.v_std, "seed": w.seed, "l2": l2_note}
+    cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
+           "qk_std": w.qk_std, "v_std": w.v_std, "seed": w.seed, "l2": l2_note}
+    if w.Hkv is not None or w.Nk is not None:
+        cfg.update({"Hkv": w.hkv, "Nk": w.nk, "n_splits": w.n_splits})
+    return cfg
+
+
+def metric_for(w):
+    """The headline metric for tensor-bound workloads; HBM bytes per second for the
+    memory-bound decoding workload (K and V are read once)."""
+    if w.bound == "hbm":
+        return f"decode attention GB/s of algorithmic HBM traffic ({w.name})", "GB/s"
+    return METRIC if w.name == HEADLINE else f"fwd attention TFLOP/s ({w.name})", UNIT
+
+
+def units_per_step(w):
+    return w.algorithmic_bytes() / 1e9 if w.bound == "hbm" else w.flops() / 1e12
+
+
+def forward_call(fa, w):
+    """The public-API call that does one step of the workload."""
+    if w.Hkv is None and w.Nk is None:
+        return lambda q, k, v, o, lse, ws, stream: fa.fa_fwd(q, k, v, o, lse, scale=w.scale, causal=w.causal,
+                                                             stream=stream)
+    return lambda q, k, v, o, lse, ws, stream: fa.fa_fwd_gqa(q, k, v, o, lse, scale=w.scale, causal=w.causal,
+                                                             n_splits=w.n_splits, workspace=ws, stream=stream)
 
 
 class ClockSampler:
@@ -168,63 +197,73 @@ def cpu_baseline(w, budget_s=12.0, max_slices=32):
     from exact_io_aware_02_gb300.inputs import sample_slices
 
     q, k, v = make_workload(w)
+    G = w.H // w.hkv
     slices = sample_slices(w.B, w.H, max_slices, w.seed + 3)
-    per_slice = w.flops() / (w.B * w.H)
+    per_slice = units_per_step(w) / (w.B * w.H)
     done, t_total = 0, 0.0
     for (b, h) in slices:
-        qa, ka, va = (t[b, h].to(torch.float64).numpy() for t in (q, k, v))
+        qa = q[b, h].to(torch.float64).numpy()
+        ka, va = (t[b, h // G].to(torch.float64).numpy() for t in (k, v))
         t0 = time.perf_counter()
-        oracle.naive_attention(qa, ka, va, w.scale, w.causal)
+        oracle.naive_attention(qa, ka, va, w.scale, w.causal, q_offset=w.nk - w.N)
         t_total += time.perf_counter() - t0
         done += 1
         if t_total >= budget_s:
             break
     del np
-    return {"value": done * per_slice / t_total / 1e12, "unit": UNIT,
+    return {"value": done * per_slice / t_total, "unit": metric_for(w)[1],
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"{done} whole (b,h) slice(s) of {w.name} (N={w.N}, d={w.d}), fp64 NumPy, "
+            "sample": f"{done} whole (b,h) query-head slice(s) of {w.name} (N={w.N}, d={w.d}), fp64 NumPy, "
                       f"{t_total:.1f} s; threads = NumPy BLAS default on the listed cores"}
 
 
 def run_reference(args, w, rank, world):
-    """Reference arm: the CPU oracle, rank 0 only."""
+    """Reference arm: the CPU oracle, rank 0 only.  Each step is one 128-row query
+    tile of one query head (its K/V head under grouping), fp64 NumPy."""
     if rank != 0:
         return
     import oracle
 
     q, k, v = make_workload(w)
+    G = w.H // w.hkv
+    q_offset = w.nk - w.N
     n_tiles = (w.N + 127) // 128
-    total_flops, total_t = 0.0, 0.0
+    total_units, total_t = 0.0, 0.0
 
     def step(s, timed):
-        nonlocal total_flops, total_t
+        nonlocal total_units, total_t
         idx = (s * 7919) % (w.B * w.H * n_tiles)
         bh, tile = divmod(idx, n_tiles)
         b, h = divmod(bh, w.H)
         rows = list(range(tile * 128, min(w.N, tile * 128 + 128)))
-        qa, ka, va = (t[b, h].to(torch.float64).numpy() for t in (q, k, v))
+        qa = q[b, h].to(torch.float64).numpy()
+        ka, va = (t[b, h // G].to(torch.float64).numpy() for t in (k, v))
         t0 = time.perf_counter()
-        oracle.naive_attention(qa, ka, va, w.scale, w.causal, rows=rows)
+        oracle.naive_attention(qa, ka, va, w.scale, w.causal, rows=rows, q_offset=q_offset)
         dt = time.perf_counter() - t0
         if timed:
-            keys = [(i + 1) if w.causal else w.N for i in rows]
-            total_flops += sum(4.0 * kk * w.d for kk in keys)
+            if w.bound == "hbm":
+                total_units += len(rows) / (w.B * w.H * w.N) * w.algorithmic_bytes() / 1e9
+            else:
+                keys = [min(w.nk, q_offset + i + 1) if w.causal else w.nk for i in rows]
+                total_units += sum(4.0 * kk * w.d for kk in keys) / 1e12
             total_t += dt
 
     for s in range(args.warmup):
         step(s, False)
     for s in range(args.steps):
         step(args.warmup + s, True)
-    value = total_flops / total_t / 1e12
+    value = total_units / total_t
+    metric, unit = metric_for(w)
     cores = len(os.sched_getaffinity(0))
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": workload_config(w, "n/a (CPU)"),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": f"{args.steps} steps of one 128-row query tile of one (b,h) "
-                                       f"slice each, fp64 NumPy"},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
+                             "sample": f"{args.steps} steps of one 128-row query tile of one query head "
+                                       f"each, fp64 NumPy"},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
 
@@ -239,12 +278,16 @@ def run_ours(args, w, rank, world, local_rank):
     q, k, v = (t.to(dev, non_blocking=True) for t in (qh, kh, vh))
     o = torch.empty_like(q)
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
+    ws_bytes = fa.fa_fwd_gqa_workspace_bytes(w.B, w.H, w.N, w.d, w.n_splits)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) if ws_bytes else None
+    step = forward_call(fa, w)
+    launches_per_step = 2 if w.n_splits > 1 else 1
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
     for _ in range(args.warmup):
         flush.zero_()
-        fa.fa_fwd(q, k, v, o, lse, scale=w.scale, causal=w.causal, stream=stream)
+        step(q, k, v, o, lse, ws, stream)
     torch.cuda.synchronize()
     if fa.fa_status(clear=True) != 0:
         raise RuntimeError("device status word set during warm-up")
@@ -262,9 +305,9 @@ def run_ours(args, w, rank, world, local_rank):
     for i in range(args.steps):
         flush.zero_()  # write a buffer larger than L2 between timed launches
         starts[i].record(stream)
-        fa.fa_fwd(q, k, v, o, lse, scale=w.scale, causal=w.causal, stream=stream)
+        step(q, k, v, o, lse, ws, stream)
         ends[i].record(stream)
-        launches += 1
+        launches += launches_per_step
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -285,7 +328,7 @@ def run_ours(args, w, rank, world, local_rank):
             e0.record(stream)
         for dst, src in ((q, qh), (k, kh), (v, vh)):
             dst.copy_(src, non_blocking=True)
-        fa.fa_fwd(q, k, v, o, lse, scale=w.scale, causal=w.causal, stream=stream)
+        step(q, k, v, o, lse, ws, stream)
         o_h.copy_(o, non_blocking=True)
         lse_h.copy_(lse, non_blocking=True)
     e1.record(stream)
@@ -295,20 +338,29 @@ def run_ours(args, w, rank, world, local_rank):
         return
 
     flops = w.flops()
-    value = job_tflops(flops, ms, world)
-    peak_tf, _, peak_kind = peaks()
-    achieved = flops / (ms * 1e-3) / 1e12
+    metric, unit = metric_for(w)
+    units = units_per_step(w)
+    value = job_rate(units, ms, world)
+    peak_tf, peak_gbs, peak_kind = peaks()
+    if w.bound == "hbm":
+        roofline = {"bound": "hbm", "achieved": units / (ms * 1e-3), "peak": peak_gbs, "unit": "GB/s",
+                    "frac": units / (ms * 1e-3) / peak_gbs, "traffic": measured_traffic(w.name),
+                    "peak_kind": f"HBM copy bandwidth, {peak_kind}",
+                    "algorithmic_flops": flops, "algorithmic_bytes": w.algorithmic_bytes()}
+    else:
+        achieved = flops / (ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
+                    "frac": achieved / peak_tf, "traffic": measured_traffic(w.name),
+                    "peak_kind": f"bf16 dense burst, {peak_kind}",
+                    "algorithmic_flops": flops, "algorithmic_bytes": w.algorithmic_bytes()}
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": workload_config(w, "flushed between timed launches (256 MiB write); "
                                      "per-launch CUDA events on the launch stream"),
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": achieved / peak_tf, "traffic": measured_traffic(w.name),
-                     "peak_kind": f"bf16 dense burst, {peak_kind}",
-                     "algorithmic_flops": flops, "algorithmic_bytes": w.algorithmic_bytes()},
-        "e2e": {"value": job_tflops(flops, e2e_ms, world), "unit": UNIT,
+        "roofline": roofline,
+        "e2e": {"value": job_rate(units, e2e_ms, world), "unit": unit,
                 "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
                 "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * lse.element_size()},
         "gpu_launches": launches,

@@ -759,6 +759,31 @@ Problem mha(const void* q, const void* k, const void* v, void* o, float* lse, in
   return Problem{q, k, v, o, lse, B, H, H, N, N, d, scale, causal, 1, nullptr, 0};
 }
 
+// ---- fixed device workspace for callers that cannot allocate (fa_fwd_gqa_static_workspace)
+// One array per device that loads this library, held until the process exits.  Host code
+// must not use the symbol itself as an address: it is a host-side stand-in.  The device
+// address comes from cudaGetSymbolAddress, taken once per device with that device current.
+constexpr size_t kStaticWorkspaceBytes = FA_STATIC_WORKSPACE_BYTES;
+__device__ __align__(256) uint8_t g_static_workspace[kStaticWorkspaceBytes];
+
+void* g_static_workspace_addr[kMaxDevices];  // device address per device, set on first use
+
+int static_workspace(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!g_static_workspace_addr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_workspace) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return FA_ERR_CUDA;
+    }
+    g_static_workspace_addr[dev] = ptr;
+  }
+  *out = g_static_workspace_addr[dev];
+  return FA_OK;
+}
+
 constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
 
 }  // namespace
@@ -781,6 +806,23 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
 size_t fa_fwd_gqa_workspace_bytes(int B, int Hq, int Nq, int d, int n_splits) {
   if (B < 1 || Hq < 1 || Nq < 1 || (d != 64 && d != 128) || n_splits < 1 || n_splits > fa::kMaxSplits) return 0;
   return fa::workspace_needed(static_cast<long long>(B) * Hq * Nq, d, n_splits);
+}
+
+int fa_fwd_gqa_static_workspace(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                                int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                                int n_splits, cudaStream_t stream) {
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  if (n_splits > 1) {
+    const size_t need = fa_fwd_gqa_workspace_bytes(B, Hq, Nq, d, n_splits);
+    if (need == 0) return FA_ERR_ARG;  // sizes fa_fwd_gqa would reject anyway
+    if (need > fa::kStaticWorkspaceBytes) return FA_ERR_WORKSPACE_TOO_LARGE;
+    const int rc = fa::static_workspace(&ws);
+    if (rc != FA_OK) return rc;
+    ws_bytes = fa::kStaticWorkspaceBytes;
+  }
+  const fa::Problem pr{q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, n_splits, ws, ws_bytes};
+  return fa::run(pr, 0, fa::kDefaultTimeoutNs, stream);
 }
 
 int fa_fwd_withheld_tile(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
@@ -810,6 +852,7 @@ const char* fa_strerror(int code) {
     case FA_ERR_LAUNCH: return "kernel launch or TMA descriptor encoding failed";
     case FA_ERR_TIMEOUT: return "a device-side barrier wait timed out";
     case FA_ERR_CUDA: return "CUDA runtime call failed";
+    case FA_ERR_WORKSPACE_TOO_LARGE: return "the split-K/V partials need more than the library's fixed workspace";
     default: return "unknown error";
   }
 }

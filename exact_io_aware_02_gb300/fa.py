@@ -21,10 +21,12 @@ FA_ERR_ARCH = -2
 FA_ERR_LAUNCH = -3
 FA_ERR_TIMEOUT = -4
 FA_ERR_CUDA = -5
+FA_ERR_WORKSPACE_TOO_LARGE = -6
+FA_STATIC_WORKSPACE_BYTES = 16 << 20
 FA_STATUS_TIMEOUT = 0x1
 
-EXPORTED = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_gqa_workspace_bytes", "fa_status",
-            "fa_fwd_withheld_tile", "fa_strerror", "fa_version")
+EXPORTED = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_gqa_workspace_bytes", "fa_fwd_gqa_static_workspace",
+            "fa_status", "fa_fwd_withheld_tile", "fa_strerror", "fa_version")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
@@ -38,6 +40,8 @@ lib.fa_fwd_gqa.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, 
 lib.fa_fwd_gqa.restype = _i
 lib.fa_fwd_gqa_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
 lib.fa_fwd_gqa_workspace_bytes.restype = ctypes.c_size_t
+lib.fa_fwd_gqa_static_workspace.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]
+lib.fa_fwd_gqa_static_workspace.restype = _i
 lib.fa_fwd_withheld_tile.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _d, _vp]
 lib.fa_fwd_withheld_tile.restype = _i
 lib.fa_status.argtypes = [_i, _vp]
@@ -116,6 +120,30 @@ def fa_fwd_gqa(q, k, v, o=None, lse=None, scale=None, causal=False, n_splits=1,
     rc = lib.fa_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
                         B, Hq, Hkv, Nq, Nk, d, float(scale), int(bool(causal)), int(n_splits),
                         ws_ptr, ws_len, _stream_handle(stream, q.device))
+    if rc != FA_OK:
+        raise FAError(rc)
+    return o, lse
+
+
+def fa_fwd_gqa_static_workspace(q, k, v, o=None, lse=None, scale=None, causal=False, n_splits=1,
+                                stream=None):
+    """fa_fwd_gqa without a workspace argument, for callers that cannot allocate device
+    memory: the split partials go to the library's fixed 16 MiB device array (shared by
+    every call on the device -- do not overlap calls on the GPU).  The outputs ``o`` and
+    ``lse`` are still the caller's; pass them preallocated to allocate nothing here."""
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape:
+        raise ValueError("q must be [B, Hq, Nq, d] and k, v [B, Hkv, Nk, d]")
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if o is None:
+        o = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Hq, Nq), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    rc = lib.fa_fwd_gqa_static_workspace(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), B, Hq, Hkv, Nq, Nk, d, float(scale),
+                                         int(bool(causal)), int(n_splits), _stream_handle(stream, q.device))
     if rc != FA_OK:
         raise FAError(rc)
     return o, lse

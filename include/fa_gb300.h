@@ -42,6 +42,8 @@ extern "C" {
 #define FA_ERR_LAUNCH   -3  /* the CUDA launch (or the TMA descriptor encoding) failed     */
 #define FA_ERR_TIMEOUT  -4  /* a device-side barrier wait gave up (see fa_status)           */
 #define FA_ERR_CUDA     -5  /* another CUDA runtime call failed                             */
+#define FA_ERR_WORKSPACE_TOO_LARGE -6  /* fa_fwd_gqa_static_workspace: the partials need more
+                                          than FA_STATIC_WORKSPACE_BYTES                      */
 
 /* Bits of the device status word (fa_status). */
 #define FA_STATUS_TIMEOUT 0x1u  /* some CTA's bounded mbarrier wait expired and it bailed out */
@@ -113,6 +115,39 @@ int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse,
 
 /* Workspace bytes fa_fwd_gqa needs for these sizes (0 for n_splits = 1 or bad sizes). */
 size_t fa_fwd_gqa_workspace_bytes(int B, int Hq, int Nq, int d, int n_splits);
+
+/*
+ * fa_fwd_gqa_static_workspace -- fa_fwd_gqa for callers that cannot allocate device
+ * memory.  (An addition of this library; the FlashAttention pages have no counterpart.)
+ *
+ * Some callers cannot call cudaMalloc at the point where they run attention: a
+ * serving loop that fixed its device-memory plan at start-up and may not allocate
+ * afterwards, or a plain C host program that has no device allocator of its own to
+ * hand out a scratch buffer.  This entry point takes the same arguments as
+ * fa_fwd_gqa minus the workspace, and uses instead a workspace array of
+ * FA_STATIC_WORKSPACE_BYTES (16 MiB) that the library defines in device memory.
+ * Every GPU that loads the library holds that array until the process exits.
+ *
+ * It allocates nothing: no cudaMalloc, cudaFree or allocating library routine.  The
+ * first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any
+ * stream capture.  Later calls reuse the address.
+ *
+ * All calls on a device share the one array, and it keeps whatever the last call
+ * left there (the kernels overwrite every byte they read, so nothing needs
+ * clearing).  Two calls whose kernels overlap on the GPU -- on different streams,
+ * say -- race on the array and corrupt each other's results: serialise them.
+ *
+ * n_splits = 1 needs no workspace and behaves exactly as fa_fwd_gqa.  If the split
+ * partials would need more than FA_STATIC_WORKSPACE_BYTES
+ * (fa_fwd_gqa_workspace_bytes(B, Hq, Nq, d, n_splits) bytes), the call returns
+ * FA_ERR_WORKSPACE_TOO_LARGE and enqueues nothing.  Other arguments and errors as for
+ * fa_fwd_gqa.
+ */
+#define FA_STATIC_WORKSPACE_BYTES (16u << 20)
+int fa_fwd_gqa_static_workspace(const void* q, const void* k, const void* v, void* o, float* lse,
+                                int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale,
+                                int causal, int n_splits, cudaStream_t stream);
 
 /*
  * fa_status -- read the device status word of the current device.

@@ -38,7 +38,7 @@ def test_library_exports_every_declared_symbol(fa):
 
 def test_strerror_and_version(fa):
     assert fa.fa_version() == 2
-    for code in (0, -1, -2, -3, -4, -5):
+    for code in (0, -1, -2, -3, -4, -5, -6):
         assert fa.fa_strerror(code) and fa.fa_strerror(code) != "unknown error"
     assert fa.fa_strerror(-99) == "unknown error"
 

@@ -6,6 +6,7 @@ package imports nothing from it.  See ``oracle/attention.py`` for the sources
 each routine follows.
 """
 from .attention import (  # noqa: F401
+    attention_backward,
     attention_probabilities,
     blocked_normalised_attention,
     blocked_online_attention,

@@ -292,6 +292,43 @@ def split_kv_attention(q, k, v, scale: float, causal: bool = False,
     return out, lse
 
 
+def attention_backward(q, k, v, do, scale: float, causal: bool = False, q_offset: int = 0):
+    """Gradients of O = softmax(scale Q K^T) V for an upstream gradient dO.
+
+    The recompute scheme of [P2] §6 (and [P1] 工程实现细节) keeps only the per-row
+    statistics of the forward; the gradients follow from the chain rule through
+    O = P V and P = softmax(S), S = scale Q K^T:
+        D_i   = sum_c dO_ic O_ic           (= sum_j P_ij dP_ij)
+        dV    = P^T dO
+        dP    = dO V^T
+        dS    = P * (dP - D)               (softmax Jacobian, row by row)
+        dQ    = scale dS K,    dK = scale dS^T Q.
+    Masked entries have P = 0, so they contribute nothing.  Rows that see no key
+    (only with offsets) have P = 0 and zero gradients.  Returns (dQ, dK, dV, D) in fp64.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k = np.asarray(k, dtype=np.float64)
+    v = np.asarray(v, dtype=np.float64)
+    do = np.asarray(do, dtype=np.float64)
+    q_pos = q_offset + np.arange(q.shape[0], dtype=np.int64)
+    k_pos = np.arange(k.shape[0], dtype=np.int64)
+    s = _scores(q, k, scale, causal, q_pos, k_pos)
+    m = s.max(axis=1)
+    seen = m > NEG_INF
+    with np.errstate(invalid="ignore"):
+        e = np.where(seen[:, None], np.exp(s - m[:, None]), 0.0)
+    l = e.sum(axis=1)
+    p = e / np.where(seen, l, 1.0)[:, None]
+    o = p @ v
+    d_row = (do * o).sum(axis=1)
+    dv = p.T @ do
+    dp = do @ v.T
+    ds = p * (dp - d_row[:, None])
+    dq = scale * (ds @ k)
+    dk = scale * (ds.T @ q)
+    return dq, dk, dv, d_row
+
+
 def naive_attention_bhnd(q, k, v, scale: float, causal: bool = False,
                          slices: Iterable | None = None, rows=None):
     """Apply ``naive_attention`` to each (b, h) slice of [B, H, N, d] arrays.

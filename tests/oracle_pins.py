@@ -309,6 +309,73 @@ def pin_split_kv(mod):
             assert np.max(np.abs(o - o_ref)) < 1e-12 and np.max(np.abs(l[fin] - l_ref[fin])) < 1e-12
 
 
+def _loss_grad_fd(mod, q, k, v, g, scale, causal, which, idx, h=1e-6):
+    """Central difference of L = sum(O * g) with respect to one input element."""
+    arrs = {"q": q, "k": k, "v": v}
+    a = arrs[which].copy()
+    a[idx] += h
+    up = dict(arrs, **{which: a})
+    o1, _ = mod.naive_attention(up["q"], up["k"], up["v"], scale, causal)
+    a[idx] -= 2 * h
+    dn = dict(arrs, **{which: a})
+    o2, _ = mod.naive_attention(dn["q"], dn["k"], dn["v"], scale, causal)
+    return ((o1 - o2) * g).sum() / (2 * h)
+
+
+def pin_backward_finite_differences(mod):
+    """The analytic gradients equal central differences of L = sum(O * dO) in every
+    element of Q, K and V (tiny inputs, fp64; error ~1e-9)."""
+    rng = _rng(14)
+    for n, d, causal, scale in ((5, 3, False, 0.7), (6, 4, True, 1.1)):
+        q, k, v, g = (rng.standard_normal((n, d)) for _ in range(4))
+        dq, dk, dv, _ = mod.attention_backward(q, k, v, g, scale, causal)
+        for which, grad in (("q", dq), ("k", dk), ("v", dv)):
+            for idx in np.ndindex(n, d):
+                fd = _loss_grad_fd(mod, q, k, v, g, scale, causal, which, idx)
+                assert abs(fd - grad[idx]) < 1e-6, (which, idx, fd, grad[idx])
+
+
+def pin_backward_torch(mod):
+    """Against torch.autograd in fp64 on the CPU (a library the oracle does not use)."""
+    import torch
+    rng = _rng(15)
+    n, d, scale = 33, 8, 0.4
+    for causal in (False, True):
+        arrs = [rng.standard_normal((n, d)) for _ in range(4)]
+        q, k, v = (torch.tensor(a, requires_grad=True) for a in arrs[:3])
+        g = torch.tensor(arrs[3])
+        s = scale * q @ k.T
+        if causal:
+            s = s.masked_fill(torch.triu(torch.ones(n, n, dtype=torch.bool), 1), float("-inf"))
+        (torch.softmax(s, dim=1) @ v * g).sum().backward()
+        dq, dk, dv, _ = mod.attention_backward(*arrs[:3], arrs[3], scale, causal)
+        for mine, ref in ((dq, q.grad), (dk, k.grad), (dv, v.grad)):
+            assert np.max(np.abs(mine - ref.numpy())) < 1e-12
+
+
+def pin_backward_invariants(mod):
+    """Rows of dS sum to zero, so the K gradients sum to zero over keys (scores are
+    invariant to adding one vector to every key); uniform attention (q = 0) gives
+    dV_j = mean over the queries that see key j of dO_i; D = rowsum(dO * O)."""
+    rng = _rng(16)
+    n, d = 20, 5
+    q, k, v, g = (rng.standard_normal((n, d)) for _ in range(4))
+    for causal in (False, True):
+        dq, dk, dv, drow = mod.attention_backward(q, k, v, g, 0.6, causal)
+        assert np.max(np.abs(dk.sum(axis=0))) < 1e-12
+        o, _ = mod.naive_attention(q, k, v, 0.6, causal)
+        assert np.max(np.abs(drow - (g * o).sum(axis=1))) < 1e-12
+    z = np.zeros((n, d))
+    dq, dk, dv, _ = mod.attention_backward(z, k, v, g, 0.6, False)
+    assert np.max(np.abs(dv - g.mean(axis=0)[None, :])) < 1e-12
+    dq, dk, dv, _ = mod.attention_backward(z, k, v, g, 0.6, True)
+    for j in range(n):
+        want = sum(g[i] / (i + 1) for i in range(j, n))
+        assert np.max(np.abs(dv[j] - want)) < 1e-12
+    # dK = scale * dS^T Q vanishes when Q = 0
+    assert np.max(np.abs(dk)) < 1e-12
+
+
 ALL_PINS = [
     pin_worked_example,
     pin_worked_example_exact,
@@ -326,4 +393,7 @@ ALL_PINS = [
     pin_offsets_and_empty_rows,
     pin_decode_alignment,
     pin_split_kv,
+    pin_backward_finite_differences,
+    pin_backward_torch,
+    pin_backward_invariants,
 ]

@@ -33,6 +33,12 @@ MUTANTS = [
     ("split merge ignores LSE_s", "np.exp(lse_s - np.where(seen, top, 0.0)[None, :])",
      "np.exp(0.0 * lse_s)", 1),
     ("split LSE drops total", "top + np.log(np.where(seen, total, 1.0))", "top + 0.0 * total", 1),
+    ("bwd: D from dP instead of O", "d_row = (do * o).sum(axis=1)", "d_row = (do * v[: do.shape[0]]).sum(axis=1)", 1),
+    ("bwd: softmax Jacobian sign", "ds = p * (dp - d_row[:, None])", "ds = p * (dp + d_row[:, None])", 1),
+    ("bwd: D dropped", "ds = p * (dp - d_row[:, None])", "ds = p * dp", 1),
+    ("bwd: dV not transposed", "dv = p.T @ do", "dv = p @ do", 1),
+    ("bwd: dK scale dropped", "dk = scale * (ds.T @ q)", "dk = (ds.T @ q)", 1),
+    ("bwd: dQ uses V", "dq = scale * (ds @ k)", "dq = scale * (ds @ v)", 1),
     ("split key offsets ignored", "rows=rows, q_offset=q_offset, k_offset=a))",
      "rows=rows, q_offset=q_offset, k_offset=0))", 1),
     ("P uses V", "return e / e.sum(axis=1)[:, None]", "return e / e.sum(axis=0)[None, :]", 1),

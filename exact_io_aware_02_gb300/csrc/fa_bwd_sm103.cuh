@@ -1,0 +1,559 @@
+// fa_bwd_sm103.cuh -- attention backward with recomputation, sm_103a.  Included once,
+// by fa_fwd_sm103.cu inside its namespace, so the two directions share one translation unit (the status
+// word, the bounded waits, the tensor-map helpers).
+//
+// The forward keeps only O and the per-row LSE; the backward rebuilds S and P on chip
+// from them (the recompute scheme of §6 of the zzszmyf.github.io notes "FlashAttention
+// 原理是什么？为什么又省显存又快" and of the aiqz.cc article's 工程实现细节 section):
+//     P = exp(scale*Q K^T - LSE),   D = rowsum(dO * O),
+//     dV = P^T dO,   dP = dO V^T,   dS = P * (dP - D),
+//     dQ = scale * dS K,   dK = scale * dS^T Q.
+//
+// Three kernels, all on one stream:
+//   fa_bwd_prep_kernel  -- D = rowsum(dO * O) (memory-bound, one warp per row);
+//   fa_bwd_dkdv_kernel  -- one CTA per 128-key tile: loops over the query tiles that see
+//                          it, recomputes S^T = K Q^T and dP^T = V dO^T, and accumulates
+//                          dV += P^T dO and dK += dS^T Q in tensor memory;
+//   fa_bwd_dq_kernel    -- one CTA per 128-query tile: loops over its key tiles,
+//                          recomputes S = Q K^T and dP = dO V^T, accumulates dQ += dS K.
+// Splitting dQ from dK/dV costs two extra products per tile pair (7 instead of 5) but
+// needs no atomics and keeps every accumulator in tensor memory.
+//
+// Both main kernels: warps 0-3 compute (one TMEM lane = one row per thread), warp 4 is
+// the TMA producer, warp 5 allocates tensor memory and issues the MMAs (converged warp,
+// elect.sync).  Every mbarrier wait is bounded, as in the forward.
+#pragma once
+
+// (included inside namespace fa)
+
+constexpr int kBwdThreads = 192;
+
+// ---------------------------------------------------------------- D = rowsum(dO * O)
+template <int D>
+__global__ void __launch_bounds__(256)
+    fa_bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                       float* __restrict__ dvec, int rows) {
+  constexpr int E = D / 32;
+  const int row = static_cast<int>((static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  const size_t base = static_cast<size_t>(row) * D + lane * E;
+  float acc = 0.f;
+  if constexpr (E == 4) {
+    const uint2 a = *reinterpret_cast<const uint2*>(o + base);
+    const uint2 b = *reinterpret_cast<const uint2*>(dout + base);
+    const uint32_t av[2] = {a.x, a.y}, bv[2] = {b.x, b.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      acc += __uint_as_float(av[i] << 16) * __uint_as_float(bv[i] << 16);
+      acc += __uint_as_float(av[i] & 0xffff0000u) * __uint_as_float(bv[i] & 0xffff0000u);
+    }
+  } else {
+    const uint32_t a = *reinterpret_cast<const uint32_t*>(o + base);
+    const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + base);
+    acc += __uint_as_float(a << 16) * __uint_as_float(b << 16);
+    acc += __uint_as_float(a & 0xffff0000u) * __uint_as_float(b & 0xffff0000u);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) dvec[row] = acc;
+}
+
+struct BwdParams {
+  const float* lse;   // [groups * R]
+  const float* dvec;  // [groups * R]
+  int groups;         // B * Hkv
+  int R;              // query rows per group (G * N)
+  int N;              // sequence length (queries and keys)
+  int n_qtiles;       // ceil(R / 128)
+  int n_ktiles;       // ceil(N / 128)
+  float scale;
+  float scale_log2;   // scale * log2(e)
+  int causal;
+  unsigned long long timeout_ns;
+};
+
+// highest sequence position of any query row in tile qt (rows straddling heads: N - 1)
+__device__ __forceinline__ int bwd_tile_max_pos(const BwdParams& p, int qt) {
+  const int r0 = qt * 128;
+  const int r1 = min(r0 + 127, p.R - 1);
+  return (r1 / p.N != r0 / p.N) ? p.N - 1 : r1 % p.N;
+}
+__device__ __forceinline__ int bwd_tile_min_pos(const BwdParams& p, int qt) {
+  const int r0 = qt * 128;
+  const int r1 = min(r0 + 127, p.R - 1);
+  return (r1 / p.N != r0 / p.N) ? 0 : r0 % p.N;
+}
+
+template <int D>
+struct BwdCfg {
+  static constexpr int kChunks = D / 64;
+  static constexpr int kChunkBytes = 128 * 128;
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kVecBytes = 2 * 128 * 4;     // LSE and D of one query tile
+  // dK/dV kernel: K, V resident; a ring of stages {Q_i, dO_i, LSE_i, D_i}
+  static constexpr int kStages = D == 128 ? 2 : 4;
+  static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;
+  static constexpr int kKVOffStage = 2 * kTileBytes;
+  static constexpr int kKVOffBar = kKVOffStage + kStages * kStageBytes;
+  // dQ kernel: Q, dO resident; a ring of K_j, V_j tiles
+  static constexpr int kSlots = D == 128 ? 4 : 8;
+  static constexpr int kQOffRing = 2 * kTileBytes;
+  static constexpr int kQOffBar = kQOffRing + kSlots * kTileBytes;
+  static constexpr int kMaxBars = 2 + 2 * (kSlots > kStages ? kSlots : kStages) + 8;
+  static constexpr int kSmemKV = kKVOffBar + kMaxBars * 8 + 16 + 1024;
+  static constexpr int kSmemQ = kQOffBar + kMaxBars * 8 + 16 + 1024;
+  static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+  static_assert(kSmemKV <= 232448 && kSmemQ <= 232448, "shared memory budget");
+};
+
+// MMA helpers shared by both kernels -------------------------------------------------
+// C[tmem, 128 x 128] = A (128 rows x D, K-major smem) * B^T (128 rows x D, K-major smem)
+template <int D>
+__device__ __forceinline__ void bwd_mma_nt(uint32_t c, uint64_t da, uint64_t db) {
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false);
+  ptx::mma_ss_i<0>(c, da, db, idesc);
+#pragma unroll
+  for (int kk = 1; kk < D / 16; ++kk) {
+    const uint64_t o = (kk >> 2) * (BwdCfg<D>::kChunkBytes >> 4) + (kk & 3) * 2;
+    ptx::mma_ss_i<1>(c, da + o, db + o, idesc);
+  }
+}
+// C[tmem, 128 x D] (+)= A[tmem, 128 x 128 bf16] * B (128 rows x D, N-contiguous smem)
+template <int D>
+__device__ __forceinline__ void bwd_mma_tn(uint32_t c, uint32_t a_tmem, uint64_t db, bool accumulate) {
+  constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, D, true);
+  if (accumulate) ptx::mma_ts_i<1>(c, a_tmem, db, idesc);
+  else ptx::mma_ts_i<0>(c, a_tmem, db, idesc);
+#pragma unroll
+  for (int kk = 1; kk < 8; ++kk) ptx::mma_ts_i<1>(c, a_tmem + kk * 8, db + kk * 128, idesc);
+}
+
+// Convert a 128-row fp32 accumulator (this thread's row) to bf16 into a 128B-swizzled
+// shared tile (the TMA layout), multiplying by `mul`.
+template <int D>
+__device__ __forceinline__ void bwd_acc_to_smem(uint32_t t_acc, uint32_t smem_tile, int row, float mul) {
+#pragma unroll 1
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t r[32];
+    ptx::tmem_ld32(t_acc + cc * 32, r);
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
+    const uint32_t base = smem_tile + (cc >> 1) * BwdCfg<D>::kChunkBytes + row * 128;
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      const int gran = (cc & 1) * 4 + g;
+      ptx::st_shared_v4(base + ((gran ^ (row & 7)) << 4), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+    }
+  }
+}
+
+// ================================================================ dK, dV
+// CTA (group bh, key tile kt).  Tensor memory: S^T [0,128) with P^T over its first 64
+// columns, dP^T [128,256) with dS^T over its first 64 columns, dV, dK after that.
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
+                       const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  // barriers: 0 kv_full, [1, 1+S) stage_full, [1+S, 1+2S) stage_empty, then s_full,
+  // pds_full, acc_final, drain
+  constexpr int S = C::kStages;
+  constexpr int kBarKV = 0, kBarFull = 1, kBarEmpty = 1 + S, kBarS = 1 + 2 * S, kBarP = kBarS + 1,
+                kBarFinal = kBarP + 1, kBarDrain = kBarFinal + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kKVOffBar + C::kMaxBars * 8);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kKVOffBar + C::kMaxBars * 8 + 4);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kKVOffBar + 8u * i; };
+  auto stage_addr = [&](int s) -> uint32_t { return sbase + C::kKVOffStage + s * C::kStageBytes; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x % p.groups;
+  const int kt = blockIdx.x / p.groups;  // causal: the first key tiles have the most work, so go first
+  // query tiles that see this key tile: causal needs some position >= kt*128
+  auto needed = [&](int qt) { return !p.causal || bwd_tile_max_pos(p, qt) >= kt * 128; };
+  int n_q = 0;
+  for (int qt = 0; qt < p.n_qtiles; ++qt) n_q += needed(qt) ? 1 : 0;
+
+  if (warp == 4 && lane == 0) {
+    ptx::mbar_init(bar(kBarKV), 1);
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(bar(kBarFull + s), 2);  // TMA bytes + the producer's LSE/D stores
+      ptx::mbar_init(bar(kBarEmpty + s), 1);
+    }
+    ptx::mbar_init(bar(kBarS), 1);
+    ptx::mbar_init(bar(kBarP), 4);
+    ptx::mbar_init(bar(kBarFinal), 1);
+    ptx::mbar_init(bar(kBarDrain), 1);
+    *abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Waiter w{abort_flag, p.timeout_ns};
+
+  if (warp == 4) {
+    // ------------------------------------------------ producer: K, V once; stages of Q, dO, LSE, D
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(bar(kBarKV), 2 * C::kTileBytes);
+      for (int c = 0; c < C::kChunks; ++c) {
+        ptx::tma_load_3d(sbase + c * C::kChunkBytes, &tm_k, bar(kBarKV), c * 64, kt * 128, bh);
+        ptx::tma_load_3d(sbase + C::kTileBytes + c * C::kChunkBytes, &tm_v, bar(kBarKV), c * 64, kt * 128, bh);
+      }
+    }
+    int u = 0, issued = 0;
+    bool ok = true;
+    for (int qt = 0; qt < p.n_qtiles && ok; ++qt) {
+      if (!needed(qt)) continue;
+      const int s = u % S, use = u / S;
+      if (use > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarEmpty + s), (use - 1) & 1));
+      if (!ok) break;
+      const uint32_t st = stage_addr(s);
+      if (lane == 0) {
+        ptx::mbar_arrive_expect_tx(bar(kBarFull + s), 2 * C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c) {
+          ptx::tma_load_3d(st + c * C::kChunkBytes, &tm_q, bar(kBarFull + s), c * 64, qt * 128, bh);
+          ptx::tma_load_3d(st + C::kTileBytes + c * C::kChunkBytes, &tm_do, bar(kBarFull + s), c * 64, qt * 128, bh);
+        }
+      }
+      // LSE and D of the tile's rows (padding rows: 0); plain loads, bounds-checked
+      float* vec = reinterpret_cast<float*>(smem + C::kKVOffStage + s * C::kStageBytes + 2 * C::kTileBytes);
+      for (int i = lane; i < 128; i += 32) {
+        const int r = qt * 128 + i;
+        const size_t g = static_cast<size_t>(bh) * p.R + r;
+        vec[i] = r < p.R ? p.lse[g] : 0.f;
+        vec[128 + i] = r < p.R ? p.dvec[g] : 0.f;
+      }
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(kBarFull + s));
+      ++u;
+      issued = u;
+    }
+    if (!ok && lane == 0) {
+      w.drain(bar(kBarKV), 0);
+      for (int v = issued - S > 0 ? issued - S : 0; v < issued; ++v) w.drain(bar(kBarFull + v % S), (v / S) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------ MMA issuer
+    const uint64_t desc_k = ptx::smem_desc_sw128(sbase, 16, 1024);
+    const uint64_t desc_v = ptx::smem_desc_sw128(sbase + C::kTileBytes, 16, 1024);
+    const uint64_t desc_stage_kmaj = ptx::smem_desc_sw128(stage_addr(0), 16, 1024);
+    const uint64_t desc_stage_nmaj = ptx::smem_desc_sw128(stage_addr(0), C::kChunkBytes, 1024);
+    constexpr uint64_t kStageStep = C::kStageBytes >> 4, kTileStep = C::kTileBytes >> 4;
+    const uint32_t t_s = tmem + C::kColS, t_dp = tmem + C::kColDP;
+    const uint32_t t_dv = tmem + C::kColAcc0, t_dk = tmem + C::kColAcc1;
+    bool ok = __all_sync(0xffffffffu, w.wait(bar(kBarKV), 0));
+    ptx::tc_fence_after();
+    for (int u = 0; ok && u <= n_q; ++u) {
+      if (u >= 1) {
+        // dV += P^T dO, dK += dS^T Q for the previous stage
+        const int sp = (u - 1) % S;
+        ok = __all_sync(0xffffffffu, w.wait(bar(kBarP), (u - 1) & 1));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) {
+          const uint64_t dq_n = desc_stage_nmaj + sp * kStageStep;
+          bwd_mma_tn<D>(t_dv, t_s, dq_n + kTileStep, u > 1);  // B = dO (N-contiguous)
+          bwd_mma_tn<D>(t_dk, t_dp, dq_n, u > 1);             // B = Q (N-contiguous)
+          ptx::tc_commit(bar(kBarEmpty + sp));
+          if (u == n_q) ptx::tc_commit(bar(kBarFinal));
+        }
+        __syncwarp();
+      }
+      if (u < n_q) {
+        const int s = u % S;
+        ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + s), (u / S) & 1));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) {
+          const uint64_t dq_k = desc_stage_kmaj + s * kStageStep;
+          bwd_mma_nt<D>(t_s, desc_k, dq_k);                  // S^T = K Q^T
+          bwd_mma_nt<D>(t_dp, desc_v, dq_k + kTileStep);     // dP^T = V dO^T
+          ptx::tc_commit(bar(kBarS));
+        }
+        __syncwarp();
+      }
+    }
+    if (ptx::elect_one()) ptx::tc_commit(bar(kBarDrain));
+    __syncwarp();
+    w.drain(bar(kBarDrain), 0);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ compute: thread = key row
+    const int row = warp * 32 + lane;
+    const int key = kt * 128 + row;
+    const bool key_valid = key < p.N;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + C::kColS, t_dp = tmem + lane_off + C::kColDP;
+    const float c2 = p.scale_log2;
+    constexpr float kLog2e = 1.4426950408889634f;
+    bool ok = true;
+    int u = 0;
+    for (int qt = 0; qt < p.n_qtiles && ok; ++qt) {
+      if (!needed(qt)) continue;
+      const int s = u % S;
+      ok = __all_sync(0xffffffffu, w.wait(bar(kBarS), u & 1));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      const float* vec = reinterpret_cast<const float*>(smem + C::kKVOffStage + s * C::kStageBytes + 2 * C::kTileBytes);
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t rs[32], rd[32];
+        ptx::tmem_ld32(t_s + cc * 32, rs);
+        ptx::tmem_ld32(t_dp + cc * 32, rd);
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float pv[2], dsv[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = cc * 32 + i + h;
+            const int qrow = qt * 128 + col;
+            const int qpos = qrow % p.N;
+            const bool live = key_valid && qrow < p.R && !(p.causal && qpos < key);
+            const float e = ptx::ex2_approx(fmaf(__uint_as_float(rs[i + h]), c2, -vec[col] * kLog2e));
+            pv[h] = live ? e : 0.f;
+            dsv[h] = pv[h] * (__uint_as_float(rd[i + h]) - vec[128 + col]);
+          }
+          pp[i / 2] = ptx::pack_bf16x2(pv[0], pv[1]);
+          pd[i / 2] = ptx::pack_bf16x2(dsv[0], dsv[1]);
+        }
+        // P^T and dS^T (bf16 pairs) over columns [16 cc, 16 cc + 16) of S^T and dP^T:
+        // those columns were read in this or an earlier chunk
+        ptx::tmem_st16(t_s + cc * 16, pp);
+        ptx::tmem_st16(t_dp + cc * 16, pd);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(kBarP));
+      ++u;
+    }
+    // epilogue: dV, scale*dK -> bf16 -> shared (K and V buffers, no longer read) -> TMA
+    if (ok && n_q > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFinal), 0));
+    if (ok && n_q > 0) {
+      ptx::tc_fence_after();
+      bwd_acc_to_smem<D>(tmem + lane_off + C::kColAcc0, sbase + C::kTileBytes, row, 1.f);
+      bwd_acc_to_smem<D>(tmem + lane_off + C::kColAcc1, sbase, row, p.scale);
+      ptx::fence_proxy_async_smem();
+    } else if (n_q == 0 && ok) {
+      // no query sees this key tile: zero gradients (the K/V tiles may still be landing)
+      ok = __all_sync(0xffffffffu, w.wait(bar(kBarKV), 0));
+      if (ok) {
+        for (int i = 0; i < 2 * C::kTileBytes / 16; i += 128)
+          ptx::st_shared_v4(sbase + (i + row) * 16, 0u, 0u, 0u, 0u);
+        ptx::fence_proxy_async_smem();
+      }
+    }
+    ptx::named_barrier(1, 128);
+    if (ok && row == 0) {
+      for (int c = 0; c < C::kChunks; ++c) {
+        ptx::tma_store_3d(&tm_dk, sbase + c * C::kChunkBytes, c * 64, kt * 128, bh);
+        ptx::tma_store_3d(&tm_dv, sbase + C::kTileBytes + c * C::kChunkBytes, c * 64, kt * 128, bh);
+      }
+      ptx::bulk_commit();
+      ptx::bulk_wait_all();
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+
+// ================================================================ dQ
+// CTA (group bh, query tile qt).  Tensor memory: S [0,128) with dS over its first 64
+// columns, dP [128,256), dQ after that.
+template <int D>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const __grid_constant__ CUtensorMap tm_dq, const BwdParams p) {
+  using C = BwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  constexpr int S = C::kSlots;
+  constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 1 + S, kBarS = 1 + 2 * S, kBarP = kBarS + 1,
+                kBarFinal = kBarP + 1, kBarDrain = kBarFinal + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kQOffBar + C::kMaxBars * 8);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kQOffBar + C::kMaxBars * 8 + 4);
+  auto bar = [&](int i) -> uint32_t { return sbase + C::kQOffBar + 8u * i; };
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bh = blockIdx.x % p.groups;
+  const int qt = p.n_qtiles - 1 - blockIdx.x / p.groups;  // causal: the last query tiles have most work
+  const int n_kv = p.causal ? min(p.n_ktiles, bwd_tile_max_pos(p, qt) / 128 + 1) : p.n_ktiles;
+
+  if (warp == 4 && lane == 0) {
+    ptx::mbar_init(bar(kBarQ), 1);
+    for (int s = 0; s < S; ++s) {
+      ptx::mbar_init(bar(kBarFull + s), 1);
+      ptx::mbar_init(bar(kBarEmpty + s), 1);
+    }
+    ptx::mbar_init(bar(kBarS), 1);
+    ptx::mbar_init(bar(kBarP), 4);
+    ptx::mbar_init(bar(kBarFinal), 1);
+    ptx::mbar_init(bar(kBarDrain), 1);
+    *abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 5) {
+    ptx::tmem_alloc(ptx::smem_addr(tmem_slot), 512);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Waiter w{abort_flag, p.timeout_ns};
+
+  if (warp == 4) {
+    // ------------------------------------------------ producer: Q, dO once; K_0, V_0, K_1, ...
+    if (lane == 0) {
+      ptx::mbar_arrive_expect_tx(bar(kBarQ), 2 * C::kTileBytes);
+      for (int c = 0; c < C::kChunks; ++c) {
+        ptx::tma_load_3d(sbase + c * C::kChunkBytes, &tm_q, bar(kBarQ), c * 64, qt * 128, bh);
+        ptx::tma_load_3d(sbase + C::kTileBytes + c * C::kChunkBytes, &tm_do, bar(kBarQ), c * 64, qt * 128, bh);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int u = 0; u < 2 * n_kv; ++u) {
+        const int s = u % S, use = u / S;
+        if (use > 0 && !w.wait(bar(kBarEmpty + s), (use - 1) & 1)) { ok = false; break; }
+        ptx::mbar_arrive_expect_tx(bar(kBarFull + s), C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+          ptx::tma_load_3d(sbase + C::kQOffRing + s * C::kTileBytes + c * C::kChunkBytes, (u & 1) ? &tm_v : &tm_k,
+                           bar(kBarFull + s), c * 64, (u >> 1) * 128, bh);
+        issued = u + 1;
+      }
+      if (!ok) {
+        w.drain(bar(kBarQ), 0);
+        for (int v = issued - S > 0 ? issued - S : 0; v < issued; ++v) w.drain(bar(kBarFull + v % S), (v / S) & 1);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 5) {
+    // ------------------------------------------------ MMA issuer
+    const uint64_t desc_q = ptx::smem_desc_sw128(sbase, 16, 1024);
+    const uint64_t desc_do = ptx::smem_desc_sw128(sbase + C::kTileBytes, 16, 1024);
+    const uint64_t desc_ring_k = ptx::smem_desc_sw128(sbase + C::kQOffRing, 16, 1024);
+    const uint64_t desc_ring_n = ptx::smem_desc_sw128(sbase + C::kQOffRing, C::kChunkBytes, 1024);
+    constexpr uint64_t kTileStep = C::kTileBytes >> 4;
+    const uint32_t t_s = tmem + C::kColS, t_dp = tmem + C::kColDP, t_dq = tmem + C::kColAcc0;
+    bool ok = __all_sync(0xffffffffu, w.wait(bar(kBarQ), 0));
+    ptx::tc_fence_after();
+    for (int j = 0; ok && j <= n_kv; ++j) {
+      if (j >= 1) {
+        // dQ += dS K_{j-1}: dS from tensor memory, K (N-contiguous) from the ring
+        const int uk = 2 * (j - 1);
+        ok = __all_sync(0xffffffffu, w.wait(bar(kBarP), (j - 1) & 1));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) {
+          bwd_mma_tn<D>(t_dq, t_s, desc_ring_n + (uk % S) * kTileStep, j > 1);
+          ptx::tc_commit(bar(kBarEmpty + uk % S));        // K_{j-1}
+          ptx::tc_commit(bar(kBarEmpty + (uk + 1) % S));  // V_{j-1}
+          if (j == n_kv) ptx::tc_commit(bar(kBarFinal));
+        }
+        __syncwarp();
+      }
+      if (j < n_kv) {
+        const int uk = 2 * j, uv = uk + 1;
+        ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + uk % S), (uk / S) & 1));
+        if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + uv % S), (uv / S) & 1));
+        if (!ok) break;
+        ptx::tc_fence_after();
+        if (ptx::elect_one()) {
+          bwd_mma_nt<D>(t_s, desc_q, desc_ring_k + (uk % S) * kTileStep);    // S = Q K^T
+          bwd_mma_nt<D>(t_dp, desc_do, desc_ring_k + (uv % S) * kTileStep);  // dP = dO V^T
+          ptx::tc_commit(bar(kBarS));
+        }
+        __syncwarp();
+      }
+    }
+    if (ptx::elect_one()) ptx::tc_commit(bar(kBarDrain));
+    __syncwarp();
+    w.drain(bar(kBarDrain), 0);
+    __syncwarp();
+  } else {
+    // ------------------------------------------------ compute: thread = query row
+    const int row = warp * 32 + lane;
+    const int qrow = qt * 128 + row;
+    const bool row_valid = qrow < p.R;
+    const int qpos = qrow % p.N;
+    const size_t g = static_cast<size_t>(bh) * p.R + (row_valid ? qrow : 0);
+    const float neg = row_valid ? -p.lse[g] * 1.4426950408889634f : 0.f;  // -LSE in log2 units
+    const float drow = row_valid ? p.dvec[g] : 0.f;
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + C::kColS, t_dp = tmem + lane_off + C::kColDP;
+    const float c2 = p.scale_log2;
+    bool ok = true;
+    for (int j = 0; ok && j < n_kv; ++j) {
+      ok = __all_sync(0xffffffffu, w.wait(bar(kBarS), j & 1));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      int lim = p.N - j * 128;  // keys past the end, and after the query when causal
+      if (p.causal && qpos - j * 128 + 1 < lim) lim = qpos - j * 128 + 1;
+      if (!row_valid) lim = 0;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t rs[32], rd[32];
+        ptx::tmem_ld32(t_s + cc * 32, rs);
+        ptx::tmem_ld32(t_dp + cc * 32, rd);
+        uint32_t pd[16];
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+          float dsv[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = cc * 32 + i + h;
+            const float e = ptx::ex2_approx(fmaf(__uint_as_float(rs[i + h]), c2, neg));
+            const float pv = col < lim ? e : 0.f;
+            dsv[h] = pv * (__uint_as_float(rd[i + h]) - drow);
+          }
+          pd[i / 2] = ptx::pack_bf16x2(dsv[0], dsv[1]);
+        }
+        ptx::tmem_st16(t_s + cc * 16, pd);  // dS over columns already read
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(kBarP));
+    }
+    if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFinal), 0));
+    if (ok && n_kv > 0) {
+      ptx::tc_fence_after();
+      bwd_acc_to_smem<D>(tmem + lane_off + C::kColAcc0, sbase, row, p.scale);  // into Q's buffer
+      ptx::fence_proxy_async_smem();
+    }
+    ptx::named_barrier(1, 128);
+    if (ok && n_kv > 0 && row == 0) {
+      for (int c = 0; c < C::kChunks; ++c) ptx::tma_store_3d(&tm_dq, sbase + c * C::kChunkBytes, c * 64, qt * 128, bh);
+      ptx::bulk_commit();
+      ptx::bulk_wait_all();
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 512);
+  }
+}
+

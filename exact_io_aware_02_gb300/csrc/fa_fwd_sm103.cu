@@ -570,6 +570,8 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) lse[row] = tot > 0.f ? m + logf(tot) : -INFINITY;
 }
 
+#include "fa_bwd_sm103.cuh"
+
 // ==================================================================== host side
 namespace {
 
@@ -628,7 +630,15 @@ int prepare_device() {
   if (cudaFuncSetAttribute(fa_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<64>::kSmemBytes) != cudaSuccess ||
       cudaFuncSetAttribute(fa_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<128>::kSmemBytes) != cudaSuccess)
+                           Cfg<128>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(fa_bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           BwdCfg<64>::kSmemKV) != cudaSuccess ||
+      cudaFuncSetAttribute(fa_bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           BwdCfg<128>::kSmemKV) != cudaSuccess ||
+      cudaFuncSetAttribute(fa_bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           BwdCfg<64>::kSmemQ) != cudaSuccess ||
+      cudaFuncSetAttribute(fa_bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           BwdCfg<128>::kSmemQ) != cudaSuccess)
     return FA_ERR_CUDA;
   g_dev_state[dev] = 1;
   return FA_OK;
@@ -759,6 +769,101 @@ Problem mha(const void* q, const void* k, const void* v, void* o, float* lse, in
   return Problem{q, k, v, o, lse, B, H, H, N, N, d, scale, causal, 1, nullptr, 0};
 }
 
+// ---- backward
+struct BwdProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;
+  int B, Hq, Hkv, N, d;
+  float scale;
+  int causal;
+};
+
+int validate_bwd(const BwdProblem& pr) {
+  const void* in[6] = {pr.q, pr.k, pr.v, pr.o, pr.lse, pr.dout};
+  const void* out[4] = {pr.dq, pr.dk, pr.dv, pr.delta};
+  for (const void* ptr : in)
+    if (!ptr || (reinterpret_cast<uintptr_t>(ptr) & 15u)) return FA_ERR_ARG;
+  for (const void* ptr : out)
+    if (!ptr || (reinterpret_cast<uintptr_t>(ptr) & 15u)) return FA_ERR_ARG;
+  if (pr.B < 1 || pr.Hq < 1 || pr.Hkv < 1 || pr.N < 1 || (pr.d != 64 && pr.d != 128)) return FA_ERR_ARG;
+  if (pr.Hq % pr.Hkv != 0) return FA_ERR_ARG;
+  if (!(pr.scale > 0.f) || !std::isfinite(pr.scale)) return FA_ERR_ARG;
+  const long long q_rows = static_cast<long long>(pr.B) * pr.Hq * pr.N;
+  const long long kv_rows = static_cast<long long>(pr.B) * pr.Hkv * pr.N;
+  if (q_rows > 2147483647LL) return FA_ERR_ARG;
+  const size_t qb = static_cast<size_t>(q_rows) * pr.d * 2, kb = static_cast<size_t>(kv_rows) * pr.d * 2;
+  const size_t lb = static_cast<size_t>(q_rows) * 4;
+  const size_t in_n[6] = {qb, kb, kb, qb, lb, qb};
+  const size_t out_n[4] = {qb, kb, kb, lb};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 6; ++j)
+      if (overlaps(out[i], out_n[i], in[j], in_n[j])) return FA_ERR_ARG;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlaps(out[i], out_n[i], out[j], out_n[j])) return FA_ERR_ARG;
+  }
+  for (const void* ptr : in)
+    if (!is_device_pointer(ptr)) return FA_ERR_ARG;
+  for (const void* ptr : out)
+    if (!is_device_pointer(ptr)) return FA_ERR_ARG;
+  return FA_OK;
+}
+
+template <int D>
+int launch_bwd(const BwdProblem& pr, unsigned long long timeout_ns, cudaStream_t stream) {
+  const int G = pr.Hq / pr.Hkv;
+  const int groups = pr.B * pr.Hkv;
+  const int R = G * pr.N;
+  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
+  if (!encode_map(&mq, pr.q, groups, R, D) || !encode_map(&mk, pr.k, groups, pr.N, D) ||
+      !encode_map(&mv, pr.v, groups, pr.N, D) || !encode_map(&mdo, pr.dout, groups, R, D) ||
+      !encode_map(&mdq, pr.dq, groups, R, D) || !encode_map(&mdk, pr.dk, groups, pr.N, D) ||
+      !encode_map(&mdv, pr.dv, groups, pr.N, D))
+    return FA_ERR_LAUNCH;
+  BwdParams p{};
+  p.lse = pr.lse;
+  p.dvec = pr.delta;
+  p.groups = groups;
+  p.R = R;
+  p.N = pr.N;
+  p.n_qtiles = (R + 127) / 128;
+  p.n_ktiles = (pr.N + 127) / 128;
+  p.scale = pr.scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(pr.scale) * 1.4426950408889634);
+  p.causal = pr.causal ? 1 : 0;
+  p.timeout_ns = timeout_ns;
+  const long long rows = static_cast<long long>(groups) * R;
+  const long long prep_blocks = (rows * 32 + 255) / 256;
+  const long long grid_kv = static_cast<long long>(groups) * p.n_ktiles;
+  const long long grid_q = static_cast<long long>(groups) * p.n_qtiles;
+  if (prep_blocks > 2147483647LL || grid_kv > 2147483647LL || grid_q > 2147483647LL) return FA_ERR_ARG;
+  fa_bwd_prep_kernel<D><<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(pr.o), static_cast<const uint16_t*>(pr.dout), pr.delta, static_cast<int>(rows));
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  fa_bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid_kv), kBwdThreads, BwdCfg<D>::kSmemKV, stream>>>(
+      mq, mk, mv, mdo, mdk, mdv, p);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  fa_bwd_dq_kernel<D><<<static_cast<unsigned>(grid_q), kBwdThreads, BwdCfg<D>::kSmemQ, stream>>>(
+      mq, mk, mv, mdo, mdq, p);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  return FA_OK;
+}
+
+int run_bwd(const BwdProblem& pr, unsigned long long timeout_ns, cudaStream_t stream) {
+  int rc = validate_bwd(pr);
+  if (rc != FA_OK) return rc;
+  rc = prepare_device();
+  if (rc != FA_OK) return rc;
+  return pr.d == 64 ? launch_bwd<64>(pr, timeout_ns, stream) : launch_bwd<128>(pr, timeout_ns, stream);
+}
+
 // ---- fixed device workspace for callers that cannot allocate (fa_fwd_gqa_static_workspace)
 // One array per device that loads this library, held until the process exits.  Host code
 // must not use the symbol itself as an address: it is a host-side stand-in.  The device
@@ -833,6 +938,13 @@ int fa_fwd_withheld_tile(const void* q, const void* k, const void* v, void* o, f
                  static_cast<unsigned long long>(wait_timeout_ms * 1e6), stream);
 }
 
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+           void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv, int N, int d, float scale,
+           int causal, cudaStream_t stream) {
+  const fa::BwdProblem pr{q, k, v, o, lse, dout, dq, dk, dv, delta, B, Hq, Hkv, N, d, scale, causal};
+  return fa::run_bwd(pr, fa::kDefaultTimeoutNs, stream);
+}
+
 int fa_status(int clear, cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
   unsigned int word = 0;
@@ -857,6 +969,6 @@ const char* fa_strerror(int code) {
   }
 }
 
-int fa_version(void) { return 2; }
+int fa_version(void) { return 3; }
 
 }  // extern "C"

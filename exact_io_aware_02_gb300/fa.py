@@ -26,7 +26,7 @@ FA_STATIC_WORKSPACE_BYTES = 16 << 20
 FA_STATUS_TIMEOUT = 0x1
 
 EXPORTED = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_gqa_workspace_bytes", "fa_fwd_gqa_static_workspace",
-            "fa_status", "fa_fwd_withheld_tile", "fa_strerror", "fa_version")
+            "fa_bwd", "fa_status", "fa_fwd_withheld_tile", "fa_strerror", "fa_version")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
@@ -44,6 +44,8 @@ lib.fa_fwd_gqa_static_workspace.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i,
 lib.fa_fwd_gqa_static_workspace.restype = _i
 lib.fa_fwd_withheld_tile.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _d, _vp]
 lib.fa_fwd_withheld_tile.restype = _i
+lib.fa_bwd.argtypes = [_vp] * 10 + [_i, _i, _i, _i, _i, _f, _i, _vp]
+lib.fa_bwd.restype = _i
 lib.fa_status.argtypes = [_i, _vp]
 lib.fa_status.restype = _i
 lib.fa_strerror.argtypes = [_i]
@@ -147,6 +149,31 @@ def fa_fwd_gqa_static_workspace(q, k, v, o=None, lse=None, scale=None, causal=Fa
     if rc != FA_OK:
         raise FAError(rc)
     return o, lse
+
+
+def fa_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, delta=None, scale=None,
+           causal=False, stream=None):
+    """Attention backward with recomputation from the forward's (o, lse).
+    q, o, dout: CUDA bf16 [B, Hq, N, d]; k, v: [B, Hkv, N, d]; lse: fp32 [B, Hq, N].
+    Returns (dq, dk, dv, delta); delta = rowsum(dout * o) in fp32.  Preallocated
+    outputs are written in place.  Raises FAError on a nonzero return code."""
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape or o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("q, o, dout must be [B, Hq, N, d] and k, v [B, Hkv, N, d]")
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    if delta is None:
+        delta = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    rc = lib.fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                    dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(),
+                    B, Hq, Hkv, N, d, float(scale), int(bool(causal)), _stream_handle(stream, q.device))
+    if rc != FA_OK:
+        raise FAError(rc)
+    return dq, dk, dv, delta
 
 
 def fa_fwd_withheld_tile(q, k, v, o=None, lse=None, scale=None, causal=False,

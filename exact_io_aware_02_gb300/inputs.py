@@ -100,6 +100,13 @@ def make_qkv_gqa(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int, seed: int,
     return q, k, v
 
 
+def make_dout(shape, seed: int, std: float = 1.0):
+    """The upstream gradient dO for the backward: CPU bf16 normals times ``std``,
+    drawn from its own Generator(seed)."""
+    g = torch.Generator().manual_seed(int(seed))
+    return (torch.randn(tuple(shape), generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
+
+
 def make_workload(w: Workload):
     if w.Hkv is None and w.Nk is None:
         return make_qkv(w.B, w.H, w.N, w.d, w.seed, w.qk_std, w.v_std)

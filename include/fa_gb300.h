@@ -150,6 +150,37 @@ int fa_fwd_gqa_static_workspace(const void* q, const void* k, const void* v, voi
                                 int causal, int n_splits, cudaStream_t stream);
 
 /*
+ * fa_bwd -- exact attention backward: dQ, dK, dV from the forward's O and LSE.
+ *
+ * The forward saves only O and the per-row LSE; this call rebuilds S = scale*Q K^T
+ * and P = exp(S - LSE) on chip, tile by tile, instead of reading an N x N matrix
+ * (§6 "Recomputation" of the zzszmyf.github.io notes "FlashAttention 原理是什么？
+ * 为什么又省显存又快"; the backward item of the aiqz.cc article's 工程实现细节
+ * section).  With D = rowsum(dO * O) it computes
+ *     dV = P^T dO,  dP = dO V^T,  dS = P * (dP - D),  dQ = scale dS K,  dK = scale dS^T Q,
+ * summing dK and dV over the G = Hq / Hkv query heads that share a K/V head.
+ *
+ * q, o, dout : device, bf16, contiguous [B, Hq, N, d].  Read only.
+ * k, v       : device, bf16, contiguous [B, Hkv, N, d].  Read only.
+ * lse        : device, fp32, [B, Hq, N] -- the forward's LSE (natural log).  Read only.
+ * dq         : device, bf16, [B, Hq, N, d].  Written.
+ * dk, dv     : device, bf16, [B, Hkv, N, d].  Written.
+ * delta      : device, fp32, [B, Hq, N].  Written with D = rowsum(dO * O) (fp32 sum of
+ *              bf16 products); the call's scratch, left holding D on return.
+ * Every pointer is 16-byte aligned; no output overlaps an input or another output.
+ * B, Hq, Hkv, N >= 1 with Hq % Hkv == 0 (queries and keys have the same length N);
+ * d is 64 or 128; scale finite and > 0; causal: nonzero = query i sees keys 0..i.
+ * B*Hq*N <= 2^31 - 1.  Three kernels are enqueued on `stream` (D, then dK/dV, then
+ * dQ); the call returns once they are enqueued.  On an error return nothing was
+ * enqueued.  A device-side wait that gives up sets FA_STATUS_TIMEOUT (fa_status).
+ *
+ * Returns FA_OK, FA_ERR_ARG, FA_ERR_ARCH or FA_ERR_LAUNCH.
+ */
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+           const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv,
+           int N, int d, float scale, int causal, cudaStream_t stream);
+
+/*
  * fa_status -- read the device status word of the current device.
  *
  * Synchronises `stream` first, then copies the word to the host.  If `clear`
@@ -176,7 +207,7 @@ int fa_fwd_withheld_tile(const void* q, const void* k, const void* v, void* o, f
 /* fa_strerror -- a static, human-readable string for a return code. */
 const char* fa_strerror(int code);
 
-/* fa_version -- the library's interface version (currently 2). */
+/* fa_version -- the library's interface version (currently 3). */
 int fa_version(void);
 
 #ifdef __cplusplus

@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(fa):
 
 
 def test_strerror_and_version(fa):
-    assert fa.fa_version() == 2
+    assert fa.fa_version() == 3
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert fa.fa_strerror(code) and fa.fa_strerror(code) != "unknown error"
     assert fa.fa_strerror(-99) == "unknown error"
@@ -70,3 +70,24 @@ def test_withheld_tile_timeout_range(fa):
              0.088, 0, 0.5, None) == fa.FA_ERR_ARG
     assert f(FAKE, FAKE + 2**30, FAKE + 2**31, FAKE + 3 * 2**30, FAKE + 2**32, 1, 1, 128, 128,
              0.088, 0, 20000.0, None) == fa.FA_ERR_ARG
+
+
+def _bwd(fa, B=1, Hq=2, Hkv=1, N=128, d=128, scale=0.088, causal=1, **ptrs):
+    names = ("q", "k", "v", "o", "lse", "dout", "dq", "dk", "dv", "delta")
+    p = {n: FAKE + i * 2**30 for i, n in enumerate(names)}
+    p.update(ptrs)
+    return fa.lib.fa_bwd(*(p[n] for n in names), B, Hq, Hkv, N, d, scale, causal, None)
+
+
+@pytest.mark.parametrize("kw", [
+    {"q": 0}, {"lse": 0}, {"dout": 0}, {"dq": 0}, {"dk": 0}, {"dv": 0}, {"delta": 0},
+    {"d": 96}, {"d": 32}, {"B": 0}, {"N": 0}, {"Hq": 3, "Hkv": 2}, {"Hkv": 0},
+    {"scale": 0.0}, {"scale": float("nan")},
+    {"dq": FAKE + 6 * 2**30 + 8}, {"delta": FAKE + 9 * 2**30 + 4},
+    {"dq": FAKE},                       # dQ overlaps Q
+    {"dk": FAKE + 6 * 2**30 + 256},     # dK overlaps dQ
+    {"delta": FAKE + 4 * 2**30},        # D overlaps LSE
+    {"B": 65536, "Hq": 65536, "Hkv": 65536, "N": 2},
+])
+def test_bwd_argument_errors_before_launch(fa, kw):
+    assert _bwd(fa, **kw) == fa.FA_ERR_ARG

@@ -13,7 +13,8 @@ accumulation, D from the forward's bf16 O): errors are measured relative to the
 size of the gradient itself, max |d| <= 2e-2 * max |ref| and mean |d| <= 1e-2 *
 mean |ref|.  A replay of exactly that rounding in fp64 on the test shapes gives
 2.5e-3 to 5.3e-3 on both measures (the upper end with score std 3), so the bounds
-leave a factor of about 2 to 4.  D = rowsum(dO * O): |dD| <= 1e-2 * max(1, |D|).
+leave a factor of about 2 to 4.  D = rowsum(dO * O) is held to the same two
+relative bounds (its error comes from the bf16 rounding of O).
 """
 from __future__ import annotations
 
@@ -55,7 +56,6 @@ def compare(o_gpu, lse_gpu, o_ref, lse_ref) -> dict:
 
 GRAD_MAX_REL = 2e-2
 GRAD_MEAN_REL = 1e-2
-DELTA_REL = 1e-2
 
 
 def grad_compare(g_gpu, g_ref) -> dict:
@@ -74,12 +74,6 @@ def grad_compare(g_gpu, g_ref) -> dict:
 
 def grad_within_tolerance(st: dict) -> bool:
     return st["finite"] and st["max_rel"] <= GRAD_MAX_REL and st["mean_rel"] <= GRAD_MEAN_REL
-
-
-def delta_within_tolerance(d_gpu, d_ref) -> bool:
-    d_gpu = np.asarray(d_gpu, dtype=np.float64)
-    d_ref = np.asarray(d_ref, dtype=np.float64)
-    return bool(np.all(np.abs(d_gpu - d_ref) <= DELTA_REL * np.maximum(1.0, np.abs(d_ref))))
 
 
 def within_tolerance(st: dict) -> bool:

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from exact_io_aware_02_gb300.inputs import make_dout, make_qkv_gqa
-from tests.parity import (delta_within_tolerance, grad_compare, grad_within_tolerance)
+from tests.parity import grad_compare, grad_within_tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -66,9 +66,8 @@ def check(q, k, v, do, res, scale, causal, kv_heads=None):
     G = Hq // Hkv
     kv_heads = kv_heads or [(b, g) for b in range(B) for g in range(Hkv)]
     ref = oracle_grads(q, k, v, do, scale, causal, kv_heads)
-    got = {n: [] for n in ("dq", "dk", "dv")}
-    want = {n: [] for n in ("dq", "dk", "dv")}
-    delta_ok = True
+    got = {n: [] for n in ("dq", "dk", "dv", "delta")}
+    want = {n: [] for n in ("dq", "dk", "dv", "delta")}
     for (b, g), (rdq, rdk, rdv, rd) in ref.items():
         got["dq"].append(_np64(dq[b, g * G:(g + 1) * G]))
         want["dq"].append(rdq)
@@ -76,10 +75,14 @@ def check(q, k, v, do, res, scale, causal, kv_heads=None):
         want["dk"].append(rdk)
         got["dv"].append(_np64(dv[b, g]))
         want["dv"].append(rdv)
-        delta_ok &= delta_within_tolerance(_np64(delta[b, g * G:(g + 1) * G]), rd)
-    stats = {n: grad_compare(np.concatenate([x.ravel() for x in got[n]]),
-                             np.concatenate([x.ravel() for x in want[n]])) for n in got}
-    return stats, delta_ok
+        got["delta"].append(_np64(delta[b, g * G:(g + 1) * G]))
+        want["delta"].append(rd)
+    return {n: grad_compare(np.concatenate([x.ravel() for x in got[n]]),
+                            np.concatenate([x.ravel() for x in want[n]])) for n in got}
+
+
+def case_stats_line(stats):
+    return " ".join("{}:{:.2e}/{:.2e}".format(n, st["max_rel"], st["mean_rel"]) for n, st in stats.items())
 
 
 CASES = [  # B, Hq, Hkv, N, d, causal
@@ -102,8 +105,8 @@ def test_bwd_parity(fa, case):
     q, k, v = make_qkv_gqa(B, Hq, Hkv, N, N, d, seed=4100 + N + d)
     do = make_dout(q.shape, seed=4200 + N + d)
     scale = 1.0 / d ** 0.5
-    stats, delta_ok = check(q, k, v, do, run(fa, q, k, v, do, causal), scale, causal)
-    assert delta_ok
+    stats = check(q, k, v, do, run(fa, q, k, v, do, causal), scale, causal)
+    print(case_stats_line(stats))
     for name, st in stats.items():
         assert grad_within_tolerance(st), (name, st)
 
@@ -112,8 +115,8 @@ def test_bwd_wide_scores(fa):
     """Score std 3 (sharp rows): the case with the largest rounding error."""
     q, k, v = make_qkv_gqa(1, 2, 2, 512, 512, 128, seed=4301, qk_std=3.0)
     do = make_dout(q.shape, seed=4302)
-    stats, delta_ok = check(q, k, v, do, run(fa, q, k, v, do, False), 1 / 128 ** 0.5, False)
-    assert delta_ok
+    stats = check(q, k, v, do, run(fa, q, k, v, do, False), 1 / 128 ** 0.5, False)
+    print(case_stats_line(stats))
     for name, st in stats.items():
         assert grad_within_tolerance(st), (name, st)
 
@@ -122,8 +125,8 @@ def test_bwd_scale_argument(fa):
     """A scale other than 1/sqrt(d) is used in both S and the dQ, dK products."""
     q, k, v = make_qkv_gqa(1, 2, 2, 200, 200, 64, seed=4401)
     do = make_dout(q.shape, seed=4402)
-    stats, delta_ok = check(q, k, v, do, run(fa, q, k, v, do, True, scale=0.05), 0.05, True)
-    assert delta_ok
+    stats = check(q, k, v, do, run(fa, q, k, v, do, True, scale=0.05), 0.05, True)
+    print(case_stats_line(stats))
     for name, st in stats.items():
         assert grad_within_tolerance(st), (name, st)
 
@@ -143,8 +146,8 @@ def test_bwd_headline_shape_sampled(fa):
     q, k, v = make_qkv_gqa(B, H, H, N, N, d, seed=20263)
     do = make_dout(q.shape, seed=20363)
     res = run(fa, q, k, v, do, True)
-    stats, delta_ok = check(q, k, v, do, res, 1 / d ** 0.5, True, kv_heads=[(0, 3), (1, 14)])
-    assert delta_ok
+    stats = check(q, k, v, do, res, 1 / d ** 0.5, True, kv_heads=[(0, 3), (1, 14)])
+    print(case_stats_line(stats))
     for name, st in stats.items():
         assert grad_within_tolerance(st), (name, st)
     assert fa.fa_status(clear=False) == 0
@@ -171,6 +174,6 @@ def test_bwd_argument_errors_on_device(fa):
     with pytest.raises(fa.FAError):
         fa.fa_bwd(q, k, v, o, lse, do, dq=dq, dk=do)     # dK aliases dO
     with pytest.raises(fa.FAError):
-        fa.fa_bwd(q.cpu(), k, v, o, lse, do, dq=dq)      # host pointer
+        fa.fa_bwd(q.cpu(), k, v, o, lse, do, dq=dq, stream=torch.cuda.current_stream())  # host pointer
     torch.cuda.synchronize()
     assert bool((dq == 7.0).all())

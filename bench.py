@@ -7,6 +7,10 @@ tile), inputs resident in HBM.  The default workload is the causal
 B=2 H=16 N=8192 d=128 forward; the metric is forward TFLOP/s with
 4*B*H*N^2*d flops, halved for causal.  Prints one JSON line (rank 0).
 
+Other workloads (--workload): grouped K/V prefill, split-K/V decoding (reported
+as HBM GB/s), and the backward of the causal prefill shape (one step = one
+fa_bwd call from the forward's O and LSE; 10*B*H*N^2*d flops, halved for causal).
+
 --impl reference times the fp64 CPU oracle on the host cores instead (each
 step: one 128-row query tile of one (b, h) slice of the same workload).
 """
@@ -29,13 +33,13 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from exact_io_aware_02_gb300.inputs import HEADLINE, WORKLOADS, make_workload  # noqa: E402
+from exact_io_aware_02_gb300.inputs import HEADLINE, WORKLOADS, make_workload, make_workload_dout  # noqa: E402
 
 METRIC = "fwd attention TFLOP/s & % of GB300 bf16 tensor peak (B=2 H=16 N=8K d=128 causal)"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
 KERNEL_FILES = [os.path.join(ROOT, "exact_io_aware_02_gb300", "csrc", f)
-                for f in ("fa_fwd_sm103.cu", "sm103_ptx.cuh")]
+                for f in ("fa_fwd_sm103.cu", "fa_bwd_sm103.cuh", "sm103_ptx.cuh")]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
@@ -99,11 +103,19 @@ def metric_for(w):
     memory-bound decoding workload (K and V are read once)."""
     if w.bound == "hbm":
         return f"decode attention GB/s of algorithmic HBM traffic ({w.name})", "GB/s"
+    if w.direction == "bwd":
+        return f"bwd attention TFLOP/s, 10*N^2*d per head, halved for causal ({w.name})", UNIT
     return METRIC if w.name == HEADLINE else f"fwd attention TFLOP/s ({w.name})", UNIT
 
 
 def units_per_step(w):
     return w.algorithmic_bytes() / 1e9 if w.bound == "hbm" else w.flops() / 1e12
+
+
+def backward_call(fa, w):
+    """One backward step through the public API: fa_bwd from the forward's O and LSE."""
+    return lambda q, k, v, o, lse, do, grads, stream: fa.fa_bwd(
+        q, k, v, o, lse, do, *grads, scale=w.scale, causal=w.causal, stream=stream)
 
 
 def forward_call(fa, w):
@@ -197,6 +209,7 @@ def cpu_baseline(w, budget_s=12.0, max_slices=32):
     from exact_io_aware_02_gb300.inputs import sample_slices
 
     q, k, v = make_workload(w)
+    do = make_workload_dout(w) if w.direction == "bwd" else None
     G = w.H // w.hkv
     slices = sample_slices(w.B, w.H, max_slices, w.seed + 3)
     per_slice = units_per_step(w) / (w.B * w.H)
@@ -205,7 +218,10 @@ def cpu_baseline(w, budget_s=12.0, max_slices=32):
         qa = q[b, h].to(torch.float64).numpy()
         ka, va = (t[b, h // G].to(torch.float64).numpy() for t in (k, v))
         t0 = time.perf_counter()
-        oracle.naive_attention(qa, ka, va, w.scale, w.causal, q_offset=w.nk - w.N)
+        if do is not None:
+            oracle.attention_backward(qa, ka, va, do[b, h].to(torch.float64).numpy(), w.scale, w.causal)
+        else:
+            oracle.naive_attention(qa, ka, va, w.scale, w.causal, q_offset=w.nk - w.N)
         t_total += time.perf_counter() - t0
         done += 1
         if t_total >= budget_s:
@@ -213,7 +229,8 @@ def cpu_baseline(w, budget_s=12.0, max_slices=32):
     del np
     return {"value": done * per_slice / t_total, "unit": metric_for(w)[1],
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"{done} whole (b,h) query-head slice(s) of {w.name} (N={w.N}, d={w.d}), fp64 NumPy, "
+            "sample": f"{done} whole (b,h) query-head slice(s) of {w.name} (N={w.N}, d={w.d}, {w.direction}), "
+                      f"fp64 NumPy, "
                       f"{t_total:.1f} s; threads = NumPy BLAS default on the listed cores"}
 
 
@@ -225,9 +242,11 @@ def run_reference(args, w, rank, world):
     import oracle
 
     q, k, v = make_workload(w)
+    do = make_workload_dout(w) if w.direction == "bwd" else None
     G = w.H // w.hkv
     q_offset = w.nk - w.N
     n_tiles = (w.N + 127) // 128
+    per_pair = 10.0 if do is not None else 4.0
     total_units, total_t = 0.0, 0.0
 
     def step(s, timed):
@@ -239,14 +258,19 @@ def run_reference(args, w, rank, world):
         qa = q[b, h].to(torch.float64).numpy()
         ka, va = (t[b, h // G].to(torch.float64).numpy() for t in (k, v))
         t0 = time.perf_counter()
-        oracle.naive_attention(qa, ka, va, w.scale, w.causal, rows=rows, q_offset=q_offset)
+        if do is not None:  # this tile's rows: dQ, and their share of dK and dV
+            oracle.attention_backward(qa[rows[0]:rows[-1] + 1], ka, va,
+                                      do[b, h, rows[0]:rows[-1] + 1].to(torch.float64).numpy(),
+                                      w.scale, w.causal, q_offset=q_offset + rows[0])
+        else:
+            oracle.naive_attention(qa, ka, va, w.scale, w.causal, rows=rows, q_offset=q_offset)
         dt = time.perf_counter() - t0
         if timed:
             if w.bound == "hbm":
                 total_units += len(rows) / (w.B * w.H * w.N) * w.algorithmic_bytes() / 1e9
             else:
                 keys = [min(w.nk, q_offset + i + 1) if w.causal else w.nk for i in rows]
-                total_units += sum(4.0 * kk * w.d for kk in keys) / 1e12
+                total_units += sum(per_pair * kk * w.d for kk in keys) / 1e12
             total_t += dt
 
     for s in range(args.warmup):
@@ -262,7 +286,7 @@ def run_reference(args, w, rank, world):
             "data": "synthetic", "config": workload_config(w, "n/a (CPU)"),
             "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                              "sample": f"{args.steps} steps of one 128-row query tile of one query head "
-                                       f"each, fp64 NumPy"},
+                                       f"each ({w.direction}), fp64 NumPy"},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
     print(json.dumps(line), flush=True)
@@ -280,14 +304,30 @@ def run_ours(args, w, rank, world, local_rank):
     lse = torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)
     ws_bytes = fa.fa_fwd_gqa_workspace_bytes(w.B, w.H, w.N, w.d, w.n_splits)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev) if ws_bytes else None
-    step = forward_call(fa, w)
-    launches_per_step = 2 if w.n_splits > 1 else 1
+    fwd = forward_call(fa, w)
+    if w.direction == "bwd":
+        # the backward's inputs: the forward's O and LSE (computed once, untimed) and dO
+        fwd(q, k, v, o, lse, ws, stream)
+        doh = make_workload_dout(w).pin_memory()
+        do = doh.to(dev, non_blocking=True)
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v),
+                 torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev))
+        bwd = backward_call(fa, w)
+        step = lambda: bwd(q, k, v, o, lse, do, grads, stream)  # noqa: E731
+        launches_per_step = 3
+        inputs = ((q, qh), (k, kh), (v, vh), (o, o.cpu().pin_memory()), (lse, lse.cpu().pin_memory()), (do, doh))
+        outputs = grads[:3]
+    else:
+        step = lambda: fwd(q, k, v, o, lse, ws, stream)  # noqa: E731
+        launches_per_step = 2 if w.n_splits > 1 else 1
+        inputs = ((q, qh), (k, kh), (v, vh))
+        outputs = (o, lse)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     torch.cuda.synchronize()
 
     for _ in range(args.warmup):
         flush.zero_()
-        step(q, k, v, o, lse, ws, stream)
+        step()
     torch.cuda.synchronize()
     if fa.fa_status(clear=True) != 0:
         raise RuntimeError("device status word set during warm-up")
@@ -305,7 +345,7 @@ def run_ours(args, w, rank, world, local_rank):
     for i in range(args.steps):
         flush.zero_()  # write a buffer larger than L2 between timed launches
         starts[i].record(stream)
-        step(q, k, v, o, lse, ws, stream)
+        step()
         ends[i].record(stream)
         launches += launches_per_step
     torch.cuda.synchronize()
@@ -318,19 +358,18 @@ def run_ours(args, w, rank, world, local_rank):
     if fa.fa_status(clear=True) != 0:
         raise RuntimeError("device status word set during the timed region")
 
-    # end to end through the public API: pinned host -> device, forward, device -> host
-    o_h = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    lse_h = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    # end to end through the public API: pinned host -> device, the step, device -> host
+    outputs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outputs]
     e2e_steps = max(1, min(args.steps, 10))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(e2e_steps + 1):
         if i == 1:
             e0.record(stream)
-        for dst, src in ((q, qh), (k, kh), (v, vh)):
+        for dst, src in inputs:
             dst.copy_(src, non_blocking=True)
-        step(q, k, v, o, lse, ws, stream)
-        o_h.copy_(o, non_blocking=True)
-        lse_h.copy_(lse, non_blocking=True)
+        step()
+        for dst, src in zip(outputs_h, outputs):
+            dst.copy_(src, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(e0.elapsed_time(e1) / e2e_steps, world, dev)
@@ -351,7 +390,9 @@ def run_ours(args, w, rank, world, local_rank):
         achieved = flops / (ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                     "frac": achieved / peak_tf, "traffic": measured_traffic(w.name),
-                    "peak_kind": f"bf16 dense burst, {peak_kind}",
+                    "peak_kind": f"bf16 dense burst, {peak_kind}"
+                                 + ("; timed over the step's three launches (D, dK/dV, dQ)"
+                                    if w.direction == "bwd" else ""),
                     "algorithmic_flops": flops, "algorithmic_bytes": w.algorithmic_bytes()}
     line = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
@@ -361,8 +402,8 @@ def run_ours(args, w, rank, world, local_rank):
                                      "per-launch CUDA events on the launch stream"),
         "roofline": roofline,
         "e2e": {"value": job_rate(units, e2e_ms, world), "unit": unit,
-                "h2d_bytes_per_step": 3 * q.numel() * q.element_size(),
-                "d2h_bytes_per_step": o.numel() * o.element_size() + lse.numel() * lse.element_size()},
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t, _ in inputs),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in outputs)},
         "gpu_launches": launches,
         "clocks": clocks,
         "kernel_ms": {"min": min(kernel_ms), "median": statistics.median(kernel_ms), "max": max(kernel_ms)},

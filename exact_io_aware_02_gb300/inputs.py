@@ -6,8 +6,8 @@ are drawn in that order from one ``torch.Generator`` as float32 normals times
 a standard deviation, then rounded to bf16 (round-to-nearest-even); the bf16
 values convert to float64 exactly on the oracle side.
 
-The workloads are the five shapes the attention forward is measured and
-checked on; each is named by what it is.
+The workloads are the shapes the attention forward and backward are measured
+and checked on; each is named by what it is.
 """
 from __future__ import annotations
 
@@ -33,6 +33,7 @@ class Workload:
     Nk: int | None = None
     n_splits: int = 1
     bound: str = "tensor"   # the roofline that bounds it: "tensor" or "hbm"
+    direction: str = "fwd"  # "fwd": O and LSE; "bwd": dQ, dK, dV from O, LSE and dO
 
     @property
     def hkv(self) -> int:
@@ -47,16 +48,22 @@ class Workload:
         return 1.0 / (self.d ** 0.5)
 
     def flops(self) -> float:
-        """4*B*H*Nq*Nk*d (two multiply-adds per query-key pair per dimension); the
-        square causal case counts half."""
-        f = 4.0 * self.B * self.H * self.N * self.nk * self.d
+        """Forward: 4*B*H*Nq*Nk*d (two products, QK^T and PV, of 2*Nq*Nk*d each).
+        Backward: 10*B*H*Nq*Nk*d (five products: dV, dP, dQ, dK and the recomputed
+        QK^T).  The square causal case counts half."""
+        per_pair = 10.0 if self.direction == "bwd" else 4.0
+        f = per_pair * self.B * self.H * self.N * self.nk * self.d
         return f / 2.0 if (self.causal and self.N == self.nk) else f
 
     def algorithmic_bytes(self) -> int:
-        """Q, K, V read once and O written once (bf16), LSE written once (fp32)."""
-        q_o = 2 * self.B * self.H * self.N * self.d * 2
-        kv = 2 * self.B * self.hkv * self.nk * self.d * 2
-        return q_o + kv + self.B * self.H * self.N * 4
+        """Forward: Q, K, V read once and O written once (bf16), LSE written once (fp32).
+        Backward: Q, K, V, O, dO read and dQ, dK, dV written once (bf16), LSE read and
+        D written once (fp32)."""
+        q_rows = self.B * self.H * self.N
+        kv_rows = self.B * self.hkv * self.nk
+        if self.direction == "bwd":
+            return (4 * q_rows + 4 * kv_rows) * self.d * 2 + 2 * q_rows * 4
+        return (2 * q_rows + 2 * kv_rows) * self.d * 2 + q_rows * 4
 
 
 WORKLOADS = {
@@ -73,6 +80,8 @@ WORKLOADS = {
         # per K/V head, the keys split 16 ways (memory-bound: reads K and V once)
         Workload("gqa_decode_nk32768_d128", 8, 32, 1, 128, False, seed=20267, Hkv=8,
                  Nk=32768, n_splits=16, bound="hbm"),
+        # the backward of the causal prefill shape: dQ, dK, dV with recomputation
+        Workload("bwd_causal_n8192_d128", 2, 16, 8192, 128, True, seed=20263, direction="bwd"),
     )
 }
 
@@ -105,6 +114,11 @@ def make_dout(shape, seed: int, std: float = 1.0):
     drawn from its own Generator(seed)."""
     g = torch.Generator().manual_seed(int(seed))
     return (torch.randn(tuple(shape), generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
+
+
+def make_workload_dout(w: Workload):
+    """dO of a backward workload: [B, H, N, d], seed = the workload's seed + 100."""
+    return make_dout((w.B, w.H, w.N, w.d), seed=w.seed + 100)
 
 
 def make_workload(w: Workload):

@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from exact_io_aware_02_gb300.inputs import make_dout, make_qkv_gqa
+from exact_io_aware_02_gb300.inputs import WORKLOADS, make_dout, make_qkv_gqa, make_workload, make_workload_dout
 from tests.parity import grad_compare, grad_within_tolerance
 
 pytestmark = pytest.mark.gpu
@@ -140,13 +140,14 @@ def test_bwd_zero_upstream_gradient(fa):
         assert bool((t == 0).all())
 
 
-def test_bwd_headline_shape_sampled(fa):
-    """The bench's launch (B=2, H=16, N=8192, d=128, causal); two heads checked in full."""
-    B, H, N, d = 2, 16, 8192, 128
-    q, k, v = make_qkv_gqa(B, H, H, N, N, d, seed=20263)
-    do = make_dout(q.shape, seed=20363)
-    res = run(fa, q, k, v, do, True)
-    stats = check(q, k, v, do, res, 1 / d ** 0.5, True, kv_heads=[(0, 3), (1, 14)])
+def test_bwd_workload_full_size_sampled(fa):
+    """The bench's backward launch (B=2, H=16, N=8192, d=128, causal) on its own
+    inputs; two heads checked in full."""
+    w = WORKLOADS["bwd_causal_n8192_d128"]
+    q, k, v = make_workload(w)
+    do = make_workload_dout(w)
+    res = run(fa, q, k, v, do, w.causal)
+    stats = check(q, k, v, do, res, w.scale, w.causal, kv_heads=[(0, 3), (1, 14)])
     print(case_stats_line(stats))
     for name, st in stats.items():
         assert grad_within_tolerance(st), (name, st)

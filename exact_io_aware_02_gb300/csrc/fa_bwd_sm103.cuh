@@ -19,14 +19,19 @@
 // Splitting dQ from dK/dV costs two extra products per tile pair (7 instead of 5) but
 // needs no atomics and keeps every accumulator in tensor memory.
 //
-// Both main kernels: warps 0-3 compute (one TMEM lane = one row per thread), warp 4 is
-// the TMA producer, warp 5 allocates tensor memory and issues the MMAs (converged warp,
-// elect.sync).  Every mbarrier wait is bounded, as in the forward.
+// Both main kernels: warps 0-7 compute -- warp w reads TMEM lane quarter w % 4 (one row
+// per thread) and column half w / 4, so two warps share each SM sub-partition; warp 8
+// is the TMA producer; warp 9 allocates tensor memory and issues the MMAs (converged
+// warp, elect.sync).  The bf16 P and dS each warp produces are packed into the first
+// half of the fp32 columns that warp itself has read, so no warp overwrites columns
+// another warp still has to read; the MMAs that consume them address the two packed
+// halves separately.  Every mbarrier wait is bounded, as in the forward.
 #pragma once
 
 // (included inside namespace fa)
 
-constexpr int kBwdThreads = 192;
+constexpr int kBwdThreads = 320;
+constexpr int kBwdComputeWarps = 8;
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
 template <int D>
@@ -79,19 +84,14 @@ __device__ __forceinline__ int bwd_tile_max_pos(const BwdParams& p, int qt) {
   const int r1 = min(r0 + 127, p.R - 1);
   return (r1 / p.N != r0 / p.N) ? p.N - 1 : r1 % p.N;
 }
-__device__ __forceinline__ int bwd_tile_min_pos(const BwdParams& p, int qt) {
-  const int r0 = qt * 128;
-  const int r1 = min(r0 + 127, p.R - 1);
-  return (r1 / p.N != r0 / p.N) ? 0 : r0 % p.N;
-}
 
 template <int D>
 struct BwdCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kChunkBytes = 128 * 128;
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kVecBytes = 2 * 128 * 4;     // LSE and D of one query tile
-  // dK/dV kernel: K, V resident; a ring of stages {Q_i, dO_i, LSE_i, D_i}
+  static constexpr int kVecBytes = 2 * 128 * 4;     // -LSE*log2(e) and D of one query tile
+  // dK/dV kernel: K, V resident; a ring of stages {Q_i, dO_i, -LSE_i log2 e, D_i}
   static constexpr int kStages = D == 128 ? 2 : 4;
   static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;
   static constexpr int kKVOffStage = 2 * kTileBytes;
@@ -119,22 +119,25 @@ __device__ __forceinline__ void bwd_mma_nt(uint32_t c, uint64_t da, uint64_t db)
     ptx::mma_ss_i<1>(c, da + o, db + o, idesc);
   }
 }
-// C[tmem, 128 x D] (+)= A[tmem, 128 x 128 bf16] * B (128 rows x D, N-contiguous smem)
+// C[tmem, 128 x D] (+)= A * B: A is 128 x 128 bf16 in tensor memory, packed by the two
+// column halves (inner index 0..63 at columns [0, 32), 64..127 at [64, 96)); B is
+// 128 rows x D, N-contiguous in shared memory.
 template <int D>
 __device__ __forceinline__ void bwd_mma_tn(uint32_t c, uint32_t a_tmem, uint64_t db, bool accumulate) {
   constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, D, true);
   if (accumulate) ptx::mma_ts_i<1>(c, a_tmem, db, idesc);
   else ptx::mma_ts_i<0>(c, a_tmem, db, idesc);
 #pragma unroll
-  for (int kk = 1; kk < 8; ++kk) ptx::mma_ts_i<1>(c, a_tmem + kk * 8, db + kk * 128, idesc);
+  for (int kk = 1; kk < 8; ++kk)
+    ptx::mma_ts_i<1>(c, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, db + kk * 128, idesc);
 }
 
-// Convert a 128-row fp32 accumulator (this thread's row) to bf16 into a 128B-swizzled
-// shared tile (the TMA layout), multiplying by `mul`.
+// Convert columns [c0, c0 + D/2) of a 128-row fp32 accumulator (this thread's row) to
+// bf16, times `mul`, into a 128B-swizzled shared tile (the TMA layout).
 template <int D>
-__device__ __forceinline__ void bwd_acc_to_smem(uint32_t t_acc, uint32_t smem_tile, int row, float mul) {
+__device__ __forceinline__ void bwd_acc_to_smem(uint32_t t_acc, uint32_t smem_tile, int row, int c0, float mul) {
 #pragma unroll 1
-  for (int cc = 0; cc < D / 32; ++cc) {
+  for (int cc = c0 / 32; cc < (c0 + D / 2) / 32; ++cc) {
     uint32_t r[32];
     ptx::tmem_ld32(t_acc + cc * 32, r);
     uint32_t pk[16];
@@ -150,9 +153,41 @@ __device__ __forceinline__ void bwd_acc_to_smem(uint32_t t_acc, uint32_t smem_ti
   }
 }
 
+// One 32-column chunk of the dK/dV kernel's elementwise step for this thread's key row:
+// P^T = exp2(S^T * scale*log2(e) - LSE*log2(e)), dS^T = P^T * (dP^T - D), both rounded to
+// bf16 pairs.  kMasked adds the per-element test (key exists, query row exists, causal
+// order); tiles that need none take the kMasked = false instance.
+template <bool kMasked>
+__device__ __forceinline__ void bwd_kv_chunk(const uint32_t (&rs)[32], const uint32_t (&rd)[32], const float* vec,
+                                             int col0, float c2, int key, bool key_valid, int n_rows, int pos0,
+                                             int N, bool causal, uint32_t (&pp)[16], uint32_t (&pd)[16]) {
+#pragma unroll
+  for (int i = 0; i < 32; i += 4) {
+    const float4 nl = *reinterpret_cast<const float4*>(vec + col0 + i);
+    const float4 dd = *reinterpret_cast<const float4*>(vec + 128 + col0 + i);
+    const float nla[4] = {nl.x, nl.y, nl.z, nl.w}, dda[4] = {dd.x, dd.y, dd.z, dd.w};
+    float pv[4], dsv[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      float e = ptx::ex2_approx(fmaf(__uint_as_float(rs[i + h]), c2, nla[h]));
+      if constexpr (kMasked) {
+        const int col = col0 + i + h;
+        const int qpos = (pos0 + col) % N;
+        e = (key_valid && col < n_rows && !(causal && qpos < key)) ? e : 0.f;
+      }
+      pv[h] = e;
+      dsv[h] = e * (__uint_as_float(rd[i + h]) - dda[h]);
+    }
+    pp[i / 2] = ptx::pack_bf16x2(pv[0], pv[1]);
+    pp[i / 2 + 1] = ptx::pack_bf16x2(pv[2], pv[3]);
+    pd[i / 2] = ptx::pack_bf16x2(dsv[0], dsv[1]);
+    pd[i / 2 + 1] = ptx::pack_bf16x2(dsv[2], dsv[3]);
+  }
+}
+
 // ================================================================ dK, dV
-// CTA (group bh, key tile kt).  Tensor memory: S^T [0,128) with P^T over its first 64
-// columns, dP^T [128,256) with dS^T over its first 64 columns, dV, dK after that.
+// CTA (group bh, key tile kt).  Tensor memory: S^T [0,128) with P^T packed into
+// [0,32) and [64,96), dP^T [128,256) with dS^T packed the same way, dV, dK after that.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -181,20 +216,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   int n_q = 0;
   for (int qt = 0; qt < p.n_qtiles; ++qt) n_q += needed(qt) ? 1 : 0;
 
-  if (warp == 4 && lane == 0) {
+  if (warp == kBwdComputeWarps && lane == 0) {
     ptx::mbar_init(bar(kBarKV), 1);
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(bar(kBarFull + s), 2);  // TMA bytes + the producer's LSE/D stores
       ptx::mbar_init(bar(kBarEmpty + s), 1);
     }
     ptx::mbar_init(bar(kBarS), 1);
-    ptx::mbar_init(bar(kBarP), 4);
+    ptx::mbar_init(bar(kBarP), kBwdComputeWarps);
     ptx::mbar_init(bar(kBarFinal), 1);
     ptx::mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kBwdComputeWarps + 1) {
     ptx::tmem_alloc(ptx::smem_addr(tmem_slot), 512);
     ptx::tmem_relinquish();
   }
@@ -203,8 +238,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Waiter w{abort_flag, p.timeout_ns};
+  constexpr float kLog2e = 1.4426950408889634f;
 
-  if (warp == 4) {
+  if (warp == kBwdComputeWarps) {
     // ------------------------------------------------ producer: K, V once; stages of Q, dO, LSE, D
     if (lane == 0) {
       ptx::mbar_arrive_expect_tx(bar(kBarKV), 2 * C::kTileBytes);
@@ -218,6 +254,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int qt = 0; qt < p.n_qtiles && ok; ++qt) {
       if (!needed(qt)) continue;
       const int s = u % S, use = u / S;
+      // -LSE*log2(e) and D of the tile's rows (padding rows: 0): eight independent,
+      // bounds-checked loads per lane, issued before the wait so their latency hides there
+      float nl[4], dd[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int r = qt * 128 + lane + 32 * j;
+        const size_t g = static_cast<size_t>(bh) * p.R + (r < p.R ? r : 0);
+        nl[j] = r < p.R ? -__ldg(p.lse + g) * kLog2e : 0.f;
+        dd[j] = r < p.R ? __ldg(p.dvec + g) : 0.f;
+      }
       if (use > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarEmpty + s), (use - 1) & 1));
       if (!ok) break;
       const uint32_t st = stage_addr(s);
@@ -228,13 +274,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ptx::tma_load_3d(st + C::kTileBytes + c * C::kChunkBytes, &tm_do, bar(kBarFull + s), c * 64, qt * 128, bh);
         }
       }
-      // LSE and D of the tile's rows (padding rows: 0); plain loads, bounds-checked
       float* vec = reinterpret_cast<float*>(smem + C::kKVOffStage + s * C::kStageBytes + 2 * C::kTileBytes);
-      for (int i = lane; i < 128; i += 32) {
-        const int r = qt * 128 + i;
-        const size_t g = static_cast<size_t>(bh) * p.R + r;
-        vec[i] = r < p.R ? p.lse[g] : 0.f;
-        vec[128 + i] = r < p.R ? p.dvec[g] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        vec[lane + 32 * j] = nl[j];
+        vec[128 + lane + 32 * j] = dd[j];
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(kBarFull + s));
@@ -246,7 +290,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       for (int v = issued - S > 0 ? issued - S : 0; v < issued; ++v) w.drain(bar(kBarFull + v % S), (v / S) & 1);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kBwdComputeWarps + 1) {
     // ------------------------------------------------ MMA issuer
     const uint64_t desc_k = ptx::smem_desc_sw128(sbase, 16, 1024);
     const uint64_t desc_v = ptx::smem_desc_sw128(sbase + C::kTileBytes, 16, 1024);
@@ -292,47 +336,43 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     w.drain(bar(kBarDrain), 0);
     __syncwarp();
   } else {
-    // ------------------------------------------------ compute: thread = key row
-    const int row = warp * 32 + lane;
+    // ------------------------------------------------ compute: thread = key row, warp = column half
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane;
     const int key = kt * 128 + row;
     const bool key_valid = key < p.N;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + C::kColS, t_dp = tmem + lane_off + C::kColDP;
+    const bool key_tile_full = kt * 128 + 128 <= p.N;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + C::kColS + half * 64, t_dp = tmem + lane_off + C::kColDP + half * 64;
     const float c2 = p.scale_log2;
-    constexpr float kLog2e = 1.4426950408889634f;
     bool ok = true;
     int u = 0;
     for (int qt = 0; qt < p.n_qtiles && ok; ++qt) {
       if (!needed(qt)) continue;
       const int s = u % S;
+      // the tile needs no mask when all 128 rows exist, all keys exist and (causal) its
+      // lowest position is at or after the key tile's last key
+      const int r0 = qt * 128;
+      const int n_rows = min(128, p.R - r0);
+      const int pos0 = r0 % p.N;
+      const bool one_head = pos0 + 128 <= p.N;
+      const bool no_mask = n_rows == 128 && key_tile_full && (!p.causal || (one_head && pos0 >= kt * 128 + 127));
       ok = __all_sync(0xffffffffu, w.wait(bar(kBarS), u & 1));
       if (!ok) break;
       ptx::tc_fence_after();
       const float* vec = reinterpret_cast<const float*>(smem + C::kKVOffStage + s * C::kStageBytes + 2 * C::kTileBytes);
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
+        const int col0 = half * 64 + cc * 32;
         uint32_t rs[32], rd[32];
-        ptx::tmem_ld32(t_s + cc * 32, rs);
-        ptx::tmem_ld32(t_dp + cc * 32, rd);
+        ptx::tmem_ld32x2(t_s + cc * 32, rs, t_dp + cc * 32, rd);
         uint32_t pp[16], pd[16];
-#pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float pv[2], dsv[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int col = cc * 32 + i + h;
-            const int qrow = qt * 128 + col;
-            const int qpos = qrow % p.N;
-            const bool live = key_valid && qrow < p.R && !(p.causal && qpos < key);
-            const float e = ptx::ex2_approx(fmaf(__uint_as_float(rs[i + h]), c2, -vec[col] * kLog2e));
-            pv[h] = live ? e : 0.f;
-            dsv[h] = pv[h] * (__uint_as_float(rd[i + h]) - vec[128 + col]);
-          }
-          pp[i / 2] = ptx::pack_bf16x2(pv[0], pv[1]);
-          pd[i / 2] = ptx::pack_bf16x2(dsv[0], dsv[1]);
-        }
-        // P^T and dS^T (bf16 pairs) over columns [16 cc, 16 cc + 16) of S^T and dP^T:
-        // those columns were read in this or an earlier chunk
+        if (no_mask)
+          bwd_kv_chunk<false>(rs, rd, vec, col0, c2, key, key_valid, n_rows, pos0, p.N, p.causal, pp, pd);
+        else
+          bwd_kv_chunk<true>(rs, rd, vec, col0, c2, key, key_valid, n_rows, pos0, p.N, p.causal, pp, pd);
+        // packed P^T / dS^T over this warp's columns [16 cc, 16 cc + 16) of its half:
+        // columns this warp read in this or the previous chunk
         ptx::tmem_st16(t_s + cc * 16, pp);
         ptx::tmem_st16(t_dp + cc * 16, pd);
       }
@@ -346,20 +386,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok && n_q > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFinal), 0));
     if (ok && n_q > 0) {
       ptx::tc_fence_after();
-      bwd_acc_to_smem<D>(tmem + lane_off + C::kColAcc0, sbase + C::kTileBytes, row, 1.f);
-      bwd_acc_to_smem<D>(tmem + lane_off + C::kColAcc1, sbase, row, p.scale);
+      bwd_acc_to_smem<D>(tmem + lane_off + C::kColAcc0, sbase + C::kTileBytes, row, half * (D / 2), 1.f);
+      bwd_acc_to_smem<D>(tmem + lane_off + C::kColAcc1, sbase, row, half * (D / 2), p.scale);
       ptx::fence_proxy_async_smem();
     } else if (n_q == 0 && ok) {
       // no query sees this key tile: zero gradients (the K/V tiles may still be landing)
       ok = __all_sync(0xffffffffu, w.wait(bar(kBarKV), 0));
       if (ok) {
-        for (int i = 0; i < 2 * C::kTileBytes / 16; i += 128)
-          ptx::st_shared_v4(sbase + (i + row) * 16, 0u, 0u, 0u, 0u);
+        const int t = threadIdx.x;  // 0..255
+        for (int i = 0; i < 2 * C::kTileBytes / 16; i += 32 * kBwdComputeWarps)
+          ptx::st_shared_v4(sbase + (i + t) * 16, 0u, 0u, 0u, 0u);
         ptx::fence_proxy_async_smem();
       }
     }
-    ptx::named_barrier(1, 128);
-    if (ok && row == 0) {
+    ptx::named_barrier(1, 32 * kBwdComputeWarps);
+    if (ok && threadIdx.x == 0) {
       for (int c = 0; c < C::kChunks; ++c) {
         ptx::tma_store_3d(&tm_dk, sbase + c * C::kChunkBytes, c * 64, kt * 128, bh);
         ptx::tma_store_3d(&tm_dv, sbase + C::kTileBytes + c * C::kChunkBytes, c * 64, kt * 128, bh);
@@ -370,15 +411,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kBwdComputeWarps + 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
 }
 
 // ================================================================ dQ
-// CTA (group bh, query tile qt).  Tensor memory: S [0,128) with dS over its first 64
-// columns, dP [128,256), dQ after that.
+// CTA (group bh, query tile qt).  Tensor memory: S [0,128) with dS packed into [0,32)
+// and [64,96), dP [128,256), dQ after that.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -400,20 +441,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int qt = p.n_qtiles - 1 - blockIdx.x / p.groups;  // causal: the last query tiles have most work
   const int n_kv = p.causal ? min(p.n_ktiles, bwd_tile_max_pos(p, qt) / 128 + 1) : p.n_ktiles;
 
-  if (warp == 4 && lane == 0) {
+  if (warp == kBwdComputeWarps && lane == 0) {
     ptx::mbar_init(bar(kBarQ), 1);
     for (int s = 0; s < S; ++s) {
       ptx::mbar_init(bar(kBarFull + s), 1);
       ptx::mbar_init(bar(kBarEmpty + s), 1);
     }
     ptx::mbar_init(bar(kBarS), 1);
-    ptx::mbar_init(bar(kBarP), 4);
+    ptx::mbar_init(bar(kBarP), kBwdComputeWarps);
     ptx::mbar_init(bar(kBarFinal), 1);
     ptx::mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
-  if (warp == 5) {
+  if (warp == kBwdComputeWarps + 1) {
     ptx::tmem_alloc(ptx::smem_addr(tmem_slot), 512);
     ptx::tmem_relinquish();
   }
@@ -423,7 +464,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Waiter w{abort_flag, p.timeout_ns};
 
-  if (warp == 4) {
+  if (warp == kBwdComputeWarps) {
     // ------------------------------------------------ producer: Q, dO once; K_0, V_0, K_1, ...
     if (lane == 0) {
       ptx::mbar_arrive_expect_tx(bar(kBarQ), 2 * C::kTileBytes);
@@ -448,7 +489,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == kBwdComputeWarps + 1) {
     // ------------------------------------------------ MMA issuer
     const uint64_t desc_q = ptx::smem_desc_sw128(sbase, 16, 1024);
     const uint64_t desc_do = ptx::smem_desc_sw128(sbase + C::kTileBytes, 16, 1024);
@@ -492,44 +533,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     w.drain(bar(kBarDrain), 0);
     __syncwarp();
   } else {
-    // ------------------------------------------------ compute: thread = query row
-    const int row = warp * 32 + lane;
+    // ------------------------------------------------ compute: thread = query row, warp = column half
+    const int quarter = warp & 3, half = warp >> 2;
+    const int row = quarter * 32 + lane;
     const int qrow = qt * 128 + row;
     const bool row_valid = qrow < p.R;
     const int qpos = qrow % p.N;
     const size_t g = static_cast<size_t>(bh) * p.R + (row_valid ? qrow : 0);
     const float neg = row_valid ? -p.lse[g] * 1.4426950408889634f : 0.f;  // -LSE in log2 units
     const float drow = row_valid ? p.dvec[g] : 0.f;
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + C::kColS, t_dp = tmem + lane_off + C::kColDP;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + C::kColS + half * 64, t_dp = tmem + lane_off + C::kColDP + half * 64;
     const float c2 = p.scale_log2;
     bool ok = true;
     for (int j = 0; ok && j < n_kv; ++j) {
       ok = __all_sync(0xffffffffu, w.wait(bar(kBarS), j & 1));
       if (!ok) break;
       ptx::tc_fence_after();
-      int lim = p.N - j * 128;  // keys past the end, and after the query when causal
+      // this row's keys in tile j: [0, lim) (past the end, and after the query when causal)
+      int lim = p.N - j * 128;
       if (p.causal && qpos - j * 128 + 1 < lim) lim = qpos - j * 128 + 1;
       if (!row_valid) lim = 0;
+      lim -= half * 64;  // relative to this warp's first column
 #pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t rs[32], rd[32];
-        ptx::tmem_ld32(t_s + cc * 32, rs);
-        ptx::tmem_ld32(t_dp + cc * 32, rd);
+        ptx::tmem_ld32x2(t_s + cc * 32, rs, t_dp + cc * 32, rd);
         uint32_t pd[16];
 #pragma unroll
         for (int i = 0; i < 32; i += 2) {
           float dsv[2];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int col = cc * 32 + i + h;
             const float e = ptx::ex2_approx(fmaf(__uint_as_float(rs[i + h]), c2, neg));
-            const float pv = col < lim ? e : 0.f;
+            const float pv = cc * 32 + i + h < lim ? e : 0.f;
             dsv[h] = pv * (__uint_as_float(rd[i + h]) - drow);
           }
           pd[i / 2] = ptx::pack_bf16x2(dsv[0], dsv[1]);
         }
-        ptx::tmem_st16(t_s + cc * 16, pd);  // dS over columns already read
+        ptx::tmem_st16(t_s + cc * 16, pd);  // dS over columns this warp already read
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -539,11 +581,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFinal), 0));
     if (ok && n_kv > 0) {
       ptx::tc_fence_after();
-      bwd_acc_to_smem<D>(tmem + lane_off + C::kColAcc0, sbase, row, p.scale);  // into Q's buffer
+      bwd_acc_to_smem<D>(tmem + lane_off + C::kColAcc0, sbase, row, half * (D / 2), p.scale);  // into Q's buffer
       ptx::fence_proxy_async_smem();
     }
-    ptx::named_barrier(1, 128);
-    if (ok && n_kv > 0 && row == 0) {
+    ptx::named_barrier(1, 32 * kBwdComputeWarps);
+    if (ok && n_kv > 0 && threadIdx.x == 0) {
       for (int c = 0; c < C::kChunks; ++c) ptx::tma_store_3d(&tm_dq, sbase + c * C::kChunkBytes, c * 64, qt * 128, bh);
       ptx::bulk_commit();
       ptx::bulk_wait_all();
@@ -551,9 +593,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   }
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kBwdComputeWarps + 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
 }
-

@@ -153,35 +153,69 @@ __device__ __forceinline__ void bwd_acc_to_smem(uint32_t t_acc, uint32_t smem_ti
   }
 }
 
-// One 32-column chunk of the dK/dV kernel's elementwise step for this thread's key row:
-// P^T = exp2(S^T * scale*log2(e) - LSE*log2(e)), dS^T = P^T * (dP^T - D), both rounded to
-// bf16 pairs.  kMasked adds the per-element test (key exists, query row exists, causal
-// order); tiles that need none take the kMasked = false instance.
+// The dK/dV kernel's first elementwise step for this thread's key row, over this warp's
+// 64 query columns: P^T = exp2(S^T * scale*log2(e) - LSE*log2(e)) into pr[] (fp32) and,
+// rounded to bf16 pairs, into tensor memory over the first 32 of the columns read.
+// kMasked adds the per-element test (key exists, query row exists, causal order);
+// tiles that need none take the kMasked = false instance.
 template <bool kMasked>
-__device__ __forceinline__ void bwd_kv_chunk(const uint32_t (&rs)[32], const uint32_t (&rd)[32], const float* vec,
-                                             int col0, float c2, int key, bool key_valid, int n_rows, int pos0,
-                                             int N, bool causal, uint32_t (&pp)[16], uint32_t (&pd)[16]) {
+__device__ __forceinline__ void bwd_kv_p(uint32_t t_s, const float* vec, int col0, float c2, int key,
+                                         bool key_valid, int n_rows, int pos0, int N, bool causal,
+                                         float (&pr)[64]) {
+  uint32_t ra[32], rb[32];
+  ptx::tmem_ld32x2(t_s, ra, t_s + 32, rb);
 #pragma unroll
-  for (int i = 0; i < 32; i += 4) {
+  for (int i = 0; i < 64; i += 4) {
     const float4 nl = *reinterpret_cast<const float4*>(vec + col0 + i);
-    const float4 dd = *reinterpret_cast<const float4*>(vec + 128 + col0 + i);
-    const float nla[4] = {nl.x, nl.y, nl.z, nl.w}, dda[4] = {dd.x, dd.y, dd.z, dd.w};
-    float pv[4], dsv[4];
+    const float nla[4] = {nl.x, nl.y, nl.z, nl.w};
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
-      float e = ptx::ex2_approx(fmaf(__uint_as_float(rs[i + h]), c2, nla[h]));
+      const uint32_t sv = i + h < 32 ? ra[i + h] : rb[i + h - 32];
+      float e = ptx::ex2_approx(fmaf(__uint_as_float(sv), c2, nla[h]));
       if constexpr (kMasked) {
         const int col = col0 + i + h;
         const int qpos = (pos0 + col) % N;
         e = (key_valid && col < n_rows && !(causal && qpos < key)) ? e : 0.f;
       }
-      pv[h] = e;
-      dsv[h] = e * (__uint_as_float(rd[i + h]) - dda[h]);
+      pr[i + h] = e;
     }
-    pp[i / 2] = ptx::pack_bf16x2(pv[0], pv[1]);
-    pp[i / 2 + 1] = ptx::pack_bf16x2(pv[2], pv[3]);
-    pd[i / 2] = ptx::pack_bf16x2(dsv[0], dsv[1]);
-    pd[i / 2 + 1] = ptx::pack_bf16x2(dsv[2], dsv[3]);
+  }
+  uint32_t pk[16];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(pr[32 * c + 2 * i], pr[32 * c + 2 * i + 1]);
+    ptx::tmem_st16(t_s + 16 * c, pk);
+  }
+}
+
+// The second step, shared by both kernels: dS = P * (dP - D) over this warp's 64 columns
+// (dP read from t_dp, D per column from dcol[] or one value for the whole row), rounded
+// to bf16 pairs into tensor memory over the first 32 of the dP columns read.
+template <bool kPerColumnD>
+__device__ __forceinline__ void bwd_ds(uint32_t t_dp, const float (&pr)[64], const float* dcol, float drow) {
+  uint32_t ra[32], rb[32];
+  ptx::tmem_ld32x2(t_dp, ra, t_dp + 32, rb);
+  float ds[64];
+#pragma unroll
+  for (int i = 0; i < 64; i += 4) {
+    float dd[4] = {drow, drow, drow, drow};
+    if constexpr (kPerColumnD) {
+      const float4 d4 = *reinterpret_cast<const float4*>(dcol + i);
+      dd[0] = d4.x; dd[1] = d4.y; dd[2] = d4.z; dd[3] = d4.w;
+    }
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint32_t dv = i + h < 32 ? ra[i + h] : rb[i + h - 32];
+      ds[i + h] = pr[i + h] * (__uint_as_float(dv) - dd[h]);
+    }
+  }
+  uint32_t pk[16];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(ds[32 * c + 2 * i], ds[32 * c + 2 * i + 1]);
+    ptx::tmem_st16(t_dp + 16 * c, pk);
   }
 }
 
@@ -199,11 +233,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = ptx::smem_addr(smem);
-  // barriers: 0 kv_full, [1, 1+S) stage_full, [1+S, 1+2S) stage_empty, then s_full,
-  // pds_full, acc_final, drain
+  // barriers: 0 kv_full, [1, 1+S) stage_full, [1+S, 1+2S) stage_empty, then S^T ready,
+  // dP^T ready, P^T written, dS^T written, accumulators final, drain
   constexpr int S = C::kStages;
-  constexpr int kBarKV = 0, kBarFull = 1, kBarEmpty = 1 + S, kBarS = 1 + 2 * S, kBarP = kBarS + 1,
-                kBarFinal = kBarP + 1, kBarDrain = kBarFinal + 1;
+  constexpr int kBarKV = 0, kBarFull = 1, kBarEmpty = 1 + S, kBarS = 1 + 2 * S, kBarDP = kBarS + 1,
+                kBarP = kBarDP + 1, kBarDS = kBarP + 1, kBarFinal = kBarDS + 1, kBarDrain = kBarFinal + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kKVOffBar + C::kMaxBars * 8);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kKVOffBar + C::kMaxBars * 8 + 4);
   auto bar = [&](int i) -> uint32_t { return sbase + C::kKVOffBar + 8u * i; };
@@ -223,7 +257,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::mbar_init(bar(kBarEmpty + s), 1);
     }
     ptx::mbar_init(bar(kBarS), 1);
+    ptx::mbar_init(bar(kBarDP), 1);
     ptx::mbar_init(bar(kBarP), kBwdComputeWarps);
+    ptx::mbar_init(bar(kBarDS), kBwdComputeWarps);
     ptx::mbar_init(bar(kBarFinal), 1);
     ptx::mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0u;
@@ -299,37 +335,57 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     constexpr uint64_t kStageStep = C::kStageBytes >> 4, kTileStep = C::kTileBytes >> 4;
     const uint32_t t_s = tmem + C::kColS, t_dp = tmem + C::kColDP;
     const uint32_t t_dv = tmem + C::kColAcc0, t_dk = tmem + C::kColAcc1;
+    // Per query tile u: S^T(u), dP^T(u) | wait P^T(u): dV(u), S^T(u+1) | wait dS^T(u):
+    // dK(u), dP^T(u+1).  S^T(u+1) overwrites P^T(u) only after dV(u) read it, and dP^T(u+1)
+    // overwrites dS^T(u) only after dK(u): the tensor pipe runs one CTA's MMAs in order.
     bool ok = __all_sync(0xffffffffu, w.wait(bar(kBarKV), 0));
     ptx::tc_fence_after();
-    for (int u = 0; ok && u <= n_q; ++u) {
-      if (u >= 1) {
-        // dV += P^T dO, dK += dS^T Q for the previous stage
-        const int sp = (u - 1) % S;
-        ok = __all_sync(0xffffffffu, w.wait(bar(kBarP), (u - 1) & 1));
-        if (!ok) break;
+    if (ok && n_q > 0) {
+      ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull), 0));
+      if (ok) {
         ptx::tc_fence_after();
         if (ptx::elect_one()) {
-          const uint64_t dq_n = desc_stage_nmaj + sp * kStageStep;
-          bwd_mma_tn<D>(t_dv, t_s, dq_n + kTileStep, u > 1);  // B = dO (N-contiguous)
-          bwd_mma_tn<D>(t_dk, t_dp, dq_n, u > 1);             // B = Q (N-contiguous)
-          ptx::tc_commit(bar(kBarEmpty + sp));
-          if (u == n_q) ptx::tc_commit(bar(kBarFinal));
+          bwd_mma_nt<D>(t_s, desc_k, desc_stage_kmaj);                // S^T = K Q^T
+          ptx::tc_commit(bar(kBarS));
+          bwd_mma_nt<D>(t_dp, desc_v, desc_stage_kmaj + kTileStep);   // dP^T = V dO^T
+          ptx::tc_commit(bar(kBarDP));
         }
         __syncwarp();
       }
-      if (u < n_q) {
-        const int s = u % S;
-        ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + s), (u / S) & 1));
+    }
+    for (int u = 0; ok && u < n_q; ++u) {
+      const int s = u % S, s1 = (u + 1) % S;
+      const bool more = u + 1 < n_q;
+      const uint64_t st_n = desc_stage_nmaj + s * kStageStep;
+      ok = __all_sync(0xffffffffu, w.wait(bar(kBarP), u & 1));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) bwd_mma_tn<D>(t_dv, t_s, st_n + kTileStep, u > 0);  // dV += P^T dO
+      __syncwarp();
+      if (more) {
+        ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + s1), ((u + 1) / S) & 1));
         if (!ok) break;
         ptx::tc_fence_after();
         if (ptx::elect_one()) {
-          const uint64_t dq_k = desc_stage_kmaj + s * kStageStep;
-          bwd_mma_nt<D>(t_s, desc_k, dq_k);                  // S^T = K Q^T
-          bwd_mma_nt<D>(t_dp, desc_v, dq_k + kTileStep);     // dP^T = V dO^T
+          bwd_mma_nt<D>(t_s, desc_k, desc_stage_kmaj + s1 * kStageStep);
           ptx::tc_commit(bar(kBarS));
         }
         __syncwarp();
       }
+      ok = __all_sync(0xffffffffu, w.wait(bar(kBarDS), u & 1));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
+        bwd_mma_tn<D>(t_dk, t_dp, st_n, u > 0);  // dK += dS^T Q (scaled in the epilogue)
+        ptx::tc_commit(bar(kBarEmpty + s));
+        if (more) {
+          bwd_mma_nt<D>(t_dp, desc_v, desc_stage_kmaj + s1 * kStageStep + kTileStep);
+          ptx::tc_commit(bar(kBarDP));
+        } else {
+          ptx::tc_commit(bar(kBarFinal));
+        }
+      }
+      __syncwarp();
     }
     if (ptx::elect_one()) ptx::tc_commit(bar(kBarDrain));
     __syncwarp();
@@ -361,25 +417,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!ok) break;
       ptx::tc_fence_after();
       const float* vec = reinterpret_cast<const float*>(smem + C::kKVOffStage + s * C::kStageBytes + 2 * C::kTileBytes);
-#pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        const int col0 = half * 64 + cc * 32;
-        uint32_t rs[32], rd[32];
-        ptx::tmem_ld32x2(t_s + cc * 32, rs, t_dp + cc * 32, rd);
-        uint32_t pp[16], pd[16];
-        if (no_mask)
-          bwd_kv_chunk<false>(rs, rd, vec, col0, c2, key, key_valid, n_rows, pos0, p.N, p.causal, pp, pd);
-        else
-          bwd_kv_chunk<true>(rs, rd, vec, col0, c2, key, key_valid, n_rows, pos0, p.N, p.causal, pp, pd);
-        // packed P^T / dS^T over this warp's columns [16 cc, 16 cc + 16) of its half:
-        // columns this warp read in this or the previous chunk
-        ptx::tmem_st16(t_s + cc * 16, pp);
-        ptx::tmem_st16(t_dp + cc * 16, pd);
-      }
+      float pr[64];
+      if (no_mask)
+        bwd_kv_p<false>(t_s, vec, half * 64, c2, key, key_valid, n_rows, pos0, p.N, p.causal, pr);
+      else
+        bwd_kv_p<true>(t_s, vec, half * 64, c2, key, key_valid, n_rows, pos0, p.N, p.causal, pr);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(kBarP));
+      ok = __all_sync(0xffffffffu, w.wait(bar(kBarDP), u & 1));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      bwd_ds<true>(t_dp, pr, vec + 128 + half * 64, 0.f);
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(kBarDS));
       ++u;
     }
     // epilogue: dV, scale*dK -> bf16 -> shared (K and V buffers, no longer read) -> TMA
@@ -418,8 +472,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ================================================================ dQ
-// CTA (group bh, query tile qt).  Tensor memory: S [0,128) with dS packed into [0,32)
-// and [64,96), dP [128,256), dQ after that.
+// CTA (group bh, query tile qt).  Tensor memory: S [0,128), dP [128,256) with dS packed
+// into [128,160) and [192,224), dQ after that.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -431,8 +485,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = ptx::smem_addr(smem);
   constexpr int S = C::kSlots;
-  constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 1 + S, kBarS = 1 + 2 * S, kBarP = kBarS + 1,
-                kBarFinal = kBarP + 1, kBarDrain = kBarFinal + 1;
+  // barriers: 0 Q/dO, [1, 1+S) ring full, [1+S, 1+2S) ring empty, then S ready, dP ready,
+  // S read (its columns free), dS written, dQ final, drain
+  constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 1 + S, kBarS = 1 + 2 * S, kBarDP = kBarS + 1,
+                kBarSFree = kBarDP + 1, kBarDS = kBarSFree + 1, kBarFinal = kBarDS + 1, kBarDrain = kBarFinal + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kQOffBar + C::kMaxBars * 8);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kQOffBar + C::kMaxBars * 8 + 4);
   auto bar = [&](int i) -> uint32_t { return sbase + C::kQOffBar + 8u * i; };
@@ -448,7 +504,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::mbar_init(bar(kBarEmpty + s), 1);
     }
     ptx::mbar_init(bar(kBarS), 1);
-    ptx::mbar_init(bar(kBarP), kBwdComputeWarps);
+    ptx::mbar_init(bar(kBarDP), 1);
+    ptx::mbar_init(bar(kBarSFree), kBwdComputeWarps);
+    ptx::mbar_init(bar(kBarDS), kBwdComputeWarps);
     ptx::mbar_init(bar(kBarFinal), 1);
     ptx::mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0u;
@@ -497,36 +555,56 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t desc_ring_n = ptx::smem_desc_sw128(sbase + C::kQOffRing, C::kChunkBytes, 1024);
     constexpr uint64_t kTileStep = C::kTileBytes >> 4;
     const uint32_t t_s = tmem + C::kColS, t_dp = tmem + C::kColDP, t_dq = tmem + C::kColAcc0;
+    // Per key tile j: S(j), dP(j) | wait S read: S(j+1) | wait dS(j): dQ(j), dP(j+1).
+    // dS(j) sits over dP(j)'s columns, so dP(j+1) is issued after dQ(j) read it.
+    auto slot = [&](int u) { return u % S; };
+    auto phase = [&](int u) { return static_cast<uint32_t>((u / S) & 1); };
     bool ok = __all_sync(0xffffffffu, w.wait(bar(kBarQ), 0));
     ptx::tc_fence_after();
-    for (int j = 0; ok && j <= n_kv; ++j) {
-      if (j >= 1) {
-        // dQ += dS K_{j-1}: dS from tensor memory, K (N-contiguous) from the ring
-        const int uk = 2 * (j - 1);
-        ok = __all_sync(0xffffffffu, w.wait(bar(kBarP), (j - 1) & 1));
-        if (!ok) break;
+    if (ok && n_kv > 0) {
+      ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + slot(0)), phase(0)));
+      if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + slot(1)), phase(1)));
+      if (ok) {
         ptx::tc_fence_after();
         if (ptx::elect_one()) {
-          bwd_mma_tn<D>(t_dq, t_s, desc_ring_n + (uk % S) * kTileStep, j > 1);
-          ptx::tc_commit(bar(kBarEmpty + uk % S));        // K_{j-1}
-          ptx::tc_commit(bar(kBarEmpty + (uk + 1) % S));  // V_{j-1}
-          if (j == n_kv) ptx::tc_commit(bar(kBarFinal));
+          bwd_mma_nt<D>(t_s, desc_q, desc_ring_k + slot(0) * kTileStep);    // S = Q K^T
+          ptx::tc_commit(bar(kBarS));
+          bwd_mma_nt<D>(t_dp, desc_do, desc_ring_k + slot(1) * kTileStep);  // dP = dO V^T
+          ptx::tc_commit(bar(kBarDP));
         }
         __syncwarp();
       }
-      if (j < n_kv) {
-        const int uk = 2 * j, uv = uk + 1;
-        ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + uk % S), (uk / S) & 1));
-        if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + uv % S), (uv / S) & 1));
+    }
+    for (int j = 0; ok && j < n_kv; ++j) {
+      const int uk = 2 * j;
+      const bool more = j + 1 < n_kv;
+      if (more) {
+        ok = __all_sync(0xffffffffu, w.wait(bar(kBarSFree), j & 1));
+        if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + slot(uk + 2)), phase(uk + 2)));
         if (!ok) break;
         ptx::tc_fence_after();
         if (ptx::elect_one()) {
-          bwd_mma_nt<D>(t_s, desc_q, desc_ring_k + (uk % S) * kTileStep);    // S = Q K^T
-          bwd_mma_nt<D>(t_dp, desc_do, desc_ring_k + (uv % S) * kTileStep);  // dP = dO V^T
+          bwd_mma_nt<D>(t_s, desc_q, desc_ring_k + slot(uk + 2) * kTileStep);
           ptx::tc_commit(bar(kBarS));
         }
         __syncwarp();
       }
+      ok = __all_sync(0xffffffffu, w.wait(bar(kBarDS), j & 1));
+      if (ok && more) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + slot(uk + 3)), phase(uk + 3)));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
+        bwd_mma_tn<D>(t_dq, t_dp, desc_ring_n + slot(uk) * kTileStep, j > 0);  // dQ += dS K
+        ptx::tc_commit(bar(kBarEmpty + slot(uk)));      // K_j
+        ptx::tc_commit(bar(kBarEmpty + slot(uk + 1)));  // V_j
+        if (more) {
+          bwd_mma_nt<D>(t_dp, desc_do, desc_ring_k + slot(uk + 3) * kTileStep);
+          ptx::tc_commit(bar(kBarDP));
+        } else {
+          ptx::tc_commit(bar(kBarFinal));
+        }
+      }
+      __syncwarp();
     }
     if (ptx::elect_one()) ptx::tc_commit(bar(kBarDrain));
     __syncwarp();
@@ -555,28 +633,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (p.causal && qpos - j * 128 + 1 < lim) lim = qpos - j * 128 + 1;
       if (!row_valid) lim = 0;
       lim -= half * 64;  // relative to this warp's first column
-#pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t rs[32], rd[32];
-        ptx::tmem_ld32x2(t_s + cc * 32, rs, t_dp + cc * 32, rd);
-        uint32_t pd[16];
+      float pr[64];
+      {
+        uint32_t ra[32], rb[32];
+        ptx::tmem_ld32x2(t_s, ra, t_s + 32, rb);
 #pragma unroll
-        for (int i = 0; i < 32; i += 2) {
-          float dsv[2];
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float e = ptx::ex2_approx(fmaf(__uint_as_float(rs[i + h]), c2, neg));
-            const float pv = cc * 32 + i + h < lim ? e : 0.f;
-            dsv[h] = pv * (__uint_as_float(rd[i + h]) - drow);
-          }
-          pd[i / 2] = ptx::pack_bf16x2(dsv[0], dsv[1]);
+        for (int i = 0; i < 64; ++i) {
+          const uint32_t sv = i < 32 ? ra[i] : rb[i - 32];
+          const float e = ptx::ex2_approx(fmaf(__uint_as_float(sv), c2, neg));
+          pr[i] = i < lim ? e : 0.f;
         }
-        ptx::tmem_st16(t_s + cc * 16, pd);  // dS over columns this warp already read
       }
+      ptx::tc_fence_before();  // S read: its columns may be overwritten
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(kBarSFree));
+      ok = __all_sync(0xffffffffu, w.wait(bar(kBarDP), j & 1));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      bwd_ds<false>(t_dp, pr, nullptr, drow);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(kBarP));
+      if (lane == 0) ptx::mbar_arrive(bar(kBarDS));
     }
     if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFinal), 0));
     if (ok && n_kv > 0) {

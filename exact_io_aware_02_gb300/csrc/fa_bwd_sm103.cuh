@@ -90,8 +90,8 @@ struct BwdCfg {
   static constexpr int kChunks = D / 64;
   static constexpr int kChunkBytes = 128 * 128;
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kVecBytes = 2 * 128 * 4;     // -LSE*log2(e) and D of one query tile
-  // dK/dV kernel: K, V resident; a ring of stages {Q_i, dO_i, -LSE_i log2 e, D_i}
+  static constexpr int kVecBytes = 2 * 128 * 4;     // -LSE*log2(e) and -D of one query tile
+  // dK/dV kernel: K, V resident; a ring of stages {Q_i, dO_i, -LSE_i log2 e, -D_i}
   static constexpr int kStages = D == 128 ? 2 : 4;
   static constexpr int kStageBytes = 2 * kTileBytes + kVecBytes;
   static constexpr int kKVOffStage = 2 * kTileBytes;
@@ -164,20 +164,28 @@ __device__ __forceinline__ void bwd_kv_p(uint32_t t_s, const float* vec, int col
                                          float (&pr)[64]) {
   uint32_t ra[32], rb[32];
   ptx::tmem_ld32x2(t_s, ra, t_s + 32, rb);
+  const float2 c2v = make_float2(c2, c2);
 #pragma unroll
   for (int i = 0; i < 64; i += 4) {
     const float4 nl = *reinterpret_cast<const float4*>(vec + col0 + i);
     const float nla[4] = {nl.x, nl.y, nl.z, nl.w};
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const uint32_t sv = i + h < 32 ? ra[i + h] : rb[i + h - 32];
-      float e = ptx::ex2_approx(fmaf(__uint_as_float(sv), c2, nla[h]));
+    for (int h = 0; h < 4; h += 2) {
+      const uint32_t s0 = i + h < 32 ? ra[i + h] : rb[i + h - 32];
+      const uint32_t s1 = i + h + 1 < 32 ? ra[i + h + 1] : rb[i + h + 1 - 32];
+      const float2 x = __ffma2_rn(make_float2(__uint_as_float(s0), __uint_as_float(s1)), c2v,
+                                  make_float2(nla[h], nla[h + 1]));
+      float e[2] = {ptx::ex2_approx(x.x), ptx::ex2_approx(x.y)};
       if constexpr (kMasked) {
-        const int col = col0 + i + h;
-        const int qpos = (pos0 + col) % N;
-        e = (key_valid && col < n_rows && !(causal && qpos < key)) ? e : 0.f;
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int col = col0 + i + h + t;
+          const int qpos = (pos0 + col) % N;
+          e[t] = (key_valid && col < n_rows && !(causal && qpos < key)) ? e[t] : 0.f;
+        }
       }
-      pr[i + h] = e;
+      pr[i + h] = e[0];
+      pr[i + h + 1] = e[1];
     }
   }
   uint32_t pk[16];
@@ -190,24 +198,30 @@ __device__ __forceinline__ void bwd_kv_p(uint32_t t_s, const float* vec, int col
 }
 
 // The second step, shared by both kernels: dS = P * (dP - D) over this warp's 64 columns
-// (dP read from t_dp, D per column from dcol[] or one value for the whole row), rounded
+// (dP read from t_dp; -D per column from neg_dcol[], or one -D for the whole row), rounded
 // to bf16 pairs into tensor memory over the first 32 of the dP columns read.
 template <bool kPerColumnD>
-__device__ __forceinline__ void bwd_ds(uint32_t t_dp, const float (&pr)[64], const float* dcol, float drow) {
+__device__ __forceinline__ void bwd_ds(uint32_t t_dp, const float (&pr)[64], const float* neg_dcol,
+                                       float neg_drow) {
   uint32_t ra[32], rb[32];
   ptx::tmem_ld32x2(t_dp, ra, t_dp + 32, rb);
   float ds[64];
 #pragma unroll
   for (int i = 0; i < 64; i += 4) {
-    float dd[4] = {drow, drow, drow, drow};
+    float nd[4] = {neg_drow, neg_drow, neg_drow, neg_drow};
     if constexpr (kPerColumnD) {
-      const float4 d4 = *reinterpret_cast<const float4*>(dcol + i);
-      dd[0] = d4.x; dd[1] = d4.y; dd[2] = d4.z; dd[3] = d4.w;
+      const float4 d4 = *reinterpret_cast<const float4*>(neg_dcol + i);
+      nd[0] = d4.x; nd[1] = d4.y; nd[2] = d4.z; nd[3] = d4.w;
     }
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const uint32_t dv = i + h < 32 ? ra[i + h] : rb[i + h - 32];
-      ds[i + h] = pr[i + h] * (__uint_as_float(dv) - dd[h]);
+    for (int h = 0; h < 4; h += 2) {
+      const uint32_t d0 = i + h < 32 ? ra[i + h] : rb[i + h - 32];
+      const uint32_t d1 = i + h + 1 < 32 ? ra[i + h + 1] : rb[i + h + 1 - 32];
+      const float2 t = __fadd2_rn(make_float2(__uint_as_float(d0), __uint_as_float(d1)),
+                                  make_float2(nd[h], nd[h + 1]));
+      const float2 r = __fmul2_rn(make_float2(pr[i + h], pr[i + h + 1]), t);
+      ds[i + h] = r.x;
+      ds[i + h + 1] = r.y;
     }
   }
   uint32_t pk[16];
@@ -290,7 +304,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     for (int qt = 0; qt < p.n_qtiles && ok; ++qt) {
       if (!needed(qt)) continue;
       const int s = u % S, use = u / S;
-      // -LSE*log2(e) and D of the tile's rows (padding rows: 0): eight independent,
+      // -LSE*log2(e) and -D of the tile's rows (padding rows: 0): eight independent,
       // bounds-checked loads per lane, issued before the wait so their latency hides there
       float nl[4], dd[4];
 #pragma unroll
@@ -298,7 +312,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int r = qt * 128 + lane + 32 * j;
         const size_t g = static_cast<size_t>(bh) * p.R + (r < p.R ? r : 0);
         nl[j] = r < p.R ? -__ldg(p.lse + g) * kLog2e : 0.f;
-        dd[j] = r < p.R ? __ldg(p.dvec + g) : 0.f;
+        dd[j] = r < p.R ? -__ldg(p.dvec + g) : 0.f;
       }
       if (use > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarEmpty + s), (use - 1) & 1));
       if (!ok) break;
@@ -619,7 +633,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int qpos = qrow % p.N;
     const size_t g = static_cast<size_t>(bh) * p.R + (row_valid ? qrow : 0);
     const float neg = row_valid ? -p.lse[g] * 1.4426950408889634f : 0.f;  // -LSE in log2 units
-    const float drow = row_valid ? p.dvec[g] : 0.f;
+    const float neg_drow = row_valid ? -p.dvec[g] : 0.f;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + lane_off + C::kColS + half * 64, t_dp = tmem + lane_off + C::kColDP + half * 64;
     const float c2 = p.scale_log2;
@@ -637,11 +651,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       {
         uint32_t ra[32], rb[32];
         ptx::tmem_ld32x2(t_s, ra, t_s + 32, rb);
+        const float2 c2v = make_float2(c2, c2), negv = make_float2(neg, neg);
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          const uint32_t sv = i < 32 ? ra[i] : rb[i - 32];
-          const float e = ptx::ex2_approx(fmaf(__uint_as_float(sv), c2, neg));
-          pr[i] = i < lim ? e : 0.f;
+        for (int i = 0; i < 64; i += 2) {
+          const float2 x = __ffma2_rn(make_float2(__uint_as_float(i < 32 ? ra[i] : rb[i - 32]),
+                                                  __uint_as_float(i < 32 ? ra[i + 1] : rb[i - 31])), c2v, negv);
+          const float e0 = ptx::ex2_approx(x.x), e1 = ptx::ex2_approx(x.y);
+          pr[i] = i < lim ? e0 : 0.f;
+          pr[i + 1] = i + 1 < lim ? e1 : 0.f;
         }
       }
       ptx::tc_fence_before();  // S read: its columns may be overwritten
@@ -650,7 +667,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, w.wait(bar(kBarDP), j & 1));
       if (!ok) break;
       ptx::tc_fence_after();
-      bwd_ds<false>(t_dp, pr, nullptr, drow);
+      bwd_ds<false>(t_dp, pr, nullptr, neg_drow);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();

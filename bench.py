@@ -38,14 +38,17 @@ from exact_io_aware_02_gb300.inputs import HEADLINE, WORKLOADS, make_workload, m
 METRIC = "fwd attention TFLOP/s & % of GB300 bf16 tensor peak (B=2 H=16 N=8K d=128 causal)"
 UNIT = "TFLOP/s"
 L2_FLUSH_BYTES = 256 << 20
-KERNEL_FILES = [os.path.join(ROOT, "exact_io_aware_02_gb300", "csrc", f)
-                for f in ("fa_fwd_sm103.cu", "fa_bwd_sm103.cuh", "sm103_ptx.cuh")]
+CSRC = os.path.join(ROOT, "exact_io_aware_02_gb300", "csrc")
+KERNEL_FILES = {  # the sources each direction's kernels are built from
+    "fwd": [os.path.join(CSRC, f) for f in ("fa_fwd_sm103.cu", "fa_common.cuh", "sm103_ptx.cuh")],
+    "bwd": [os.path.join(CSRC, f) for f in ("fa_bwd_sm103.cu", "fa_common.cuh", "sm103_ptx.cuh")],
+}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
-def kernel_digest() -> str:
+def kernel_digest(direction: str = "fwd") -> str:
     h = hashlib.sha256()
-    for f in KERNEL_FILES:
+    for f in KERNEL_FILES[direction]:
         h.update(open(f, "rb").read())
     return h.hexdigest()[:16]
 
@@ -55,7 +58,7 @@ def measured_traffic(workload: str):
     on the current kernel source (same digest); else None."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    digest = kernel_digest()
+    digest = kernel_digest(WORKLOADS[workload].direction)
     for line in open(TRAFFIC_FILE, encoding="utf-8"):
         parts = line.split()
         if len(parts) >= 3 and not line.startswith("#") and parts[0] == workload and parts[1] == digest:

@@ -1,6 +1,4 @@
-// fa_bwd_sm103.cuh -- attention backward with recomputation, sm_103a.  Included once,
-// by fa_fwd_sm103.cu inside its namespace, so the two directions share one translation unit (the status
-// word, the bounded waits, the tensor-map helpers).
+// fa_bwd_sm103.cu -- exact attention backward with recomputation (dQ, dK, dV), GB300, sm_103a.
 //
 // The forward keeps only O and the per-row LSE; the backward rebuilds S and P on chip
 // from them (the recompute scheme of §6 of the zzszmyf.github.io notes "FlashAttention
@@ -26,9 +24,9 @@
 // half of the fp32 columns that warp itself has read, so no warp overwrites columns
 // another warp still has to read; the MMAs that consume them address the two packed
 // halves separately.  Every mbarrier wait is bounded, as in the forward.
-#pragma once
+#include "fa_common.cuh"
 
-// (included inside namespace fa)
+namespace fa {
 
 constexpr int kBwdThreads = 320;
 constexpr int kBwdComputeWarps = 8;
@@ -693,3 +691,153 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::tmem_dealloc(tmem, 512);
   }
 }
+
+// ==================================================================== host side
+namespace {
+
+std::mutex g_bwd_dev_mutex;
+int g_bwd_dev_state[kMaxDevices];  // 0 unknown, 1 ready, -1 wrong arch
+
+// Architecture check and the backward kernels' shared-memory limits, once per device.
+int prepare_device_bwd() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_bwd_dev_mutex);
+  if (g_bwd_dev_state[dev] == 1) return FA_OK;
+  if (g_bwd_dev_state[dev] == -1) return FA_ERR_ARCH;
+  const int arch = check_arch(dev);
+  if (arch != FA_OK) {
+    if (arch == FA_ERR_ARCH) g_bwd_dev_state[dev] = -1;
+    return arch;
+  }
+  if (cudaFuncSetAttribute(fa_bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           BwdCfg<64>::kSmemKV) != cudaSuccess ||
+      cudaFuncSetAttribute(fa_bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           BwdCfg<128>::kSmemKV) != cudaSuccess ||
+      cudaFuncSetAttribute(fa_bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           BwdCfg<64>::kSmemQ) != cudaSuccess ||
+      cudaFuncSetAttribute(fa_bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           BwdCfg<128>::kSmemQ) != cudaSuccess)
+    return FA_ERR_CUDA;
+  g_bwd_dev_state[dev] = 1;
+  return FA_OK;
+}
+
+struct BwdProblem {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+  float* delta;
+  int B, Hq, Hkv, N, d;
+  float scale;
+  int causal;
+};
+
+int validate_bwd(const BwdProblem& pr) {
+  const void* in[6] = {pr.q, pr.k, pr.v, pr.o, pr.lse, pr.dout};
+  const void* out[4] = {pr.dq, pr.dk, pr.dv, pr.delta};
+  for (const void* ptr : in)
+    if (!ptr || (reinterpret_cast<uintptr_t>(ptr) & 15u)) return FA_ERR_ARG;
+  for (const void* ptr : out)
+    if (!ptr || (reinterpret_cast<uintptr_t>(ptr) & 15u)) return FA_ERR_ARG;
+  if (pr.B < 1 || pr.Hq < 1 || pr.Hkv < 1 || pr.N < 1 || (pr.d != 64 && pr.d != 128)) return FA_ERR_ARG;
+  if (pr.Hq % pr.Hkv != 0) return FA_ERR_ARG;
+  if (!(pr.scale > 0.f) || !std::isfinite(pr.scale)) return FA_ERR_ARG;
+  const long long q_rows = static_cast<long long>(pr.B) * pr.Hq * pr.N;
+  const long long kv_rows = static_cast<long long>(pr.B) * pr.Hkv * pr.N;
+  if (q_rows > 2147483647LL) return FA_ERR_ARG;
+  const size_t qb = static_cast<size_t>(q_rows) * pr.d * 2, kb = static_cast<size_t>(kv_rows) * pr.d * 2;
+  const size_t lb = static_cast<size_t>(q_rows) * 4;
+  const size_t in_n[6] = {qb, kb, kb, qb, lb, qb};
+  const size_t out_n[4] = {qb, kb, kb, lb};
+  for (int i = 0; i < 4; ++i) {
+    for (int j = 0; j < 6; ++j)
+      if (overlaps(out[i], out_n[i], in[j], in_n[j])) return FA_ERR_ARG;
+    for (int j = i + 1; j < 4; ++j)
+      if (overlaps(out[i], out_n[i], out[j], out_n[j])) return FA_ERR_ARG;
+  }
+  for (const void* ptr : in)
+    if (!is_device_pointer(ptr)) return FA_ERR_ARG;
+  for (const void* ptr : out)
+    if (!is_device_pointer(ptr)) return FA_ERR_ARG;
+  return FA_OK;
+}
+
+template <int D>
+int launch_bwd(const BwdProblem& pr, unsigned long long timeout_ns, cudaStream_t stream) {
+  const int G = pr.Hq / pr.Hkv;
+  const int groups = pr.B * pr.Hkv;
+  const int R = G * pr.N;
+  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
+  if (!encode_map(&mq, pr.q, groups, R, D) || !encode_map(&mk, pr.k, groups, pr.N, D) ||
+      !encode_map(&mv, pr.v, groups, pr.N, D) || !encode_map(&mdo, pr.dout, groups, R, D) ||
+      !encode_map(&mdq, pr.dq, groups, R, D) || !encode_map(&mdk, pr.dk, groups, pr.N, D) ||
+      !encode_map(&mdv, pr.dv, groups, pr.N, D))
+    return FA_ERR_LAUNCH;
+  BwdParams p{};
+  p.lse = pr.lse;
+  p.dvec = pr.delta;
+  p.groups = groups;
+  p.R = R;
+  p.N = pr.N;
+  p.n_qtiles = (R + 127) / 128;
+  p.n_ktiles = (pr.N + 127) / 128;
+  p.scale = pr.scale;
+  p.scale_log2 = static_cast<float>(static_cast<double>(pr.scale) * 1.4426950408889634);
+  p.causal = pr.causal ? 1 : 0;
+  p.timeout_ns = timeout_ns;
+  const long long rows = static_cast<long long>(groups) * R;
+  const long long prep_blocks = (rows * 32 + 255) / 256;
+  const long long grid_kv = static_cast<long long>(groups) * p.n_ktiles;
+  const long long grid_q = static_cast<long long>(groups) * p.n_qtiles;
+  if (prep_blocks > 2147483647LL || grid_kv > 2147483647LL || grid_q > 2147483647LL) return FA_ERR_ARG;
+  fa_bwd_prep_kernel<D><<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
+      static_cast<const uint16_t*>(pr.o), static_cast<const uint16_t*>(pr.dout), pr.delta, static_cast<int>(rows));
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  fa_bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid_kv), kBwdThreads, BwdCfg<D>::kSmemKV, stream>>>(
+      mq, mk, mv, mdo, mdk, mdv, p);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  fa_bwd_dq_kernel<D><<<static_cast<unsigned>(grid_q), kBwdThreads, BwdCfg<D>::kSmemQ, stream>>>(
+      mq, mk, mv, mdo, mdq, p);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  return FA_OK;
+}
+
+int run_bwd(const BwdProblem& pr, unsigned long long timeout_ns, cudaStream_t stream) {
+  int rc = validate_bwd(pr);
+  if (rc != FA_OK) return rc;
+  rc = prepare_device_bwd();
+  if (rc != FA_OK) return rc;
+  return pr.d == 64 ? launch_bwd<64>(pr, timeout_ns, stream) : launch_bwd<128>(pr, timeout_ns, stream);
+}
+
+}  // namespace
+
+int bwd_status_word(int clear) {
+  unsigned int word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_status, sizeof(word)) != cudaSuccess) return FA_ERR_CUDA;
+  if (clear) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(g_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
+  }
+  return static_cast<int>(word & 0x7fffffffu);
+}
+
+}  // namespace fa
+
+extern "C" {
+
+int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
+           void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv, int N, int d, float scale,
+           int causal, cudaStream_t stream) {
+  const fa::BwdProblem pr{q, k, v, o, lse, dout, dq, dk, dv, delta, B, Hq, Hkv, N, d, scale, causal};
+  return fa::run_bwd(pr, fa::kDefaultTimeoutNs, stream);
+}
+
+}  // extern "C"

@@ -46,12 +46,9 @@
 #include <cstring>
 #include <mutex>
 
-#include "fa_gb300.h"
-#include "sm103_ptx.cuh"
+#include "fa_common.cuh"
 
 namespace fa {
-
-__device__ unsigned int g_status;
 
 constexpr int kThreads = 384;  // 3 warpgroups: softmax 0, softmax 1, producer + MMA
 constexpr uint32_t kSoftmaxRegs = 216;  // setmaxnreg split of the 384 x 168 launch budget:
@@ -118,37 +115,6 @@ __device__ __forceinline__ int causal_tile_limit(const Params& p, int qt) {
   const int max_pos = (r1 / p.Nq != r0 / p.Nq) ? p.q_offset + p.Nq - 1 : p.q_offset + r1 % p.Nq;
   return max_pos < 0 ? 0 : max_pos / 128 + 1;
 }
-
-// Bounded mbarrier waits.  `wait` gives up when the CTA's abort flag is set or
-// the deadline passes (then it sets the flag and the device status word);
-// `drain` ignores the abort flag (used to wait for in-flight work on the way out).
-struct Waiter {
-  volatile uint32_t* abort_flag;
-  unsigned long long timeout_ns;
-
-  __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    return slow(bar, parity, true);
-  }
-  __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity) const {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    return slow(bar, parity, false);
-  }
-  __device__ __forceinline__ bool slow(uint32_t bar, uint32_t parity, bool honour_abort) const {
-    const uint64_t t0 = ptx::globaltimer_ns();
-    while (true) {
-#pragma unroll 1
-      for (int i = 0; i < 16; ++i)
-        if (ptx::mbar_try_wait(bar, parity)) return true;
-      if (honour_abort && *abort_flag) return false;
-      if (ptx::globaltimer_ns() - t0 > timeout_ns) {
-        *abort_flag = 1u;
-        atomicOr(&g_status, FA_STATUS_TIMEOUT);
-        return false;
-      }
-    }
-  }
-};
 
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -570,92 +536,32 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) lse[row] = tot > 0.f ? m + logf(tot) : -INFINITY;
 }
 
-#include "fa_bwd_sm103.cuh"
-
 // ==================================================================== host side
 namespace {
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* f = nullptr;
-    cudaDriverEntryPointQueryResult q{};
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(f);
-  });
-  return fn;
-}
-
-// [heads, rows, d] bf16 viewed as 3-D; box = 64 columns (128 bytes) x 128 rows x 1 head.
-bool encode_map(CUtensorMap* m, const void* base, int heads, int rows, int d) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(rows),
-                              static_cast<cuuint64_t>(heads)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 2, static_cast<cuuint64_t>(rows) * d * 2};
-  const cuuint32_t box[3] = {64, 128, 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-constexpr int kMaxDevices = 64;
 constexpr int kMaxSplits = 1024;
 std::mutex g_dev_mutex;
 int g_dev_state[kMaxDevices];  // 0 unknown, 1 ready, -1 wrong arch
 
+// Architecture check and the forward kernels' shared-memory limits, once per device.
 int prepare_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_dev_mutex);
   if (g_dev_state[dev] == 1) return FA_OK;
   if (g_dev_state[dev] == -1) return FA_ERR_ARCH;
-  int major = 0, minor = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return FA_ERR_CUDA;
-  if (major != 10 || minor != 3) {
-    g_dev_state[dev] = -1;
-    return FA_ERR_ARCH;
+  const int arch = check_arch(dev);
+  if (arch != FA_OK) {
+    if (arch == FA_ERR_ARCH) g_dev_state[dev] = -1;
+    return arch;
   }
   if (cudaFuncSetAttribute(fa_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<64>::kSmemBytes) != cudaSuccess ||
       cudaFuncSetAttribute(fa_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           Cfg<128>::kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(fa_bwd_dkdv_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           BwdCfg<64>::kSmemKV) != cudaSuccess ||
-      cudaFuncSetAttribute(fa_bwd_dkdv_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           BwdCfg<128>::kSmemKV) != cudaSuccess ||
-      cudaFuncSetAttribute(fa_bwd_dq_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           BwdCfg<64>::kSmemQ) != cudaSuccess ||
-      cudaFuncSetAttribute(fa_bwd_dq_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           BwdCfg<128>::kSmemQ) != cudaSuccess)
+                           Cfg<128>::kSmemBytes) != cudaSuccess)
     return FA_ERR_CUDA;
   g_dev_state[dev] = 1;
   return FA_OK;
-}
-
-bool is_device_pointer(const void* ptr) {
-  cudaPointerAttributes a{};
-  if (cudaPointerGetAttributes(&a, ptr) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
-}
-
-bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
-  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
-  return na > 0 && nb > 0 && x < y + nb && y < x + na;
 }
 
 struct Problem {
@@ -671,8 +577,6 @@ struct Problem {
   void* workspace;
   size_t workspace_bytes;
 };
-
-size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 // bytes of workspace for n_splits > 1: fp32 partial O, then partial LSE
 size_t workspace_needed(long long rows, int d, int n_splits) {
@@ -769,101 +673,6 @@ Problem mha(const void* q, const void* k, const void* v, void* o, float* lse, in
   return Problem{q, k, v, o, lse, B, H, H, N, N, d, scale, causal, 1, nullptr, 0};
 }
 
-// ---- backward
-struct BwdProblem {
-  const void* q;
-  const void* k;
-  const void* v;
-  const void* o;
-  const float* lse;
-  const void* dout;
-  void* dq;
-  void* dk;
-  void* dv;
-  float* delta;
-  int B, Hq, Hkv, N, d;
-  float scale;
-  int causal;
-};
-
-int validate_bwd(const BwdProblem& pr) {
-  const void* in[6] = {pr.q, pr.k, pr.v, pr.o, pr.lse, pr.dout};
-  const void* out[4] = {pr.dq, pr.dk, pr.dv, pr.delta};
-  for (const void* ptr : in)
-    if (!ptr || (reinterpret_cast<uintptr_t>(ptr) & 15u)) return FA_ERR_ARG;
-  for (const void* ptr : out)
-    if (!ptr || (reinterpret_cast<uintptr_t>(ptr) & 15u)) return FA_ERR_ARG;
-  if (pr.B < 1 || pr.Hq < 1 || pr.Hkv < 1 || pr.N < 1 || (pr.d != 64 && pr.d != 128)) return FA_ERR_ARG;
-  if (pr.Hq % pr.Hkv != 0) return FA_ERR_ARG;
-  if (!(pr.scale > 0.f) || !std::isfinite(pr.scale)) return FA_ERR_ARG;
-  const long long q_rows = static_cast<long long>(pr.B) * pr.Hq * pr.N;
-  const long long kv_rows = static_cast<long long>(pr.B) * pr.Hkv * pr.N;
-  if (q_rows > 2147483647LL) return FA_ERR_ARG;
-  const size_t qb = static_cast<size_t>(q_rows) * pr.d * 2, kb = static_cast<size_t>(kv_rows) * pr.d * 2;
-  const size_t lb = static_cast<size_t>(q_rows) * 4;
-  const size_t in_n[6] = {qb, kb, kb, qb, lb, qb};
-  const size_t out_n[4] = {qb, kb, kb, lb};
-  for (int i = 0; i < 4; ++i) {
-    for (int j = 0; j < 6; ++j)
-      if (overlaps(out[i], out_n[i], in[j], in_n[j])) return FA_ERR_ARG;
-    for (int j = i + 1; j < 4; ++j)
-      if (overlaps(out[i], out_n[i], out[j], out_n[j])) return FA_ERR_ARG;
-  }
-  for (const void* ptr : in)
-    if (!is_device_pointer(ptr)) return FA_ERR_ARG;
-  for (const void* ptr : out)
-    if (!is_device_pointer(ptr)) return FA_ERR_ARG;
-  return FA_OK;
-}
-
-template <int D>
-int launch_bwd(const BwdProblem& pr, unsigned long long timeout_ns, cudaStream_t stream) {
-  const int G = pr.Hq / pr.Hkv;
-  const int groups = pr.B * pr.Hkv;
-  const int R = G * pr.N;
-  CUtensorMap mq, mk, mv, mdo, mdq, mdk, mdv;
-  if (!encode_map(&mq, pr.q, groups, R, D) || !encode_map(&mk, pr.k, groups, pr.N, D) ||
-      !encode_map(&mv, pr.v, groups, pr.N, D) || !encode_map(&mdo, pr.dout, groups, R, D) ||
-      !encode_map(&mdq, pr.dq, groups, R, D) || !encode_map(&mdk, pr.dk, groups, pr.N, D) ||
-      !encode_map(&mdv, pr.dv, groups, pr.N, D))
-    return FA_ERR_LAUNCH;
-  BwdParams p{};
-  p.lse = pr.lse;
-  p.dvec = pr.delta;
-  p.groups = groups;
-  p.R = R;
-  p.N = pr.N;
-  p.n_qtiles = (R + 127) / 128;
-  p.n_ktiles = (pr.N + 127) / 128;
-  p.scale = pr.scale;
-  p.scale_log2 = static_cast<float>(static_cast<double>(pr.scale) * 1.4426950408889634);
-  p.causal = pr.causal ? 1 : 0;
-  p.timeout_ns = timeout_ns;
-  const long long rows = static_cast<long long>(groups) * R;
-  const long long prep_blocks = (rows * 32 + 255) / 256;
-  const long long grid_kv = static_cast<long long>(groups) * p.n_ktiles;
-  const long long grid_q = static_cast<long long>(groups) * p.n_qtiles;
-  if (prep_blocks > 2147483647LL || grid_kv > 2147483647LL || grid_q > 2147483647LL) return FA_ERR_ARG;
-  fa_bwd_prep_kernel<D><<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
-      static_cast<const uint16_t*>(pr.o), static_cast<const uint16_t*>(pr.dout), pr.delta, static_cast<int>(rows));
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
-  fa_bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid_kv), kBwdThreads, BwdCfg<D>::kSmemKV, stream>>>(
-      mq, mk, mv, mdo, mdk, mdv, p);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
-  fa_bwd_dq_kernel<D><<<static_cast<unsigned>(grid_q), kBwdThreads, BwdCfg<D>::kSmemQ, stream>>>(
-      mq, mk, mv, mdo, mdq, p);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
-  return FA_OK;
-}
-
-int run_bwd(const BwdProblem& pr, unsigned long long timeout_ns, cudaStream_t stream) {
-  int rc = validate_bwd(pr);
-  if (rc != FA_OK) return rc;
-  rc = prepare_device();
-  if (rc != FA_OK) return rc;
-  return pr.d == 64 ? launch_bwd<64>(pr, timeout_ns, stream) : launch_bwd<128>(pr, timeout_ns, stream);
-}
-
 // ---- fixed device workspace for callers that cannot allocate (fa_fwd_gqa_static_workspace)
 // One array per device that loads this library, held until the process exits.  Host code
 // must not use the symbol itself as an address: it is a host-side stand-in.  The device
@@ -889,9 +698,11 @@ int static_workspace(void** out) {
   return FA_OK;
 }
 
-constexpr unsigned long long kDefaultTimeoutNs = 2000000000ull;  // 2 s per wait
-
 }  // namespace
+
+// status word of the backward translation unit (fa_bwd_sm103.cu): read, optionally cleared
+int bwd_status_word(int clear);
+
 }  // namespace fa
 
 extern "C" {
@@ -938,13 +749,6 @@ int fa_fwd_withheld_tile(const void* q, const void* k, const void* v, void* o, f
                  static_cast<unsigned long long>(wait_timeout_ms * 1e6), stream);
 }
 
-int fa_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse, const void* dout,
-           void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv, int N, int d, float scale,
-           int causal, cudaStream_t stream) {
-  const fa::BwdProblem pr{q, k, v, o, lse, dout, dq, dk, dv, delta, B, Hq, Hkv, N, d, scale, causal};
-  return fa::run_bwd(pr, fa::kDefaultTimeoutNs, stream);
-}
-
 int fa_status(int clear, cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return FA_ERR_CUDA;
   unsigned int word = 0;
@@ -953,7 +757,9 @@ int fa_status(int clear, cudaStream_t stream) {
     const unsigned int zero = 0;
     if (cudaMemcpyToSymbol(fa::g_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
   }
-  return static_cast<int>(word & 0x7fffffffu);
+  const int bwd_word = fa::bwd_status_word(clear);  // the backward translation unit's word
+  if (bwd_word < 0) return bwd_word;
+  return static_cast<int>((word | static_cast<unsigned int>(bwd_word)) & 0x7fffffffu);
 }
 
 const char* fa_strerror(int code) {

@@ -95,13 +95,17 @@ struct BwdCfg {
   static constexpr int kKVOffStage = 2 * kTileBytes;
   static constexpr int kKVOffBar = kKVOffStage + kStages * kStageBytes;
   // dQ kernel: Q, dO resident; a ring of K_j, V_j tiles
-  static constexpr int kSlots = D == 128 ? 4 : 8;
+  static constexpr int kSlots = D == 128 ? 5 : 12;
+  static constexpr int kPrefetchAhead = 4;  // producer tiles fetched into L2 ahead of their load
   static constexpr int kQOffRing = 2 * kTileBytes;
   static constexpr int kQOffBar = kQOffRing + kSlots * kTileBytes;
   static constexpr int kMaxBars = 2 + 2 * (kSlots > kStages ? kSlots : kStages) + 8;
   static constexpr int kSmemKV = kKVOffBar + kMaxBars * 8 + 16 + 1024;
   static constexpr int kSmemQ = kQOffBar + kMaxBars * 8 + 16 + 1024;
+  // dK/dV kernel tensor memory: S^T, dP^T, dV, dK
   static constexpr uint32_t kColS = 0, kColDP = 128, kColAcc0 = 256, kColAcc1 = 256 + D;
+  // dQ kernel tensor memory: two S buffers (key tiles alternate), dP, dQ
+  static constexpr uint32_t kQColS = 0, kQColDP = 256, kQColDQ = 384;
   static_assert(kSmemKV <= 232448 && kSmemQ <= 232448, "shared memory budget");
 };
 
@@ -197,9 +201,9 @@ __device__ __forceinline__ void bwd_kv_p(uint32_t t_s, const float* vec, int col
 
 // The second step, shared by both kernels: dS = P * (dP - D) over this warp's 64 columns
 // (dP read from t_dp; -D per column from neg_dcol[], or one -D for the whole row), rounded
-// to bf16 pairs into tensor memory over the first 32 of the dP columns read.
+// to bf16 pairs into 32 tensor-memory columns at t_dst (columns this warp has read).
 template <bool kPerColumnD>
-__device__ __forceinline__ void bwd_ds(uint32_t t_dp, const float (&pr)[64], const float* neg_dcol,
+__device__ __forceinline__ void bwd_ds(uint32_t t_dp, uint32_t t_dst, const float (&pr)[64], const float* neg_dcol,
                                        float neg_drow) {
   uint32_t ra[32], rb[32];
   ptx::tmem_ld32x2(t_dp, ra, t_dp + 32, rb);
@@ -227,7 +231,7 @@ __device__ __forceinline__ void bwd_ds(uint32_t t_dp, const float (&pr)[64], con
   for (int c = 0; c < 2; ++c) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(ds[32 * c + 2 * i], ds[32 * c + 2 * i + 1]);
-    ptx::tmem_st16(t_dp + 16 * c, pk);
+    ptx::tmem_st16(t_dst + 16 * c, pk);
   }
 }
 
@@ -441,7 +445,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ok = __all_sync(0xffffffffu, w.wait(bar(kBarDP), u & 1));
       if (!ok) break;
       ptx::tc_fence_after();
-      bwd_ds<true>(t_dp, pr, vec + 128 + half * 64, 0.f);
+      bwd_ds<true>(t_dp, t_dp, pr, vec + 128 + half * 64, 0.f);
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
@@ -484,8 +488,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 }
 
 // ================================================================ dQ
-// CTA (group bh, query tile qt).  Tensor memory: S [0,128), dP [128,256) with dS packed
-// into [128,160) and [192,224), dQ after that.
+// CTA (group bh, query tile qt).  Tensor memory: S of even key tiles [0,128), of odd key
+// tiles [128,256); dP [256,384); dQ after that.  dS(j) is packed over the S(j) columns
+// the P step has read, so S(j+1) is already resident while dS(j) is computed.
 template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -497,10 +502,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = ptx::smem_addr(smem);
   constexpr int S = C::kSlots;
-  // barriers: 0 Q/dO, [1, 1+S) ring full, [1+S, 1+2S) ring empty, then S ready, dP ready,
-  // S read (its columns free), dS written, dQ final, drain
-  constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 1 + S, kBarS = 1 + 2 * S, kBarDP = kBarS + 1,
-                kBarSFree = kBarDP + 1, kBarDS = kBarSFree + 1, kBarFinal = kBarDS + 1, kBarDrain = kBarFinal + 1;
+  // barriers: 0 Q/dO, [1, 1+S) ring full, [1+S, 1+2S) ring empty, then S ready (one per
+  // S buffer), dP ready, dS written, dQ final, drain
+  constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 1 + S, kBarS = 1 + 2 * S, kBarDP = kBarS + 2,
+                kBarDS = kBarDP + 1, kBarFinal = kBarDS + 1, kBarDrain = kBarFinal + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kQOffBar + C::kMaxBars * 8);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kQOffBar + C::kMaxBars * 8 + 4);
   auto bar = [&](int i) -> uint32_t { return sbase + C::kQOffBar + 8u * i; };
@@ -516,8 +521,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::mbar_init(bar(kBarEmpty + s), 1);
     }
     ptx::mbar_init(bar(kBarS), 1);
+    ptx::mbar_init(bar(kBarS + 1), 1);
     ptx::mbar_init(bar(kBarDP), 1);
-    ptx::mbar_init(bar(kBarSFree), kBwdComputeWarps);
     ptx::mbar_init(bar(kBarDS), kBwdComputeWarps);
     ptx::mbar_init(bar(kBarFinal), 1);
     ptx::mbar_init(bar(kBarDrain), 1);
@@ -544,8 +549,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       int issued = 0;
       bool ok = true;
+      auto prefetch = [&](int u) {
+        if (u < 2 * n_kv)
+          for (int c = 0; c < C::kChunks; ++c)
+            ptx::tma_prefetch_3d((u & 1) ? &tm_v : &tm_k, c * 64, (u >> 1) * 128, bh);
+      };
+      for (int u = 0; u < C::kPrefetchAhead; ++u) prefetch(u);
       for (int u = 0; u < 2 * n_kv; ++u) {
         const int s = u % S, use = u / S;
+        prefetch(u + C::kPrefetchAhead);
         if (use > 0 && !w.wait(bar(kBarEmpty + s), (use - 1) & 1)) { ok = false; break; }
         ptx::mbar_arrive_expect_tx(bar(kBarFull + s), C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
@@ -566,57 +578,48 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint64_t desc_ring_k = ptx::smem_desc_sw128(sbase + C::kQOffRing, 16, 1024);
     const uint64_t desc_ring_n = ptx::smem_desc_sw128(sbase + C::kQOffRing, C::kChunkBytes, 1024);
     constexpr uint64_t kTileStep = C::kTileBytes >> 4;
-    const uint32_t t_s = tmem + C::kColS, t_dp = tmem + C::kColDP, t_dq = tmem + C::kColAcc0;
-    // Per key tile j: S(j), dP(j) | wait S read: S(j+1) | wait dS(j): dQ(j), dP(j+1).
-    // dS(j) sits over dP(j)'s columns, so dP(j+1) is issued after dQ(j) read it.
+    const uint32_t t_s = tmem + C::kQColS, t_dp = tmem + C::kQColDP, t_dq = tmem + C::kQColDQ;
+    // Order: S(0), dP(0), S(1); then per key tile j, once dS(j) is written: dP(j+1),
+    // dQ(j) += dS(j) K_j, S(j+2) into the buffer dS(j) occupies (after dQ(j) read it: the
+    // tensor pipe runs one CTA's MMAs in order).  K_j is released after dQ(j), V_j after dP(j).
     auto slot = [&](int u) { return u % S; };
     auto phase = [&](int u) { return static_cast<uint32_t>((u / S) & 1); };
-    bool ok = __all_sync(0xffffffffu, w.wait(bar(kBarQ), 0));
-    ptx::tc_fence_after();
-    if (ok && n_kv > 0) {
-      ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + slot(0)), phase(0)));
-      if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + slot(1)), phase(1)));
-      if (ok) {
-        ptx::tc_fence_after();
-        if (ptx::elect_one()) {
-          bwd_mma_nt<D>(t_s, desc_q, desc_ring_k + slot(0) * kTileStep);    // S = Q K^T
-          ptx::tc_commit(bar(kBarS));
-          bwd_mma_nt<D>(t_dp, desc_do, desc_ring_k + slot(1) * kTileStep);  // dP = dO V^T
-          ptx::tc_commit(bar(kBarDP));
-        }
-        __syncwarp();
-      }
-    }
-    for (int j = 0; ok && j < n_kv; ++j) {
-      const int uk = 2 * j;
-      const bool more = j + 1 < n_kv;
-      if (more) {
-        ok = __all_sync(0xffffffffu, w.wait(bar(kBarSFree), j & 1));
-        if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + slot(uk + 2)), phase(uk + 2)));
-        if (!ok) break;
-        ptx::tc_fence_after();
-        if (ptx::elect_one()) {
-          bwd_mma_nt<D>(t_s, desc_q, desc_ring_k + slot(uk + 2) * kTileStep);
-          ptx::tc_commit(bar(kBarS));
-        }
-        __syncwarp();
-      }
-      ok = __all_sync(0xffffffffu, w.wait(bar(kBarDS), j & 1));
-      if (ok && more) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFull + slot(uk + 3)), phase(uk + 3)));
-      if (!ok) break;
+    auto issue_s = [&](int j) -> bool {  // S(j) = Q K_j^T into buffer j % 2
+      if (!__all_sync(0xffffffffu, w.wait(bar(kBarFull + slot(2 * j)), phase(2 * j)))) return false;
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
-        bwd_mma_tn<D>(t_dq, t_dp, desc_ring_n + slot(uk) * kTileStep, j > 0);  // dQ += dS K
-        ptx::tc_commit(bar(kBarEmpty + slot(uk)));      // K_j
-        ptx::tc_commit(bar(kBarEmpty + slot(uk + 1)));  // V_j
-        if (more) {
-          bwd_mma_nt<D>(t_dp, desc_do, desc_ring_k + slot(uk + 3) * kTileStep);
-          ptx::tc_commit(bar(kBarDP));
-        } else {
-          ptx::tc_commit(bar(kBarFinal));
-        }
+        bwd_mma_nt<D>(t_s + (j & 1) * 128, desc_q, desc_ring_k + slot(2 * j) * kTileStep);
+        ptx::tc_commit(bar(kBarS + (j & 1)));
       }
       __syncwarp();
+      return true;
+    };
+    auto issue_dp = [&](int j) -> bool {  // dP(j) = dO V_j^T
+      if (!__all_sync(0xffffffffu, w.wait(bar(kBarFull + slot(2 * j + 1)), phase(2 * j + 1)))) return false;
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
+        bwd_mma_nt<D>(t_dp, desc_do, desc_ring_k + slot(2 * j + 1) * kTileStep);
+        ptx::tc_commit(bar(kBarDP));
+        ptx::tc_commit(bar(kBarEmpty + slot(2 * j + 1)));  // V_j: read by this product only
+      }
+      __syncwarp();
+      return true;
+    };
+    bool ok = __all_sync(0xffffffffu, w.wait(bar(kBarQ), 0));
+    ptx::tc_fence_after();
+    if (ok && n_kv > 0) ok = issue_s(0) && issue_dp(0) && (n_kv < 2 || issue_s(1));
+    for (int j = 0; ok && j < n_kv; ++j) {
+      ok = __all_sync(0xffffffffu, w.wait(bar(kBarDS), j & 1));
+      if (!ok) break;
+      ptx::tc_fence_after();
+      if (j + 1 < n_kv && !(ok = issue_dp(j + 1))) break;
+      if (ptx::elect_one()) {
+        bwd_mma_tn<D>(t_dq, t_s + (j & 1) * 128, desc_ring_n + slot(2 * j) * kTileStep, j > 0);  // dQ += dS K
+        ptx::tc_commit(bar(kBarEmpty + slot(2 * j)));  // K_j
+        if (j + 1 == n_kv) ptx::tc_commit(bar(kBarFinal));
+      }
+      __syncwarp();
+      if (j + 2 < n_kv && !(ok = issue_s(j + 2))) break;
     }
     if (ptx::elect_one()) ptx::tc_commit(bar(kBarDrain));
     __syncwarp();
@@ -633,11 +636,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float neg = row_valid ? -p.lse[g] * 1.4426950408889634f : 0.f;  // -LSE in log2 units
     const float neg_drow = row_valid ? -p.dvec[g] : 0.f;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + C::kColS + half * 64, t_dp = tmem + lane_off + C::kColDP + half * 64;
+    const uint32_t t_s0 = tmem + lane_off + C::kQColS + half * 64, t_dp = tmem + lane_off + C::kQColDP + half * 64;
     const float c2 = p.scale_log2;
     bool ok = true;
     for (int j = 0; ok && j < n_kv; ++j) {
-      ok = __all_sync(0xffffffffu, w.wait(bar(kBarS), j & 1));
+      const uint32_t t_s = t_s0 + (j & 1) * 128;
+      ok = __all_sync(0xffffffffu, w.wait(bar(kBarS + (j & 1)), (j >> 1) & 1));
       if (!ok) break;
       ptx::tc_fence_after();
       // this row's keys in tile j: [0, lim) (past the end, and after the query when causal)
@@ -659,13 +663,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           pr[i + 1] = i + 1 < lim ? e1 : 0.f;
         }
       }
-      ptx::tc_fence_before();  // S read: its columns may be overwritten
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(kBarSFree));
       ok = __all_sync(0xffffffffu, w.wait(bar(kBarDP), j & 1));
       if (!ok) break;
       ptx::tc_fence_after();
-      bwd_ds<false>(t_dp, pr, nullptr, neg_drow);
+      bwd_ds<false>(t_dp, t_s, pr, nullptr, neg_drow);  // dS over the S columns just read
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
@@ -674,7 +675,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFinal), 0));
     if (ok && n_kv > 0) {
       ptx::tc_fence_after();
-      bwd_acc_to_smem<D>(tmem + lane_off + C::kColAcc0, sbase, row, half * (D / 2), p.scale);  // into Q's buffer
+      bwd_acc_to_smem<D>(tmem + lane_off + C::kQColDQ, sbase, row, half * (D / 2), p.scale);  // into Q's buffer
       ptx::fence_proxy_async_smem();
     }
     ptx::named_barrier(1, 32 * kBwdComputeWarps);

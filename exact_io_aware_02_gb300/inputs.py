@@ -82,6 +82,8 @@ WORKLOADS = {
                  Nk=32768, n_splits=16, bound="hbm"),
         # the backward of the causal prefill shape: dQ, dK, dV with recomputation
         Workload("bwd_causal_n8192_d128", 2, 16, 8192, 128, True, seed=20263, direction="bwd"),
+        # a small backward (inputs of 16 MiB per tensor) for full-section profiler captures
+        Workload("bwd_causal_n2048_d128", 2, 16, 2048, 128, True, seed=20268, direction="bwd"),
     )
 }
 

@@ -140,10 +140,14 @@ def test_bwd_zero_upstream_gradient(fa):
         assert bool((t == 0).all())
 
 
-def test_bwd_workload_full_size_sampled(fa):
-    """The bench's backward launch (B=2, H=16, N=8192, d=128, causal) on its own
+BWD_WORKLOADS = [n for n, w in WORKLOADS.items() if w.direction == "bwd"]
+
+
+@pytest.mark.parametrize("name", BWD_WORKLOADS)
+def test_bwd_workload_full_size_sampled(fa, name):
+    """The bench's backward launches (B=2, H=16, causal, N=8192 or 2048) on their own
     inputs; two heads checked in full."""
-    w = WORKLOADS["bwd_causal_n8192_d128"]
+    w = WORKLOADS[name]
     q, k, v = make_workload(w)
     do = make_workload_dout(w)
     res = run(fa, q, k, v, do, w.causal)

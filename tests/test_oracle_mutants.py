@@ -79,3 +79,55 @@ def test_mutant_is_caught(name, old, new, count):
         except Exception:  # noqa: BLE001 -- any failure of a pin counts
             caught.append(pin.__name__)
     assert caught, f"mutant '{name}' passed every pin"
+
+
+# ---------------------------------------------------------------- the FP8 oracle
+from tests.oracle_pins_fp8 import FP8_PINS  # noqa: E402
+
+FP8_SRC = os.path.join(os.path.dirname(SRC), "fp8.py")
+
+FP8_MUTANTS = [
+    ("e4m3 bias 8", "(1.0 + m / 8.0) * 2.0 ** (e - 7)", "(1.0 + m / 8.0) * 2.0 ** (e - 8)", 1),
+    ("e4m3 keeps the NaN code", "if e == 15 and m == 7:", "if e == 16:", 1),
+    ("e4m3 no subnormals", "vals.append(m * E4M3_SUBNORMAL_STEP)", "vals.append(0.0 if m else 0.0)", 1),
+    ("ties away from zero", "((a - lo == hi - a) & (idx % 2 == 0))", "(a - lo == hi - a)", 1),
+    ("ties to odd", "((a - lo == hi - a) & (idx % 2 == 0))", "((a - lo == hi - a) & (idx % 2 == 1))", 1),
+    ("overflow to NaN instead of saturating", "return np.copysign(r, x)",
+     "return np.copysign(np.where(np.abs(x) >= 464.0, np.nan, r), x)", 1),
+    ("rotation signs ignored", "return (x * np.asarray(signs, dtype=np.float64)) @ hadamard(d) / np.sqrt(d)",
+     "return x @ hadamard(d) / np.sqrt(d)", 1),
+    ("rotation not normalised", "return (x * np.asarray(signs, dtype=np.float64)) @ hadamard(d) / np.sqrt(d)",
+     "return (x * np.asarray(signs, dtype=np.float64)) @ hadamard(d) / d", 1),
+    ("Hadamard block sign", "h = np.block([[h, h], [h, -h]])", "h = np.block([[h, h], [-h, h]])", 1),
+    ("scale from the wrong maximum", "s = amax / E4M3_MAX if amax > 0.0 else 1.0",
+     "s = amax / 240.0 if amax > 0.0 else 1.0", 1),
+    ("one scale per tensor", "blk = x[t * block_rows:(t + 1) * block_rows]", "blk = x", 1),
+    ("dequantise forgets the scale", "return codes * row_scale[:, None]", "return codes", 1),
+    ("V rotated too", "for x in (qr, kr, np.asarray(v, dtype=np.float64)):",
+     "for x in (qr, kr, rotate(v, signs)):", 1),
+    ("only Q rotated", "kr = rotate(k, signs) if rotate_qk else", "kr = k if rotate_qk else", 1),
+]
+
+
+def _load_fp8_mutant(old, new, count):
+    import oracle.attention as exact
+    src = open(FP8_SRC, encoding="utf-8").read()
+    assert src.count(old) >= count, f"mutation site not found: {old!r}"
+    mutated = src.replace(old, new, count).replace("from .attention import naive_attention", "")
+    mod = types.ModuleType("oracle_fp8_mutant")
+    mod.__dict__["naive_attention"] = exact.naive_attention
+    exec(compile(mutated, "oracle_fp8_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.filterwarnings("ignore::RuntimeWarning")
+@pytest.mark.parametrize("name,old,new,count", FP8_MUTANTS, ids=[m[0] for m in FP8_MUTANTS])
+def test_fp8_mutant_is_caught(name, old, new, count):
+    mod = _load_fp8_mutant(old, new, count)
+    caught = []
+    for pin in FP8_PINS:
+        try:
+            pin(mod)
+        except Exception:  # noqa: BLE001 -- any failure of a pin counts
+            caught.append(pin.__name__)
+    assert caught, f"mutant '{name}' passed every pin"

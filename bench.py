@@ -33,7 +33,8 @@ if ROOT not in sys.path:
 
 import torch  # noqa: E402
 
-from exact_io_aware_02_gb300.inputs import HEADLINE, WORKLOADS, make_workload, make_workload_dout  # noqa: E402
+from exact_io_aware_02_gb300.inputs import (HEADLINE, WORKLOADS, make_workload, make_workload_dout,  # noqa: E402
+                                            make_workload_signs)
 
 METRIC = "fwd attention TFLOP/s & % of GB300 bf16 tensor peak (B=2 H=16 N=8K d=128 causal)"
 UNIT = "TFLOP/s"
@@ -42,6 +43,7 @@ CSRC = os.path.join(ROOT, "exact_io_aware_02_gb300", "csrc")
 KERNEL_FILES = {  # the sources each direction's kernels are built from
     "fwd": [os.path.join(CSRC, f) for f in ("fa_fwd_sm103.cu", "fa_common.cuh", "sm103_ptx.cuh")],
     "bwd": [os.path.join(CSRC, f) for f in ("fa_bwd_sm103.cu", "fa_common.cuh", "sm103_ptx.cuh")],
+    "fp8": [os.path.join(CSRC, f) for f in ("fa_fp8_sm103.cu", "fa_common.cuh", "sm103_ptx.cuh")],
 }
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
@@ -108,6 +110,8 @@ def metric_for(w):
         return f"decode attention GB/s of algorithmic HBM traffic ({w.name})", "GB/s"
     if w.direction == "bwd":
         return f"bwd attention TFLOP/s, 10*N^2*d per head, halved for causal ({w.name})", UNIT
+    if w.direction == "fp8":
+        return f"fp8 (E4M3) fwd attention TFLOP/s, 4*N^2*d per head, halved for causal ({w.name})", UNIT
     return METRIC if w.name == HEADLINE else f"fwd attention TFLOP/s ({w.name})", UNIT
 
 
@@ -209,10 +213,12 @@ def cpu_baseline(w, budget_s=12.0, max_slices=32):
     about ``budget_s`` seconds of CPU work; TFLOP/s counted like the GPU metric."""
     import numpy as np
     import oracle
+    import oracle.fp8 as oracle_fp8
     from exact_io_aware_02_gb300.inputs import sample_slices
 
     q, k, v = make_workload(w)
     do = make_workload_dout(w) if w.direction == "bwd" else None
+    signs = make_workload_signs(w).numpy().astype(np.float64) if w.direction == "fp8" else None
     G = w.H // w.hkv
     slices = sample_slices(w.B, w.H, max_slices, w.seed + 3)
     per_slice = units_per_step(w) / (w.B * w.H)
@@ -223,13 +229,14 @@ def cpu_baseline(w, budget_s=12.0, max_slices=32):
         t0 = time.perf_counter()
         if do is not None:
             oracle.attention_backward(qa, ka, va, do[b, h].to(torch.float64).numpy(), w.scale, w.causal)
+        elif signs is not None:
+            oracle_fp8.fp8_attention(qa, ka, va, w.scale, w.causal, signs)
         else:
             oracle.naive_attention(qa, ka, va, w.scale, w.causal, q_offset=w.nk - w.N)
         t_total += time.perf_counter() - t0
         done += 1
         if t_total >= budget_s:
             break
-    del np
     return {"value": done * per_slice / t_total, "unit": metric_for(w)[1],
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
             "sample": f"{done} whole (b,h) query-head slice(s) of {w.name} (N={w.N}, d={w.d}, {w.direction}), "
@@ -242,10 +249,13 @@ def run_reference(args, w, rank, world):
     tile of one query head (its K/V head under grouping), fp64 NumPy."""
     if rank != 0:
         return
+    import numpy as np
     import oracle
+    import oracle.fp8 as oracle_fp8
 
     q, k, v = make_workload(w)
     do = make_workload_dout(w) if w.direction == "bwd" else None
+    signs = make_workload_signs(w).numpy().astype(np.float64) if w.direction == "fp8" else None
     G = w.H // w.hkv
     q_offset = w.nk - w.N
     n_tiles = (w.N + 127) // 128
@@ -265,6 +275,8 @@ def run_reference(args, w, rank, world):
             oracle.attention_backward(qa[rows[0]:rows[-1] + 1], ka, va,
                                       do[b, h, rows[0]:rows[-1] + 1].to(torch.float64).numpy(),
                                       w.scale, w.causal, q_offset=q_offset + rows[0])
+        elif signs is not None:
+            oracle_fp8.fp8_attention(qa, ka, va, w.scale, w.causal, signs, rows=rows)
         else:
             oracle.naive_attention(qa, ka, va, w.scale, w.causal, rows=rows, q_offset=q_offset)
         dt = time.perf_counter() - t0
@@ -320,6 +332,15 @@ def run_ours(args, w, rank, world, local_rank):
         launches_per_step = 3
         inputs = ((q, qh), (k, kh), (v, vh), (o, o.cpu().pin_memory()), (lse, lse.cpu().pin_memory()), (do, doh))
         outputs = grads[:3]
+    elif w.direction == "fp8":
+        signs_h = make_workload_signs(w).pin_memory()
+        signs = signs_h.to(dev, non_blocking=True)
+        ws8 = torch.empty(fa.fa_fwd_fp8_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
+        step = lambda: fa.fa_fwd_fp8(q, k, v, signs, o, lse, scale=w.scale, causal=w.causal,  # noqa: E731
+                                     workspace=ws8, stream=stream)
+        launches_per_step = 2  # quantisation, attention
+        inputs = ((q, qh), (k, kh), (v, vh), (signs, signs_h))
+        outputs = (o, lse)
     else:
         step = lambda: fwd(q, k, v, o, lse, ws, stream)  # noqa: E731
         launches_per_step = 2 if w.n_splits > 1 else 1
@@ -391,16 +412,20 @@ def run_ours(args, w, rank, world, local_rank):
                     "algorithmic_flops": flops, "algorithmic_bytes": w.algorithmic_bytes()}
     else:
         achieved = flops / (ms * 1e-3) / 1e12
+        peak_label = f"bf16 dense burst, {peak_kind}"
+        if w.direction == "fp8":  # E4M3 dense = the measured bf16 peak x 2 (nominal 4.5 / 2.25 PFLOP/s)
+            peak_tf, peak_label = 2.0 * peak_tf, f"E4M3 dense = 2 x bf16 dense burst ({peak_kind})"
         roofline = {"bound": "tensor", "achieved": achieved, "peak": peak_tf, "unit": "TFLOP/s",
                     "frac": achieved / peak_tf, "traffic": measured_traffic(w.name),
-                    "peak_kind": f"bf16 dense burst, {peak_kind}"
-                                 + ("; timed over the step's three launches (D, dK/dV, dQ)"
-                                    if w.direction == "bwd" else ""),
+                    "peak_kind": peak_label
+                                 + {"bwd": "; timed over the step's three launches (D, dK/dV, dQ)",
+                                    "fp8": "; timed over the step's two launches (quantisation, attention)"}
+                                 .get(w.direction, ""),
                     "algorithmic_flops": flops, "algorithmic_bytes": w.algorithmic_bytes()}
     line = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "vs_baseline": None, "dtype": "e4m3" if w.direction == "fp8" else "bf16", "data": "synthetic",
         "config": workload_config(w, "flushed between timed launches (256 MiB write); "
                                      "per-launch CUDA events on the launch stream"),
         "roofline": roofline,

@@ -90,6 +90,21 @@ bool encode_map(CUtensorMap* m, const void* base, int heads, int rows, int d) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [heads, rows, row_bytes] bytes viewed as 3-D; box = 128 bytes x 128 rows x 1 head.
+bool encode_map_u8(CUtensorMap* m, const void* base, int heads, int rows, int row_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(row_bytes), static_cast<cuuint64_t>(rows),
+                              static_cast<cuuint64_t>(heads)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(row_bytes),
+                                 static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(row_bytes)};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // FA_OK when device `dev` is compute capability 10.3, FA_ERR_ARCH when it is not.
 int check_arch(int dev) {
   int major = 0, minor = 0;

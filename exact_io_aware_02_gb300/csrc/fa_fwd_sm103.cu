@@ -700,8 +700,10 @@ int static_workspace(void** out) {
 
 }  // namespace
 
-// status word of the backward translation unit (fa_bwd_sm103.cu): read, optionally cleared
+// status words of the backward (fa_bwd_sm103.cu) and FP8 (fa_fp8_sm103.cu) translation
+// units: read, optionally cleared
 int bwd_status_word(int clear);
+int fp8_status_word(int clear);
 
 }  // namespace fa
 
@@ -757,9 +759,12 @@ int fa_status(int clear, cudaStream_t stream) {
     const unsigned int zero = 0;
     if (cudaMemcpyToSymbol(fa::g_status, &zero, sizeof(zero)) != cudaSuccess) return FA_ERR_CUDA;
   }
-  const int bwd_word = fa::bwd_status_word(clear);  // the backward translation unit's word
+  const int bwd_word = fa::bwd_status_word(clear);  // the other translation units' words
   if (bwd_word < 0) return bwd_word;
-  return static_cast<int>((word | static_cast<unsigned int>(bwd_word)) & 0x7fffffffu);
+  const int fp8_word = fa::fp8_status_word(clear);
+  if (fp8_word < 0) return fp8_word;
+  return static_cast<int>((word | static_cast<unsigned int>(bwd_word) | static_cast<unsigned int>(fp8_word)) &
+                          0x7fffffffu);
 }
 
 const char* fa_strerror(int code) {

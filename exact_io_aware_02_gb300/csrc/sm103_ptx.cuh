@@ -299,6 +299,35 @@ __device__ __forceinline__ void mma_ts_i(uint32_t d_tmem, uint32_t a_tmem, uint6
       : "memory");
 }
 
+// Instruction descriptor, kind::f8f6f4: A and B E4M3 (format code 0), D f32, both operands
+// K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3_f32(int M, int N) {
+  return (1u << 4)                                   // D format: f32
+         | (0u << 7)                                 // A format: E4M3
+         | (0u << 10)                                // B format: E4M3
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+// 8-bit MMAs (K = 32 per instruction): A and B from shared memory, or A from tensor memory
+template <int kAccumulate>
+__device__ __forceinline__ void mma_ss_f8_i(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "n"(kAccumulate)
+      : "memory");
+}
+template <int kAccumulate>
+__device__ __forceinline__ void mma_ts_f8_i(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "n"(kAccumulate)
+      : "memory");
+}
+
 // true in exactly one lane of the (fully converged) warp
 __device__ __forceinline__ bool elect_one() {
   uint32_t pred = 0;
@@ -335,6 +364,18 @@ __device__ __forceinline__ void regs_decrease() {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t r;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// Four floats to E4M3 (round to nearest even, saturating at +-448), element 0 in the
+// lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float e0, float e1, float e2, float e3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(e0), "f"(e1), "f"(e2), "f"(e3));
   return r;
 }
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,

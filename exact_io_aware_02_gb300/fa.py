@@ -26,7 +26,8 @@ FA_STATIC_WORKSPACE_BYTES = 16 << 20
 FA_STATUS_TIMEOUT = 0x1
 
 EXPORTED = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_gqa_workspace_bytes", "fa_fwd_gqa_static_workspace",
-            "fa_bwd", "fa_status", "fa_fwd_withheld_tile", "fa_strerror", "fa_version")
+            "fa_bwd", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "fa_status", "fa_fwd_withheld_tile",
+            "fa_strerror", "fa_version")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
@@ -46,6 +47,10 @@ lib.fa_fwd_withheld_tile.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f
 lib.fa_fwd_withheld_tile.restype = _i
 lib.fa_bwd.argtypes = [_vp] * 10 + [_i, _i, _i, _i, _i, _f, _i, _vp]
 lib.fa_bwd.restype = _i
+lib.fa_fwd_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, ctypes.c_size_t, _vp]
+lib.fa_fwd_fp8.restype = _i
+lib.fa_fwd_fp8_workspace_bytes.argtypes = [_i, _i, _i, _i]
+lib.fa_fwd_fp8_workspace_bytes.restype = ctypes.c_size_t
 lib.fa_status.argtypes = [_i, _vp]
 lib.fa_status.restype = _i
 lib.fa_strerror.argtypes = [_i]
@@ -174,6 +179,35 @@ def fa_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, delta=None, scale=N
     if rc != FA_OK:
         raise FAError(rc)
     return dq, dk, dv, delta
+
+
+def fa_fwd_fp8_workspace_bytes(B, H, N, d) -> int:
+    return int(lib.fa_fwd_fp8_workspace_bytes(B, H, N, d))
+
+
+def fa_fwd_fp8(q, k, v, signs, o=None, lse=None, scale=None, causal=False, workspace=None, stream=None):
+    """FP8 attention forward (block-wise E4M3 with incoherent processing).  q, k, v: CUDA
+    bf16 [B, H, N, 128]; signs: CUDA int8 [128] (the rotation's random signs).  Returns
+    (o, lse).  ``workspace`` (a CUDA uint8 tensor of fa_fwd_fp8_workspace_bytes bytes,
+    256-byte aligned) is allocated here when omitted; afterwards it holds the quantised
+    tensors and their scales (layout in include/fa_gb300.h)."""
+    if q.dim() != 4 or q.shape != k.shape or q.shape != v.shape:
+        raise ValueError("q, k, v must share one [B, H, N, d] shape")
+    B, H, N, d = q.shape
+    o = torch.empty_like(q) if o is None else o
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    ws_bytes = fa_fwd_fp8_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    rc = lib.fa_fwd_fp8(q.data_ptr(), k.data_ptr(), v.data_ptr(), signs.data_ptr(), o.data_ptr(),
+                        lse.data_ptr(), B, H, N, d, float(scale), int(bool(causal)), workspace.data_ptr(),
+                        workspace.numel() * workspace.element_size(), _stream_handle(stream, q.device))
+    if rc != FA_OK:
+        raise FAError(rc)
+    return o, lse
 
 
 def fa_fwd_withheld_tile(q, k, v, o=None, lse=None, scale=None, causal=False,

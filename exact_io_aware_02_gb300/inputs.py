@@ -33,7 +33,8 @@ class Workload:
     Nk: int | None = None
     n_splits: int = 1
     bound: str = "tensor"   # the roofline that bounds it: "tensor" or "hbm"
-    direction: str = "fwd"  # "fwd": O and LSE; "bwd": dQ, dK, dV from O, LSE and dO
+    direction: str = "fwd"  # "fwd": O and LSE; "bwd": dQ, dK, dV from O, LSE and dO;
+                            # "fp8": O and LSE with E4M3 products (fa_fwd_fp8)
 
     @property
     def hkv(self) -> int:
@@ -84,6 +85,9 @@ WORKLOADS = {
         Workload("bwd_causal_n8192_d128", 2, 16, 8192, 128, True, seed=20263, direction="bwd"),
         # a small backward (inputs of 16 MiB per tensor) for full-section profiler captures
         Workload("bwd_causal_n2048_d128", 2, 16, 2048, 128, True, seed=20268, direction="bwd"),
+        # the causal prefill shape through the FP8 path (same inputs as the bf16 headline)
+        Workload("fp8_causal_n8192_d128", 2, 16, 8192, 128, True, seed=20263, direction="fp8"),
+        Workload("fp8_causal_n2048_d128", 2, 16, 2048, 128, True, seed=20268, direction="fp8"),
     )
 }
 
@@ -116,6 +120,18 @@ def make_dout(shape, seed: int, std: float = 1.0):
     drawn from its own Generator(seed)."""
     g = torch.Generator().manual_seed(int(seed))
     return (torch.randn(tuple(shape), generator=g, dtype=torch.float32) * std).to(torch.bfloat16)
+
+
+def make_signs(d: int, seed: int):
+    """The incoherent-processing rotation's random signs: CPU int8 [d] of +1 / -1 drawn
+    from Generator(seed)."""
+    g = torch.Generator().manual_seed(int(seed))
+    return (torch.randint(0, 2, (d,), generator=g) * 2 - 1).to(torch.int8)
+
+
+def make_workload_signs(w: Workload):
+    """The rotation signs of an FP8 workload: seed = the workload's seed + 200."""
+    return make_signs(w.d, w.seed + 200)
 
 
 def make_workload_dout(w: Workload):

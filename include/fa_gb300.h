@@ -150,6 +150,45 @@ int fa_fwd_gqa_static_workspace(const void* q, const void* k, const void* v, voi
                                 int causal, int n_splits, cudaStream_t stream);
 
 /*
+ * fa_fwd_fp8 -- attention forward with FP8 (E4M3) tensor-core products: block-wise
+ * quantisation with incoherent processing (§10 item ③ and §12.2 of the zzszmyf.github.io
+ * notes "FlashAttention 原理是什么？为什么又省显存又快").
+ *
+ * Q and K are rotated row by row, q' = (q * signs) H / sqrt(128) with H the 128 x 128
+ * Hadamard matrix, which leaves every score q.k unchanged and spreads outlier coordinates.
+ * Q', K' and V are then quantised per 128-row tile of each (batch, head) to E4M3 codes with
+ * one fp32 scale per tile (max|x| / 448).  The scores come from E4M3 products with fp32
+ * accumulation and the descales; P is rounded to E4M3 for its product with V.  O and LSE have
+ * the meaning they have in fa_fwd (LSE from the unrounded P).
+ *
+ * q, k, v   : device, bf16, contiguous [B, H, N, 128].  Read only.  16-byte aligned.
+ * signs     : device, int8 [128]; a negative entry means -1, any other +1.  Read only.
+ * o, lse    : device, bf16 [B, H, N, 128] and fp32 [B, H, N].  Written.
+ * d         : must be 128.  N >= 1 and ceil(N / 128) <= 1024.  scale finite and > 0.
+ * causal    : nonzero = query i sees keys 0..i.
+ * workspace : device, 256-byte aligned, at least fa_fwd_fp8_workspace_bytes(B, H, N, d)
+ *             bytes, with N_pad = 128 * ceil(N / 128) and T = N_pad / 128:
+ *               [0, C)        Q' codes, E4M3 [B*H, N_pad, 128]
+ *               [C, 2C)       K' codes, E4M3 [B*H, N_pad, 128]
+ *               [2C, 3C)      V codes transposed, E4M3 [B*H, 128, N_pad]
+ *               then three fp32 arrays [B*H, T] of tile scales (Q', K', V), each at a
+ *               256-byte boundary; C = B*H*N_pad*128 rounded up to 256.
+ *             Rows past N hold zero codes.  The call writes it; it is left holding the
+ *             quantised tensors.
+ * No output may overlap an input or the workspace.  Two kernels are enqueued on `stream`;
+ * on an error return nothing was enqueued.  A device-side wait that gives up sets
+ * FA_STATUS_TIMEOUT.
+ *
+ * Returns FA_OK, FA_ERR_ARG, FA_ERR_ARCH or FA_ERR_LAUNCH.
+ */
+int fa_fwd_fp8(const void* q, const void* k, const void* v, const signed char* signs, void* o,
+               float* lse, int B, int H, int N, int d, float scale, int causal, void* workspace,
+               size_t workspace_bytes, cudaStream_t stream);
+
+/* Bytes of workspace fa_fwd_fp8 needs (0 for sizes it would reject: d != 128, B, H, N < 1). */
+size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d);
+
+/*
  * fa_bwd -- exact attention backward: dQ, dK, dV from the forward's O and LSE.
  *
  * The forward saves only O and the per-row LSE; this call rebuilds S = scale*Q K^T

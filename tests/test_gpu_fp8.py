@@ -1,0 +1,225 @@
+"""GPU parity of fa_fwd_fp8 (block-wise E4M3 attention with incoherent processing) against
+the fp64 FP8 oracle (oracle/fp8.py), through the C ABI.
+
+Two stages are checked.
+* The quantisation, code by code: the workspace holds the E4M3 codes of Q', K' (rotated)
+  and V (transposed) and their tile scales.  The kernel rotates in fp32 and the oracle in
+  fp64, so a value that lies within fp32 rounding of an E4M3 tie may round the other way:
+  every code must equal the oracle's or sit one E4M3 step from it, and nearly all must be
+  equal.  Scales agree to fp32 rounding.
+* The attention.  The oracle's reference is the exact attention of its dequantised Q', K'
+  and V; the kernel also rounds P to E4M3 before the product with V.  The size of that one
+  rounding is measured on the same inputs with the oracle's P-rounded variant (m_P), and the
+  kernel must stay within mean|dO| <= 1.5 mean(m_P) + 1e-3 and max|dO| <= 2 max(m_P) + 2e-2.
+  LSE does not see the P rounding: |dLSE| <= 1e-3 max(1, |LSE|).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.attention as exact
+import oracle.fp8 as f8
+from exact_io_aware_02_gb300.inputs import (WORKLOADS, make_qkv, make_signs, make_workload, make_workload_signs,
+                                            sample_rows, sample_slices)
+
+pytestmark = pytest.mark.gpu
+D = 128
+
+
+@pytest.fixture(scope="module")
+def fa():
+    import __graft_entry__ as entry
+    entry.build()
+    from exact_io_aware_02_gb300 import fa as mod
+    if not torch.cuda.is_available():
+        pytest.fail("a GPU test ran without a GPU")
+    mod.fa_status(clear=True)
+    return mod
+
+
+def _np(t):
+    return t.to(torch.float64).cpu().numpy()
+
+
+def run(fa, q, k, v, signs, causal, scale=None):
+    dev = torch.device("cuda")
+    B, H, N, _ = q.shape
+    ws = torch.empty(fa.fa_fwd_fp8_workspace_bytes(B, H, N, D), dtype=torch.uint8, device=dev)
+    o, lse = fa.fa_fwd_fp8(q.to(dev), k.to(dev), v.to(dev), signs.to(dev), scale=scale, causal=causal,
+                           workspace=ws)
+    torch.cuda.synchronize()
+    return o.cpu(), lse.cpu(), ws.cpu()
+
+
+def decode_workspace(ws, B, H, N):
+    """q8, k8 [BH, N_pad, 128], v8 [BH, N_pad, 128] (un-transposed) as floats; scales."""
+    BH, n_pad = B * H, (N + 127) // 128 * 128
+    T = n_pad // 128
+    C = (BH * n_pad * D + 255) // 256 * 256
+    SC = (BH * T * 4 + 255) // 256 * 256
+
+    def codes(off, shape):
+        return ws[off:off + BH * n_pad * D].view(torch.float8_e4m3fn).to(torch.float64).reshape(shape).numpy()
+    q8 = codes(0, (BH, n_pad, D))
+    k8 = codes(C, (BH, n_pad, D))
+    v8 = codes(2 * C, (BH, D, n_pad)).transpose(0, 2, 1)
+
+    def scales(off):
+        return ws[off:off + BH * T * 4].view(torch.float32).to(torch.float64).reshape(BH, T).numpy()
+    return q8, k8, v8, scales(3 * C), scales(3 * C + SC), scales(3 * C + 2 * SC)
+
+
+def e4m3_step(x):
+    a = np.abs(x)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -6)))
+    return np.where(a < 2.0 ** -6, 2.0 ** -9, 2.0 ** (e - 3))
+
+
+def check_codes(got, want):
+    equal = got == want
+    near = np.abs(got - want) <= e4m3_step(np.maximum(np.abs(got), np.abs(want))) * (1 + 1e-9)
+    return float(equal.mean()), bool(near.all())
+
+
+CASES = [  # B, H, N, causal, qk_std
+    (1, 2, 128, False, 1.0),
+    (1, 2, 1000, True, 1.0),     # ragged last tile
+    (2, 2, 2048, True, 1.0),
+    (1, 2, 640, False, 3.0),     # sharp rows
+    (1, 1, 1, True, 1.0),        # one row
+    (1, 3, 129, False, 1.0),     # one row past a tile
+]
+IDS = ["b{}h{}n{}{}_std{}".format(b, h, n, "c" if c else "", int(s)) for b, h, n, c, s in CASES]
+
+
+@pytest.mark.parametrize("case", CASES, ids=IDS)
+def test_fp8_quantisation_matches_oracle(fa, case):
+    B, H, N, causal, std = case
+    q, k, v = make_qkv(B, H, N, D, seed=8100 + N, qk_std=std)
+    signs = make_signs(D, 8200 + N)
+    _, _, ws = run(fa, q, k, v, signs, causal)
+    q8, k8, v8, sq, sk, sv = decode_workspace(ws, B, H, N)
+    s = signs.numpy().astype(np.float64)
+    n_pad = q8.shape[1]
+    for bh in range(B * H):
+        b, h = divmod(bh, H)
+        for got, gs, src, rot in ((q8, sq, q, True), (k8, sk, k, True), (v8, sv, v, False)):
+            x = _np(src[b, h])
+            x = f8.rotate(x, s) if rot else x
+            codes, scales = f8.quantize_blocks(x)
+            assert np.allclose(gs[bh], scales, rtol=2e-6, atol=0)
+            frac, near = check_codes(got[bh, :N], codes)
+            assert near and frac > 0.995, (frac, near)
+            assert not np.any(got[bh, N:n_pad])  # padding rows hold zero codes
+
+
+def fp8_stats(o, lse, q, k, v, signs, causal, scale, heads, rows=None):
+    s = signs.numpy().astype(np.float64)
+    out = {"d_mean": [], "d_max": 0.0, "m_mean": [], "m_max": 0.0, "lse": 0.0, "n": []}
+    for b, h in heads:
+        qa, ka, va = _np(q[b, h]), _np(k[b, h]), _np(v[b, h])
+        ro, rl = f8.fp8_attention(qa, ka, va, scale, causal, s, rows=rows)
+        mo, _ = f8.fp8_attention(qa, ka, va, scale, causal, s, rows=rows, quantize_p=True)
+        go = _np(o[b, h]) if rows is None else _np(o[b, h])[rows]
+        gl = _np(lse[b, h]) if rows is None else _np(lse[b, h])[rows]
+        d = np.abs(go - ro)
+        m = np.abs(mo - ro)
+        out["d_mean"].append(d.mean())
+        out["m_mean"].append(m.mean())
+        out["n"].append(d.size)
+        out["d_max"] = max(out["d_max"], float(d.max()))
+        out["m_max"] = max(out["m_max"], float(m.max()))
+        out["lse"] = max(out["lse"], float(np.max(np.abs(gl - rl) / np.maximum(1.0, np.abs(rl)))))
+        assert np.all(np.isfinite(go)) and np.all(np.isfinite(gl))
+    w = np.array(out["n"], dtype=np.float64)
+    out["d_mean"] = float(np.average(out["d_mean"], weights=w))
+    out["m_mean"] = float(np.average(out["m_mean"], weights=w))
+    return out
+
+
+def within(st):
+    return (st["d_mean"] <= 1.5 * st["m_mean"] + 1e-3 and st["d_max"] <= 2 * st["m_max"] + 2e-2
+            and st["lse"] <= 1e-3)
+
+
+@pytest.mark.parametrize("case", CASES, ids=IDS)
+def test_fp8_attention_parity(fa, case):
+    B, H, N, causal, std = case
+    q, k, v = make_qkv(B, H, N, D, seed=8100 + N, qk_std=std)
+    signs = make_signs(D, 8200 + N)
+    scale = 1.0 / math.sqrt(D)
+    o, lse, _ = run(fa, q, k, v, signs, causal)
+    st = fp8_stats(o, lse, q, k, v, signs, causal, scale, [(b, h) for b in range(B) for h in range(H)])
+    print(case, st)
+    assert within(st), st
+
+
+def test_fp8_close_to_exact_attention(fa):
+    """The FP8 result is as close to exact (bf16-input) attention as the method's own
+    model: RMSE within 1.25x of the oracle's P-rounded FP8 attention."""
+    B, H, N = 1, 2, 1024
+    q, k, v = make_qkv(B, H, N, D, seed=8301)
+    signs = make_signs(D, 8302)
+    o, _, _ = run(fa, q, k, v, signs, True)
+    s = signs.numpy().astype(np.float64)
+    for h in range(H):
+        qa, ka, va = _np(q[0, h]), _np(k[0, h]), _np(v[0, h])
+        oe, _ = exact.naive_attention(qa, ka, va, 1 / math.sqrt(D), True)
+        om, _ = f8.fp8_attention(qa, ka, va, 1 / math.sqrt(D), True, s, quantize_p=True)
+        rmse_k = float(np.sqrt(np.mean((_np(o[0, h]) - oe) ** 2)))
+        rmse_m = float(np.sqrt(np.mean((om - oe) ** 2)))
+        print("rmse kernel", rmse_k, "model", rmse_m)
+        assert rmse_k <= 1.25 * rmse_m + 1e-4
+
+
+FP8_WORKLOADS = [n for n, w in WORKLOADS.items() if w.direction == "fp8"]
+
+
+@pytest.mark.parametrize("name", FP8_WORKLOADS)
+def test_fp8_workload_full_size_sampled(fa, name):
+    w = WORKLOADS[name]
+    q, k, v = make_workload(w)
+    signs = make_workload_signs(w)
+    o, lse, _ = run(fa, q, k, v, signs, w.causal)
+    heads = sample_slices(w.B, w.H, 2, w.seed + 1)
+    rows = sample_rows(w.N, 256, w.seed + 2)
+    st = fp8_stats(o, lse, q, k, v, signs, w.causal, w.scale, heads, rows)
+    print(name, st)
+    assert within(st), st
+    assert torch.isfinite(o.to(torch.float32)).all() and torch.isfinite(lse).all()
+    assert fa.fa_status(clear=False) == 0
+
+
+def test_fp8_repeatable_and_status_clean(fa):
+    q, k, v = make_qkv(1, 2, 700, D, seed=8401)
+    signs = make_signs(D, 8402)
+    a = run(fa, q, k, v, signs, True)
+    b = run(fa, q, k, v, signs, True)
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+    assert fa.fa_status(clear=False) == 0
+
+
+def test_fp8_argument_errors(fa):
+    dev = torch.device("cuda")
+    q, k, v = (t.to(dev) for t in make_qkv(1, 1, 256, D, seed=8501))
+    signs = make_signs(D, 8502).to(dev)
+    o = torch.full_like(q, 5.0)
+    lse = torch.full((1, 1, 256), 5.0, device=dev)
+    need = fa.fa_fwd_fp8_workspace_bytes(1, 1, 256, D)
+    assert fa.fa_fwd_fp8_workspace_bytes(1, 1, 256, 64) == 0
+    ws = torch.empty(need + 512, dtype=torch.uint8, device=dev)
+    with pytest.raises(fa.FAError):  # workspace too small
+        fa.fa_fwd_fp8(q, k, v, signs, o, lse, workspace=ws[: need - 256])
+    with pytest.raises(fa.FAError):  # workspace not 256-byte aligned
+        fa.fa_fwd_fp8(q, k, v, signs, o, lse, workspace=ws[16: need + 16])
+    with pytest.raises(fa.FAError):  # d = 64 is not supported
+        q64 = torch.zeros((1, 1, 256, 64), dtype=torch.bfloat16, device=dev)
+        fa.fa_fwd_fp8(q64, q64.clone(), q64.clone(), signs, workspace=ws)
+    with pytest.raises(fa.FAError):  # output overlaps the workspace
+        fa.fa_fwd_fp8(q, k, v, signs, ws[:256 * D * 2].view(torch.bfloat16).view(1, 1, 256, D), lse,
+                      workspace=ws)
+    torch.cuda.synchronize()
+    assert bool((o == 5.0).all()) and bool((lse == 5.0).all())

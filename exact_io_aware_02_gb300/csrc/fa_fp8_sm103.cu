@@ -29,7 +29,7 @@
 namespace fa {
 
 constexpr int kFp8D = 128;
-constexpr int kQuantThreads = 256;  // 8 warps x 16 rows
+constexpr int kQuantThreads = 512;  // 16 warps x 8 rows
 constexpr int kFp8Threads = 384;
 constexpr uint32_t kFp8SoftmaxRegs = 216;
 constexpr uint32_t kFp8OtherRegs = 72;
@@ -49,100 +49,139 @@ struct QuantParams {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// One CTA per 128-row tile of Q, K or V; 16 warps of 8 rows.
+//   Q and K: four lanes per row, 32 consecutive columns each.  The rotation (v * sigma) H /
+//   sqrt(128) is the fast Walsh-Hadamard transform: butterflies (a, b) -> (a + b, a - b) (the
+//   lower index keeps the sum) at distances 1 .. 16 inside the lane (packed f32x2 adds) and
+//   32, 64 across the row's four lanes (shuffles).
+//   V: one lane per 4 columns of the warp's 8 rows, written transposed (8 keys per store).
+// The tile's largest magnitude sets the scale, so the rows stay in registers between the
+// maximum and the quantisation.
 __global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const QuantParams p) {
   const int which = blockIdx.y;  // 0 Q, 1 K, 2 V
   const int tile = blockIdx.x % p.n_tiles;
   const int bh = blockIdx.x / p.n_tiles;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __shared__ float warp_max[kQuantThreads / 32];
-  const bool rotate = which < 2;
-  float sg[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) sg[e] = (rotate && p.signs[4 * lane + e] < 0) ? -1.f : 1.f;
-  // this lane holds columns 4*lane .. 4*lane+3 of the warp's 16 rows
   // select the tensor with plain branches (indexing the parameter arrays by a runtime value
   // would copy them to local memory)
   const uint16_t* src = which == 0 ? p.src[0] : (which == 1 ? p.src[1] : p.src[2]);
   uint8_t* dst = which == 0 ? p.dst[0] : (which == 1 ? p.dst[1] : p.dst[2]);
   float* scales = which == 0 ? p.scales[0] : (which == 1 ? p.scales[1] : p.scales[2]);
-  float x[16][4];
+  const int r0 = tile * 128 + warp * 8;  // this warp's 8 rows
   float amax = 0.f;
+  if (which < 2) {
+    const int seg = lane & 3, row = r0 + (lane >> 2);
+    float x[32];
+    if (row < p.N) {
+      const uint4* s4 = reinterpret_cast<const uint4*>(src + (static_cast<size_t>(bh) * p.N + row) * kFp8D + 32 * seg);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    const int r = tile * 128 + warp * 16 + i;
-    float v[4] = {0.f, 0.f, 0.f, 0.f};
-    if (r < p.N) {
-      const uint2 raw = *reinterpret_cast<const uint2*>(src + (static_cast<size_t>(bh) * p.N + r) * kFp8D + 4 * lane);
-      v[0] = bf16_lo(raw.x);
-      v[1] = bf16_hi(raw.x);
-      v[2] = bf16_lo(raw.y);
-      v[3] = bf16_hi(raw.y);
-    }
-    if (rotate) {
-      // (v * sigma) H / sqrt(128): butterflies (a, b) -> (a + b, a - b) at distances 1, 2
-      // inside the lane and 4 .. 64 across lanes (the lower index keeps the sum)
+      for (int c = 0; c < 4; ++c) {
+        const uint4 raw = s4[c];
+        const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] *= sg[e];
-      float a = v[0], b = v[1];
-      v[0] = a + b;
-      v[1] = a - b;
-      a = v[2];
-      b = v[3];
-      v[2] = a + b;
-      v[3] = a - b;
-      a = v[0];
-      b = v[2];
-      v[0] = a + b;
-      v[2] = a - b;
-      a = v[1];
-      b = v[3];
-      v[1] = a + b;
-      v[3] = a - b;
-#pragma unroll
-      for (int m = 1; m < 32; m <<= 1) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float o = __shfl_xor_sync(0xffffffffu, v[e], m);
-          v[e] = (lane & m) ? o - v[e] : v[e] + o;
+        for (int i = 0; i < 4; ++i) {
+          x[8 * c + 2 * i] = bf16_lo(wv[i]);
+          x[8 * c + 2 * i + 1] = bf16_hi(wv[i]);
         }
       }
+    } else {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) v[e] *= 0.08838834764831845f;  // 1 / sqrt(128)
+      for (int i = 0; i < 32; ++i) x[i] = 0.f;
+    }
+    // signs of this lane's 32 columns (two 16-byte loads): the sign bit of each int8 is
+    // moved onto the float's sign bit
+    {
+      const uint4* sp = reinterpret_cast<const uint4*>(p.signs + 32 * seg);
+      const uint4 s0 = sp[0], s1 = sp[1];
+      const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        x[i] = __uint_as_float(__float_as_uint(x[i]) ^ ((sw[i >> 2] << (24 - 8 * (i & 3))) & 0x80000000u));
     }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      x[i][e] = v[e];
-      amax = fmaxf(amax, fabsf(v[e]));
+    for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+      for (int i = 0; i < 32; i += 2 * h) {
+#pragma unroll
+        for (int k = 0; k < h; k += 2) {
+          if (h == 1) {
+            const float a = x[i], b = x[i + 1];
+            x[i] = a + b;
+            x[i + 1] = a - b;
+          } else {
+            const float2 a = make_float2(x[i + k], x[i + k + 1]), b = make_float2(x[i + k + h], x[i + k + h + 1]);
+            const float2 su = __fadd2_rn(a, b), df = __fadd2_rn(a, make_float2(-b.x, -b.y));
+            x[i + k] = su.x;
+            x[i + k + 1] = su.y;
+            x[i + k + h] = df.x;
+            x[i + k + h + 1] = df.y;
+          }
+        }
+      }
     }
-  }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  if (lane == 0) warp_max[warp] = amax;
-  __syncthreads();
-  amax = warp_max[0];
+    for (int m = 1; m < 4; m <<= 1) {  // distances 32 and 64: lanes seg ^ 1, seg ^ 2
+      const float sgn = (seg & m) ? -1.f : 1.f;
 #pragma unroll
-  for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
-  const float s = amax > 0.f ? amax / 448.f : 1.f;
-  const float inv = amax > 0.f ? 448.f / amax : 1.f;
-  if (threadIdx.x == 0) scales[static_cast<size_t>(bh) * p.n_tiles + tile] = s;
-  if (rotate) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int r = tile * 128 + warp * 16 + i;  // rows past N hold zeros
-      *reinterpret_cast<uint32_t*>(dst + (static_cast<size_t>(bh) * p.n_pad + r) * kFp8D + 4 * lane) =
-          ptx::pack_e4m3x4(x[i][0] * inv, x[i][1] * inv, x[i][2] * inv, x[i][3] * inv);
+      for (int i = 0; i < 32; ++i) {
+        const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
+        x[i] = fmaf(x[i], sgn, o);  // lower: x + o, upper: o - x
+      }
     }
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      x[i] *= 0.08838834764831845f;  // 1 / sqrt(128)
+      amax = fmaxf(amax, fabsf(x[i]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) warp_max[warp] = amax;
+    __syncthreads();
+    amax = warp_max[0];
+#pragma unroll
+    for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
+    const float inv = amax > 0.f ? 448.f / amax : 1.f;
+    if (threadIdx.x == 0) scales[static_cast<size_t>(bh) * p.n_tiles + tile] = amax > 0.f ? amax / 448.f : 1.f;
+    uint32_t wd[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      wd[i] = ptx::pack_e4m3x4(x[4 * i] * inv, x[4 * i + 1] * inv, x[4 * i + 2] * inv, x[4 * i + 3] * inv);
+    uint4* d4 = reinterpret_cast<uint4*>(dst + (static_cast<size_t>(bh) * p.n_pad + row) * kFp8D + 32 * seg);
+    d4[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);  // rows past N hold zeros
+    d4[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
   } else {
-    // V transposed: column c = 4*lane + e of the 16 keys tile*128 + warp*16 + [0, 16)
+    float v[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int r = r0 + i;
+      v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.f;
+      if (r < p.N) {
+        const uint2 raw = *reinterpret_cast<const uint2*>(src + (static_cast<size_t>(bh) * p.N + r) * kFp8D + 4 * lane);
+        v[i][0] = bf16_lo(raw.x);
+        v[i][1] = bf16_hi(raw.x);
+        v[i][2] = bf16_lo(raw.y);
+        v[i][3] = bf16_hi(raw.y);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(v[i][e]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) warp_max[warp] = amax;
+    __syncthreads();
+    amax = warp_max[0];
+#pragma unroll
+    for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
+    const float inv = amax > 0.f ? 448.f / amax : 1.f;
+    if (threadIdx.x == 0) scales[static_cast<size_t>(bh) * p.n_tiles + tile] = amax > 0.f ? amax / 448.f : 1.f;
+    // V transposed: column c = 4*lane + e, keys r0 .. r0+7 (8 bytes per store)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      uint32_t wd[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        wd[j] = ptx::pack_e4m3x4(x[4 * j][e] * inv, x[4 * j + 1][e] * inv, x[4 * j + 2][e] * inv,
-                                 x[4 * j + 3][e] * inv);
-      *reinterpret_cast<uint4*>(dst + (static_cast<size_t>(bh) * kFp8D + 4 * lane + e) * p.n_pad +
-                                tile * 128 + warp * 16) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      const uint32_t lo = ptx::pack_e4m3x4(v[0][e] * inv, v[1][e] * inv, v[2][e] * inv, v[3][e] * inv);
+      const uint32_t hi = ptx::pack_e4m3x4(v[4][e] * inv, v[5][e] * inv, v[6][e] * inv, v[7][e] * inv);
+      *reinterpret_cast<uint2*>(dst + (static_cast<size_t>(bh) * kFp8D + 4 * lane + e) * p.n_pad + r0) =
+          make_uint2(lo, hi);
     }
   }
 }
@@ -572,7 +611,8 @@ int validate_fp8(const Fp8Problem& pr, Fp8Layout* L) {
     return FA_ERR_ARG;
   fp8_layout(BH, pr.N, L);
   if (pr.workspace_bytes < L->total || (reinterpret_cast<uintptr_t>(pr.workspace) & 255u)) return FA_ERR_ARG;
-  for (const void* ptr : {pr.q, pr.k, pr.v, static_cast<const void*>(pr.o), static_cast<const void*>(pr.lse)})
+  for (const void* ptr : {pr.q, pr.k, pr.v, static_cast<const void*>(pr.signs), static_cast<const void*>(pr.o),
+                          static_cast<const void*>(pr.lse)})
     if (reinterpret_cast<uintptr_t>(ptr) & 15u) return FA_ERR_ARG;
   const size_t tb = static_cast<size_t>(BH) * pr.N * kFp8D * 2, lb = static_cast<size_t>(BH) * pr.N * 4;
   const struct { const void* p; size_t n; } in[4] = {{pr.q, tb}, {pr.k, tb}, {pr.v, tb}, {pr.signs, kFp8D}};

@@ -162,7 +162,8 @@ int fa_fwd_gqa_static_workspace(const void* q, const void* k, const void* v, voi
  * the meaning they have in fa_fwd (LSE from the unrounded P).
  *
  * q, k, v   : device, bf16, contiguous [B, H, N, 128].  Read only.  16-byte aligned.
- * signs     : device, int8 [128]; a negative entry means -1, any other +1.  Read only.
+ * signs     : device, int8 [128], 16-byte aligned; a negative entry means -1, any other +1.
+ *             Read only.
  * o, lse    : device, bf16 [B, H, N, 128] and fp32 [B, H, N].  Written.
  * d         : must be 128.  N >= 1 and ceil(N / 128) <= 1024.  scale finite and > 0.
  * causal    : nonzero = query i sees keys 0..i.

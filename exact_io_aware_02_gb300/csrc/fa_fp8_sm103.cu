@@ -190,7 +190,6 @@ __global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const Quant
 struct Fp8Cfg {
   static constexpr int kTileBytes = 128 * 128;  // 128 rows x 128 E4M3
   static constexpr int kSlots = 10;             // K_0, Vt_0, K_1, Vt_1, ...
-  static constexpr int kPrefetchAhead = 8;
   static constexpr int kOffQ = 0;
   static constexpr int kOffRing = 2 * kTileBytes;
   static constexpr int kOffTab = kOffRing + kSlots * kTileBytes;  // per K/V tile: s_k, log2 gain, 1/gain
@@ -313,18 +312,9 @@ __global__ void __launch_bounds__(kFp8Threads, 1)
     if (lane == 0) ptx::mbar_arrive(bar(C::kBarTab));
     if (lane == 0) {
       const int n_ring = 2 * nmax;
-      for (int u = 0; u < n_ring && u < C::kPrefetchAhead; ++u) {
-        if (u & 1) ptx::tma_prefetch_3d(&tm_vt, (u >> 1) * 128, 0, bh);
-        else ptx::tma_prefetch_3d(&tm_k, 0, (u >> 1) * 128, bh);
-      }
       int issued = 0;
       bool ok = true;
       for (int u = 0; u < n_ring; ++u) {
-        const int up = u + C::kPrefetchAhead;
-        if (up < n_ring) {
-          if (up & 1) ptx::tma_prefetch_3d(&tm_vt, (up >> 1) * 128, 0, bh);
-          else ptx::tma_prefetch_3d(&tm_k, 0, (up >> 1) * 128, bh);
-        }
         const int slot = u % C::kSlots, use = u / C::kSlots;
         if (use > 0 && !w.wait(bar(C::kBarEmpty + slot), (use - 1) & 1)) { ok = false; break; }
         ptx::mbar_arrive_expect_tx(bar(C::kBarFull + slot), C::kTileBytes);

@@ -63,7 +63,6 @@ struct Cfg {
   // One ring of K/V tiles in the order the MMA warp consumes and releases them:
   // K_0, V_0, K_1, V_1, ...  (tile u is K_{u/2} for even u, V_{u/2} for odd u)
   static constexpr int kSlots = D == 128 ? 5 : 12;
-  static constexpr int kPrefetchAhead = 8;  // ring tiles fetched into L2 ahead of their load
   static constexpr int kOffQ = 0;                  // Q_0, Q_1 (reused for the O staging)
   static constexpr int kOffRing = 2 * kTileBytes;
   static constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
@@ -202,17 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                            bar(C::kBarQ), c * 64, qt1 * 128, bh);
       const int n_tiles = 2 * nmax;
       const int skip = p.withhold_v0 ? 1 : -1;  // test hook: tile 1 (V_0) is never loaded
-      // warm L2 with the first tiles; then each load prefetches the tile kPrefetchAhead later
-      for (int u = 0; u < n_tiles && u < C::kPrefetchAhead; ++u)
-        for (int c = 0; c < C::kChunks; ++c)
-          ptx::tma_prefetch_3d((u & 1) ? &tm_v : &tm_k, c * 64, (t_lo + (u >> 1)) * 128, bh);
       int issued = 0;
       bool ok = true;
       for (int u = 0; u < n_tiles; ++u) {
-        const int up = u + C::kPrefetchAhead;
-        if (up < n_tiles)
-          for (int c = 0; c < C::kChunks; ++c)
-            ptx::tma_prefetch_3d((up & 1) ? &tm_v : &tm_k, c * 64, (t_lo + (up >> 1)) * 128, bh);
         const int slot = u % C::kSlots, use = u / C::kSlots;
         if (use > 0 && !w.wait(bar(C::kBarEmpty + slot), (use - 1) & 1)) { ok = false; break; }
         if (u != skip) {

@@ -73,6 +73,8 @@ struct BwdParams {
   float scale;
   float scale_log2;   // scale * log2(e)
   int causal;
+  int withhold;      // test hook: the dK/dV producer never loads stage 0's tiles and the dQ
+                     // producer never loads V_0, so those waits can only give up
   unsigned long long timeout_ns;
 };
 
@@ -319,7 +321,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (use > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarEmpty + s), (use - 1) & 1));
       if (!ok) break;
       const uint32_t st = stage_addr(s);
-      if (lane == 0) {
+      if (lane == 0 && !(p.withhold && u == 0)) {
         ptx::mbar_arrive_expect_tx(bar(kBarFull + s), 2 * C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) {
           ptx::tma_load_3d(st + c * C::kChunkBytes, &tm_q, bar(kBarFull + s), c * 64, qt * 128, bh);
@@ -339,7 +341,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     if (!ok && lane == 0) {
       w.drain(bar(kBarKV), 0);
-      for (int v = issued - S > 0 ? issued - S : 0; v < issued; ++v) w.drain(bar(kBarFull + v % S), (v / S) & 1);
+      for (int v = issued - S > 0 ? issued - S : 0; v < issued; ++v)
+        if (!(p.withhold && v == 0)) w.drain(bar(kBarFull + v % S), (v / S) & 1);
     }
     __syncwarp();
   } else if (warp == kBwdComputeWarps + 1) {
@@ -559,15 +562,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int s = u % S, use = u / S;
         prefetch(u + C::kPrefetchAhead);
         if (use > 0 && !w.wait(bar(kBarEmpty + s), (use - 1) & 1)) { ok = false; break; }
+        issued = u + 1;
+        if (p.withhold && u == 1) continue;  // test hook: V_0 is never loaded
         ptx::mbar_arrive_expect_tx(bar(kBarFull + s), C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c)
           ptx::tma_load_3d(sbase + C::kQOffRing + s * C::kTileBytes + c * C::kChunkBytes, (u & 1) ? &tm_v : &tm_k,
                            bar(kBarFull + s), c * 64, (u >> 1) * 128, bh);
-        issued = u + 1;
       }
       if (!ok) {
         w.drain(bar(kBarQ), 0);
-        for (int v = issued - S > 0 ? issued - S : 0; v < issued; ++v) w.drain(bar(kBarFull + v % S), (v / S) & 1);
+        for (int v = issued - S > 0 ? issued - S : 0; v < issued; ++v)
+          if (!(p.withhold && v == 1)) w.drain(bar(kBarFull + v % S), (v / S) & 1);
       }
     }
     __syncwarp();
@@ -771,7 +776,7 @@ int validate_bwd(const BwdProblem& pr) {
 }
 
 template <int D>
-int launch_bwd(const BwdProblem& pr, unsigned long long timeout_ns, cudaStream_t stream) {
+int launch_bwd(const BwdProblem& pr, int withhold, unsigned long long timeout_ns, cudaStream_t stream) {
   const int G = pr.Hq / pr.Hkv;
   const int groups = pr.B * pr.Hkv;
   const int R = G * pr.N;
@@ -792,6 +797,7 @@ int launch_bwd(const BwdProblem& pr, unsigned long long timeout_ns, cudaStream_t
   p.scale = pr.scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(pr.scale) * 1.4426950408889634);
   p.causal = pr.causal ? 1 : 0;
+  p.withhold = withhold;
   p.timeout_ns = timeout_ns;
   const long long rows = static_cast<long long>(groups) * R;
   const long long prep_blocks = (rows * 32 + 255) / 256;
@@ -810,12 +816,13 @@ int launch_bwd(const BwdProblem& pr, unsigned long long timeout_ns, cudaStream_t
   return FA_OK;
 }
 
-int run_bwd(const BwdProblem& pr, unsigned long long timeout_ns, cudaStream_t stream) {
+int run_bwd(const BwdProblem& pr, int withhold, unsigned long long timeout_ns, cudaStream_t stream) {
   int rc = validate_bwd(pr);
   if (rc != FA_OK) return rc;
   rc = prepare_device_bwd();
   if (rc != FA_OK) return rc;
-  return pr.d == 64 ? launch_bwd<64>(pr, timeout_ns, stream) : launch_bwd<128>(pr, timeout_ns, stream);
+  return pr.d == 64 ? launch_bwd<64>(pr, withhold, timeout_ns, stream)
+                    : launch_bwd<128>(pr, withhold, timeout_ns, stream);
 }
 
 }  // namespace
@@ -838,7 +845,15 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv, int N, int d, float scale,
            int causal, cudaStream_t stream) {
   const fa::BwdProblem pr{q, k, v, o, lse, dout, dq, dk, dv, delta, B, Hq, Hkv, N, d, scale, causal};
-  return fa::run_bwd(pr, fa::kDefaultTimeoutNs, stream);
+  return fa::run_bwd(pr, 0, fa::kDefaultTimeoutNs, stream);
+}
+
+int fa_bwd_withheld_tile(const void* q, const void* k, const void* v, const void* o, const float* lse,
+                         const void* dout, void* dq, void* dk, void* dv, float* delta, int B, int Hq, int Hkv,
+                         int N, int d, float scale, int causal, double wait_timeout_ms, cudaStream_t stream) {
+  if (!(wait_timeout_ms >= 1.0 && wait_timeout_ms <= 10000.0)) return FA_ERR_ARG;
+  const fa::BwdProblem pr{q, k, v, o, lse, dout, dq, dk, dv, delta, B, Hq, Hkv, N, d, scale, causal};
+  return fa::run_bwd(pr, 1, static_cast<unsigned long long>(wait_timeout_ms * 1e6), stream);
 }
 
 }  // extern "C"

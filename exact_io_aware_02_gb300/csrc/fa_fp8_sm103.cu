@@ -221,6 +221,7 @@ struct Fp8Params {
   float scale;
   float scale_log2;      // scale * log2(e)
   int causal;
+  int withhold;          // test hook: the producer never loads Vt_0
   unsigned long long timeout_ns;
 };
 
@@ -317,16 +318,17 @@ __global__ void __launch_bounds__(kFp8Threads, 1)
       for (int u = 0; u < n_ring; ++u) {
         const int slot = u % C::kSlots, use = u / C::kSlots;
         if (use > 0 && !w.wait(bar(C::kBarEmpty + slot), (use - 1) & 1)) { ok = false; break; }
+        issued = u + 1;
+        if (p.withhold && u == 1) continue;  // test hook: Vt_0 is never loaded
         ptx::mbar_arrive_expect_tx(bar(C::kBarFull + slot), C::kTileBytes);
         const uint32_t dst = sbase + C::kOffRing + slot * C::kTileBytes;
         if (u & 1) ptx::tma_load_3d(dst, &tm_vt, bar(C::kBarFull + slot), (u >> 1) * 128, 0, bh);  // Vt_j: keys x d
         else ptx::tma_load_3d(dst, &tm_k, bar(C::kBarFull + slot), 0, (u >> 1) * 128, bh);        // K_j
-        issued = u + 1;
       }
       if (!ok) {
         w.drain(bar(C::kBarQ), 0);
         for (int u = issued - C::kSlots > 0 ? issued - C::kSlots : 0; u < issued; ++u)
-          w.drain(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1);
+          if (!(p.withhold && u == 1)) w.drain(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1);
       }
     }
     __syncwarp();
@@ -619,7 +621,7 @@ int validate_fp8(const Fp8Problem& pr, Fp8Layout* L) {
   return FA_OK;
 }
 
-int run_fp8(const Fp8Problem& pr, cudaStream_t stream) {
+int run_fp8(const Fp8Problem& pr, int withhold, unsigned long long timeout_ns, cudaStream_t stream) {
   Fp8Layout L{};
   int rc = validate_fp8(pr, &L);
   if (rc != FA_OK) return rc;
@@ -658,7 +660,8 @@ int run_fp8(const Fp8Problem& pr, cudaStream_t stream) {
   p.scale = pr.scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(pr.scale) * 1.4426950408889634);
   p.causal = pr.causal ? 1 : 0;
-  p.timeout_ns = kDefaultTimeoutNs;
+  p.withhold = withhold;
+  p.timeout_ns = timeout_ns;
   fa_fp8_quant_kernel<<<dim3(static_cast<unsigned>(BH * n_tiles), 3), kQuantThreads, 0, stream>>>(qp);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   fa_fp8_fwd_kernel<<<static_cast<unsigned>(BH * p.n_cta_q), kFp8Threads, Fp8Cfg::kSmemBytes, stream>>>(mq, mk, mvt,
@@ -694,7 +697,15 @@ int fa_fwd_fp8(const void* q, const void* k, const void* v, const signed char* s
                int B, int H, int N, int d, float scale, int causal, void* workspace, size_t workspace_bytes,
                cudaStream_t stream) {
   const fa::Fp8Problem pr{q, k, v, signs, o, lse, B, H, N, d, scale, causal, workspace, workspace_bytes};
-  return fa::run_fp8(pr, stream);
+  return fa::run_fp8(pr, 0, fa::kDefaultTimeoutNs, stream);
+}
+
+int fa_fwd_fp8_withheld_tile(const void* q, const void* k, const void* v, const signed char* signs, void* o,
+                             float* lse, int B, int H, int N, int d, float scale, int causal, void* workspace,
+                             size_t workspace_bytes, double wait_timeout_ms, cudaStream_t stream) {
+  if (!(wait_timeout_ms >= 1.0 && wait_timeout_ms <= 10000.0)) return FA_ERR_ARG;
+  const fa::Fp8Problem pr{q, k, v, signs, o, lse, B, H, N, d, scale, causal, workspace, workspace_bytes};
+  return fa::run_fp8(pr, 1, static_cast<unsigned long long>(wait_timeout_ms * 1e6), stream);
 }
 
 }  // extern "C"

@@ -27,7 +27,7 @@ FA_STATUS_TIMEOUT = 0x1
 
 EXPORTED = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_gqa_workspace_bytes", "fa_fwd_gqa_static_workspace",
             "fa_bwd", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "fa_status", "fa_fwd_withheld_tile",
-            "fa_strerror", "fa_version")
+            "fa_bwd_withheld_tile", "fa_fwd_fp8_withheld_tile", "fa_strerror", "fa_version")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
@@ -51,6 +51,10 @@ lib.fa_fwd_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i,
 lib.fa_fwd_fp8.restype = _i
 lib.fa_fwd_fp8_workspace_bytes.argtypes = [_i, _i, _i, _i]
 lib.fa_fwd_fp8_workspace_bytes.restype = ctypes.c_size_t
+lib.fa_bwd_withheld_tile.argtypes = [_vp] * 10 + [_i, _i, _i, _i, _i, _f, _i, _d, _vp]
+lib.fa_bwd_withheld_tile.restype = _i
+lib.fa_fwd_fp8_withheld_tile.argtypes = [_vp] * 6 + [_i, _i, _i, _i, _f, _i, _vp, ctypes.c_size_t, _d, _vp]
+lib.fa_fwd_fp8_withheld_tile.restype = _i
 lib.fa_status.argtypes = [_i, _vp]
 lib.fa_status.restype = _i
 lib.fa_strerror.argtypes = [_i]
@@ -219,6 +223,32 @@ def fa_fwd_withheld_tile(q, k, v, o=None, lse=None, scale=None, causal=False,
     return lib.fa_fwd_withheld_tile(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                     lse.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
                                     float(wait_timeout_ms), _stream_handle(stream, q.device))
+
+
+def fa_bwd_withheld_tile(q, k, v, o, lse, dout, wait_timeout_ms=50.0, causal=False, stream=None) -> int:
+    """Test hook: fa_bwd with the first dK/dV stage and V tile 0 of the dQ kernel never
+    loaded; returns the C return code (outputs are allocated here and discarded)."""
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    delta = torch.empty((B, Hq, N), dtype=torch.float32, device=q.device)
+    return lib.fa_bwd_withheld_tile(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(),
+                                    dout.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), delta.data_ptr(),
+                                    B, Hq, Hkv, N, d, 1.0 / d ** 0.5, int(bool(causal)), float(wait_timeout_ms),
+                                    _stream_handle(stream, q.device))
+
+
+def fa_fwd_fp8_withheld_tile(q, k, v, signs, wait_timeout_ms=50.0, causal=False, stream=None) -> int:
+    """Test hook: fa_fwd_fp8 with V tile 0 never loaded; returns the C return code."""
+    B, H, N, d = q.shape
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    ws_bytes = fa_fwd_fp8_workspace_bytes(B, H, N, d)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=q.device)
+    return lib.fa_fwd_fp8_withheld_tile(q.data_ptr(), k.data_ptr(), v.data_ptr(), signs.data_ptr(), o.data_ptr(),
+                                        lse.data_ptr(), B, H, N, d, 1.0 / d ** 0.5, int(bool(causal)),
+                                        ws.data_ptr(), ws_bytes, float(wait_timeout_ms),
+                                        _stream_handle(stream, q.device))
 
 
 def fa_status(clear=False, stream=None) -> int:

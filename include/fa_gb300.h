@@ -244,6 +244,24 @@ int fa_fwd_withheld_tile(const void* q, const void* k, const void* v, void* o, f
                          int B, int H, int N, int d, float scale, int causal,
                          double wait_timeout_ms, cudaStream_t stream);
 
+/*
+ * fa_bwd_withheld_tile, fa_fwd_fp8_withheld_tile -- the same test hook for the backward
+ * and the FP8 forward.  Same arguments as fa_bwd / fa_fwd_fp8, plus wait_timeout_ms in
+ * [1, 10000].  The backward's dK/dV producer never loads its first stage and its dQ
+ * producer never loads V tile 0; the FP8 kernel's producer never loads V tile 0.  The
+ * waits for them give up after about wait_timeout_ms, every CTA cleans up and returns,
+ * and FA_STATUS_TIMEOUT is set; the outputs are unspecified afterwards.
+ */
+int fa_bwd_withheld_tile(const void* q, const void* k, const void* v, const void* o,
+                         const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                         float* delta, int B, int Hq, int Hkv, int N, int d, float scale,
+                         int causal, double wait_timeout_ms, cudaStream_t stream);
+int fa_fwd_fp8_withheld_tile(const void* q, const void* k, const void* v,
+                             const signed char* signs, void* o, float* lse, int B, int H,
+                             int N, int d, float scale, int causal, void* workspace,
+                             size_t workspace_bytes, double wait_timeout_ms,
+                             cudaStream_t stream);
+
 /* fa_strerror -- a static, human-readable string for a return code. */
 const char* fa_strerror(int code);
 

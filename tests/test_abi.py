@@ -64,6 +64,17 @@ def test_argument_errors_before_launch(fa, kw):
     assert _call(fa, **kw) == fa.FA_ERR_ARG
 
 
+def test_bwd_and_fp8_withheld_timeout_range(fa):
+    b = fa.lib.fa_bwd_withheld_tile
+    args = [FAKE + i * 2**30 for i in range(10)] + [1, 2, 1, 128, 128, 0.088, 1]
+    assert b(*args, 0.5, None) == fa.FA_ERR_ARG
+    assert b(*args, 20000.0, None) == fa.FA_ERR_ARG
+    f8 = fa.lib.fa_fwd_fp8_withheld_tile
+    args8 = [FAKE + i * 2**30 for i in range(6)] + [1, 1, 128, 128, 0.088, 0, FAKE + 7 * 2**30, 1 << 20]
+    assert f8(*args8, 0.0, None) == fa.FA_ERR_ARG
+    assert f8(*args8, 1e9, None) == fa.FA_ERR_ARG
+
+
 def test_withheld_tile_timeout_range(fa):
     f = fa.lib.fa_fwd_withheld_tile
     assert f(FAKE, FAKE + 2**30, FAKE + 2**31, FAKE + 3 * 2**30, FAKE + 2**32, 1, 1, 128, 128,

@@ -15,21 +15,23 @@
 //     (the factors are folded into the exp2 argument), and O = O~ * max_t s_v,t / (64 l).
 //     The rescale threshold is 2^2, so p <= 4 and P8 <= 256 stays inside E4M3's range.
 //
-// Two kernels on the caller's stream:
-//   fa_fp8_quant_kernel -- one CTA per 128-row tile of Q, K or V: the rotation (Q, K; a
-//                          Walsh-Hadamard butterfly in registers and warp shuffles), the
-//                          tile maximum, the scale and the codes.  V is written transposed
-//                          (d rows x keys): the K-major layout its product with P needs.
-//   fa_fp8_fwd_kernel   -- the bf16 forward's structure (two 128-row query tiles per CTA; a
-//                          TMA producer warp; an MMA warp; two softmax warpgroups) with
-//                          16 KB E4M3 tiles, a 10-slot K/V ring and kind::f8f6f4 MMAs.
+// Four kernels on the caller's stream:
+//   fa_fp8_rotmat_kernel -- the 128 x 128 rotation matrix (sigma_k times the Hadamard signs)
+//                           in bf16, into the workspace;
+//   fa_fp8_rot_kernel    -- one CTA per 128-row tile of Q or K: the rotation as one bf16
+//                           tensor-core product, the tile maximum, the scale and the codes;
+//   fa_fp8_vquant_kernel -- one CTA per 128-key tile of V: the scale and the codes, written
+//                           transposed (d rows x keys), the K-major layout of V's product
+//                           with P;
+//   fa_fp8_fwd_kernel    -- the bf16 forward's structure (two 128-row query tiles per CTA; a
+//                           TMA producer warp; an MMA warp; two softmax warpgroups) with
+//                           16 KB E4M3 tiles, a 10-slot K/V ring and kind::f8f6f4 MMAs.
 // d = 128, one head per K/V head, queries and keys of the same length, no split.
 #include "fa_common.cuh"
 
 namespace fa {
 
 constexpr int kFp8D = 128;
-constexpr int kQuantThreads = 512;  // 16 warps x 8 rows
 constexpr int kFp8Threads = 384;
 constexpr uint32_t kFp8SoftmaxRegs = 216;
 constexpr uint32_t kFp8OtherRegs = 72;
@@ -39,150 +41,204 @@ constexpr int kFp8MaxKvTiles = 1024;              // N <= 131072
 
 // ==================================================================== quantisation
 struct QuantParams {
-  const uint16_t* src[3];  // q, k, v: bf16 [BH, N, 128]
   uint8_t* dst[3];         // q8, k8: [BH, N_pad, 128]; vt8: [BH, 128, N_pad]
   float* scales[3];        // [BH, n_tiles]
   const int8_t* signs;     // [128], negative = -1
   int N, n_tiles, n_pad;
+  unsigned long long timeout_ns;
 };
 
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+// ==================================================================== rotation on the tensor core
+// The rotation of a tile, X' = (X * sigma) H / sqrt(128), is the product X R^T with the fixed
+// 128 x 128 matrix R[c][k] = sigma_k (-1)^popcount(c & k) (H is symmetric): +-1 entries, exact in
+// bf16, so one bf16 tcgen05 product with fp32 accumulation computes it exactly up to the
+// fp32 sums.  fa_fp8_rotmat_kernel writes R (row c, 128 bf16 each) once per call;
+// fa_fp8_rot_kernel then does, per 128-row tile of Q or K: TMA loads of the tile and of R,
+// one 128 x 128 x 128 product into tensor memory, and the epilogue (one row per thread): the
+// scaling by 1 / sqrt(128), the tile maximum, the scale and the E4M3 codes.
+constexpr int kRotThreads = 128;
+constexpr int kRotSmemBytes = 4 * 128 * 128 + 1024;  // X and R tiles, + slack for 1024-B alignment
 
-// One CTA per 128-row tile of Q, K or V; 16 warps of 8 rows.
-//   Q and K: four lanes per row, 32 consecutive columns each.  The rotation (v * sigma) H /
-//   sqrt(128) is the fast Walsh-Hadamard transform: butterflies (a, b) -> (a + b, a - b) (the
-//   lower index keeps the sum) at distances 1 .. 16 inside the lane (packed f32x2 adds) and
-//   32, 64 across the row's four lanes (shuffles).
-//   V: one lane per 4 columns of the warp's 8 rows, written transposed (8 keys per store).
-// The tile's largest magnitude sets the scale, so the rows stay in registers between the
-// maximum and the quantisation.
-__global__ void __launch_bounds__(kQuantThreads) fa_fp8_quant_kernel(const QuantParams p) {
-  const int which = blockIdx.y;  // 0 Q, 1 K, 2 V
+__global__ void __launch_bounds__(256) fa_fp8_rotmat_kernel(const int8_t* __restrict__ signs, uint16_t* __restrict__ r) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < kFp8D * kFp8D; i += gridDim.x * blockDim.x) {
+    const int c = i / kFp8D, k = i % kFp8D;
+    const bool neg = (signs[k] < 0) != ((__popc(c & k) & 1) != 0);
+    r[i] = neg ? 0xBF80u : 0x3F80u;  // bf16 -1.0 / +1.0
+  }
+}
+
+__global__ void __launch_bounds__(kRotThreads) fa_fp8_rot_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                                 const __grid_constant__ CUtensorMap tm_k,
+                                                                 const __grid_constant__ CUtensorMap tm_r,
+                                                                 const QuantParams p) {
+  constexpr int kChunk = 128 * 128;  // 128 rows x 64 bf16 (one swizzle atom wide)
+  extern __shared__ uint8_t rsm_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);  // X: [0, 32 KB), R: [32 KB, 64 KB)
+  __shared__ uint64_t bars[2];                  // tiles loaded, product done
+  __shared__ uint32_t tmem_slot, abort_flag;
+  __shared__ float warp_max[kRotThreads / 32];
+  const int which = blockIdx.y;  // 0 Q, 1 K
   const int tile = blockIdx.x % p.n_tiles;
   const int bh = blockIdx.x / p.n_tiles;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __shared__ float warp_max[kQuantThreads / 32];
-  // select the tensor with plain branches (indexing the parameter arrays by a runtime value
-  // would copy them to local memory)
-  const uint16_t* src = which == 0 ? p.src[0] : (which == 1 ? p.src[1] : p.src[2]);
-  uint8_t* dst = which == 0 ? p.dst[0] : (which == 1 ? p.dst[1] : p.dst[2]);
-  float* scales = which == 0 ? p.scales[0] : (which == 1 ? p.scales[1] : p.scales[2]);
-  const int r0 = tile * 128 + warp * 8;  // this warp's 8 rows
+  const uint32_t bar_load = ptx::smem_addr(&bars[0]), bar_mma = ptx::smem_addr(&bars[1]);
+  if (threadIdx.x == 0) {
+    ptx::mbar_init(bar_load, 1);
+    ptx::mbar_init(bar_mma, 1);
+    abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0) {
+    ptx::tmem_alloc(ptx::smem_addr(&tmem_slot), 128);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  const Waiter w{&abort_flag, p.timeout_ns};
+  bool ok = true, issued = false;
+  if (warp == 0) {
+    if (lane == 0) {
+      const CUtensorMap* mx = which == 0 ? &tm_q : &tm_k;
+      ptx::mbar_arrive_expect_tx(bar_load, 4 * kChunk);
+      for (int c = 0; c < 2; ++c) {
+        ptx::tma_load_3d(sbase + c * kChunk, mx, bar_load, c * 64, tile * 128, bh);  // rows past N: zeros
+        ptx::tma_load_3d(sbase + (2 + c) * kChunk, &tm_r, bar_load, c * 64, 0, 0);
+      }
+    }
+    ok = __all_sync(0xffffffffu, w.wait(bar_load, 0));
+    if (ok) {
+      ptx::tc_fence_after();
+      if (ptx::elect_one()) {
+        constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false);
+        const uint64_t da = ptx::smem_desc_sw128(sbase, 16, 1024), db = ptx::smem_desc_sw128(sbase + 2 * kChunk, 16, 1024);
+        ptx::mma_ss_i<0>(tmem, da, db, idesc);
+#pragma unroll
+        for (int kk = 1; kk < kFp8D / 16; ++kk) {
+          const uint64_t o = (kk >> 2) * (kChunk >> 4) + (kk & 3) * 2;
+          ptx::mma_ss_i<1>(tmem, da + o, db + o, idesc);
+        }
+        ptx::tc_commit(bar_mma);
+      }
+      __syncwarp();
+      issued = true;
+    } else if (lane == 0) {
+      w.drain(bar_load, 0);  // let the copies land before the memory is released
+    }
+  }
+  ok = __syncthreads_and(ok);
+  float x[128];
   float amax = 0.f;
-  if (which < 2) {
-    const int seg = lane & 3, row = r0 + (lane >> 2);
-    float x[32];
-    if (row < p.N) {
-      const uint4* s4 = reinterpret_cast<const uint4*>(src + (static_cast<size_t>(bh) * p.N + row) * kFp8D + 32 * seg);
+  if (ok) {
+    ok = __all_sync(0xffffffffu, w.wait(bar_mma, 0));
+    if (ok) {
+      ptx::tc_fence_after();
+      uint32_t raw[128];
+      ptx::tmem_ld128(tmem + (static_cast<uint32_t>(warp * 32) << 16), raw);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const uint4 raw = s4[c];
-        const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          x[8 * c + 2 * i] = bf16_lo(wv[i]);
-          x[8 * c + 2 * i + 1] = bf16_hi(wv[i]);
-        }
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 32; ++i) x[i] = 0.f;
-    }
-    // signs of this lane's 32 columns (two 16-byte loads): the sign bit of each int8 is
-    // moved onto the float's sign bit
-    {
-      const uint4* sp = reinterpret_cast<const uint4*>(p.signs + 32 * seg);
-      const uint4 s0 = sp[0], s1 = sp[1];
-      const uint32_t sw[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-      for (int i = 0; i < 32; ++i)
-        x[i] = __uint_as_float(__float_as_uint(x[i]) ^ ((sw[i >> 2] << (24 - 8 * (i & 3))) & 0x80000000u));
-    }
-#pragma unroll
-    for (int h = 1; h < 32; h <<= 1) {
-#pragma unroll
-      for (int i = 0; i < 32; i += 2 * h) {
-#pragma unroll
-        for (int k = 0; k < h; k += 2) {
-          if (h == 1) {
-            const float a = x[i], b = x[i + 1];
-            x[i] = a + b;
-            x[i + 1] = a - b;
-          } else {
-            const float2 a = make_float2(x[i + k], x[i + k + 1]), b = make_float2(x[i + k + h], x[i + k + h + 1]);
-            const float2 su = __fadd2_rn(a, b), df = __fadd2_rn(a, make_float2(-b.x, -b.y));
-            x[i + k] = su.x;
-            x[i + k + 1] = su.y;
-            x[i + k + h] = df.x;
-            x[i + k + h + 1] = df.y;
-          }
-        }
+      for (int i = 0; i < 128; ++i) {
+        x[i] = __uint_as_float(raw[i]) * 0.08838834764831845f;  // 1 / sqrt(128)
+        amax = fmaxf(amax, fabsf(x[i]));
       }
     }
+  }
 #pragma unroll
-    for (int m = 1; m < 4; m <<= 1) {  // distances 32 and 64: lanes seg ^ 1, seg ^ 2
-      const float sgn = (seg & m) ? -1.f : 1.f;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const float o = __shfl_xor_sync(0xffffffffu, x[i], m);
-        x[i] = fmaf(x[i], sgn, o);  // lower: x + o, upper: o - x
-      }
-    }
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      x[i] *= 0.08838834764831845f;  // 1 / sqrt(128)
-      amax = fmaxf(amax, fabsf(x[i]));
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if (lane == 0) warp_max[warp] = amax;
-    __syncthreads();
-    amax = warp_max[0];
-#pragma unroll
-    for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if (lane == 0) warp_max[warp] = amax;
+  ok = __syncthreads_and(ok);
+  if (ok) {
+    amax = fmaxf(fmaxf(warp_max[0], warp_max[1]), fmaxf(warp_max[2], warp_max[3]));
     const float inv = amax > 0.f ? 448.f / amax : 1.f;
+    float* scales = which == 0 ? p.scales[0] : p.scales[1];
+    uint8_t* dst = which == 0 ? p.dst[0] : p.dst[1];
     if (threadIdx.x == 0) scales[static_cast<size_t>(bh) * p.n_tiles + tile] = amax > 0.f ? amax / 448.f : 1.f;
-    uint32_t wd[8];
+    uint4* d4 = reinterpret_cast<uint4*>(dst + (static_cast<size_t>(bh) * p.n_pad + tile * 128 + threadIdx.x) * kFp8D);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      wd[i] = ptx::pack_e4m3x4(x[4 * i] * inv, x[4 * i + 1] * inv, x[4 * i + 2] * inv, x[4 * i + 3] * inv);
-    uint4* d4 = reinterpret_cast<uint4*>(dst + (static_cast<size_t>(bh) * p.n_pad + row) * kFp8D + 32 * seg);
-    d4[0] = make_uint4(wd[0], wd[1], wd[2], wd[3]);  // rows past N hold zeros
-    d4[1] = make_uint4(wd[4], wd[5], wd[6], wd[7]);
-  } else {
-    float v[8][4];
+    for (int g = 0; g < 8; ++g) {
+      uint32_t wd[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int r = r0 + i;
-      v[i][0] = v[i][1] = v[i][2] = v[i][3] = 0.f;
-      if (r < p.N) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(src + (static_cast<size_t>(bh) * p.N + r) * kFp8D + 4 * lane);
-        v[i][0] = bf16_lo(raw.x);
-        v[i][1] = bf16_hi(raw.x);
-        v[i][2] = bf16_lo(raw.y);
-        v[i][3] = bf16_hi(raw.y);
-      }
-#pragma unroll
-      for (int e = 0; e < 4; ++e) amax = fmaxf(amax, fabsf(v[i][e]));
+      for (int i = 0; i < 4; ++i)
+        wd[i] = ptx::pack_e4m3x4(x[16 * g + 4 * i] * inv, x[16 * g + 4 * i + 1] * inv, x[16 * g + 4 * i + 2] * inv,
+                                 x[16 * g + 4 * i + 3] * inv);
+      d4[g] = make_uint4(wd[0], wd[1], wd[2], wd[3]);  // rows past N hold zeros
     }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if (lane == 0) warp_max[warp] = amax;
+  }
+  if (warp == 0 && issued) w.drain(bar_mma, 0);  // the product completes before its memory is freed
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, 128);
+  }
+}
+
+// V: one CTA per 128-key tile.  The bf16 tile arrives by TMA (two 64-column chunks, 128-byte
+// swizzle); thread c then reads column c down the 128 keys (consecutive threads read
+// consecutive columns of one row, so the reads spread over the banks), takes the tile
+// maximum with the other threads, and writes row c of the transposed codes: the 128 keys of
+// column c, 128 contiguous bytes.
+constexpr int kVThreads = 128;
+constexpr int kVSmemBytes = 2 * 128 * 128 + 1024;
+
+__global__ void __launch_bounds__(kVThreads) fa_fp8_vquant_kernel(const __grid_constant__ CUtensorMap tm_v,
+                                                                  const QuantParams p) {
+  constexpr int kChunk = 128 * 128;
+  extern __shared__ uint8_t vsm_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(vsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  __shared__ float warp_max[kVThreads / 32];
+  const int tile = blockIdx.x % p.n_tiles, bh = blockIdx.x / p.n_tiles;
+  const int c = threadIdx.x, warp = c >> 5, lane = c & 31;
+  const uint32_t b = ptx::smem_addr(&bar);
+  if (c == 0) {
+    ptx::mbar_init(b, 1);
+    abort_flag = 0u;
+    ptx::fence_mbar_init();
+  }
+  __syncthreads();
+  const Waiter w{&abort_flag, p.timeout_ns};
+  if (c == 0) {
+    ptx::mbar_arrive_expect_tx(b, 2 * kChunk);
+    for (int h = 0; h < 2; ++h) ptx::tma_load_3d(sbase + h * kChunk, &tm_v, b, h * 64, tile * 128, bh);  // rows past N: 0
+  }
+  bool ok = __syncthreads_and(w.wait(b, 0));
+  if (!ok) {
+    if (c == 0) w.drain(b, 0);
     __syncthreads();
-    amax = warp_max[0];
+    return;
+  }
+  // column c: chunk c / 64, 16-byte granule (c % 64) / 8 of each 128-byte row, swizzled by row % 8
+  const uint32_t col_base = sbase + (c >> 6) * kChunk + (c & 7) * 2;
+  const int gran = (c & 63) >> 3;
+  float v[128];
+  float amax = 0.f;
 #pragma unroll
-    for (int w = 1; w < kQuantThreads / 32; ++w) amax = fmaxf(amax, warp_max[w]);
-    const float inv = amax > 0.f ? 448.f / amax : 1.f;
-    if (threadIdx.x == 0) scales[static_cast<size_t>(bh) * p.n_tiles + tile] = amax > 0.f ? amax / 448.f : 1.f;
-    // V transposed: column c = 4*lane + e, keys r0 .. r0+7 (8 bytes per store)
+  for (int r = 0; r < 128; ++r) {
+    uint16_t bits;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(bits) : "r"(col_base + r * 128 + ((gran ^ (r & 7)) << 4)));
+    v[r] = __uint_as_float(static_cast<uint32_t>(bits) << 16);
+    amax = fmaxf(amax, fabsf(v[r]));
+  }
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t lo = ptx::pack_e4m3x4(v[0][e] * inv, v[1][e] * inv, v[2][e] * inv, v[3][e] * inv);
-      const uint32_t hi = ptx::pack_e4m3x4(v[4][e] * inv, v[5][e] * inv, v[6][e] * inv, v[7][e] * inv);
-      *reinterpret_cast<uint2*>(dst + (static_cast<size_t>(bh) * kFp8D + 4 * lane + e) * p.n_pad + r0) =
-          make_uint2(lo, hi);
-    }
+  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+  if (lane == 0) warp_max[warp] = amax;
+  __syncthreads();
+  amax = fmaxf(fmaxf(warp_max[0], warp_max[1]), fmaxf(warp_max[2], warp_max[3]));
+  const float inv = amax > 0.f ? 448.f / amax : 1.f;
+  if (c == 0) p.scales[2][static_cast<size_t>(bh) * p.n_tiles + tile] = amax > 0.f ? amax / 448.f : 1.f;
+  uint4* d4 = reinterpret_cast<uint4*>(p.dst[2] + (static_cast<size_t>(bh) * kFp8D + c) * p.n_pad + tile * 128);
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    uint32_t wd[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      wd[i] = ptx::pack_e4m3x4(v[16 * g + 4 * i] * inv, v[16 * g + 4 * i + 1] * inv, v[16 * g + 4 * i + 2] * inv,
+                               v[16 * g + 4 * i + 3] * inv);
+    d4[g] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
   }
 }
 
@@ -553,16 +609,21 @@ int prepare_device_fp8() {
     return arch;
   }
   if (cudaFuncSetAttribute(fa_fp8_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Fp8Cfg::kSmemBytes) !=
-      cudaSuccess)
+          cudaSuccess ||
+      cudaFuncSetAttribute(fa_fp8_rot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRotSmemBytes) !=
+          cudaSuccess ||
+      cudaFuncSetAttribute(fa_fp8_vquant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmemBytes) !=
+          cudaSuccess)
     return FA_ERR_CUDA;
   g_fp8_dev_state[dev] = 1;
   return FA_OK;
 }
 
 // Workspace: q8 [BH, N_pad, 128], k8 [BH, N_pad, 128], vt8 [BH, 128, N_pad] (E4M3 codes), then
-// the fp32 scales of Q', K' and V [BH, N_pad / 128] each; every section 256-byte aligned.
+// the fp32 scales of Q', K' and V [BH, N_pad / 128] each, then the 128 x 128 bf16 rotation
+// matrix; every section 256-byte aligned.
 struct Fp8Layout {
-  size_t q8, k8, vt8, sq, sk, sv, total;
+  size_t q8, k8, vt8, sq, sk, sv, rot, total;
 };
 
 bool fp8_layout(long long BH, long long N, Fp8Layout* L) {
@@ -575,7 +636,8 @@ bool fp8_layout(long long BH, long long N, Fp8Layout* L) {
   L->sq = 3 * codes;
   L->sk = L->sq + sc;
   L->sv = L->sk + sc;
-  L->total = L->sv + sc;
+  L->rot = L->sv + sc;
+  L->total = L->rot + static_cast<size_t>(kFp8D) * kFp8D * 2;
   return true;
 }
 
@@ -631,9 +693,6 @@ int run_fp8(const Fp8Problem& pr, int withhold, unsigned long long timeout_ns, c
   const int n_tiles = (pr.N + 127) / 128, n_pad = n_tiles * 128;
   uint8_t* ws = static_cast<uint8_t*>(pr.workspace);
   QuantParams qp{};
-  qp.src[0] = static_cast<const uint16_t*>(pr.q);
-  qp.src[1] = static_cast<const uint16_t*>(pr.k);
-  qp.src[2] = static_cast<const uint16_t*>(pr.v);
   qp.dst[0] = ws + L.q8;
   qp.dst[1] = ws + L.k8;
   qp.dst[2] = ws + L.vt8;
@@ -644,9 +703,14 @@ int run_fp8(const Fp8Problem& pr, int withhold, unsigned long long timeout_ns, c
   qp.N = pr.N;
   qp.n_tiles = n_tiles;
   qp.n_pad = n_pad;
-  CUtensorMap mq, mk, mvt, mo;
+  qp.timeout_ns = timeout_ns;
+  CUtensorMap mq, mk, mvt, mo, mxq, mxk, mxv, mr;
+  uint16_t* rot = reinterpret_cast<uint16_t*>(ws + L.rot);
   if (!encode_map_u8(&mq, ws + L.q8, BH, n_pad, kFp8D) || !encode_map_u8(&mk, ws + L.k8, BH, n_pad, kFp8D) ||
-      !encode_map_u8(&mvt, ws + L.vt8, BH, kFp8D, n_pad) || !encode_map(&mo, pr.o, BH, pr.N, kFp8D))
+      !encode_map_u8(&mvt, ws + L.vt8, BH, kFp8D, n_pad) || !encode_map(&mo, pr.o, BH, pr.N, kFp8D) ||
+      !encode_map(&mxq, pr.q, BH, pr.N, kFp8D) || !encode_map(&mxk, pr.k, BH, pr.N, kFp8D) ||
+      !encode_map(&mxv, pr.v, BH, pr.N, kFp8D) ||
+      !encode_map(&mr, rot, 1, kFp8D, kFp8D))
     return FA_ERR_LAUNCH;
   Fp8Params p{};
   p.scale_q = qp.scales[0];
@@ -662,7 +726,12 @@ int run_fp8(const Fp8Problem& pr, int withhold, unsigned long long timeout_ns, c
   p.causal = pr.causal ? 1 : 0;
   p.withhold = withhold;
   p.timeout_ns = timeout_ns;
-  fa_fp8_quant_kernel<<<dim3(static_cast<unsigned>(BH * n_tiles), 3), kQuantThreads, 0, stream>>>(qp);
+  fa_fp8_rotmat_kernel<<<kFp8D * kFp8D / 256, 256, 0, stream>>>(pr.signs, rot);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  fa_fp8_rot_kernel<<<dim3(static_cast<unsigned>(BH * n_tiles), 2), kRotThreads, kRotSmemBytes, stream>>>(mxq, mxk,
+                                                                                                         mr, qp);
+  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  fa_fp8_vquant_kernel<<<static_cast<unsigned>(BH * n_tiles), kVThreads, kVSmemBytes, stream>>>(mxv, qp);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   fa_fp8_fwd_kernel<<<static_cast<unsigned>(BH * p.n_cta_q), kFp8Threads, Fp8Cfg::kSmemBytes, stream>>>(mq, mk, mvt,
                                                                                                        mo, p);

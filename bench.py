@@ -338,7 +338,7 @@ def run_ours(args, w, rank, world, local_rank):
         ws8 = torch.empty(fa.fa_fwd_fp8_workspace_bytes(w.B, w.H, w.N, w.d), dtype=torch.uint8, device=dev)
         step = lambda: fa.fa_fwd_fp8(q, k, v, signs, o, lse, scale=w.scale, causal=w.causal,  # noqa: E731
                                      workspace=ws8, stream=stream)
-        launches_per_step = 4  # rotation matrix, Q/K rotation + quantisation, V quantisation, attention
+        launches_per_step = 2  # preparation (rotation + quantisation), attention
         inputs = ((q, qh), (k, kh), (v, vh), (signs, signs_h))
         outputs = (o, lse)
     else:
@@ -419,7 +419,7 @@ def run_ours(args, w, rank, world, local_rank):
                     "frac": achieved / peak_tf, "traffic": measured_traffic(w.name),
                     "peak_kind": peak_label
                                  + {"bwd": "; timed over the step's three launches (D, dK/dV, dQ)",
-                                    "fp8": "; timed over the step's four launches (rotation matrix, Q/K and V quantisation, attention)"}
+                                    "fp8": "; timed over the step's two launches (rotation and quantisation, attention)"}
                                  .get(w.direction, ""),
                     "algorithmic_flops": flops, "algorithmic_bytes": w.algorithmic_bytes()}
     line = {

@@ -15,17 +15,15 @@
 //     (the factors are folded into the exp2 argument), and O = O~ * max_t s_v,t / (64 l).
 //     The rescale threshold is 2^2, so p <= 4 and P8 <= 256 stays inside E4M3's range.
 //
-// Four kernels on the caller's stream:
-//   fa_fp8_rotmat_kernel -- the 128 x 128 rotation matrix (sigma_k times the Hadamard signs)
-//                           in bf16, into the workspace;
-//   fa_fp8_rot_kernel    -- one CTA per 128-row tile of Q or K: the rotation as one bf16
-//                           tensor-core product, the tile maximum, the scale and the codes;
-//   fa_fp8_vquant_kernel -- one CTA per 128-key tile of V: the scale and the codes, written
-//                           transposed (d rows x keys), the K-major layout of V's product
-//                           with P;
-//   fa_fp8_fwd_kernel    -- the bf16 forward's structure (two 128-row query tiles per CTA; a
-//                           TMA producer warp; an MMA warp; two softmax warpgroups) with
-//                           16 KB E4M3 tiles, a 10-slot K/V ring and kind::f8f6f4 MMAs.
+// Two kernels on the caller's stream:
+//   fa_fp8_prep_kernel -- persistent, two CTAs per SM: the rotation of every 128-row tile of Q
+//                         and K as one bf16 tensor-core product with the 128 x 128 rotation
+//                         matrix, and the tile maximum, scale and E4M3 codes of Q', K' and V;
+//                         V is written transposed (d rows x keys), the K-major layout of its
+//                         product with P;
+//   fa_fp8_fwd_kernel  -- the bf16 forward's structure (two 128-row query tiles per CTA; a
+//                         TMA producer warp; an MMA warp; two softmax warpgroups) with
+//                         16 KB E4M3 tiles, a 10-slot K/V ring and kind::f8f6f4 MMAs.
 // d = 128, one head per K/V head, queries and keys of the same length, no split.
 #include "fa_common.cuh"
 
@@ -44,201 +42,225 @@ struct QuantParams {
   uint8_t* dst[3];         // q8, k8: [BH, N_pad, 128]; vt8: [BH, 128, N_pad]
   float* scales[3];        // [BH, n_tiles]
   const int8_t* signs;     // [128], negative = -1
-  int N, n_tiles, n_pad;
+  int BH, N, n_tiles, n_pad;
   unsigned long long timeout_ns;
 };
 
-// ==================================================================== rotation on the tensor core
-// The rotation of a tile, X' = (X * sigma) H / sqrt(128), is the product X R^T with the fixed
-// 128 x 128 matrix R[c][k] = sigma_k (-1)^popcount(c & k) (H is symmetric): +-1 entries, exact in
-// bf16, so one bf16 tcgen05 product with fp32 accumulation computes it exactly up to the
-// fp32 sums.  fa_fp8_rotmat_kernel writes R (row c, 128 bf16 each) once per call;
-// fa_fp8_rot_kernel then does, per 128-row tile of Q or K: TMA loads of the tile and of R,
-// one 128 x 128 x 128 product into tensor memory, and the epilogue (one row per thread): the
-// scaling by 1 / sqrt(128), the tile maximum, the scale and the E4M3 codes.
-constexpr int kRotThreads = 128;
-constexpr int kRotSmemBytes = 4 * 128 * 128 + 1024;  // X and R tiles, + slack for 1024-B alignment
+// ==================================================================== preparation
+// One persistent kernel prepares all three tensors.  The rotation of a Q or K tile,
+// X' = (X * sigma) H / sqrt(128), is the product X R^T with the fixed 128 x 128 matrix
+// R[c][k] = sigma_k (-1)^popcount(c & k) (H is symmetric).  R's entries are +-1, exact in bf16,
+// so one bf16 tcgen05 product with fp32 accumulation gives the rotation up to the fp32 sums.
+// Work items are the 128-row tiles of Q, then of K, then of V, over all heads; CTA b takes
+// items b, b + grid, ...  Per CTA (two per SM):
+//   warp 0    -- TMA producer: each item's bf16 tile into a two-stage ring;
+//   warp 1    -- MMA issuer: per Q or K item one 128 x 128 x 128 product X R^T into one of two
+//                tensor-memory accumulators (128 columns each), so that the epilogue of one
+//                tile overlaps the product of the next;
+//   warps 2-5 -- epilogue, one row (Q, K) or one column (V) per thread: the tile maximum, the
+//                scale and the E4M3 codes.  Q and K codes are (X R^T) * 448 / max|X R^T|: the
+//                1/sqrt(128) cancels in the codes and enters the scale only.  V is read from
+//                the ring column by column and written transposed (d rows x keys).
+// R is built once per CTA in shared memory, in the 128-byte-swizzled K-major layout that the
+// product reads.
+constexpr int kPrepThreads = 192;
+constexpr int kPrepChunk = 128 * 128;           // 128 rows x 64 bf16 (one swizzle atom wide)
+constexpr int kPrepTile = 2 * kPrepChunk;       // one bf16 128 x 128 tile
+constexpr int kPrepOffR = 0;
+constexpr int kPrepOffRing = kPrepTile;         // two stages
+constexpr int kPrepSmemBytes = 3 * kPrepTile + 1024;  // + slack for 1024-B alignment
+constexpr uint32_t kPrepTmemCols = 256;
 
-__global__ void __launch_bounds__(256) fa_fp8_rotmat_kernel(const int8_t* __restrict__ signs, uint16_t* __restrict__ r) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < kFp8D * kFp8D; i += gridDim.x * blockDim.x) {
-    const int c = i / kFp8D, k = i % kFp8D;
-    const bool neg = (signs[k] < 0) != ((__popc(c & k) & 1) != 0);
-    r[i] = neg ? 0xBF80u : 0x3F80u;  // bf16 -1.0 / +1.0
-  }
-}
+struct PrepBars {
+  uint64_t full[2], empty[2], acc_full[2], acc_empty[2], drain;
+};
 
-__global__ void __launch_bounds__(kRotThreads) fa_fp8_rot_kernel(const __grid_constant__ CUtensorMap tm_q,
-                                                                 const __grid_constant__ CUtensorMap tm_k,
-                                                                 const __grid_constant__ CUtensorMap tm_r,
-                                                                 const QuantParams p) {
-  constexpr int kChunk = 128 * 128;  // 128 rows x 64 bf16 (one swizzle atom wide)
-  extern __shared__ uint8_t rsm_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(rsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sbase = ptx::smem_addr(smem);  // X: [0, 32 KB), R: [32 KB, 64 KB)
-  __shared__ uint64_t bars[2];                  // tiles loaded, product done
+__global__ void __launch_bounds__(kPrepThreads, 2) fa_fp8_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
+                                                                       const __grid_constant__ CUtensorMap tm_k,
+                                                                       const __grid_constant__ CUtensorMap tm_v,
+                                                                       const QuantParams p) {
+  extern __shared__ uint8_t psm_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(psm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = ptx::smem_addr(smem);
+  __shared__ PrepBars bars;
   __shared__ uint32_t tmem_slot, abort_flag;
-  __shared__ float warp_max[kRotThreads / 32];
-  const int which = blockIdx.y;  // 0 Q, 1 K
-  const int tile = blockIdx.x % p.n_tiles;
-  const int bh = blockIdx.x / p.n_tiles;
+  __shared__ float warp_max[2][4];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t bar_load = ptx::smem_addr(&bars[0]), bar_mma = ptx::smem_addr(&bars[1]);
+  const int per = p.BH * p.n_tiles;  // items per tensor
+  const int n_items = 3 * per;
+  auto ba = [](uint64_t& x) { return ptx::smem_addr(&x); };
   if (threadIdx.x == 0) {
-    ptx::mbar_init(bar_load, 1);
-    ptx::mbar_init(bar_mma, 1);
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(ba(bars.full[i]), 1);
+      ptx::mbar_init(ba(bars.empty[i]), 1);      // the MMA's commit (Q, K) or one epilogue thread (V)
+      ptx::mbar_init(ba(bars.acc_full[i]), 1);
+      ptx::mbar_init(ba(bars.acc_empty[i]), 4);  // one arrive per epilogue warp
+    }
+    ptx::mbar_init(ba(bars.drain), 1);
     abort_flag = 0u;
     ptx::fence_mbar_init();
   }
-  if (warp == 0) {
-    ptx::tmem_alloc(ptx::smem_addr(&tmem_slot), 128);
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(&tmem_slot), kPrepTmemCols);
     ptx::tmem_relinquish();
   }
+  // R: chunk ch holds columns k = 64 ch .. 64 ch + 63 of every row c; 16-byte granule g of a
+  // row holds k = 64 ch + 8 g .. + 7 and sits at position g ^ (c mod 8)
+  for (int gi = threadIdx.x; gi < 2 * 128 * 8; gi += kPrepThreads) {
+    const int ch = gi >> 10, c = (gi >> 3) & 127, g = gi & 7;
+    const int k0 = ch * 64 + g * 8;
+    uint32_t wd[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int ka = k0 + 2 * e, kb = ka + 1;
+      const bool na = (p.signs[ka] < 0) != ((__popc(c & ka) & 1) != 0);
+      const bool nb = (p.signs[kb] < 0) != ((__popc(c & kb) & 1) != 0);
+      wd[e] = (na ? 0xBF80u : 0x3F80u) | ((nb ? 0xBF80u : 0x3F80u) << 16);  // bf16 -1.0 / +1.0
+    }
+    ptx::st_shared_v4(sbase + kPrepOffR + ch * kPrepChunk + c * 128 + ((g ^ (c & 7)) << 4), wd[0], wd[1], wd[2],
+                      wd[3]);
+  }
+  ptx::fence_proxy_async_smem();  // R is read by the tensor core (async proxy)
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = tmem_slot;
   const Waiter w{&abort_flag, p.timeout_ns};
-  bool ok = true, issued = false;
+
   if (warp == 0) {
+    // ================================================================ TMA producer
     if (lane == 0) {
-      const CUtensorMap* mx = which == 0 ? &tm_q : &tm_k;
-      ptx::mbar_arrive_expect_tx(bar_load, 4 * kChunk);
-      for (int c = 0; c < 2; ++c) {
-        ptx::tma_load_3d(sbase + c * kChunk, mx, bar_load, c * 64, tile * 128, bh);  // rows past N: zeros
-        ptx::tma_load_3d(sbase + (2 + c) * kChunk, &tm_r, bar_load, c * 64, 0, 0);
+      int k = 0, issued = 0;
+      bool ok = true;
+      for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++k) {
+        const int s = k & 1;
+        if (k >= 2 && !w.wait(ba(bars.empty[s]), ((k >> 1) - 1) & 1)) { ok = false; break; }
+        const int which = it / per, rem = it - which * per;
+        const int bh = rem / p.n_tiles, tile = rem - bh * p.n_tiles;
+        const CUtensorMap* m = which == 0 ? &tm_q : (which == 1 ? &tm_k : &tm_v);
+        ptx::mbar_arrive_expect_tx(ba(bars.full[s]), kPrepTile);
+        for (int c = 0; c < 2; ++c)  // rows past N arrive as zeros
+          ptx::tma_load_3d(sbase + kPrepOffRing + s * kPrepTile + c * kPrepChunk, m, ba(bars.full[s]), c * 64,
+                           tile * 128, bh);
+        issued = k + 1;
       }
+      if (!ok)  // let the copies in flight land before the CTA's memory is released
+        for (int kk = issued > 2 ? issued - 2 : 0; kk < issued; ++kk) w.drain(ba(bars.full[kk & 1]), (kk >> 1) & 1);
     }
-    ok = __all_sync(0xffffffffu, w.wait(bar_load, 0));
-    if (ok) {
+    __syncwarp();
+  } else if (warp == 1) {
+    // ================================================================ MMA issuer
+    constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, 128, false);
+    const uint64_t db = ptx::smem_desc_sw128(sbase + kPrepOffR, 16, 1024);
+    const uint64_t da0 = ptx::smem_desc_sw128(sbase + kPrepOffRing, 16, 1024);
+    int k = 0, m = 0;
+    for (int it = blockIdx.x; it < 2 * per; it += gridDim.x, ++k, ++m) {  // Q and K items come first
+      const int s = k & 1, buf = m & 1;
+      bool ok = __all_sync(0xffffffffu, w.wait(ba(bars.full[s]), (k >> 1) & 1));
+      if (ok && m >= 2) ok = __all_sync(0xffffffffu, w.wait(ba(bars.acc_empty[buf]), ((m >> 1) - 1) & 1));
+      if (!ok) break;
       ptx::tc_fence_after();
+      const uint64_t da = da0 + static_cast<uint64_t>(s) * (kPrepTile >> 4);
+      const uint32_t acc = tmem + buf * 128;
       if (ptx::elect_one()) {
-        constexpr uint32_t idesc = ptx::idesc_bf16_f32(128, 128, false);
-        const uint64_t da = ptx::smem_desc_sw128(sbase, 16, 1024), db = ptx::smem_desc_sw128(sbase + 2 * kChunk, 16, 1024);
-        ptx::mma_ss_i<0>(tmem, da, db, idesc);
+        ptx::mma_ss_i<0>(acc, da, db, kIdesc);
 #pragma unroll
         for (int kk = 1; kk < kFp8D / 16; ++kk) {
-          const uint64_t o = (kk >> 2) * (kChunk >> 4) + (kk & 3) * 2;
-          ptx::mma_ss_i<1>(tmem, da + o, db + o, idesc);
+          const uint64_t o = (kk >> 2) * (kPrepChunk >> 4) + (kk & 3) * 2;
+          ptx::mma_ss_i<1>(acc, da + o, db + o, kIdesc);
         }
-        ptx::tc_commit(bar_mma);
+        ptx::tc_commit(ba(bars.acc_full[buf]));
+        ptx::tc_commit(ba(bars.empty[s]));
       }
       __syncwarp();
-      issued = true;
-    } else if (lane == 0) {
-      w.drain(bar_load, 0);  // let the copies land before the memory is released
     }
-  }
-  ok = __syncthreads_and(ok);
-  float x[128];
-  float amax = 0.f;
-  if (ok) {
-    ok = __all_sync(0xffffffffu, w.wait(bar_mma, 0));
-    if (ok) {
-      ptx::tc_fence_after();
-      uint32_t raw[128];
-      ptx::tmem_ld128(tmem + (static_cast<uint32_t>(warp * 32) << 16), raw);
+    // every product issued completes before tensor memory is freed
+    if (ptx::elect_one()) ptx::tc_commit(ba(bars.drain));
+    __syncwarp();
+    w.drain(ba(bars.drain), 0);
+    __syncwarp();
+  } else {
+    // ================================================================ epilogue
+    // After a failed wait the warps keep walking the items (every wait then returns at
+    // once), so that the four warps always meet the same named barriers.
+    const int quarter = warp & 3;  // tensor-memory lane quarter of this warp
+    const int ew = warp - 2;
+    const int c = quarter * 32 + lane;  // row (Q, K) or column (V) of this thread
+    bool ok = true;
+    int k = 0, m = 0;
+    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++k) {
+      const int which = it / per, rem = it - which * per;
+      const int bh = rem / p.n_tiles, tile = rem - bh * p.n_tiles;
+      const int s = k & 1;
+      float x[128];
+      float amax = 0.f;
+      if (which < 2) {
+        const int buf = m & 1;
+        ok = ok && __all_sync(0xffffffffu, w.wait(ba(bars.acc_full[buf]), (m >> 1) & 1));
+        if (ok) {
+          ptx::tc_fence_after();
+          uint32_t raw[128];
+          ptx::tmem_ld128(tmem + buf * 128 + (static_cast<uint32_t>(quarter * 32) << 16), raw);
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        x[i] = __uint_as_float(raw[i]) * 0.08838834764831845f;  // 1 / sqrt(128)
-        amax = fmaxf(amax, fabsf(x[i]));
+          for (int i = 0; i < 128; ++i) {
+            x[i] = __uint_as_float(raw[i]);
+            amax = fmaxf(amax, fabsf(x[i]));
+          }
+          ptx::tc_fence_before();
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(ba(bars.acc_empty[buf]));
+        ++m;
+      } else {
+        ok = ok && __all_sync(0xffffffffu, w.wait(ba(bars.full[s]), (k >> 1) & 1));
+        if (ok) {
+          // column c: chunk c / 64, 16-byte granule (c mod 64) / 8 of each 128-byte row,
+          // swizzled by row mod 8
+          const uint32_t col_base = sbase + kPrepOffRing + s * kPrepTile + (c >> 6) * kPrepChunk + (c & 7) * 2;
+          const int gran = (c & 63) >> 3;
+#pragma unroll
+          for (int r = 0; r < 128; ++r) {
+            uint16_t bits;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(bits) : "r"(col_base + r * 128 + ((gran ^ (r & 7)) << 4)));
+            x[r] = __uint_as_float(static_cast<uint32_t>(bits) << 16);
+            amax = fmaxf(amax, fabsf(x[r]));
+          }
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+      if (lane == 0) warp_max[k & 1][ew] = amax;
+      ptx::named_barrier(1, 128);
+      if (which == 2 && ew == 0 && lane == 0) ptx::mbar_arrive(ba(bars.empty[s]));  // every column has been read
+      if (!ok) continue;
+      amax = fmaxf(fmaxf(warp_max[k & 1][0], warp_max[k & 1][1]), fmaxf(warp_max[k & 1][2], warp_max[k & 1][3]));
+      const float inv = amax > 0.f ? 448.f / amax : 1.f;
+      float* scales = which == 0 ? p.scales[0] : (which == 1 ? p.scales[1] : p.scales[2]);
+      uint8_t* dst = which == 0 ? p.dst[0] : (which == 1 ? p.dst[1] : p.dst[2]);
+      if (c == 0) {
+        const float sc = which < 2 ? amax * 0.08838834764831845f : amax;  // Q, K: max|X R^T| / sqrt(128)
+        scales[static_cast<size_t>(bh) * p.n_tiles + tile] = amax > 0.f ? sc / 448.f : 1.f;
+      }
+      // Q, K: row c of the tile (rows past N hold zero codes); V: row c of the transposed tile
+      const size_t off = which < 2 ? (static_cast<size_t>(bh) * p.n_pad + tile * 128 + c) * kFp8D
+                                   : (static_cast<size_t>(bh) * kFp8D + c) * p.n_pad + tile * 128;
+      uint4* d4 = reinterpret_cast<uint4*>(dst + off);
+#pragma unroll
+      for (int g = 0; g < 8; ++g) {
+        uint32_t wd[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          wd[i] = ptx::pack_e4m3x4(x[16 * g + 4 * i] * inv, x[16 * g + 4 * i + 1] * inv, x[16 * g + 4 * i + 2] * inv,
+                                   x[16 * g + 4 * i + 3] * inv);
+        d4[g] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
       }
     }
   }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  if (lane == 0) warp_max[warp] = amax;
-  ok = __syncthreads_and(ok);
-  if (ok) {
-    amax = fmaxf(fmaxf(warp_max[0], warp_max[1]), fmaxf(warp_max[2], warp_max[3]));
-    const float inv = amax > 0.f ? 448.f / amax : 1.f;
-    float* scales = which == 0 ? p.scales[0] : p.scales[1];
-    uint8_t* dst = which == 0 ? p.dst[0] : p.dst[1];
-    if (threadIdx.x == 0) scales[static_cast<size_t>(bh) * p.n_tiles + tile] = amax > 0.f ? amax / 448.f : 1.f;
-    uint4* d4 = reinterpret_cast<uint4*>(dst + (static_cast<size_t>(bh) * p.n_pad + tile * 128 + threadIdx.x) * kFp8D);
-#pragma unroll
-    for (int g = 0; g < 8; ++g) {
-      uint32_t wd[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        wd[i] = ptx::pack_e4m3x4(x[16 * g + 4 * i] * inv, x[16 * g + 4 * i + 1] * inv, x[16 * g + 4 * i + 2] * inv,
-                                 x[16 * g + 4 * i + 3] * inv);
-      d4[g] = make_uint4(wd[0], wd[1], wd[2], wd[3]);  // rows past N hold zeros
-    }
-  }
-  if (warp == 0 && issued) w.drain(bar_mma, 0);  // the product completes before its memory is freed
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, 128);
-  }
-}
-
-// V: one CTA per 128-key tile.  The bf16 tile arrives by TMA (two 64-column chunks, 128-byte
-// swizzle); thread c then reads column c down the 128 keys (consecutive threads read
-// consecutive columns of one row, so the reads spread over the banks), takes the tile
-// maximum with the other threads, and writes row c of the transposed codes: the 128 keys of
-// column c, 128 contiguous bytes.
-constexpr int kVThreads = 128;
-constexpr int kVSmemBytes = 2 * 128 * 128 + 1024;
-
-__global__ void __launch_bounds__(kVThreads) fa_fp8_vquant_kernel(const __grid_constant__ CUtensorMap tm_v,
-                                                                  const QuantParams p) {
-  constexpr int kChunk = 128 * 128;
-  extern __shared__ uint8_t vsm_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(vsm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const uint32_t sbase = ptx::smem_addr(smem);
-  __shared__ uint64_t bar;
-  __shared__ uint32_t abort_flag;
-  __shared__ float warp_max[kVThreads / 32];
-  const int tile = blockIdx.x % p.n_tiles, bh = blockIdx.x / p.n_tiles;
-  const int c = threadIdx.x, warp = c >> 5, lane = c & 31;
-  const uint32_t b = ptx::smem_addr(&bar);
-  if (c == 0) {
-    ptx::mbar_init(b, 1);
-    abort_flag = 0u;
-    ptx::fence_mbar_init();
-  }
-  __syncthreads();
-  const Waiter w{&abort_flag, p.timeout_ns};
-  if (c == 0) {
-    ptx::mbar_arrive_expect_tx(b, 2 * kChunk);
-    for (int h = 0; h < 2; ++h) ptx::tma_load_3d(sbase + h * kChunk, &tm_v, b, h * 64, tile * 128, bh);  // rows past N: 0
-  }
-  bool ok = __syncthreads_and(w.wait(b, 0));
-  if (!ok) {
-    if (c == 0) w.drain(b, 0);
-    __syncthreads();
-    return;
-  }
-  // column c: chunk c / 64, 16-byte granule (c % 64) / 8 of each 128-byte row, swizzled by row % 8
-  const uint32_t col_base = sbase + (c >> 6) * kChunk + (c & 7) * 2;
-  const int gran = (c & 63) >> 3;
-  float v[128];
-  float amax = 0.f;
-#pragma unroll
-  for (int r = 0; r < 128; ++r) {
-    uint16_t bits;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(bits) : "r"(col_base + r * 128 + ((gran ^ (r & 7)) << 4)));
-    v[r] = __uint_as_float(static_cast<uint32_t>(bits) << 16);
-    amax = fmaxf(amax, fabsf(v[r]));
-  }
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-  if (lane == 0) warp_max[warp] = amax;
-  __syncthreads();
-  amax = fmaxf(fmaxf(warp_max[0], warp_max[1]), fmaxf(warp_max[2], warp_max[3]));
-  const float inv = amax > 0.f ? 448.f / amax : 1.f;
-  if (c == 0) p.scales[2][static_cast<size_t>(bh) * p.n_tiles + tile] = amax > 0.f ? amax / 448.f : 1.f;
-  uint4* d4 = reinterpret_cast<uint4*>(p.dst[2] + (static_cast<size_t>(bh) * kFp8D + c) * p.n_pad + tile * 128);
-#pragma unroll
-  for (int g = 0; g < 8; ++g) {
-    uint32_t wd[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-      wd[i] = ptx::pack_e4m3x4(v[16 * g + 4 * i] * inv, v[16 * g + 4 * i + 1] * inv, v[16 * g + 4 * i + 2] * inv,
-                               v[16 * g + 4 * i + 3] * inv);
-    d4[g] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    ptx::tmem_dealloc(tmem, kPrepTmemCols);
   }
 }
 
@@ -596,6 +618,7 @@ namespace {
 
 std::mutex g_fp8_dev_mutex;
 int g_fp8_dev_state[kMaxDevices];
+int g_fp8_sms[kMaxDevices];  // SM count per device, for the persistent preparation grid
 
 int prepare_device_fp8() {
   int dev = 0;
@@ -610,20 +633,19 @@ int prepare_device_fp8() {
   }
   if (cudaFuncSetAttribute(fa_fp8_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, Fp8Cfg::kSmemBytes) !=
           cudaSuccess ||
-      cudaFuncSetAttribute(fa_fp8_rot_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRotSmemBytes) !=
+      cudaFuncSetAttribute(fa_fp8_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kPrepSmemBytes) !=
           cudaSuccess ||
-      cudaFuncSetAttribute(fa_fp8_vquant_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kVSmemBytes) !=
-          cudaSuccess)
+      cudaDeviceGetAttribute(&g_fp8_sms[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      g_fp8_sms[dev] < 1)
     return FA_ERR_CUDA;
   g_fp8_dev_state[dev] = 1;
   return FA_OK;
 }
 
 // Workspace: q8 [BH, N_pad, 128], k8 [BH, N_pad, 128], vt8 [BH, 128, N_pad] (E4M3 codes), then
-// the fp32 scales of Q', K' and V [BH, N_pad / 128] each, then the 128 x 128 bf16 rotation
-// matrix; every section 256-byte aligned.
+// the fp32 scales of Q', K' and V [BH, N_pad / 128] each; every section 256-byte aligned.
 struct Fp8Layout {
-  size_t q8, k8, vt8, sq, sk, sv, rot, total;
+  size_t q8, k8, vt8, sq, sk, sv, total;
 };
 
 bool fp8_layout(long long BH, long long N, Fp8Layout* L) {
@@ -636,8 +658,7 @@ bool fp8_layout(long long BH, long long N, Fp8Layout* L) {
   L->sq = 3 * codes;
   L->sk = L->sq + sc;
   L->sv = L->sk + sc;
-  L->rot = L->sv + sc;
-  L->total = L->rot + static_cast<size_t>(kFp8D) * kFp8D * 2;
+  L->total = L->sv + sc;
   return true;
 }
 
@@ -700,17 +721,16 @@ int run_fp8(const Fp8Problem& pr, int withhold, unsigned long long timeout_ns, c
   qp.scales[1] = reinterpret_cast<float*>(ws + L.sk);
   qp.scales[2] = reinterpret_cast<float*>(ws + L.sv);
   qp.signs = pr.signs;
+  qp.BH = BH;
   qp.N = pr.N;
   qp.n_tiles = n_tiles;
   qp.n_pad = n_pad;
   qp.timeout_ns = timeout_ns;
-  CUtensorMap mq, mk, mvt, mo, mxq, mxk, mxv, mr;
-  uint16_t* rot = reinterpret_cast<uint16_t*>(ws + L.rot);
+  CUtensorMap mq, mk, mvt, mo, mxq, mxk, mxv;
   if (!encode_map_u8(&mq, ws + L.q8, BH, n_pad, kFp8D) || !encode_map_u8(&mk, ws + L.k8, BH, n_pad, kFp8D) ||
       !encode_map_u8(&mvt, ws + L.vt8, BH, kFp8D, n_pad) || !encode_map(&mo, pr.o, BH, pr.N, kFp8D) ||
       !encode_map(&mxq, pr.q, BH, pr.N, kFp8D) || !encode_map(&mxk, pr.k, BH, pr.N, kFp8D) ||
-      !encode_map(&mxv, pr.v, BH, pr.N, kFp8D) ||
-      !encode_map(&mr, rot, 1, kFp8D, kFp8D))
+      !encode_map(&mxv, pr.v, BH, pr.N, kFp8D))
     return FA_ERR_LAUNCH;
   Fp8Params p{};
   p.scale_q = qp.scales[0];
@@ -726,12 +746,11 @@ int run_fp8(const Fp8Problem& pr, int withhold, unsigned long long timeout_ns, c
   p.causal = pr.causal ? 1 : 0;
   p.withhold = withhold;
   p.timeout_ns = timeout_ns;
-  fa_fp8_rotmat_kernel<<<kFp8D * kFp8D / 256, 256, 0, stream>>>(pr.signs, rot);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
-  fa_fp8_rot_kernel<<<dim3(static_cast<unsigned>(BH * n_tiles), 2), kRotThreads, kRotSmemBytes, stream>>>(mxq, mxk,
-                                                                                                         mr, qp);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
-  fa_fp8_vquant_kernel<<<static_cast<unsigned>(BH * n_tiles), kVThreads, kVSmemBytes, stream>>>(mxv, qp);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  const long long items = 3LL * BH * n_tiles;
+  const int grid = static_cast<int>(items < 2LL * g_fp8_sms[dev] ? items : 2LL * g_fp8_sms[dev]);
+  fa_fp8_prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(mxq, mxk, mxv, qp);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   fa_fp8_fwd_kernel<<<static_cast<unsigned>(BH * p.n_cta_q), kFp8Threads, Fp8Cfg::kSmemBytes, stream>>>(mq, mk, mvt,
                                                                                                        mo, p);

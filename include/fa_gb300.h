@@ -173,8 +173,7 @@ int fa_fwd_gqa_static_workspace(const void* q, const void* k, const void* v, voi
  *               [C, 2C)       K' codes, E4M3 [B*H, N_pad, 128]
  *               [2C, 3C)      V codes transposed, E4M3 [B*H, 128, N_pad]
  *               then three fp32 arrays [B*H, T] of tile scales (Q', K', V), each at a
- *               256-byte boundary, then the 128 x 128 bf16 rotation matrix;
- *               C = B*H*N_pad*128 rounded up to 256.
+ *               256-byte boundary;  C = B*H*N_pad*128 rounded up to 256.
  *             Rows past N hold zero codes.  The call writes it; it is left holding the
  *             quantised tensors.
  * No output may overlap an input or the workspace.  Two kernels are enqueued on `stream`;

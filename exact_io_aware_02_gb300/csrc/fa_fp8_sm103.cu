@@ -39,7 +39,6 @@ constexpr int kFp8MaxKvTiles = 1024;              // N <= 131072
 
 // ==================================================================== quantisation
 struct QuantParams {
-  uint8_t* dst[3];         // q8, k8: [BH, N_pad, 128]; vt8: [BH, 128, N_pad]
   float* scales[3];        // [BH, n_tiles]
   const int8_t* signs;     // [128], negative = -1
   int BH, N, n_tiles, n_pad;
@@ -52,49 +51,58 @@ struct QuantParams {
 // R[c][k] = sigma_k (-1)^popcount(c & k) (H is symmetric).  R's entries are +-1, exact in bf16,
 // so one bf16 tcgen05 product with fp32 accumulation gives the rotation up to the fp32 sums.
 // Work items are the 128-row tiles of Q, then of K, then of V, over all heads; CTA b takes
-// items b, b + grid, ...  Per CTA (two per SM):
-//   warp 0    -- TMA producer: each item's bf16 tile into a two-stage ring;
-//   warp 1    -- MMA issuer: per Q or K item one 128 x 128 x 128 product X R^T into one of two
-//                tensor-memory accumulators (128 columns each), so that the epilogue of one
-//                tile overlaps the product of the next;
-//   warps 2-5 -- epilogue, one row (Q, K) or one column (V) per thread: the tile maximum, the
-//                scale and the E4M3 codes.  Q and K codes are (X R^T) * 448 / max|X R^T|: the
+// items b, b + grid, ...  One CTA per SM:
+//   warp 0    -- TMA producer: each item's bf16 tile into a four-stage ring;
+//   warp 1    -- MMA issuer: per Q or K item one 128 x 128 x 128 product X R^T into one of four
+//                tensor-memory accumulators (128 columns each), so that the epilogues of
+//                earlier tiles overlap the products of later ones;
+//   warps 2-9 -- epilogue in two warpgroups, which take the CTA's even and odd items; one row
+//                (Q, K) or one column (V) per thread: the tile maximum, the scale and the E4M3
+//                codes.  The codes go to shared memory (each group has two 16 KB buffers, in
+//                the 128-byte swizzle) and leave by TMA store, a whole tile at a time.  Q and K codes are (X R^T) * 448 / max|X R^T|: the
 //                1/sqrt(128) cancels in the codes and enters the scale only.  V is read from
 //                the ring column by column and written transposed (d rows x keys).
 // R is built once per CTA in shared memory, in the 128-byte-swizzled K-major layout that the
 // product reads.
-constexpr int kPrepThreads = 192;
+constexpr int kPrepThreads = 320;
+constexpr int kPrepStages = 4;
 constexpr int kPrepChunk = 128 * 128;           // 128 rows x 64 bf16 (one swizzle atom wide)
 constexpr int kPrepTile = 2 * kPrepChunk;       // one bf16 128 x 128 tile
 constexpr int kPrepOffR = 0;
-constexpr int kPrepOffRing = kPrepTile;         // two stages
-constexpr int kPrepSmemBytes = 3 * kPrepTile + 1024;  // + slack for 1024-B alignment
-constexpr uint32_t kPrepTmemCols = 256;
+constexpr int kPrepOffRing = kPrepTile;
+constexpr int kPrepOffStage = kPrepOffRing + kPrepStages * kPrepTile;  // [group][buffer] 16 KB code tiles
+constexpr int kPrepSmemBytes = kPrepOffStage + 4 * 128 * 128 + 1024;   // + slack for 1024-B alignment
+constexpr uint32_t kPrepTmemCols = 512;  // four 128-column accumulators
 
 struct PrepBars {
-  uint64_t full[2], empty[2], acc_full[2], acc_empty[2], drain;
+  uint64_t full[kPrepStages], empty[kPrepStages], acc_full[4], acc_empty[4], drain;
 };
 
-__global__ void __launch_bounds__(kPrepThreads, 2) fa_fp8_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
+__global__ void __launch_bounds__(kPrepThreads, 1) fa_fp8_prep_kernel(const __grid_constant__ CUtensorMap tm_q,
                                                                        const __grid_constant__ CUtensorMap tm_k,
                                                                        const __grid_constant__ CUtensorMap tm_v,
+                                                                       const __grid_constant__ CUtensorMap tm_q8,
+                                                                       const __grid_constant__ CUtensorMap tm_k8,
+                                                                       const __grid_constant__ CUtensorMap tm_vt8,
                                                                        const QuantParams p) {
   extern __shared__ uint8_t psm_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(psm_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = ptx::smem_addr(smem);
   __shared__ PrepBars bars;
   __shared__ uint32_t tmem_slot, abort_flag;
-  __shared__ float warp_max[2][4];
+  __shared__ float warp_max[2][2][4];  // [epilogue group][item parity][warp]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int per = p.BH * p.n_tiles;  // items per tensor
   const int n_items = 3 * per;
   auto ba = [](uint64_t& x) { return ptx::smem_addr(&x); };
   if (threadIdx.x == 0) {
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kPrepStages; ++i) {
       ptx::mbar_init(ba(bars.full[i]), 1);
-      ptx::mbar_init(ba(bars.empty[i]), 1);      // the MMA's commit (Q, K) or one epilogue thread (V)
+      ptx::mbar_init(ba(bars.empty[i]), 1);  // the MMA's commit (Q, K) or one epilogue thread (V)
+    }
+    for (int i = 0; i < 4; ++i) {
       ptx::mbar_init(ba(bars.acc_full[i]), 1);
-      ptx::mbar_init(ba(bars.acc_empty[i]), 4);  // one arrive per epilogue warp
+      ptx::mbar_init(ba(bars.acc_empty[i]), 4);  // one arrive per warp of the epilogue group
     }
     ptx::mbar_init(ba(bars.drain), 1);
     abort_flag = 0u;
@@ -133,8 +141,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fa_fp8_prep_kernel(const __gr
       int k = 0, issued = 0;
       bool ok = true;
       for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++k) {
-        const int s = k & 1;
-        if (k >= 2 && !w.wait(ba(bars.empty[s]), ((k >> 1) - 1) & 1)) { ok = false; break; }
+        const int s = k % kPrepStages, use = k / kPrepStages;
+        if (use > 0 && !w.wait(ba(bars.empty[s]), (use - 1) & 1)) { ok = false; break; }
         const int which = it / per, rem = it - which * per;
         const int bh = rem / p.n_tiles, tile = rem - bh * p.n_tiles;
         const CUtensorMap* m = which == 0 ? &tm_q : (which == 1 ? &tm_k : &tm_v);
@@ -145,7 +153,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fa_fp8_prep_kernel(const __gr
         issued = k + 1;
       }
       if (!ok)  // let the copies in flight land before the CTA's memory is released
-        for (int kk = issued > 2 ? issued - 2 : 0; kk < issued; ++kk) w.drain(ba(bars.full[kk & 1]), (kk >> 1) & 1);
+        for (int kk = issued > kPrepStages ? issued - kPrepStages : 0; kk < issued; ++kk)
+          w.drain(ba(bars.full[kk % kPrepStages]), (kk / kPrepStages) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -153,11 +162,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fa_fp8_prep_kernel(const __gr
     constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(128, 128, false);
     const uint64_t db = ptx::smem_desc_sw128(sbase + kPrepOffR, 16, 1024);
     const uint64_t da0 = ptx::smem_desc_sw128(sbase + kPrepOffRing, 16, 1024);
-    int k = 0, m = 0;
-    for (int it = blockIdx.x; it < 2 * per; it += gridDim.x, ++k, ++m) {  // Q and K items come first
-      const int s = k & 1, buf = m & 1;
-      bool ok = __all_sync(0xffffffffu, w.wait(ba(bars.full[s]), (k >> 1) & 1));
-      if (ok && m >= 2) ok = __all_sync(0xffffffffu, w.wait(ba(bars.acc_empty[buf]), ((m >> 1) - 1) & 1));
+    // Q and K items come first in every CTA's list, so the k-th item is the k-th product;
+    // accumulator k mod 4 belongs to epilogue group k mod 2
+    int k = 0;
+    for (int it = blockIdx.x; it < 2 * per; it += gridDim.x, ++k) {
+      const int s = k % kPrepStages, buf = k & 3;
+      bool ok = __all_sync(0xffffffffu, w.wait(ba(bars.full[s]), (k / kPrepStages) & 1));
+      if (ok && k >= 4) ok = __all_sync(0xffffffffu, w.wait(ba(bars.acc_empty[buf]), ((k >> 2) - 1) & 1));
       if (!ok) break;
       ptx::tc_fence_after();
       const uint64_t da = da0 + static_cast<uint64_t>(s) * (kPrepTile >> 4);
@@ -184,19 +195,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fa_fp8_prep_kernel(const __gr
     // After a failed wait the warps keep walking the items (every wait then returns at
     // once), so that the four warps always meet the same named barriers.
     const int quarter = warp & 3;  // tensor-memory lane quarter of this warp
-    const int ew = warp - 2;
+    const int grp = (warp - 2) >> 2, ew = (warp - 2) & 3;
     const int c = quarter * 32 + lane;  // row (Q, K) or column (V) of this thread
     bool ok = true;
-    int k = 0, m = 0;
-    for (int it = blockIdx.x; it < n_items; it += gridDim.x, ++k) {
+    for (int it = blockIdx.x + grp * gridDim.x, k = grp; it < n_items; it += 2 * gridDim.x, k += 2) {
       const int which = it / per, rem = it - which * per;
       const int bh = rem / p.n_tiles, tile = rem - bh * p.n_tiles;
-      const int s = k & 1;
+      const int s = k % kPrepStages;
       float x[128];
       float amax = 0.f;
       if (which < 2) {
-        const int buf = m & 1;
-        ok = ok && __all_sync(0xffffffffu, w.wait(ba(bars.acc_full[buf]), (m >> 1) & 1));
+        const int buf = k & 3;
+        ok = ok && __all_sync(0xffffffffu, w.wait(ba(bars.acc_full[buf]), (k >> 2) & 1));
         if (ok) {
           ptx::tc_fence_after();
           uint32_t raw[128];
@@ -210,9 +220,8 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fa_fp8_prep_kernel(const __gr
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(ba(bars.acc_empty[buf]));
-        ++m;
       } else {
-        ok = ok && __all_sync(0xffffffffu, w.wait(ba(bars.full[s]), (k >> 1) & 1));
+        ok = ok && __all_sync(0xffffffffu, w.wait(ba(bars.full[s]), (k / kPrepStages) & 1));
         if (ok) {
           // column c: chunk c / 64, 16-byte granule (c mod 64) / 8 of each 128-byte row,
           // swizzled by row mod 8
@@ -229,32 +238,48 @@ __global__ void __launch_bounds__(kPrepThreads, 2) fa_fp8_prep_kernel(const __gr
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-      if (lane == 0) warp_max[k & 1][ew] = amax;
-      ptx::named_barrier(1, 128);
-      if (which == 2 && ew == 0 && lane == 0) ptx::mbar_arrive(ba(bars.empty[s]));  // every column has been read
-      if (!ok) continue;
-      amax = fmaxf(fmaxf(warp_max[k & 1][0], warp_max[k & 1][1]), fmaxf(warp_max[k & 1][2], warp_max[k & 1][3]));
-      const float inv = amax > 0.f ? 448.f / amax : 1.f;
-      float* scales = which == 0 ? p.scales[0] : (which == 1 ? p.scales[1] : p.scales[2]);
-      uint8_t* dst = which == 0 ? p.dst[0] : (which == 1 ? p.dst[1] : p.dst[2]);
-      if (c == 0) {
-        const float sc = which < 2 ? amax * 0.08838834764831845f : amax;  // Q, K: max|X R^T| / sqrt(128)
-        scales[static_cast<size_t>(bh) * p.n_tiles + tile] = amax > 0.f ? sc / 448.f : 1.f;
+      const int par = (k >> 1) & 1;  // also the group's code buffer for this item
+      const bool leader = ew == 0 && lane == 0;
+      if (lane == 0) warp_max[grp][par][ew] = amax;
+      if (leader) ptx::bulk_wait_read<1>();  // the store of two items ago has left this buffer
+      ptx::named_barrier(1 + grp, 128);
+      if (which == 2 && leader) ptx::mbar_arrive(ba(bars.empty[s]));  // every column has been read
+      // A warp whose wait failed skips the work but not the barriers, so that the four warps
+      // of the group always meet the same two barriers per item.
+      if (ok) {
+        amax = fmaxf(fmaxf(warp_max[grp][par][0], warp_max[grp][par][1]),
+                     fmaxf(warp_max[grp][par][2], warp_max[grp][par][3]));
+        const float inv = amax > 0.f ? 448.f / amax : 1.f;
+        float* scales = which == 0 ? p.scales[0] : (which == 1 ? p.scales[1] : p.scales[2]);
+        if (c == 0) {
+          const float sc = which < 2 ? amax * 0.08838834764831845f : amax;  // Q, K: max|X R^T| / sqrt(128)
+          scales[static_cast<size_t>(bh) * p.n_tiles + tile] = amax > 0.f ? sc / 448.f : 1.f;
+        }
+        // Q, K: row c of the tile (rows past N hold zero codes); V: row c of the transposed
+        // tile.  Granule g of row c sits at position g ^ (c mod 8) (the tensor map's 128-byte
+        // swizzle).
+        const uint32_t row_addr = sbase + kPrepOffStage + (grp * 2 + par) * (128 * 128) + c * 128;
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          uint32_t wd[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            wd[i] = ptx::pack_e4m3x4(x[16 * g + 4 * i] * inv, x[16 * g + 4 * i + 1] * inv,
+                                     x[16 * g + 4 * i + 2] * inv, x[16 * g + 4 * i + 3] * inv);
+          ptx::st_shared_v4(row_addr + ((g ^ (c & 7)) << 4), wd[0], wd[1], wd[2], wd[3]);
+        }
+        ptx::fence_proxy_async_smem();
       }
-      // Q, K: row c of the tile (rows past N hold zero codes); V: row c of the transposed tile
-      const size_t off = which < 2 ? (static_cast<size_t>(bh) * p.n_pad + tile * 128 + c) * kFp8D
-                                   : (static_cast<size_t>(bh) * kFp8D + c) * p.n_pad + tile * 128;
-      uint4* d4 = reinterpret_cast<uint4*>(dst + off);
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        uint32_t wd[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          wd[i] = ptx::pack_e4m3x4(x[16 * g + 4 * i] * inv, x[16 * g + 4 * i + 1] * inv, x[16 * g + 4 * i + 2] * inv,
-                                   x[16 * g + 4 * i + 3] * inv);
-        d4[g] = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      ptx::named_barrier(1 + grp, 128);
+      if (ok && leader) {
+        const uint32_t src = sbase + kPrepOffStage + (grp * 2 + par) * (128 * 128);
+        if (which == 0) ptx::tma_store_3d(&tm_q8, src, 0, tile * 128, bh);
+        else if (which == 1) ptx::tma_store_3d(&tm_k8, src, 0, tile * 128, bh);
+        else ptx::tma_store_3d(&tm_vt8, src, tile * 128, 0, bh);
+        ptx::bulk_commit();
       }
     }
+    if (ew == 0 && lane == 0) ptx::bulk_wait_all();  // the stores have completed before the CTA exits
   }
   ptx::tc_fence_before();
   __syncthreads();
@@ -714,9 +739,6 @@ int run_fp8(const Fp8Problem& pr, int withhold, unsigned long long timeout_ns, c
   const int n_tiles = (pr.N + 127) / 128, n_pad = n_tiles * 128;
   uint8_t* ws = static_cast<uint8_t*>(pr.workspace);
   QuantParams qp{};
-  qp.dst[0] = ws + L.q8;
-  qp.dst[1] = ws + L.k8;
-  qp.dst[2] = ws + L.vt8;
   qp.scales[0] = reinterpret_cast<float*>(ws + L.sq);
   qp.scales[1] = reinterpret_cast<float*>(ws + L.sk);
   qp.scales[2] = reinterpret_cast<float*>(ws + L.sv);
@@ -749,8 +771,8 @@ int run_fp8(const Fp8Problem& pr, int withhold, unsigned long long timeout_ns, c
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
   const long long items = 3LL * BH * n_tiles;
-  const int grid = static_cast<int>(items < 2LL * g_fp8_sms[dev] ? items : 2LL * g_fp8_sms[dev]);
-  fa_fp8_prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(mxq, mxk, mxv, qp);
+  const int grid = static_cast<int>(items < g_fp8_sms[dev] ? items : g_fp8_sms[dev]);
+  fa_fp8_prep_kernel<<<grid, kPrepThreads, kPrepSmemBytes, stream>>>(mxq, mxk, mxv, mq, mk, mvt, qp);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   fa_fp8_fwd_kernel<<<static_cast<unsigned>(BH * p.n_cta_q), kFp8Threads, Fp8Cfg::kSmemBytes, stream>>>(mq, mk, mvt,
                                                                                                        mo, p);

@@ -41,6 +41,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -689,6 +690,134 @@ int static_workspace(void** out) {
   return FA_OK;
 }
 
+// ---- pipelined host-to-host forward (fa_fwd_host)
+// Per device: one stream for host-to-device copies, one for device-to-host copies, two for
+// the chunks' kernels (a causal chunk's longest CTA sets its kernel's duration however few
+// heads it holds, so consecutive chunks run side by side on the SMs), and a pool of events;
+// created on first use and kept until the process exits.  The mutex serialises the
+// enqueueing of whole calls, so that two host threads never interleave their records of
+// the shared events.
+constexpr int kMaxChunks = 64;
+constexpr int kDefaultChunks = 8;
+constexpr int kComputeStreams = 2;
+struct HostPipe {
+  cudaStream_t in = nullptr, out = nullptr, comp[kComputeStreams] = {};
+  cudaEvent_t start = nullptr, done = nullptr, loaded[kMaxChunks] = {}, computed[kMaxChunks] = {};
+  std::mutex mu;
+  bool ready = false;
+};
+HostPipe g_pipe[kMaxDevices];
+
+int host_pipe(int dev, HostPipe** out) {
+  HostPipe& hp = g_pipe[dev];
+  if (!hp.ready) {
+    const unsigned flags = cudaEventDisableTiming;
+    for (int i = 0; i < kComputeStreams; ++i)
+      if (cudaStreamCreateWithFlags(&hp.comp[i], cudaStreamNonBlocking) != cudaSuccess) return FA_ERR_CUDA;
+    if (cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.start, flags) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp.done, flags) != cudaSuccess)
+      return FA_ERR_CUDA;
+    for (int c = 0; c < kMaxChunks; ++c)
+      if (cudaEventCreateWithFlags(&hp.loaded[c], flags) != cudaSuccess ||
+          cudaEventCreateWithFlags(&hp.computed[c], flags) != cudaSuccess)
+        return FA_ERR_CUDA;
+    hp.ready = true;
+  }
+  *out = &hp;
+  return FA_OK;
+}
+
+bool is_pinned_host(const void* ptr) {
+  cudaPointerAttributes attr{};
+  if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return attr.type == cudaMemoryTypeHost;
+}
+
+struct HostBuffers {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+};
+
+int run_host(const HostBuffers& h, const Problem& pr, int groups_per_chunk, cudaStream_t stream) {
+  if (pr.n_splits != 1) return FA_ERR_ARG;
+  int rc = validate(pr);
+  if (rc != FA_OK) return rc;
+  if (!h.q || !h.k || !h.v || !h.o || !h.lse || groups_per_chunk < 0) return FA_ERR_ARG;
+  const int G = pr.Hq / pr.Hkv, groups = pr.B * pr.Hkv;
+  const size_t R = static_cast<size_t>(G) * pr.Nq;
+  const size_t row_bytes = static_cast<size_t>(pr.d) * 2;
+  const size_t qb = groups * R * row_bytes, kb = static_cast<size_t>(groups) * pr.Nk * row_bytes;
+  const size_t lb = groups * R * 4;
+  const struct { const void* p; size_t n; } in[3] = {{h.q, qb}, {h.k, kb}, {h.v, kb}};
+  for (const auto& x : in)
+    if (overlaps(h.o, qb, x.p, x.n) || overlaps(h.lse, lb, x.p, x.n)) return FA_ERR_ARG;
+  if (overlaps(h.o, qb, h.lse, lb)) return FA_ERR_ARG;
+  for (const void* ptr : {h.q, h.k, h.v, static_cast<const void*>(h.o), static_cast<const void*>(h.lse)})
+    if (!is_pinned_host(ptr)) return FA_ERR_ARG;
+  rc = prepare_device();
+  if (rc != FA_OK) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_pipe[dev].mu);
+  HostPipe* hp = nullptr;
+  rc = host_pipe(dev, &hp);
+  if (rc != FA_OK) return rc;
+  // chunks of whole K/V groups: contiguous rows of Q, O, LSE (R per group) and K, V (Nk)
+  int per = groups_per_chunk > 0 ? groups_per_chunk : (groups + kDefaultChunks - 1) / kDefaultChunks;
+  if ((groups + per - 1) / per > kMaxChunks) per = (groups + kMaxChunks - 1) / kMaxChunks;
+  const int n_chunks = (groups + per - 1) / per;
+  auto at = [](const void* base, size_t off) { return static_cast<const uint8_t*>(base) + off; };
+  auto at_mut = [](void* base, size_t off) { return static_cast<uint8_t*>(base) + off; };
+  if (cudaEventRecord(hp->start, stream) != cudaSuccess || cudaStreamWaitEvent(hp->in, hp->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->out, hp->start, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  for (int i = 0; i < kComputeStreams; ++i)
+    if (cudaStreamWaitEvent(hp->comp[i], hp->start, 0) != cudaSuccess) return FA_ERR_CUDA;
+  for (int c = 0; c < n_chunks; ++c) {
+    const int g0 = c * per, ng = std::min(per, groups - g0);
+    const size_t q_off = g0 * R * row_bytes, q_len = ng * R * row_bytes;
+    const size_t k_off = static_cast<size_t>(g0) * pr.Nk * row_bytes, k_len = static_cast<size_t>(ng) * pr.Nk * row_bytes;
+    const size_t l_off = g0 * R * 4, l_len = ng * R * 4;
+    if (cudaMemcpyAsync(at_mut(const_cast<void*>(pr.q), q_off), at(h.q, q_off), q_len, cudaMemcpyHostToDevice, hp->in) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(at_mut(const_cast<void*>(pr.k), k_off), at(h.k, k_off), k_len, cudaMemcpyHostToDevice, hp->in) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(at_mut(const_cast<void*>(pr.v), k_off), at(h.v, k_off), k_len, cudaMemcpyHostToDevice, hp->in) !=
+            cudaSuccess ||
+        cudaEventRecord(hp->loaded[c], hp->in) != cudaSuccess)
+      return FA_ERR_CUDA;
+    cudaStream_t cs = hp->comp[c % kComputeStreams];
+    if (cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess) return FA_ERR_CUDA;
+    Problem sub = pr;
+    sub.q = at(pr.q, q_off);
+    sub.k = at(pr.k, k_off);
+    sub.v = at(pr.v, k_off);
+    sub.o = at_mut(pr.o, q_off);
+    sub.lse = reinterpret_cast<float*>(at_mut(pr.lse, l_off));
+    sub.B = 1;
+    sub.Hq = ng * G;
+    sub.Hkv = ng;
+    rc = pr.d == 64 ? launch<64>(sub, 0, kDefaultTimeoutNs, cs) : launch<128>(sub, 0, kDefaultTimeoutNs, cs);
+    if (rc != FA_OK) return rc;
+    if (cudaEventRecord(hp->computed[c], cs) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->out, hp->computed[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(at_mut(h.o, q_off), at(pr.o, q_off), q_len, cudaMemcpyDeviceToHost, hp->out) != cudaSuccess ||
+        cudaMemcpyAsync(at_mut(h.lse, l_off), at(pr.lse, l_off), l_len, cudaMemcpyDeviceToHost, hp->out) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  if (cudaEventRecord(hp->done, hp->out) != cudaSuccess || cudaStreamWaitEvent(stream, hp->done, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
 }  // namespace
 
 // status words of the backward (fa_bwd_sm103.cu) and FP8 (fa_fp8_sm103.cu) translation
@@ -732,6 +861,13 @@ int fa_fwd_gqa_static_workspace(const void* q, const void* k, const void* v, voi
   }
   const fa::Problem pr{q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, n_splits, ws, ws_bytes};
   return fa::run(pr, 0, fa::kDefaultTimeoutNs, stream);
+}
+
+int fa_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                void* q, void* k, void* v, void* o, float* lse, int B, int Hq, int Hkv, int Nq, int Nk, int d,
+                float scale, int causal, int groups_per_chunk, cudaStream_t stream) {
+  const fa::Problem pr{q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, 1, nullptr, 0};
+  return fa::run_host(fa::HostBuffers{q_host, k_host, v_host, o_host, lse_host}, pr, groups_per_chunk, stream);
 }
 
 int fa_fwd_withheld_tile(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,

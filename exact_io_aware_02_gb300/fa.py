@@ -26,7 +26,7 @@ FA_STATIC_WORKSPACE_BYTES = 16 << 20
 FA_STATUS_TIMEOUT = 0x1
 
 EXPORTED = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_gqa_workspace_bytes", "fa_fwd_gqa_static_workspace",
-            "fa_bwd", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "fa_status", "fa_fwd_withheld_tile",
+            "fa_fwd_host", "fa_bwd", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "fa_status", "fa_fwd_withheld_tile",
             "fa_bwd_withheld_tile", "fa_fwd_fp8_withheld_tile", "fa_strerror", "fa_version")
 
 if not os.path.exists(LIB_PATH):
@@ -43,6 +43,8 @@ lib.fa_fwd_gqa_workspace_bytes.argtypes = [_i, _i, _i, _i, _i]
 lib.fa_fwd_gqa_workspace_bytes.restype = ctypes.c_size_t
 lib.fa_fwd_gqa_static_workspace.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]
 lib.fa_fwd_gqa_static_workspace.restype = _i
+lib.fa_fwd_host.argtypes = [_vp] * 10 + [_i, _i, _i, _i, _i, _i, _f, _i, _i, _vp]
+lib.fa_fwd_host.restype = _i
 lib.fa_fwd_withheld_tile.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _d, _vp]
 lib.fa_fwd_withheld_tile.restype = _i
 lib.fa_bwd.argtypes = [_vp] * 10 + [_i, _i, _i, _i, _i, _f, _i, _vp]
@@ -134,6 +136,29 @@ def fa_fwd_gqa(q, k, v, o=None, lse=None, scale=None, causal=False, n_splits=1,
     if rc != FA_OK:
         raise FAError(rc)
     return o, lse
+
+
+def fa_fwd_host(q_host, k_host, v_host, o_host, lse_host, q, k, v, o, lse, scale=None, causal=False,
+                groups_per_chunk=0, stream=None):
+    """Host-to-host forward with the copies overlapped with the attention, chunk by chunk.
+
+    q_host, k_host, v_host, o_host, lse_host: pinned CPU tensors (``pin_memory()``) in the
+    layouts of fa_fwd_gqa; q, k, v, o, lse: CUDA tensors of the same shapes (q, k, v receive
+    the copies).  Enqueues on ``stream`` and returns; synchronise it before reading o_host.
+    """
+    if q.dim() != 4 or k.dim() != 4 or k.shape != v.shape:
+        raise ValueError("q must be [B, Hq, Nq, d] and k, v [B, Hkv, Nk, d]")
+    B, Hq, Nq, d = q.shape
+    Hkv, Nk = k.shape[1], k.shape[2]
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    rc = lib.fa_fwd_host(q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(), o_host.data_ptr(),
+                         lse_host.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                         lse.data_ptr(), B, Hq, Hkv, Nq, Nk, d, float(scale), int(bool(causal)),
+                         int(groups_per_chunk), _stream_handle(stream, q.device))
+    if rc != FA_OK:
+        raise FAError(rc)
+    return o_host, lse_host
 
 
 def fa_fwd_gqa_static_workspace(q, k, v, o=None, lse=None, scale=None, causal=False, n_splits=1,

@@ -150,6 +150,44 @@ int fa_fwd_gqa_static_workspace(const void* q, const void* k, const void* v, voi
                                 int causal, int n_splits, cudaStream_t stream);
 
 /*
+ * fa_fwd_host -- fa_fwd_gqa (n_splits = 1) from host inputs to host outputs, with the
+ * copies overlapped with the attention.  (An addition of this library: the pages'
+ * IO-aware scheduling stops at HBM; this carries the same idea to the host link.)
+ *
+ * The K/V groups (b, hkv) are cut into chunks of groups_per_chunk groups (0 = about
+ * eight chunks; at most 64 chunks).  Chunk c's Q, K and V rows are copied host to
+ * device on a copy stream of the library's; its forward runs, as soon as they have
+ * landed, on one of two compute streams of the library's (alternating, so consecutive
+ * chunks share the SMs); and its O and LSE rows go back on a second copy stream while
+ * later chunks load and run.  Host-to-device copies, the kernels and device-to-host
+ * copies of different chunks therefore overlap.  A chunk's kernel is the same as
+ * fa_fwd_gqa's on those groups, so the results are bitwise those of fa_fwd_gqa.
+ *
+ * q_host, k_host, v_host : page-locked host memory (cudaHostAlloc / cudaMallocHost /
+ *                  cudaHostRegister), the layouts of fa_fwd_gqa's q, k, v.  Read.
+ * o_host, lse_host : page-locked host memory, the layouts of o and lse.  Written.
+ * q, k, v, o, lse : device buffers of the full tensors, as for fa_fwd_gqa; q, k and v
+ *                  are written here (they receive the copies).
+ * Other arguments as for fa_fwd_gqa with n_splits = 1.
+ *
+ * Ownership and ordering: the caller owns every buffer; the call allocates no memory.
+ * The first call on a device creates the library's four streams and its events
+ * (kept until exit).  The call's work starts after the work already enqueued on
+ * `stream`, and `stream` waits for the call's last copy: synchronise `stream` before
+ * reading o_host / lse_host or reusing any buffer.  Calls on a device are enqueued one
+ * at a time (a mutex); their copies share the two streams.
+ *
+ * Returns FA_OK; FA_ERR_ARG for the arguments fa_fwd_gqa rejects, a null or pageable
+ * host buffer, host outputs that overlap host inputs or each other, or a negative
+ * groups_per_chunk; FA_ERR_ARCH; FA_ERR_LAUNCH; FA_ERR_CUDA if a stream, event or
+ * copy call fails (work already enqueued then stays enqueued).
+ */
+int fa_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                float* lse_host, void* q, void* k, void* v, void* o, float* lse, int B, int Hq,
+                int Hkv, int Nq, int Nk, int d, float scale, int causal, int groups_per_chunk,
+                cudaStream_t stream);
+
+/*
  * fa_fwd_fp8 -- attention forward with FP8 (E4M3) tensor-core products: block-wise
  * quantisation with incoherent processing (§10 item ③ and §12.2 of the zzszmyf.github.io
  * notes "FlashAttention 原理是什么？为什么又省显存又快").

@@ -102,3 +102,14 @@ def _bwd(fa, B=1, Hq=2, Hkv=1, N=128, d=128, scale=0.088, causal=1, **ptrs):
 ])
 def test_bwd_argument_errors_before_launch(fa, kw):
     assert _bwd(fa, **kw) == fa.FA_ERR_ARG
+
+
+def test_host_entry_argument_errors(fa):
+    f = fa.lib.fa_fwd_host
+    dev = [FAKE + i * 2**30 for i in range(5)]
+    host = [FAKE + (8 + i) * 2**30 for i in range(5)]
+    tail = [1, 2, 2, 128, 128, 128, 0.088, 0]
+    assert f(*([0] + host[1:]), *dev, *tail, 0, None) == fa.FA_ERR_ARG  # null host input
+    assert f(*host, *dev, *tail, -1, None) == fa.FA_ERR_ARG              # negative chunk size
+    assert f(*host, *dev, 1, 2, 2, 128, 128, 96, 0.088, 0, 0, None) == fa.FA_ERR_ARG  # d = 96
+

@@ -116,7 +116,10 @@ __device__ __forceinline__ int causal_tile_limit(const Params& p, int qt) {
   return max_pos < 0 ? 0 : max_pos / 128 + 1;
 }
 
-template <int D>
+// kDual: one query tile per group and n_splits > 1 (decoding).  The CTA's two tile slots then
+// take the same query rows over splits 2c and 2c+1: two independent softmax/product chains
+// per SM, each with its own K/V tiles in the ring.
+template <int D, bool kDual>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -136,7 +139,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- which (group, query-tile pair, K/V split) this CTA owns
   int bid = blockIdx.x;
   int bh, cta_q, split = 0;
-  if (p.n_splits == 1 && p.causal) {  // longest first: the last query tiles have the most K/V tiles
+  if constexpr (kDual) {
+    const int pairs = (p.n_splits + 1) / 2;
+    split = 2 * (bid % pairs);
+    bh = bid / pairs;
+    cta_q = 0;
+  } else if (p.n_splits == 1 && p.causal) {  // longest first: the last query tiles have the most K/V tiles
     cta_q = p.n_cta_q - 1 - bid / p.groups;
     bh = bid % p.groups;
   } else {  // group-major: CTAs of one K/V head run together and share K/V in L2
@@ -145,18 +153,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     bh = bid / p.n_cta_q;
     cta_q = bid % p.n_cta_q;
   }
-  const int qt0 = 2 * cta_q;
-  const int qt1 = qt0 + 1;
-  const bool has1 = qt1 < p.n_qtiles;
-  // K/V tiles [t_lo, t_hi) of this split; causal tiles end at the last visible key
-  const int t_lo = split * p.split_tiles;
-  const int t_hi = min(t_lo + p.split_tiles, p.n_kv_tiles);
-  auto tiles_for = [&](int qt) {
-    const int hi = p.causal ? min(t_hi, causal_tile_limit(p, qt)) : t_hi;
-    return hi > t_lo ? hi - t_lo : 0;
+  const int qt0 = kDual ? 0 : 2 * cta_q;
+  const int qt1 = kDual ? 0 : qt0 + 1;
+  const bool has1 = kDual ? split + 1 < p.n_splits : qt1 < p.n_qtiles;
+  // K/V tiles [lo_t, hi_t) of tile slot t's split; causal tiles end at the last visible key
+  const int split1 = kDual ? split + 1 : split;
+  const int lo0 = split * p.split_tiles, lo1 = split1 * p.split_tiles;
+  auto tiles_for = [&](int qt, int lo) {
+    const int hi0 = min(lo + p.split_tiles, p.n_kv_tiles);
+    const int hi = p.causal ? min(hi0, causal_tile_limit(p, qt)) : hi0;
+    return hi > lo ? hi - lo : 0;
   };
-  const int n0 = tiles_for(qt0);  // K/V tiles visited by query tile 0
-  const int n1 = has1 ? tiles_for(qt1) : 0;
+  const int n0 = tiles_for(qt0, lo0);  // K/V tiles visited by tile slot 0
+  const int n1 = has1 ? tiles_for(qt1, lo1) : 0;
   const int nmax = n0 > n1 ? n0 : n1;
 
   if (warp == 8 && lane == 0) {
@@ -200,10 +209,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < C::kChunks; ++c)
           ptx::tma_load_3d(sbase + C::kOffQ + C::kTileBytes + c * C::kChunkBytes, &tm_q,
                            bar(C::kBarQ), c * 64, qt1 * 128, bh);
-      const int n_tiles = 2 * nmax;
+      const int n_tiles = kDual ? 0 : 2 * nmax;
       const int skip = p.withhold_v0 ? 1 : -1;  // test hook: tile 1 (V_0) is never loaded
       int issued = 0;
       bool ok = true;
+      if constexpr (kDual) {
+        // ring order = the MMA warp's order: per step j and slot t, V_t(j-1) then K_t(j)
+        auto load = [&](int kv_tile, bool is_v) -> bool {
+          const int u = issued, slot = u % C::kSlots, use = u / C::kSlots;
+          if (use > 0 && !w.wait(bar(C::kBarEmpty + slot), (use - 1) & 1)) return false;
+          ptx::mbar_arrive_expect_tx(bar(C::kBarFull + slot), C::kTileBytes);
+          for (int c = 0; c < C::kChunks; ++c)
+            ptx::tma_load_3d(sbase + C::kOffRing + slot * C::kTileBytes + c * C::kChunkBytes, is_v ? &tm_v : &tm_k,
+                             bar(C::kBarFull + slot), c * 64, kv_tile * 128, bh);
+          issued = u + 1;
+          return true;
+        };
+        for (int j = 0; ok && j <= nmax; ++j)
+          for (int t = 0; ok && t < 2; ++t) {
+            const int nt = t ? n1 : n0, lo = t ? lo1 : lo0;
+            if (j >= 1 && j - 1 < nt) ok = load(lo + j - 1, true);
+            if (ok && j < nt) ok = load(lo + j, false);
+          }
+      }
       for (int u = 0; u < n_tiles; ++u) {
         const int slot = u % C::kSlots, use = u / C::kSlots;
         if (use > 0 && !w.wait(bar(C::kBarEmpty + slot), (use - 1) & 1)) { ok = false; break; }
@@ -212,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const CUtensorMap* m = (u & 1) ? &tm_v : &tm_k;
           for (int c = 0; c < C::kChunks; ++c)
             ptx::tma_load_3d(sbase + C::kOffRing + slot * C::kTileBytes + c * C::kChunkBytes, m,
-                             bar(C::kBarFull + slot), c * 64, (t_lo + (u >> 1)) * 128, bh);
+                             bar(C::kBarFull + slot), c * 64, (lo0 + (u >> 1)) * 128, bh);
         }
         issued = u + 1;
       }
@@ -238,7 +266,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t desc_v_ring = ptx::smem_desc_sw128(sbase + C::kOffRing, C::kChunkBytes, 1024);
     bool ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarQ), 0));
     ptx::tc_fence_after();
-    for (int j = 0; ok && j <= nmax; ++j) {
+    if constexpr (kDual) {
+      // each tile slot has K/V tiles of its own, consumed (and released) in ring order
+      int u = 0;
+      for (int j = 0; ok && j <= nmax; ++j) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          const int nt = t ? n1 : n0;
+          if (j >= 1 && j - 1 < nt) {
+            ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1));
+            if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarPFull + t), (j - 1) & 1));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint64_t dv = desc_v_ring + static_cast<uint64_t>(u % C::kSlots) * kSlotStep;
+            const uint32_t t_o = tmem + C::kColO + t * D;
+            const uint32_t t_p = tmem + C::kColS + t * 128;
+            if (ptx::elect_one()) {
+              if (j > 1) ptx::mma_ts_i<1>(t_o, t_p, dv, kIdescPV);
+              else ptx::mma_ts_i<0>(t_o, t_p, dv, kIdescPV);
+#pragma unroll
+              for (int kk = 1; kk < 8; ++kk) ptx::mma_ts_i<1>(t_o, t_p + kk * 8, dv + kk * 128, kIdescPV);
+              if (j - 1 == nt - 1) ptx::tc_commit(bar(C::kBarOFinal + t));
+              ptx::tc_commit(bar(C::kBarEmpty + u % C::kSlots));
+            }
+            __syncwarp();
+            ++u;
+          }
+          if (j < nt) {
+            ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1));
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const uint64_t dk = desc_k_ring + static_cast<uint64_t>(u % C::kSlots) * kSlotStep;
+            const uint32_t t_s = tmem + C::kColS + t * 128;
+            const uint64_t dq = t ? desc_q1 : desc_q0;
+            if (ptx::elect_one()) {
+              ptx::mma_ss_i<0>(t_s, dq, dk, kIdescQK);
+#pragma unroll
+              for (int kk = 1; kk < D / 16; ++kk) {
+                const uint64_t o = (kk >> 2) * (C::kChunkBytes >> 4) + (kk & 3) * 2;
+                ptx::mma_ss_i<1>(t_s, dq + o, dk + o, kIdescQK);
+              }
+              ptx::tc_commit(bar(C::kBarSFull + t));
+              ptx::tc_commit(bar(C::kBarEmpty + u % C::kSlots));
+            }
+            __syncwarp();
+            ++u;
+          }
+        }
+      }
+    }
+    for (int j = 0; ok && !kDual && j <= nmax; ++j) {
       const int uk = 2 * j, uv = 2 * j - 1;  // ring tiles K_j and V_{j-1}
       if (j >= 1) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + uv % C::kSlots), (uv / C::kSlots) & 1));
       if (!ok) break;
@@ -330,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
       }
       // mask: keys past the end of the sequence, and keys after the query when causal
-      const int col0 = (t_lo + j) * 128;
+      const int col0 = ((t ? lo1 : lo0) + j) * 128;
       int lim = p.Nk - col0;
       if (p.causal && qpos - col0 + 1 < lim) lim = qpos - col0 + 1;
       if (lim < 128) {
@@ -409,6 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // LSE = -inf.  One split: O -> bf16 -> shared (Q_t's buffer) -> TMA store.  Several
     // splits: fp32 partial O and partial LSE straight to the workspace for the combine.
     const bool tile_exists = t == 0 || has1;
+    const int my_split = t ? split1 : split;  // the partials this tile slot writes (n_splits > 1)
     const size_t grow = static_cast<size_t>(bh) * p.R + qrow;  // row in [B*Hq*Nq]
     const bool row_valid = qrow < p.R;
     const uint32_t so = sbase + C::kOffQ + t * C::kTileBytes;
@@ -438,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::fence_proxy_async_smem();
     } else if (ok && p.n_splits > 1) {
       ptx::tc_fence_after();
-      float4* dst = reinterpret_cast<float4*>(p.o_part + (static_cast<size_t>(split) * p.groups * p.R + grow) * D);
+      float4* dst = reinterpret_cast<float4*>(p.o_part + (static_cast<size_t>(my_split) * p.groups * p.R + grow) * D);
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t r[32];
@@ -450,7 +528,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
         }
       }
-      if (row_valid) p.lse_part[static_cast<size_t>(split) * p.groups * p.R + grow] = lse_row;
+      if (row_valid) p.lse_part[static_cast<size_t>(my_split) * p.groups * p.R + grow] = lse_row;
     } else if (tile_exists && nt == 0 && row_valid) {
       // no K/V tile of this split is visible to the tile: the empty result
       if (p.n_splits == 1) {
@@ -458,9 +536,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
         p.lse[grow] = -INFINITY;
       } else {
-        float4* dst = reinterpret_cast<float4*>(p.o_part + (static_cast<size_t>(split) * p.groups * p.R + grow) * D);
+        float4* dst = reinterpret_cast<float4*>(p.o_part + (static_cast<size_t>(my_split) * p.groups * p.R + grow) * D);
         for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        p.lse_part[static_cast<size_t>(split) * p.groups * p.R + grow] = -INFINITY;
+        p.lse_part[static_cast<size_t>(my_split) * p.groups * p.R + grow] = -INFINITY;
       }
     }
     ptx::named_barrier(1 + t, 128);
@@ -547,9 +625,13 @@ int prepare_device() {
     if (arch == FA_ERR_ARCH) g_dev_state[dev] = -1;
     return arch;
   }
-  if (cudaFuncSetAttribute(fa_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(fa_fwd_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<64>::kSmemBytes) != cudaSuccess ||
-      cudaFuncSetAttribute(fa_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+      cudaFuncSetAttribute(fa_fwd_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<128>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(fa_fwd_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<64>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(fa_fwd_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<128>::kSmemBytes) != cudaSuccess)
     return FA_ERR_CUDA;
   g_dev_state[dev] = 1;
@@ -637,11 +719,16 @@ int launch(const Problem& pr, int withhold_v0, unsigned long long timeout_ns, cu
   p.scale = pr.scale;
   p.scale_log2 = static_cast<float>(static_cast<double>(pr.scale) * 1.4426950408889634);
   p.causal = pr.causal ? 1 : 0;
+  const bool dual = p.n_qtiles == 1 && pr.n_splits > 1;
   p.withhold_v0 = withhold_v0;
   p.timeout_ns = timeout_ns;
-  const long long grid = static_cast<long long>(groups) * p.n_cta_q * pr.n_splits;
+  const long long grid = dual ? static_cast<long long>(groups) * ((pr.n_splits + 1) / 2)
+                              : static_cast<long long>(groups) * p.n_cta_q * pr.n_splits;
   if (grid > 2147483647LL) return FA_ERR_ARG;
-  fa_fwd_kernel<D><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(mq, mk, mv, mo, p);
+  if (dual)
+    fa_fwd_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(mq, mk, mv, mo, p);
+  else
+    fa_fwd_kernel<D, false><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(mq, mk, mv, mo, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   if (pr.n_splits > 1) {
     const long long blocks = (rows * 32 + 255) / 256;

@@ -81,7 +81,7 @@ WORKLOADS = {
         # per K/V head (memory-bound: reads K and V once); the keys are split 7 ways, so
         # that the 64 groups x 7 splits = 448 CTAs are about three waves on 148 SMs
         Workload("gqa_decode_nk32768_d128", 8, 32, 1, 128, False, seed=20267, Hkv=8,
-                 Nk=32768, n_splits=7, bound="hbm"),
+                 Nk=32768, n_splits=4, bound="hbm"),
         # the backward of the causal prefill shape: dQ, dK, dV with recomputation
         Workload("bwd_causal_n8192_d128", 2, 16, 8192, 128, True, seed=20263, direction="bwd"),
         # a small backward (inputs of 16 MiB per tensor) for full-section profiler captures

@@ -785,7 +785,34 @@ int static_workspace(void** out) {
 // enqueueing of whole calls, so that two host threads never interleave their records of
 // the shared events.
 constexpr int kMaxChunks = 64;
-constexpr int kDefaultChunks = 8;
+// Default chunking.  When the host link binds (its copies take longer than the attention),
+// at most seven chunks with the boundaries at 8, 14, 20, 25, 29, 31 and 32 thirty-seconds of
+// the groups (rounded; empty chunks dropped): 32 groups give 8, 6, 6, 5, 4, 2, 1.  Large early
+// chunks keep the link busy with few launches; small late ones shorten the tail (the last
+// chunk's kernel and its copy back), which no later copy hides.  When the attention binds,
+// eight equal chunks: a small last chunk would add the length of its longest causal CTA.
+// The two times are estimated with the rates measured on GB300: about 200 GB/s per direction
+// on the host link and about 1.3 PFLOP/s of attention.  (Causal N = 8192, d = 128, 32 groups:
+// 1.22 ms against 1.27 ms with equal chunks; causal N = 32768: 6.6 against 7.1 ms the other
+// way round.)
+constexpr double kHostLinkBytesPerSec = 2.0e11;
+constexpr double kAttentionFlopsPerSec = 1.3e15;
+int default_chunks(int groups, double copy_bytes, double flops, int (&sizes)[kMaxChunks]) {
+  int n = 0;
+  if (flops / kAttentionFlopsPerSec >= 0.8 * copy_bytes / kHostLinkBytesPerSec) {
+    const int per = (groups + 7) / 8;
+    for (int g = 0; g < groups; g += per) sizes[n++] = std::min(per, groups - g);
+    return n;
+  }
+  constexpr int kBounds[7] = {8, 14, 20, 25, 29, 31, 32};
+  int prev = 0;
+  for (int i = 0; i < 7; ++i) {
+    const int b = static_cast<int>((static_cast<long long>(groups) * kBounds[i] + 16) / 32);
+    if (b > prev) sizes[n++] = b - prev;
+    prev = b;
+  }
+  return n;
+}
 constexpr int kComputeStreams = 2;
 struct HostPipe {
   cudaStream_t in = nullptr, out = nullptr, comp[kComputeStreams] = {};
@@ -858,9 +885,19 @@ int run_host(const HostBuffers& h, const Problem& pr, int groups_per_chunk, cuda
   rc = host_pipe(dev, &hp);
   if (rc != FA_OK) return rc;
   // chunks of whole K/V groups: contiguous rows of Q, O, LSE (R per group) and K, V (Nk)
-  int per = groups_per_chunk > 0 ? groups_per_chunk : (groups + kDefaultChunks - 1) / kDefaultChunks;
-  if ((groups + per - 1) / per > kMaxChunks) per = (groups + kMaxChunks - 1) / kMaxChunks;
-  const int n_chunks = (groups + per - 1) / per;
+  int sizes[kMaxChunks];
+  int n_chunks = 0;
+  if (groups_per_chunk > 0) {
+    int per = groups_per_chunk;
+    if ((groups + per - 1) / per > kMaxChunks) per = (groups + kMaxChunks - 1) / kMaxChunks;
+    for (int g = 0; g < groups; g += per) sizes[n_chunks++] = std::min(per, groups - g);
+  } else {
+    // bytes that cross the link (Q, K, V in; O, LSE out) and the attention's flops (the causal
+    // fraction taken as one half)
+    const double bytes = 2.0 * qb + 2.0 * kb + lb;
+    const double flops = 4.0 * static_cast<double>(pr.B) * pr.Hq * pr.Nq * pr.Nk * pr.d * (pr.causal ? 0.5 : 1.0);
+    n_chunks = default_chunks(groups, bytes, flops, sizes);
+  }
   auto at = [](const void* base, size_t off) { return static_cast<const uint8_t*>(base) + off; };
   auto at_mut = [](void* base, size_t off) { return static_cast<uint8_t*>(base) + off; };
   if (cudaEventRecord(hp->start, stream) != cudaSuccess || cudaStreamWaitEvent(hp->in, hp->start, 0) != cudaSuccess ||
@@ -868,8 +905,8 @@ int run_host(const HostBuffers& h, const Problem& pr, int groups_per_chunk, cuda
     return FA_ERR_CUDA;
   for (int i = 0; i < kComputeStreams; ++i)
     if (cudaStreamWaitEvent(hp->comp[i], hp->start, 0) != cudaSuccess) return FA_ERR_CUDA;
-  for (int c = 0; c < n_chunks; ++c) {
-    const int g0 = c * per, ng = std::min(per, groups - g0);
+  for (int c = 0, g0 = 0; c < n_chunks; g0 += sizes[c], ++c) {
+    const int ng = sizes[c];
     const size_t q_off = g0 * R * row_bytes, q_len = ng * R * row_bytes;
     const size_t k_off = static_cast<size_t>(g0) * pr.Nk * row_bytes, k_len = static_cast<size_t>(ng) * pr.Nk * row_bytes;
     const size_t l_off = g0 * R * 4, l_len = ng * R * 4;

@@ -154,8 +154,11 @@ int fa_fwd_gqa_static_workspace(const void* q, const void* k, const void* v, voi
  * copies overlapped with the attention.  (An addition of this library: the pages'
  * IO-aware scheduling stops at HBM; this carries the same idea to the host link.)
  *
- * The K/V groups (b, hkv) are cut into chunks of groups_per_chunk groups (0 = about
- * eight chunks; at most 64 chunks).  Chunk c's Q, K and V rows are copied host to
+ * The K/V groups (b, hkv) are cut into chunks of groups_per_chunk groups (at most 64
+ * chunks).  groups_per_chunk = 0 picks a default: when the copies take longer than the
+ * attention (estimated at about 200 GB/s per direction and 1.3 PFLOP/s), at most seven
+ * chunks of decreasing size (a quarter of the groups first, one thirty-second last);
+ * otherwise eight equal chunks.  Chunk c's Q, K and V rows are copied host to
  * device on a copy stream of the library's; its forward runs, as soon as they have
  * landed, on one of two compute streams of the library's (alternating, so consecutive
  * chunks share the SMs); and its O and LSE rows go back on a second copy stream while

@@ -135,6 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // the split combine (if any) may be scheduled now; it waits for this grid to complete
+  ptx::griddep_launch_dependents();
 
   // ---- which (group, query-tile pair, K/V split) this CTA owns
   int bid = blockIdx.x;
@@ -567,6 +569,7 @@ __global__ void __launch_bounds__(256)
     fa_combine_kernel(const float* __restrict__ o_part, const float* __restrict__ lse_part,
                       uint16_t* __restrict__ o, float* __restrict__ lse, int rows, int n_splits) {
   constexpr int E = D / 32;  // elements per lane
+  ptx::griddep_wait();  // launched behind the split kernel: its partials are complete and visible
   const int row = static_cast<int>((static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
@@ -732,9 +735,23 @@ int launch(const Problem& pr, int withhold_v0, unsigned long long timeout_ns, cu
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   if (pr.n_splits > 1) {
     const long long blocks = (rows * 32 + 255) / 256;
-    fa_combine_kernel<D><<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        p.o_part, p.lse_part, static_cast<uint16_t*>(pr.o), pr.lse, static_cast<int>(rows), pr.n_splits);
-    if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+    // programmatic dependent launch: the combine's CTAs are scheduled while the split kernel
+    // runs and start the moment it completes, without a launch gap
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, fa_combine_kernel<D>, static_cast<const float*>(p.o_part),
+                           static_cast<const float*>(p.lse_part), static_cast<uint16_t*>(pr.o), pr.lse,
+                           static_cast<int>(rows), pr.n_splits) != cudaSuccess ||
+        cudaGetLastError() != cudaSuccess)
+      return FA_ERR_LAUNCH;
   }
   return FA_OK;
 }

@@ -64,6 +64,15 @@ def test_argument_errors_before_launch(fa, kw):
     assert _call(fa, **kw) == fa.FA_ERR_ARG
 
 
+def test_fp8_sequence_limit(fa):
+    """The FP8 forward keeps per-tile tables of at most 1024 key tiles: N = 131072 is the
+    largest length it accepts; one more row is rejected before any CUDA call."""
+    ws = fa.lib.fa_fwd_fp8_workspace_bytes
+    assert ws(1, 1, 131072, 128) > 0
+    args = [FAKE + i * 2**30 for i in range(6)]
+    assert fa.lib.fa_fwd_fp8(*args, 1, 1, 131073, 128, 0.088, 0, FAKE + 7 * 2**30, 1 << 40, None) == fa.FA_ERR_ARG
+
+
 def test_bwd_and_fp8_withheld_timeout_range(fa):
     b = fa.lib.fa_bwd_withheld_tile
     args = [FAKE + i * 2**30 for i in range(10)] + [1, 2, 1, 128, 128, 0.088, 1]

@@ -144,6 +144,25 @@ def test_large_constant_scores(fa, c):
         assert np.max(np.abs(_np64(lse[0, 0]) - (s + np.log(cnt)))) <= 1e-3 * max(1.0, abs(s) + 6)
 
 
+def test_near_uniform_attention(fa):
+    """A scale near zero makes every visible key weigh the same: O is the mean of the visible
+    V rows and LSE = ln(count) (plus a term of order scale * |q.k|)."""
+    N, d = 700, 128
+    q, k, v = make_qkv(1, 2, N, d, seed=91)
+    scale = 1e-6
+    for causal in (False, True):
+        o, lse = run(fa, q, k, v, scale, causal)
+        for h in range(2):
+            ro, rl = oracle.naive_attention(_np64(q[0, h]), _np64(k[0, h]), _np64(v[0, h]), scale, causal)
+            st = compare(_np64(o[0, h]), _np64(lse[0, h]), ro, rl)
+            assert within_tolerance(st), st
+            vv = _np64(v[0, h])
+            mean = np.cumsum(vv, axis=0) / np.arange(1, N + 1)[:, None] if causal else np.broadcast_to(vv.mean(0), vv.shape)
+            assert np.max(np.abs(_np64(o[0, h]) - mean)) <= 1e-2
+            cnt = np.arange(1, N + 1) if causal else np.full(N, N)
+            assert np.max(np.abs(_np64(lse[0, h]) - np.log(cnt))) <= 1e-3 * np.log(N) + 1e-3
+
+
 def test_causal_row_zero_closed_form(fa):
     q, k, v = make_qkv(2, 2, 512, 128, seed=5)
     scale = 1.0 / math.sqrt(128)

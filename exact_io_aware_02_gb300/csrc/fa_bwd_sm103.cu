@@ -825,6 +825,112 @@ int run_bwd(const BwdProblem& pr, int withhold, unsigned long long timeout_ns, c
                     : launch_bwd<128>(pr, withhold, timeout_ns, stream);
 }
 
+// ---- pipelined host-to-host backward (fa_bwd_host): chunks of K/V groups, each chunk's six
+// inputs copied in on the library's copy stream, its three kernels on one of two compute
+// streams, and its dQ, dK, dV copied out on the second copy stream while later chunks load and
+// run.  A chunk's kernels are fa_bwd's on those groups, so the results are fa_bwd's.
+struct BwdHost {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* o;
+  const float* lse;
+  const void* dout;
+  void* dq;
+  void* dk;
+  void* dv;
+};
+
+int run_bwd_host(const BwdHost& h, const BwdProblem& pr, int groups_per_chunk, cudaStream_t stream) {
+  int rc = validate_bwd(pr);
+  if (rc != FA_OK) return rc;
+  const void* hin[6] = {h.q, h.k, h.v, h.o, h.lse, h.dout};
+  const void* hout[3] = {h.dq, h.dk, h.dv};
+  for (const void* ptr : hin)
+    if (!ptr) return FA_ERR_ARG;
+  for (const void* ptr : hout)
+    if (!ptr) return FA_ERR_ARG;
+  if (groups_per_chunk < 0) return FA_ERR_ARG;
+  const int G = pr.Hq / pr.Hkv, groups = pr.B * pr.Hkv;
+  const size_t R = static_cast<size_t>(G) * pr.N;  // query rows per group
+  const size_t row_bytes = static_cast<size_t>(pr.d) * 2;
+  const size_t qb = groups * R * row_bytes, kb = static_cast<size_t>(groups) * pr.N * row_bytes;
+  const size_t lb = groups * R * 4;
+  const size_t hin_n[6] = {qb, kb, kb, qb, lb, qb};
+  const size_t hout_n[3] = {qb, kb, kb};
+  for (int i = 0; i < 3; ++i) {
+    for (int j = 0; j < 6; ++j)
+      if (overlaps(hout[i], hout_n[i], hin[j], hin_n[j])) return FA_ERR_ARG;
+    for (int j = i + 1; j < 3; ++j)
+      if (overlaps(hout[i], hout_n[i], hout[j], hout_n[j])) return FA_ERR_ARG;
+  }
+  for (const void* ptr : hin)
+    if (!is_pinned_host(ptr)) return FA_ERR_ARG;
+  for (const void* ptr : hout)
+    if (!is_pinned_host(ptr)) return FA_ERR_ARG;
+  rc = prepare_device_bwd();
+  if (rc != FA_OK) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_pipe[dev].mu);
+  HostPipe* hp = nullptr;
+  rc = host_pipe(dev, &hp);
+  if (rc != FA_OK) return rc;
+  // chunk starts need no alignment beyond a row: Q-like and K-like rows are 128 or 256 bytes,
+  // and the kernels read LSE and D one float per row
+  int sizes[kMaxChunks];
+  const double bytes = 5.0 * qb + 4.0 * kb + lb;  // in: q, k, v, o, lse, dO; out: dq, dk, dv
+  const double flops = 10.0 * static_cast<double>(pr.B) * pr.Hq * pr.N * pr.N * pr.d * (pr.causal ? 0.5 : 1.0);
+  const int n_chunks = chunk_sizes(groups, groups_per_chunk, bytes, flops / kBackwardFlopsPerSec, sizes);
+  auto at = [](const void* base, size_t off) { return static_cast<const uint8_t*>(base) + off; };
+  auto at_mut = [](void* base, size_t off) { return static_cast<uint8_t*>(base) + off; };
+  if (cudaEventRecord(hp->start, stream) != cudaSuccess || cudaStreamWaitEvent(hp->in, hp->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->out, hp->start, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  for (int i = 0; i < kComputeStreams; ++i)
+    if (cudaStreamWaitEvent(hp->comp[i], hp->start, 0) != cudaSuccess) return FA_ERR_CUDA;
+  for (int c = 0, g0 = 0; c < n_chunks; g0 += sizes[c], ++c) {
+    const int ng = sizes[c];
+    const size_t q_off = g0 * R * row_bytes, q_len = ng * R * row_bytes;
+    const size_t k_off = static_cast<size_t>(g0) * pr.N * row_bytes, k_len = static_cast<size_t>(ng) * pr.N * row_bytes;
+    const size_t l_off = g0 * R * 4, l_len = ng * R * 4;
+    const struct { void* dst; const void* src; size_t off, len; } in[6] = {
+        {const_cast<void*>(pr.q), h.q, q_off, q_len},       {const_cast<void*>(pr.k), h.k, k_off, k_len},
+        {const_cast<void*>(pr.v), h.v, k_off, k_len},       {const_cast<void*>(pr.o), h.o, q_off, q_len},
+        {const_cast<float*>(pr.lse), h.lse, l_off, l_len},  {const_cast<void*>(pr.dout), h.dout, q_off, q_len}};
+    for (const auto& x : in)
+      if (cudaMemcpyAsync(at_mut(x.dst, x.off), at(x.src, x.off), x.len, cudaMemcpyHostToDevice, hp->in) != cudaSuccess)
+        return FA_ERR_CUDA;
+    cudaStream_t cs = hp->comp[c % kComputeStreams];
+    if (cudaEventRecord(hp->loaded[c], hp->in) != cudaSuccess || cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess)
+      return FA_ERR_CUDA;
+    BwdProblem sub = pr;
+    sub.q = at(pr.q, q_off);
+    sub.k = at(pr.k, k_off);
+    sub.v = at(pr.v, k_off);
+    sub.o = at(pr.o, q_off);
+    sub.lse = reinterpret_cast<const float*>(at(pr.lse, l_off));
+    sub.dout = at(pr.dout, q_off);
+    sub.dq = at_mut(pr.dq, q_off);
+    sub.dk = at_mut(pr.dk, k_off);
+    sub.dv = at_mut(pr.dv, k_off);
+    sub.delta = reinterpret_cast<float*>(at_mut(pr.delta, l_off));
+    sub.B = 1;
+    sub.Hq = ng * G;
+    sub.Hkv = ng;
+    rc = pr.d == 64 ? launch_bwd<64>(sub, 0, kDefaultTimeoutNs, cs) : launch_bwd<128>(sub, 0, kDefaultTimeoutNs, cs);
+    if (rc != FA_OK) return rc;
+    if (cudaEventRecord(hp->computed[c], cs) != cudaSuccess || cudaStreamWaitEvent(hp->out, hp->computed[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(at_mut(h.dq, q_off), at(pr.dq, q_off), q_len, cudaMemcpyDeviceToHost, hp->out) != cudaSuccess ||
+        cudaMemcpyAsync(at_mut(h.dk, k_off), at(pr.dk, k_off), k_len, cudaMemcpyDeviceToHost, hp->out) != cudaSuccess ||
+        cudaMemcpyAsync(at_mut(h.dv, k_off), at(pr.dv, k_off), k_len, cudaMemcpyDeviceToHost, hp->out) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  if (cudaEventRecord(hp->done, hp->out) != cudaSuccess || cudaStreamWaitEvent(stream, hp->done, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
 }  // namespace
 
 int bwd_status_word(int clear) {
@@ -846,6 +952,16 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            int causal, cudaStream_t stream) {
   const fa::BwdProblem pr{q, k, v, o, lse, dout, dq, dk, dv, delta, B, Hq, Hkv, N, d, scale, causal};
   return fa::run_bwd(pr, 0, fa::kDefaultTimeoutNs, stream);
+}
+
+int fa_bwd_host(const void* q_host, const void* k_host, const void* v_host, const void* o_host,
+                const float* lse_host, const void* dout_host, void* dq_host, void* dk_host, void* dv_host,
+                void* q, void* k, void* v, void* o, float* lse, void* dout, void* dq, void* dk, void* dv,
+                float* delta, int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                int groups_per_chunk, cudaStream_t stream) {
+  const fa::BwdProblem pr{q, k, v, o, lse, dout, dq, dk, dv, delta, B, Hq, Hkv, N, d, scale, causal};
+  const fa::BwdHost h{q_host, k_host, v_host, o_host, lse_host, dout_host, dq_host, dk_host, dv_host};
+  return fa::run_bwd_host(h, pr, groups_per_chunk, stream);
 }
 
 int fa_bwd_withheld_tile(const void* q, const void* k, const void* v, const void* o, const float* lse,

@@ -794,81 +794,7 @@ int static_workspace(void** out) {
   return FA_OK;
 }
 
-// ---- pipelined host-to-host forward (fa_fwd_host)
-// Per device: one stream for host-to-device copies, one for device-to-host copies, two for
-// the chunks' kernels (a causal chunk's longest CTA sets its kernel's duration however few
-// heads it holds, so consecutive chunks run side by side on the SMs), and a pool of events;
-// created on first use and kept until the process exits.  The mutex serialises the
-// enqueueing of whole calls, so that two host threads never interleave their records of
-// the shared events.
-constexpr int kMaxChunks = 64;
-// Default chunking.  When the host link binds (its copies take longer than the attention),
-// at most seven chunks with the boundaries at 8, 14, 20, 25, 29, 31 and 32 thirty-seconds of
-// the groups (rounded; empty chunks dropped): 32 groups give 8, 6, 6, 5, 4, 2, 1.  Large early
-// chunks keep the link busy with few launches; small late ones shorten the tail (the last
-// chunk's kernel and its copy back), which no later copy hides.  When the attention binds,
-// eight equal chunks: a small last chunk would add the length of its longest causal CTA.
-// The two times are estimated with the rates measured on GB300: about 200 GB/s per direction
-// on the host link and about 1.3 PFLOP/s of attention.  (Causal N = 8192, d = 128, 32 groups:
-// 1.22 ms against 1.27 ms with equal chunks; causal N = 32768: 6.6 against 7.1 ms the other
-// way round.)
-constexpr double kHostLinkBytesPerSec = 2.0e11;
-constexpr double kAttentionFlopsPerSec = 1.3e15;
-int default_chunks(int groups, double copy_bytes, double flops, int (&sizes)[kMaxChunks]) {
-  int n = 0;
-  if (flops / kAttentionFlopsPerSec >= 0.8 * copy_bytes / kHostLinkBytesPerSec) {
-    const int per = (groups + 7) / 8;
-    for (int g = 0; g < groups; g += per) sizes[n++] = std::min(per, groups - g);
-    return n;
-  }
-  constexpr int kBounds[7] = {8, 14, 20, 25, 29, 31, 32};
-  int prev = 0;
-  for (int i = 0; i < 7; ++i) {
-    const int b = static_cast<int>((static_cast<long long>(groups) * kBounds[i] + 16) / 32);
-    if (b > prev) sizes[n++] = b - prev;
-    prev = b;
-  }
-  return n;
-}
-constexpr int kComputeStreams = 2;
-struct HostPipe {
-  cudaStream_t in = nullptr, out = nullptr, comp[kComputeStreams] = {};
-  cudaEvent_t start = nullptr, done = nullptr, loaded[kMaxChunks] = {}, computed[kMaxChunks] = {};
-  std::mutex mu;
-  bool ready = false;
-};
-HostPipe g_pipe[kMaxDevices];
-
-int host_pipe(int dev, HostPipe** out) {
-  HostPipe& hp = g_pipe[dev];
-  if (!hp.ready) {
-    const unsigned flags = cudaEventDisableTiming;
-    for (int i = 0; i < kComputeStreams; ++i)
-      if (cudaStreamCreateWithFlags(&hp.comp[i], cudaStreamNonBlocking) != cudaSuccess) return FA_ERR_CUDA;
-    if (cudaStreamCreateWithFlags(&hp.in, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&hp.out, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&hp.start, flags) != cudaSuccess ||
-        cudaEventCreateWithFlags(&hp.done, flags) != cudaSuccess)
-      return FA_ERR_CUDA;
-    for (int c = 0; c < kMaxChunks; ++c)
-      if (cudaEventCreateWithFlags(&hp.loaded[c], flags) != cudaSuccess ||
-          cudaEventCreateWithFlags(&hp.computed[c], flags) != cudaSuccess)
-        return FA_ERR_CUDA;
-    hp.ready = true;
-  }
-  *out = &hp;
-  return FA_OK;
-}
-
-bool is_pinned_host(const void* ptr) {
-  cudaPointerAttributes attr{};
-  if (cudaPointerGetAttributes(&attr, ptr) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  return attr.type == cudaMemoryTypeHost;
-}
-
+// ---- pipelined host-to-host forward (fa_fwd_host); the pipeline itself is in fa_common.cuh
 struct HostBuffers {
   const void* q;
   const void* k;
@@ -903,18 +829,11 @@ int run_host(const HostBuffers& h, const Problem& pr, int groups_per_chunk, cuda
   if (rc != FA_OK) return rc;
   // chunks of whole K/V groups: contiguous rows of Q, O, LSE (R per group) and K, V (Nk)
   int sizes[kMaxChunks];
-  int n_chunks = 0;
-  if (groups_per_chunk > 0) {
-    int per = groups_per_chunk;
-    if ((groups + per - 1) / per > kMaxChunks) per = (groups + kMaxChunks - 1) / kMaxChunks;
-    for (int g = 0; g < groups; g += per) sizes[n_chunks++] = std::min(per, groups - g);
-  } else {
-    // bytes that cross the link (Q, K, V in; O, LSE out) and the attention's flops (the causal
-    // fraction taken as one half)
-    const double bytes = 2.0 * qb + 2.0 * kb + lb;
-    const double flops = 4.0 * static_cast<double>(pr.B) * pr.Hq * pr.Nq * pr.Nk * pr.d * (pr.causal ? 0.5 : 1.0);
-    n_chunks = default_chunks(groups, bytes, flops, sizes);
-  }
+  // bytes that cross the link (Q, K, V in; O, LSE out) and the attention's flops (the causal
+  // fraction taken as one half)
+  const double bytes = 2.0 * qb + 2.0 * kb + lb;
+  const double flops = 4.0 * static_cast<double>(pr.B) * pr.Hq * pr.Nq * pr.Nk * pr.d * (pr.causal ? 0.5 : 1.0);
+  const int n_chunks = chunk_sizes(groups, groups_per_chunk, bytes, flops / kForwardFlopsPerSec, sizes);
   auto at = [](const void* base, size_t off) { return static_cast<const uint8_t*>(base) + off; };
   auto at_mut = [](void* base, size_t off) { return static_cast<uint8_t*>(base) + off; };
   if (cudaEventRecord(hp->start, stream) != cudaSuccess || cudaStreamWaitEvent(hp->in, hp->start, 0) != cudaSuccess ||

@@ -26,7 +26,7 @@ FA_STATIC_WORKSPACE_BYTES = 16 << 20
 FA_STATUS_TIMEOUT = 0x1
 
 EXPORTED = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_gqa_workspace_bytes", "fa_fwd_gqa_static_workspace",
-            "fa_fwd_host", "fa_bwd", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "fa_status", "fa_fwd_withheld_tile",
+            "fa_fwd_host", "fa_bwd", "fa_bwd_host", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "fa_status", "fa_fwd_withheld_tile",
             "fa_bwd_withheld_tile", "fa_fwd_fp8_withheld_tile", "fa_strerror", "fa_version")
 
 if not os.path.exists(LIB_PATH):
@@ -49,6 +49,8 @@ lib.fa_fwd_withheld_tile.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f
 lib.fa_fwd_withheld_tile.restype = _i
 lib.fa_bwd.argtypes = [_vp] * 10 + [_i, _i, _i, _i, _i, _f, _i, _vp]
 lib.fa_bwd.restype = _i
+lib.fa_bwd_host.argtypes = [_vp] * 19 + [_i, _i, _i, _i, _i, _f, _i, _i, _vp]
+lib.fa_bwd_host.restype = _i
 lib.fa_fwd_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, ctypes.c_size_t, _vp]
 lib.fa_fwd_fp8.restype = _i
 lib.fa_fwd_fp8_workspace_bytes.argtypes = [_i, _i, _i, _i]
@@ -208,6 +210,27 @@ def fa_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, delta=None, scale=N
     if rc != FA_OK:
         raise FAError(rc)
     return dq, dk, dv, delta
+
+
+def fa_bwd_host(host_inputs, host_outputs, dev_inputs, dev_outputs, delta, scale=None, causal=False,
+                groups_per_chunk=0, stream=None):
+    """Host-to-host backward with the copies overlapped with the kernels, chunk by chunk.
+
+    host_inputs: pinned CPU (q, k, v, o, lse, dout); host_outputs: pinned CPU (dq, dk, dv);
+    dev_inputs / dev_outputs: CUDA tensors of the same shapes (the inputs receive the copies);
+    delta: CUDA fp32 [B, Hq, N].  Enqueues on ``stream``; synchronise it before reading the
+    host outputs."""
+    q, k = dev_inputs[0], dev_inputs[1]
+    B, Hq, N, d = q.shape
+    Hkv = k.shape[1]
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    ptrs = [t.data_ptr() for t in (*host_inputs, *host_outputs, *dev_inputs, *dev_outputs, delta)]
+    rc = lib.fa_bwd_host(*ptrs, B, Hq, Hkv, N, d, float(scale), int(bool(causal)), int(groups_per_chunk),
+                         _stream_handle(stream, q.device))
+    if rc != FA_OK:
+        raise FAError(rc)
+    return host_outputs
 
 
 def fa_fwd_fp8_workspace_bytes(B, H, N, d) -> int:

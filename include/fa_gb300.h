@@ -262,6 +262,34 @@ int fa_bwd(const void* q, const void* k, const void* v, const void* o, const flo
            int N, int d, float scale, int causal, cudaStream_t stream);
 
 /*
+ * fa_bwd_host -- fa_bwd from host inputs to host outputs, with the copies overlapped with
+ * the kernels.  (An addition of this library, like fa_fwd_host.)
+ *
+ * The K/V groups are cut into chunks (groups_per_chunk each, at most 64 chunks; 0 picks a
+ * default as fa_fwd_host does, with the backward's time estimated at about 0.85 PFLOP/s).
+ * Chunk c's rows of q, k, v, o, lse and dout are copied host to device on a copy stream of
+ * the library's, fa_bwd's three kernels run on them on one of two compute streams, and the
+ * chunk's dq, dk and dv rows go back on a second copy stream while later chunks load and run.
+ * A chunk's kernels are fa_bwd's on those groups, so the results are bitwise fa_bwd's.
+ *
+ * q_host .. dout_host : page-locked host memory, the layouts of fa_bwd's inputs.  Read.
+ * dq_host, dk_host, dv_host : page-locked host memory, the layouts of dq, dk, dv.  Written.
+ * q .. dout, dq, dk, dv, delta : device buffers as for fa_bwd; the inputs receive the
+ *                  copies; delta (D = rowsum(dO * O)) stays on the device.
+ * Other arguments as for fa_bwd.
+ *
+ * Ownership, ordering and errors as for fa_fwd_host: the call allocates no memory, starts
+ * after the work already on `stream`, and `stream` waits for its last copy.  FA_ERR_ARG also
+ * for a null or pageable host buffer, host outputs that overlap host inputs or each other, or
+ * a negative groups_per_chunk.
+ */
+int fa_bwd_host(const void* q_host, const void* k_host, const void* v_host, const void* o_host,
+                const float* lse_host, const void* dout_host, void* dq_host, void* dk_host,
+                void* dv_host, void* q, void* k, void* v, void* o, float* lse, void* dout, void* dq,
+                void* dk, void* dv, float* delta, int B, int Hq, int Hkv, int N, int d, float scale,
+                int causal, int groups_per_chunk, cudaStream_t stream);
+
+/*
  * fa_status -- read the device status word of the current device.
  *
  * Synchronises `stream` first, then copies the word to the host.  If `clear`

@@ -122,3 +122,12 @@ def test_host_entry_argument_errors(fa):
     assert f(*host, *dev, *tail, -1, None) == fa.FA_ERR_ARG              # negative chunk size
     assert f(*host, *dev, 1, 2, 2, 128, 128, 96, 0.088, 0, 0, None) == fa.FA_ERR_ARG  # d = 96
 
+
+def test_bwd_host_entry_argument_errors(fa):
+    f = fa.lib.fa_bwd_host
+    host = [FAKE + (20 + i) * 2**30 for i in range(9)]
+    dev = [FAKE + i * 2**30 for i in range(10)]
+    tail = [1, 2, 2, 128, 128, 0.088, 0]
+    assert f(*([0] + host[1:]), *dev, *tail, 0, None) == fa.FA_ERR_ARG  # null host input
+    assert f(*host, *dev, *tail, -1, None) == fa.FA_ERR_ARG              # negative chunk size
+

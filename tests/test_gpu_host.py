@@ -1,9 +1,10 @@
-"""GPU tests of fa_fwd_host: the forward from pinned host buffers to pinned host buffers,
-with the copies of one chunk of K/V groups overlapped with the attention of another.
+"""GPU tests of fa_fwd_host and fa_bwd_host: the forward and the backward from pinned host
+buffers to pinned host buffers, with the copies of one chunk of K/V groups overlapped with the
+kernels of another.
 
-Each chunk runs fa_fwd_gqa's kernel on its groups, so the results must equal
-fa_fwd_gqa's bit for bit, whatever the chunking; one case is also checked against the
-fp64 oracle."""
+Each chunk runs the device entry's kernels on its groups, so the results must equal
+fa_fwd_gqa's (fa_bwd's) bit for bit, whatever the chunking; one forward case is also checked
+against the fp64 oracle."""
 import math
 
 import pytest
@@ -106,4 +107,56 @@ def test_host_argument_errors(fa):
         fa.fa_fwd_host(qh, kh, vh, oh, lh, qd, kd, vd, od, ld, groups_per_chunk=-1)
     with pytest.raises(fa.FAError):  # device output over a device input
         fa.fa_fwd_host(qh, kh, vh, oh, lh, qd, kd, vd, qd, ld)
+    torch.cuda.synchronize()
+
+
+BWD_CASES = [  # B, Hq, Hkv, N, d, causal
+    (2, 4, 4, 1000, 128, True),   # ragged, causal
+    (1, 8, 2, 300, 64, False),    # grouped K/V heads, d = 64
+    (3, 2, 1, 77, 128, True),     # tiny ragged rows per group
+]
+
+
+@pytest.mark.parametrize("case", BWD_CASES, ids=lambda c: "B{}Hq{}Hkv{}N{}d{}{}".format(*c[:5], "c" if c[5] else "n"))
+@pytest.mark.parametrize("groups_per_chunk", [0, 1, 1000])
+def test_bwd_host_equals_device_call(fa, case, groups_per_chunk):
+    from exact_io_aware_02_gb300.inputs import make_dout
+    B, Hq, Hkv, N, d, causal = case
+    dev = torch.device("cuda")
+    q, k, v = make_qkv_gqa(B, Hq, Hkv, N, N, d, seed=9500 + N + d)
+    do = make_dout(q.shape, seed=9600 + N)
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = fa.fa_fwd_gqa(qd, kd, vd, causal=causal)
+    ref = fa.fa_bwd(qd, kd, vd, o, lse, dod, causal=causal)
+    torch.cuda.synchronize()
+    hin = tuple(t.cpu().contiguous().pin_memory() for t in (q, k, v, o, lse, do))
+    hout = tuple(torch.full(t.shape, 7.0, dtype=t.dtype).pin_memory() for t in (q, k, v))
+    din = tuple(torch.zeros_like(t) for t in (qd, kd, vd, o, lse, dod))
+    dout_ = tuple(torch.empty_like(t) for t in (qd, kd, vd))
+    delta = torch.empty_like(lse)
+    fa.fa_bwd_host(hin, hout, din, dout_, delta, causal=causal, groups_per_chunk=groups_per_chunk)
+    torch.cuda.synchronize()
+    for got, want in zip(hout, ref[:3]):
+        assert torch.equal(got, want.cpu())
+    assert torch.equal(delta, ref[3])
+    assert fa.fa_status(clear=False) == 0
+
+
+def test_bwd_host_argument_errors(fa):
+    from exact_io_aware_02_gb300.inputs import make_dout
+    dev = torch.device("cuda")
+    q, k, v = make_qkv_gqa(1, 2, 2, 256, 256, 128, seed=9700)
+    do = make_dout(q.shape, seed=9701)
+    lse = torch.zeros((1, 2, 256), dtype=torch.float32)
+    hin = tuple(t.pin_memory() for t in (q, k, v, q.clone(), lse, do))
+    hout = tuple(torch.empty_like(t).pin_memory() for t in (q, k, v))
+    din = tuple(t.to(dev) for t in (q, k, v, q, lse, do))
+    dout_ = tuple(torch.empty(t.shape, dtype=t.dtype, device=dev) for t in (q, k, v))
+    delta = torch.empty((1, 2, 256), dtype=torch.float32, device=dev)
+    with pytest.raises(fa.FAError):  # pageable host input
+        fa.fa_bwd_host((q,) + hin[1:], hout, din, dout_, delta)
+    with pytest.raises(fa.FAError):  # host output over a host input
+        fa.fa_bwd_host(hin, (hin[0],) + hout[1:], din, dout_, delta)
+    with pytest.raises(fa.FAError):  # negative chunk size
+        fa.fa_bwd_host(hin, hout, din, dout_, delta, groups_per_chunk=-1)
     torch.cuda.synchronize()

@@ -339,7 +339,7 @@ def run_ours(args, w, rank, world, local_rank):
         step = lambda: fa.fa_fwd_fp8(q, k, v, signs, o, lse, scale=w.scale, causal=w.causal,  # noqa: E731
                                      workspace=ws8, stream=stream)
         launches_per_step = 2  # preparation (rotation + quantisation), attention
-        inputs = ((q, qh), (k, kh), (v, vh), (signs, signs_h))
+        inputs = ((q, qh), (k, kh), (v, vh))  # the rotation signs stay on the device
         outputs = (o, lse)
     else:
         step = lambda: fwd(q, k, v, o, lse, ws, stream)  # noqa: E731
@@ -383,9 +383,9 @@ def run_ours(args, w, rank, world, local_rank):
         raise RuntimeError("device status word set during the timed region")
 
     # end to end through the public API: pinned host -> device, the step, device -> host.  The
-    # one-split forward and the backward use fa_fwd_host / fa_bwd_host, which overlap the
-    # copies of one chunk of heads with the kernels of another; the other steps copy, run and
-    # copy back in turn.
+    # one-split forward, the FP8 forward and the backward use fa_fwd_host / fa_fwd_fp8_host /
+    # fa_bwd_host, which overlap the copies of one chunk of heads with the kernels of another
+    # (the FP8 signs stay on the device); the other steps copy, run and copy back in turn.
     outputs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outputs]
     e2e_steps = max(1, min(args.steps, 10))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -396,6 +396,10 @@ def run_ours(args, w, rank, world, local_rank):
         if host_pipelined:
             fa.fa_fwd_host(qh, kh, vh, outputs_h[0], outputs_h[1], q, k, v, o, lse, scale=w.scale,
                            causal=w.causal, stream=stream)
+            continue
+        if w.direction == "fp8":
+            fa.fa_fwd_fp8_host(qh, kh, vh, outputs_h[0], outputs_h[1], q, k, v, signs, o, lse, ws8,
+                               scale=w.scale, causal=w.causal, stream=stream)
             continue
         if w.direction == "bwd":
             fa.fa_bwd_host(tuple(h for _, h in inputs), tuple(outputs_h), tuple(dv for dv, _ in inputs),

@@ -729,13 +729,11 @@ int validate_fp8(const Fp8Problem& pr, Fp8Layout* L) {
   return FA_OK;
 }
 
-int run_fp8(const Fp8Problem& pr, int withhold, unsigned long long timeout_ns, cudaStream_t stream) {
+// The two kernels of a validated problem (the workspace laid out for its B*H heads).
+int launch_fp8(const Fp8Problem& pr, int withhold, unsigned long long timeout_ns, cudaStream_t stream) {
   Fp8Layout L{};
-  int rc = validate_fp8(pr, &L);
-  if (rc != FA_OK) return rc;
-  rc = prepare_device_fp8();
-  if (rc != FA_OK) return rc;
   const int BH = pr.B * pr.H;
+  fp8_layout(BH, pr.N, &L);
   const int n_tiles = (pr.N + 127) / 128, n_pad = n_tiles * 128;
   uint8_t* ws = static_cast<uint8_t*>(pr.workspace);
   QuantParams qp{};
@@ -780,6 +778,106 @@ int run_fp8(const Fp8Problem& pr, int withhold, unsigned long long timeout_ns, c
   return FA_OK;
 }
 
+int run_fp8(const Fp8Problem& pr, int withhold, unsigned long long timeout_ns, cudaStream_t stream) {
+  Fp8Layout L{};
+  int rc = validate_fp8(pr, &L);
+  if (rc != FA_OK) return rc;
+  rc = prepare_device_fp8();
+  if (rc != FA_OK) return rc;
+  return launch_fp8(pr, withhold, timeout_ns, stream);
+}
+
+// ---- pipelined host-to-host FP8 forward (fa_fwd_fp8_host): chunks of heads, each chunk's Q,
+// K, V copied in on the library's copy stream, its two kernels on one of two compute streams
+// (each with its own part of the workspace), its O and LSE copied out on the second copy
+// stream while later chunks load and run.
+struct Fp8Host {
+  const void* q;
+  const void* k;
+  const void* v;
+  void* o;
+  float* lse;
+};
+constexpr double kFp8FlopsPerSec = 1.35e15;  // the two kernels, measured on the causal N = 8192 step
+
+int run_fp8_host(const Fp8Host& h, const Fp8Problem& pr, int groups_per_chunk, cudaStream_t stream) {
+  Fp8Layout L{};
+  int rc = validate_fp8(pr, &L);
+  if (rc != FA_OK) return rc;
+  if (!h.q || !h.k || !h.v || !h.o || !h.lse || groups_per_chunk < 0) return FA_ERR_ARG;
+  const int BH = pr.B * pr.H;
+  const size_t head_bytes = static_cast<size_t>(pr.N) * kFp8D * 2, tb = BH * head_bytes;
+  const size_t lb = static_cast<size_t>(BH) * pr.N * 4;
+  const struct { const void* p; size_t n; } in[3] = {{h.q, tb}, {h.k, tb}, {h.v, tb}};
+  for (const auto& x : in)
+    if (overlaps(h.o, tb, x.p, x.n) || overlaps(h.lse, lb, x.p, x.n)) return FA_ERR_ARG;
+  if (overlaps(h.o, tb, h.lse, lb)) return FA_ERR_ARG;
+  for (const void* ptr : {h.q, h.k, h.v, static_cast<const void*>(h.o), static_cast<const void*>(h.lse)})
+    if (!is_pinned_host(ptr)) return FA_ERR_ARG;
+  rc = prepare_device_fp8();
+  if (rc != FA_OK) return rc;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_pipe[dev].mu);
+  HostPipe* hp = nullptr;
+  rc = host_pipe(dev, &hp);
+  if (rc != FA_OK) return rc;
+  int sizes[kMaxChunks];
+  const double bytes = 4.0 * tb + lb;  // q, k, v in; o, lse out
+  const double flops = 4.0 * static_cast<double>(BH) * pr.N * pr.N * kFp8D * (pr.causal ? 0.5 : 1.0);
+  const int n_chunks = chunk_sizes(BH, groups_per_chunk, bytes, flops / kFp8FlopsPerSec, sizes);
+  // a part of the workspace per compute stream, laid out for the largest chunk; one stream
+  // when two parts do not fit
+  int largest = 0;
+  for (int c = 0; c < n_chunks; ++c) largest = std::max(largest, sizes[c]);
+  Fp8Layout Lc{};
+  fp8_layout(largest, pr.N, &Lc);
+  const size_t part = align256(Lc.total);
+  const int n_streams = 2 * part <= pr.workspace_bytes ? kComputeStreams : 1;
+  auto at = [](const void* base, size_t off) { return static_cast<const uint8_t*>(base) + off; };
+  auto at_mut = [](void* base, size_t off) { return static_cast<uint8_t*>(base) + off; };
+  if (cudaEventRecord(hp->start, stream) != cudaSuccess || cudaStreamWaitEvent(hp->in, hp->start, 0) != cudaSuccess ||
+      cudaStreamWaitEvent(hp->out, hp->start, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  for (int i = 0; i < kComputeStreams; ++i)
+    if (cudaStreamWaitEvent(hp->comp[i], hp->start, 0) != cudaSuccess) return FA_ERR_CUDA;
+  for (int c = 0, h0 = 0; c < n_chunks; h0 += sizes[c], ++c) {
+    const int nh = sizes[c];
+    const size_t off = h0 * head_bytes, len = nh * head_bytes;
+    const size_t l_off = static_cast<size_t>(h0) * pr.N * 4, l_len = static_cast<size_t>(nh) * pr.N * 4;
+    if (cudaMemcpyAsync(at_mut(const_cast<void*>(pr.q), off), at(h.q, off), len, cudaMemcpyHostToDevice, hp->in) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(at_mut(const_cast<void*>(pr.k), off), at(h.k, off), len, cudaMemcpyHostToDevice, hp->in) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(at_mut(const_cast<void*>(pr.v), off), at(h.v, off), len, cudaMemcpyHostToDevice, hp->in) !=
+            cudaSuccess ||
+        cudaEventRecord(hp->loaded[c], hp->in) != cudaSuccess)
+      return FA_ERR_CUDA;
+    const int si = c % n_streams;
+    cudaStream_t cs = hp->comp[si];
+    if (cudaStreamWaitEvent(cs, hp->loaded[c], 0) != cudaSuccess) return FA_ERR_CUDA;
+    Fp8Problem sub = pr;
+    sub.q = at(pr.q, off);
+    sub.k = at(pr.k, off);
+    sub.v = at(pr.v, off);
+    sub.o = at_mut(pr.o, off);
+    sub.lse = reinterpret_cast<float*>(at_mut(pr.lse, l_off));
+    sub.B = 1;
+    sub.H = nh;
+    sub.workspace = at_mut(pr.workspace, si * part);
+    sub.workspace_bytes = part;
+    rc = launch_fp8(sub, 0, kDefaultTimeoutNs, cs);
+    if (rc != FA_OK) return rc;
+    if (cudaEventRecord(hp->computed[c], cs) != cudaSuccess || cudaStreamWaitEvent(hp->out, hp->computed[c], 0) != cudaSuccess ||
+        cudaMemcpyAsync(at_mut(h.o, off), at(pr.o, off), len, cudaMemcpyDeviceToHost, hp->out) != cudaSuccess ||
+        cudaMemcpyAsync(at_mut(h.lse, l_off), at(pr.lse, l_off), l_len, cudaMemcpyDeviceToHost, hp->out) != cudaSuccess)
+      return FA_ERR_CUDA;
+  }
+  if (cudaEventRecord(hp->done, hp->out) != cudaSuccess || cudaStreamWaitEvent(stream, hp->done, 0) != cudaSuccess)
+    return FA_ERR_CUDA;
+  return FA_OK;
+}
+
 }  // namespace
 
 int fp8_status_word(int clear) {
@@ -808,6 +906,14 @@ int fa_fwd_fp8(const void* q, const void* k, const void* v, const signed char* s
                cudaStream_t stream) {
   const fa::Fp8Problem pr{q, k, v, signs, o, lse, B, H, N, d, scale, causal, workspace, workspace_bytes};
   return fa::run_fp8(pr, 0, fa::kDefaultTimeoutNs, stream);
+}
+
+int fa_fwd_fp8_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
+                    void* q, void* k, void* v, const signed char* signs, void* o, float* lse, int B, int H, int N,
+                    int d, float scale, int causal, void* workspace, size_t workspace_bytes, int groups_per_chunk,
+                    cudaStream_t stream) {
+  const fa::Fp8Problem pr{q, k, v, signs, o, lse, B, H, N, d, scale, causal, workspace, workspace_bytes};
+  return fa::run_fp8_host(fa::Fp8Host{q_host, k_host, v_host, o_host, lse_host}, pr, groups_per_chunk, stream);
 }
 
 int fa_fwd_fp8_withheld_tile(const void* q, const void* k, const void* v, const signed char* signs, void* o,

@@ -26,7 +26,7 @@ FA_STATIC_WORKSPACE_BYTES = 16 << 20
 FA_STATUS_TIMEOUT = 0x1
 
 EXPORTED = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_gqa_workspace_bytes", "fa_fwd_gqa_static_workspace",
-            "fa_fwd_host", "fa_bwd", "fa_bwd_host", "fa_fwd_fp8", "fa_fwd_fp8_workspace_bytes", "fa_status", "fa_fwd_withheld_tile",
+            "fa_fwd_host", "fa_bwd", "fa_bwd_host", "fa_fwd_fp8", "fa_fwd_fp8_host", "fa_fwd_fp8_workspace_bytes", "fa_status", "fa_fwd_withheld_tile",
             "fa_bwd_withheld_tile", "fa_fwd_fp8_withheld_tile", "fa_strerror", "fa_version")
 
 if not os.path.exists(LIB_PATH):
@@ -53,6 +53,8 @@ lib.fa_bwd_host.argtypes = [_vp] * 19 + [_i, _i, _i, _i, _i, _f, _i, _i, _vp]
 lib.fa_bwd_host.restype = _i
 lib.fa_fwd_fp8.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, ctypes.c_size_t, _vp]
 lib.fa_fwd_fp8.restype = _i
+lib.fa_fwd_fp8_host.argtypes = [_vp] * 11 + [_i, _i, _i, _i, _f, _i, _vp, ctypes.c_size_t, _i, _vp]
+lib.fa_fwd_fp8_host.restype = _i
 lib.fa_fwd_fp8_workspace_bytes.argtypes = [_i, _i, _i, _i]
 lib.fa_fwd_fp8_workspace_bytes.restype = ctypes.c_size_t
 lib.fa_bwd_withheld_tile.argtypes = [_vp] * 10 + [_i, _i, _i, _i, _i, _f, _i, _d, _vp]
@@ -210,6 +212,23 @@ def fa_bwd(q, k, v, o, lse, dout, dq=None, dk=None, dv=None, delta=None, scale=N
     if rc != FA_OK:
         raise FAError(rc)
     return dq, dk, dv, delta
+
+
+def fa_fwd_fp8_host(q_host, k_host, v_host, o_host, lse_host, q, k, v, signs, o, lse, workspace, scale=None,
+                    causal=False, groups_per_chunk=0, stream=None):
+    """Host-to-host FP8 forward with the copies overlapped with the kernels, chunk by chunk.
+    Host tensors pinned; q, k, v, o, lse, signs, workspace on the device as for fa_fwd_fp8."""
+    B, H, N, d = q.shape
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    rc = lib.fa_fwd_fp8_host(q_host.data_ptr(), k_host.data_ptr(), v_host.data_ptr(), o_host.data_ptr(),
+                             lse_host.data_ptr(), q.data_ptr(), k.data_ptr(), v.data_ptr(), signs.data_ptr(),
+                             o.data_ptr(), lse.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
+                             workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                             int(groups_per_chunk), _stream_handle(stream, q.device))
+    if rc != FA_OK:
+        raise FAError(rc)
+    return o_host, lse_host
 
 
 def fa_bwd_host(host_inputs, host_outputs, dev_inputs, dev_outputs, delta, scale=None, causal=False,

@@ -227,6 +227,31 @@ int fa_fwd_fp8(const void* q, const void* k, const void* v, const signed char* s
                float* lse, int B, int H, int N, int d, float scale, int causal, void* workspace,
                size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * fa_fwd_fp8_host -- fa_fwd_fp8 from host inputs to host outputs, with the copies overlapped
+ * with the kernels.  (An addition of this library, like fa_fwd_host.)
+ *
+ * The B*H heads are cut into chunks (groups_per_chunk heads each, at most 64 chunks; 0 picks
+ * the default of fa_fwd_host, with the two kernels' time estimated at about 1.35 PFLOP/s).
+ * Chunk c's rows of q, k and v are copied host to device on a copy stream of the library's,
+ * fa_fwd_fp8's two kernels run on them on one of two compute streams, and the chunk's o and
+ * lse rows go back on a second copy stream.  Each compute stream uses its own part of the
+ * workspace, laid out for the largest chunk; when two parts do not fit in workspace_bytes all
+ * chunks run on one compute stream.  The results are bitwise fa_fwd_fp8's; the workspace is
+ * scratch (its contents after the call are not specified).
+ *
+ * q_host, k_host, v_host : page-locked host memory, bf16 [B, H, N, 128].  Read.
+ * o_host, lse_host : page-locked host memory, the layouts of o and lse.  Written.
+ * q, k, v, o, lse, signs, workspace : device buffers as for fa_fwd_fp8; q, k, v receive the
+ *                  copies.
+ * Other arguments, ownership, ordering and errors as for fa_fwd_fp8 and fa_fwd_host.
+ */
+int fa_fwd_fp8_host(const void* q_host, const void* k_host, const void* v_host, void* o_host,
+                    float* lse_host, void* q, void* k, void* v, const signed char* signs, void* o,
+                    float* lse, int B, int H, int N, int d, float scale, int causal,
+                    void* workspace, size_t workspace_bytes, int groups_per_chunk,
+                    cudaStream_t stream);
+
 /* Bytes of workspace fa_fwd_fp8 needs (0 for sizes it would reject: d != 128, B, H, N < 1). */
 size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d);
 

@@ -223,3 +223,48 @@ def test_fp8_argument_errors(fa):
                       workspace=ws)
     torch.cuda.synchronize()
     assert bool((o == 5.0).all()) and bool((lse == 5.0).all())
+
+
+@pytest.mark.parametrize("groups_per_chunk", [0, 1, 3])
+def test_fp8_host_equals_device_call(fa, groups_per_chunk):
+    """fa_fwd_fp8_host runs fa_fwd_fp8's kernels per chunk of heads: bitwise the same O, LSE."""
+    dev = torch.device("cuda")
+    B, H, N = 2, 3, 700
+    q, k, v = make_qkv(B, H, N, D, seed=8601)
+    signs = make_signs(D, 8602).to(dev)
+    need = fa.fa_fwd_fp8_workspace_bytes(B, H, N, D)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    o_ref, l_ref = fa.fa_fwd_fp8(q.to(dev), k.to(dev), v.to(dev), signs, causal=True, workspace=ws)
+    torch.cuda.synchronize()
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.full(q.shape, 7.0, dtype=torch.bfloat16).pin_memory()
+    lh = torch.full((B, H, N), 7.0, dtype=torch.float32).pin_memory()
+    qd, kd, vd = (torch.zeros(t.shape, dtype=t.dtype, device=dev) for t in (q, k, v))
+    od = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    ws2 = torch.empty(need, dtype=torch.uint8, device=dev)
+    fa.fa_fwd_fp8_host(qh, kh, vh, oh, lh, qd, kd, vd, signs, od, ld, ws2, causal=True,
+                       groups_per_chunk=groups_per_chunk)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())
+    assert fa.fa_status(clear=False) == 0
+
+
+def test_fp8_host_one_stream_when_workspace_is_tight(fa):
+    """A workspace that holds one chunk's layout but not two runs the chunks on one stream."""
+    dev = torch.device("cuda")
+    B, H, N = 1, 2, 256
+    q, k, v = make_qkv(B, H, N, D, seed=8701)
+    signs = make_signs(D, 8702).to(dev)
+    need = fa.fa_fwd_fp8_workspace_bytes(B, H, N, D)
+    o_ref, l_ref = fa.fa_fwd_fp8(q.to(dev), k.to(dev), v.to(dev), signs, causal=False)
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty(q.shape, dtype=torch.bfloat16).pin_memory()
+    lh = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    qd, kd, vd = (torch.zeros(t.shape, dtype=t.dtype, device=dev) for t in (q, k, v))
+    od = torch.empty(q.shape, dtype=torch.bfloat16, device=dev)
+    ld = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)  # holds two 1-head parts at most
+    fa.fa_fwd_fp8_host(qh, kh, vh, oh, lh, qd, kd, vd, signs, od, ld, ws, causal=False, groups_per_chunk=2)
+    torch.cuda.synchronize()
+    assert torch.equal(oh, o_ref.cpu()) and torch.equal(lh, l_ref.cpu())

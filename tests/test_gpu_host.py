@@ -160,3 +160,35 @@ def test_bwd_host_argument_errors(fa):
     with pytest.raises(fa.FAError):  # negative chunk size
         fa.fa_bwd_host(hin, hout, din, dout_, delta, groups_per_chunk=-1)
     torch.cuda.synchronize()
+
+
+def test_host_calls_from_two_threads(fa):
+    """Two host threads call fa_fwd_host at once on their own streams: the library enqueues
+    whole calls one at a time (its events are shared), and both results are exact."""
+    import threading
+    dev = torch.device("cuda")
+    probs = [make_qkv_gqa(1, 6, 6, 640, 640, 128, seed=9800 + i) for i in range(2)]
+    want = []
+    for q, k, v in probs:
+        o, lse = fa.fa_fwd(q.to(dev), k.to(dev), v.to(dev), causal=True)
+        want.append((o.cpu(), lse.cpu()))
+    torch.cuda.synchronize()
+    got = [None, None]
+    errors = []
+
+    def work(i):
+        try:
+            torch.cuda.set_device(0)
+            s = torch.cuda.Stream()
+            for _ in range(3):
+                got[i] = host_run(fa, *probs[i], True, 2, stream=s)
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(e)
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for (oh, lh), (o, lse) in zip(got, want):
+        assert torch.equal(oh, o) and torch.equal(lh, lse)

@@ -78,8 +78,8 @@ WORKLOADS = {
         # grouped K/V heads (8 query heads per K/V head), causal prefill
         Workload("gqa_causal_n8192_d128", 1, 32, 8192, 128, True, seed=20266, Hkv=4),
         # decoding: one new query per head against a 32K-key cache, 4 query heads
-        # per K/V head (memory-bound: reads K and V once); the keys are split 7 ways, so
-        # that the 64 groups x 7 splits = 448 CTAs are about three waves on 148 SMs
+        # per K/V head (memory-bound: reads K and V once); the keys are split 4 ways, which
+        # the decode kernel runs as 64 groups x 2 CTAs of two splits each (one wave)
         Workload("gqa_decode_nk32768_d128", 8, 32, 1, 128, False, seed=20267, Hkv=8,
                  Nk=32768, n_splits=4, bound="hbm"),
         # the backward of the causal prefill shape: dQ, dK, dV with recomputation

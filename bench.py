@@ -48,10 +48,35 @@ KERNEL_FILES = {  # the sources each direction's kernels are built from
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
 
 
+def _code_only(text: str) -> str:
+    """The source without its comments and with runs of white space collapsed, so that the
+    digest changes with the code, not with its wording."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # string or character literal: copied whole
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def kernel_digest(direction: str = "fwd") -> str:
+    """sha256 prefix of the code (comments removed) the direction's kernels are built from."""
     h = hashlib.sha256()
     for f in KERNEL_FILES[direction]:
-        h.update(open(f, "rb").read())
+        h.update(_code_only(open(f, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 

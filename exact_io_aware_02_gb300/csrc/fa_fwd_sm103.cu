@@ -35,6 +35,11 @@
 // Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 and O_1 after
 // that (d columns each).  P_t overwrites the first 64 columns of S_t (bf16 pairs).
 //
+// Also here: split-K/V (FlashDecoding) with fa_combine_kernel, launched as a programmatic
+// dependent of the split kernel; the decode instance fa_fwd_kernel<D, true>, whose CTA runs
+// one group's query rows over two splits as two independent chains; and fa_fwd_host, the
+// host-to-host forward whose copies overlap the kernels chunk by chunk.
+//
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA raises a
 // status bit, waits for its own copies and MMAs in flight, frees its tensor
 // memory and returns.

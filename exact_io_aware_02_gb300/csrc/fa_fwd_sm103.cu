@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nt = t ? n1 : n0;
           if (j >= 1 && j - 1 < nt) {
             ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1));
-            if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarPFull + t), (j - 1) & 1));
+            ptx::named_barrier(3 + t, 160);  // P_t(j-1) handed over (see the non-dual loop)
             if (!ok) break;
             ptx::tc_fence_after();
             const uint64_t dv = desc_v_ring + static_cast<uint64_t>(u % C::kSlots) * kSlotStep;
@@ -333,9 +333,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < 2; ++t) {
         const int nt = t ? n1 : n0;
         if (j >= 1 && j - 1 < nt) {
-          // O_t += P_t V_{j-1}: P from tensor memory (8 columns per 16 keys), V from the ring
-          ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarPFull + t), (j - 1) & 1));
-          if (!ok) break;
+          // O_t += P_t V_{j-1}: P from tensor memory (8 columns per 16 keys), V from the ring.
+          // The hand-off is a hardware named barrier (tile t's four softmax warps arrive,
+          // this warp waits), which wakes far sooner than an mbarrier wait.  It cannot hang:
+          // the softmax warps arrive once per K/V step whatever happens, after waits of their
+          // own that are bounded.
+          ptx::named_barrier(3 + t, 160);
           ptx::tc_fence_after();
           const uint32_t t_o = tmem + C::kColO + t * D;
           const uint32_t t_p = tmem + C::kColS + t * 128;
@@ -401,10 +404,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY;  // running max of the raw scores q.k (scale > 0)
     float l_run = 0.f;        // running sum of 2^((s - m_run) * c2)
     float lp_run = 0.f;       // the same sum over the bf16-rounded terms
+    // One arrive at the P hand-off barrier per K/V step, whatever happens: the MMA warp waits
+    // there without a timeout.  After a failed wait the remaining steps only arrive.
     bool ok = nt > 0;
-    for (int j = 0; ok && j < nt; ++j) {
-      ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarSFull + t), j & 1));
-      if (!ok) break;
+    for (int j = 0; j < nt; ++j) {
+      if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarSFull + t), j & 1));
+      if (!ok) {
+        ptx::named_barrier_arrive(3 + t, 160);
+        continue;
+      }
       ptx::tc_fence_after();
       float s[128];
       {
@@ -487,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(C::kBarPFull + t));
+      ptx::named_barrier_arrive(3 + t, 160);  // P_t(j) handed over to the MMA warp
     }
     // ---- epilogue: O = O~ / l, LSE = m*scale + ln l; a row that saw no key gets O = 0 and
     // LSE = -inf.  One split: O -> bf16 -> shared (Q_t's buffer) -> TMA store.  Several

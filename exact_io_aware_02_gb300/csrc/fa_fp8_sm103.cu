@@ -302,8 +302,7 @@ struct Fp8Cfg {
   static constexpr int kBarFull = 1;
   static constexpr int kBarEmpty = kBarFull + kSlots;
   static constexpr int kBarSFull = kBarEmpty + kSlots;
-  static constexpr int kBarPFull = kBarSFull + 2;
-  static constexpr int kBarOFinal = kBarPFull + 2;
+  static constexpr int kBarOFinal = kBarSFull + 2;
   static constexpr int kBarDrain = kBarOFinal + 2;
   static constexpr int kBarTab = kBarDrain + 1;
   static constexpr int kNumBars = kBarTab + 1;
@@ -368,7 +367,6 @@ __global__ void __launch_bounds__(kFp8Threads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(bar(C::kBarSFull + t), 1);
-      ptx::mbar_init(bar(C::kBarPFull + t), 4);
       ptx::mbar_init(bar(C::kBarOFinal + t), 1);
     }
     ptx::mbar_init(bar(C::kBarDrain), 1);
@@ -458,8 +456,10 @@ __global__ void __launch_bounds__(kFp8Threads, 1)
       for (int t = 0; t < 2; ++t) {
         const int nt = t ? n1 : n0;
         if (j >= 1 && j - 1 < nt) {
-          ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarPFull + t), (j - 1) & 1));
-          if (!ok) break;
+          // P8_t(j-1) handed over through a hardware named barrier: tile t's four softmax
+          // warps arrive, this warp waits (no timeout; the softmax warps arrive once per K/V
+          // step whatever happens, and never for step j before S_t(j) is complete)
+          ptx::named_barrier(4 + t, 160);
           ptx::tc_fence_after();
           const uint32_t t_o = tmem + C::kColO + t * kFp8D;
           const uint32_t t_p = tmem + C::kColS + t * 128;
@@ -517,8 +517,13 @@ __global__ void __launch_bounds__(kFp8Threads, 1)
     const float c2 = p.scale_log2;
     float m_run = -INFINITY;  // running max of the true scores q'.k'
     float l_run = 0.f;        // running sum of 2^((s - m_run) * c2)
+    // One arrive at the P hand-off barrier per K/V step, whatever happens; after a failed
+    // wait the remaining steps only arrive (the loop after this one), each once S_t of its
+    // step is complete (a wait that ignores the abort flag and ends at the deadline), so that
+    // no arrival runs ahead into a later phase of the named barrier.
     bool ok = nt > 0 && __all_sync(0xffffffffu, w.wait(bar(C::kBarTab), 0));
-    for (int j = 0; ok && j < nt; ++j) {
+    int j = 0;
+    for (; ok && j < nt; ++j) {
       ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarSFull + t), j & 1));
       if (!ok) break;
       ptx::tc_fence_after();
@@ -588,8 +593,9 @@ __global__ void __launch_bounds__(kFp8Threads, 1)
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(C::kBarPFull + t));
+      ptx::named_barrier_arrive(4 + t, 160);  // P8_t(j) handed over to the MMA warp
     }
+    for (; j < nt && w.drain(bar(C::kBarSFull + t), j & 1); ++j) ptx::named_barrier_arrive(4 + t, 160);
     // ---- epilogue: O = O~ s_v,max / (64 l) -> bf16 -> shared (Q_t's buffer and the next
     // 16 KB) -> TMA store; LSE = m scale + ln l
     const size_t grow = static_cast<size_t>(bh) * p.N + qpos;

@@ -76,8 +76,7 @@ struct Cfg {
   static constexpr int kBarFull = 1;
   static constexpr int kBarEmpty = kBarFull + kSlots;
   static constexpr int kBarSFull = kBarEmpty + kSlots;  // one per query tile
-  static constexpr int kBarPFull = kBarSFull + 2;
-  static constexpr int kBarOFinal = kBarPFull + 2;
+  static constexpr int kBarOFinal = kBarSFull + 2;
   static constexpr int kBarDrain = kBarOFinal + 2;
   static constexpr int kNumBars = kBarDrain + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
@@ -183,7 +182,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       ptx::mbar_init(bar(C::kBarSFull + t), 1);
-      ptx::mbar_init(bar(C::kBarPFull + t), 4);  // one arrive per softmax warp
       ptx::mbar_init(bar(C::kBarOFinal + t), 1);
     }
     ptx::mbar_init(bar(C::kBarDrain), 1);
@@ -282,8 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int nt = t ? n1 : n0;
           if (j >= 1 && j - 1 < nt) {
             ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1));
-            ptx::named_barrier(3 + t, 160);  // P_t(j-1) handed over (see the non-dual loop)
             if (!ok) break;
+            ptx::named_barrier(3 + t, 160);  // P_t(j-1) handed over (see the non-dual loop)
             ptx::tc_fence_after();
             const uint64_t dv = desc_v_ring + static_cast<uint64_t>(u % C::kSlots) * kSlotStep;
             const uint32_t t_o = tmem + C::kColO + t * D;
@@ -335,9 +333,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (j >= 1 && j - 1 < nt) {
           // O_t += P_t V_{j-1}: P from tensor memory (8 columns per 16 keys), V from the ring.
           // The hand-off is a hardware named barrier (tile t's four softmax warps arrive,
-          // this warp waits), which wakes far sooner than an mbarrier wait.  It cannot hang:
-          // the softmax warps arrive once per K/V step whatever happens, after waits of their
-          // own that are bounded.
+          // this warp waits), which wakes far sooner than an mbarrier wait.  It has no
+          // timeout, so the softmax warps arrive once per K/V step whatever happens, and never
+          // for step j before S_t(j) is complete (issued after this warp's wait for step j-1).
           ptx::named_barrier(3 + t, 160);
           ptx::tc_fence_after();
           const uint32_t t_o = tmem + C::kColO + t * D;
@@ -405,14 +403,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l_run = 0.f;        // running sum of 2^((s - m_run) * c2)
     float lp_run = 0.f;       // the same sum over the bf16-rounded terms
     // One arrive at the P hand-off barrier per K/V step, whatever happens: the MMA warp waits
-    // there without a timeout.  After a failed wait the remaining steps only arrive.
+    // there without a timeout.  After a failed wait the remaining steps only arrive (the loop
+    // after this one), each once S_t of its step is complete, so that no arrival runs ahead
+    // into a later step's barrier phase: S_t(j) is issued after the MMA warp's wait for step
+    // j-1, and the MMA warp cannot wait for step j before issuing it.  That wait ignores the
+    // abort flag; once the MMA warp has left its loop it ends at the deadline, and the
+    // arrivals stop.
     bool ok = nt > 0;
-    for (int j = 0; j < nt; ++j) {
-      if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarSFull + t), j & 1));
-      if (!ok) {
-        ptx::named_barrier_arrive(3 + t, 160);
-        continue;
-      }
+    int j = 0;
+    for (; j < nt; ++j) {
+      ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarSFull + t), j & 1));
+      if (!ok) break;
       ptx::tc_fence_after();
       float s[128];
       {
@@ -497,6 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       ptx::named_barrier_arrive(3 + t, 160);  // P_t(j) handed over to the MMA warp
     }
+    for (; j < nt && w.drain(bar(C::kBarSFull + t), j & 1); ++j) ptx::named_barrier_arrive(3 + t, 160);
     // ---- epilogue: O = O~ / l, LSE = m*scale + ln l; a row that saw no key gets O = 0 and
     // LSE = -inf.  One split: O -> bf16 -> shared (Q_t's buffer) -> TMA store.  Several
     // splits: fp32 partial O and partial LSE straight to the workspace for the combine.

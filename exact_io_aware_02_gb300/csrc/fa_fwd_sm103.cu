@@ -402,6 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY;  // running max of the raw scores q.k (scale > 0)
     float l_run = 0.f;        // running sum of 2^((s - m_run) * c2)
     float lp_run = 0.f;       // the same sum over the bf16-rounded terms
+    // d = 128: S_t is read in two halves and P written in four parts, which shortens the
+    // softmax's span from S ready to P handed over.  d = 64 keeps one load and two stores:
+    // its softmax is bound by instruction issue (half the tensor work per exp), and the extra
+    // instructions cost it more than the shorter span wins.
+    constexpr bool kSplitS = D == 128;
     // One arrive at the P hand-off barrier per K/V step, whatever happens: the MMA warp waits
     // there without a timeout.  After a failed wait the remaining steps only arrive (the loop
     // after this one), each once S_t of its step is complete, so that no arrival runs ahead
@@ -415,32 +420,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarSFull + t), j & 1));
       if (!ok) break;
       ptx::tc_fence_after();
-      float s[128];
-      {
-        uint32_t r[128];
-        ptx::tmem_ld128(t_s, r);
-#pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
-      }
       // mask: keys past the end of the sequence, and keys after the query when causal
       const int col0 = ((t ? lo1 : lo0) + j) * 128;
       int lim = p.Nk - col0;
       if (p.causal && qpos - col0 + 1 < lim) lim = qpos - col0 + 1;
-      if (lim < 128) {
+      float s[128];
+      float mx0, mx1, mx2, mx3;
+      if constexpr (kSplitS) {
+        // S_t in two 64-column halves: the row max of the first runs while the second lands
+        uint32_t rb[64];
+        {
+          uint32_t ra[64];
+          ptx::tmem_ld64_nowait(t_s, ra);
+          ptx::tmem_wait_ld64(ra);
+          ptx::tmem_ld64_nowait(t_s + 64, rb);
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= lim) s[c] = -INFINITY;
-      }
-      float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+          for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(ra[i]);
+        }
+        if (lim < 64) {
 #pragma unroll
-      for (int c = 4; c < 124; c += 8) {
-        mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
-        mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
-        mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
-        mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
+          for (int c = 0; c < 64; ++c)
+            if (c >= lim) s[c] = -INFINITY;
+        }
+        mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int c = 4; c < 60; c += 8) {
+          mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
+          mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
+          mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
+          mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
+        }
+        mx0 = ptx::fmax3(mx0, s[60], s[61]);
+        mx1 = ptx::fmax3(mx1, s[62], s[63]);
+        ptx::tmem_wait_ld64(rb);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) s[64 + i] = __uint_as_float(rb[i]);
+        if (lim < 128) {
+#pragma unroll
+          for (int c = 64; c < 128; ++c)
+            if (c >= lim) s[c] = -INFINITY;
+        }
+#pragma unroll
+        for (int c = 64; c < 128; c += 8) {
+          mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
+          mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
+          mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
+          mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
+        }
+      } else {
+        {
+          uint32_t r[128];
+          ptx::tmem_ld128(t_s, r);
+#pragma unroll
+          for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
+        }
+        if (lim < 128) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) s[c] = -INFINITY;
+        }
+        mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int c = 4; c < 124; c += 8) {
+          mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
+          mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
+          mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
+          mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
+        }
+        mx0 = ptx::fmax3(mx0, s[124], s[125]);
+        mx1 = ptx::fmax3(mx1, s[126], s[127]);
       }
-      mx0 = ptx::fmax3(mx0, s[124], s[125]);
-      mx1 = ptx::fmax3(mx1, s[126], s[127]);
       const float tile_max = fmaxf(ptx::fmax3(mx0, mx1, mx2), mx3);
       const float m_new = fmaxf(m_run, tile_max);
       // Keep the old reference unless the max grew by more than 2^8: l and O~ share the
@@ -451,7 +500,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // a row that has seen no unmasked key yet keeps m = -inf: its terms are all 0
       const float neg = m_ref == -INFINITY ? 0.f : -m_ref * c2;
       // P = 2^(s*c2 - m_ref*c2), rounded to bf16 pairs for the P V product and written over
-      // the first 64 columns of S_t (first half while the second is computed).  Two running
+      // the first 64 columns of S_t, a part at a time while the rest is computed (four parts
+      // with the split S load, two otherwise, so the last store is short).  Two running
       // sums: l_run over the fp32 values (for LSE) and lp_run over the rounded values the
       // tensor core multiplies (for O = sum(P v) / sum(P), a convex combination of V rows).
       __syncwarp();  // reconverge after the per-row mask before the warp-wide TMEM stores
@@ -469,7 +519,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         se[i & 3] = __fadd2_rn(se[i & 3], make_float2(e0, e1));
         sp[i & 3] = __fadd2_rn(sp[i & 3], make_float2(__uint_as_float(pk[i] << 16),
                                                       __uint_as_float(pk[i] & 0xffff0000u)));
-        if (i == 31 || i == 63) {  // P_t columns [0,32) (keys 0-63), then [32,64)
+        if constexpr (kSplitS) {
+          if ((i & 15) == 15) {  // P_t columns [i-15, i]: keys 2(i-15) to 2i+1
+            uint32_t part[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) part[k] = pk[i - 15 + k];
+            ptx::tmem_st16(t_s + (i - 15), part);
+          }
+        } else if (i == 31 || i == 63) {  // P_t columns [0,32) (keys 0-63), then [32,64)
           uint32_t half[32];
 #pragma unroll
           for (int k = 0; k < 32; ++k) half[k] = pk[i - 31 + k];

@@ -541,13 +541,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       // correction O~ *= r, before P_t(j) is handed over: PV_t(j-1) has completed (the commit
       // behind S_t(j) covers it) and PV_t(j) waits for the arrive below
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-#pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
-          uint32_t r[32];
-          ptx::tmem_ld32(t_o + cc * 32, r);
+        if constexpr (kSplitS) {  // all 128 columns of O_t in one load (S and P are dead here)
+          uint32_t r[128];
+          ptx::tmem_ld128(t_o, r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
-          ptx::tmem_st32(t_o + cc * 32, r);
+          for (int i = 0; i < 128; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t part[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) part[i] = r[cc * 32 + i];
+            ptx::tmem_st32(t_o + cc * 32, part);
+          }
+        } else {
+#pragma unroll 1
+          for (int cc = 0; cc < D / 32; ++cc) {
+            uint32_t r[32];
+            ptx::tmem_ld32(t_o + cc * 32, r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
+            ptx::tmem_st32(t_o + cc * 32, r);
+          }
         }
       }
       ptx::tmem_wait_st();

@@ -479,7 +479,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         ptx::tma_store_3d(&tm_dv, sbase + C::kTileBytes + c * C::kChunkBytes, c * 64, kt * 128, bh);
       }
       ptx::bulk_commit();
-      ptx::bulk_wait_all();
+      ptx::bulk_wait_read<0>();  // the stores have read their staging: the CTA may exit
     }
   }
   ptx::tc_fence_before();
@@ -687,7 +687,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok && n_kv > 0 && threadIdx.x == 0) {
       for (int c = 0; c < C::kChunks; ++c) ptx::tma_store_3d(&tm_dq, sbase + c * C::kChunkBytes, c * 64, qt * 128, bh);
       ptx::bulk_commit();
-      ptx::bulk_wait_all();
+      ptx::bulk_wait_read<0>();  // the store has read its staging: the CTA may exit
     }
   }
   ptx::tc_fence_before();

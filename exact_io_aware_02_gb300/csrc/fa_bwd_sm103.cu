@@ -30,6 +30,15 @@ namespace fa {
 
 constexpr int kBwdThreads = 320;
 constexpr int kBwdComputeWarps = 8;
+// The compute warps hand P^T and dS^T (dK/dV kernel) and dS (dQ kernel) to the MMA warp through
+// hardware named barriers: the compute warps arrive (bar.arrive), the MMA warp waits
+// (bar.sync), which wakes far sooner than an mbarrier wait.  The epilogue's barrier among the
+// compute warps is ID 1.  A bar.sync has no timeout, so the compute warps arrive once per step
+// whatever happens, and never for step u before the input of step u (an S or dP tile, issued
+// after the MMA warp's wait for step u-1) is complete; after a failed wait of their own they
+// wait for that input with a wait that ignores the abort flag and ends at the deadline.
+constexpr uint32_t kNbP = 2, kNbDS = 3;
+constexpr uint32_t kHandOffThreads = 32 * (kBwdComputeWarps + 1);
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
 template <int D>
@@ -255,7 +264,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // dP^T ready, P^T written, dS^T written, accumulators final, drain
   constexpr int S = C::kStages;
   constexpr int kBarKV = 0, kBarFull = 1, kBarEmpty = 1 + S, kBarS = 1 + 2 * S, kBarDP = kBarS + 1,
-                kBarP = kBarDP + 1, kBarDS = kBarP + 1, kBarFinal = kBarDS + 1, kBarDrain = kBarFinal + 1;
+                kBarFinal = kBarDP + 1, kBarDrain = kBarFinal + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kKVOffBar + C::kMaxBars * 8);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kKVOffBar + C::kMaxBars * 8 + 4);
   auto bar = [&](int i) -> uint32_t { return sbase + C::kKVOffBar + 8u * i; };
@@ -276,8 +285,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     ptx::mbar_init(bar(kBarS), 1);
     ptx::mbar_init(bar(kBarDP), 1);
-    ptx::mbar_init(bar(kBarP), kBwdComputeWarps);
-    ptx::mbar_init(bar(kBarDS), kBwdComputeWarps);
     ptx::mbar_init(bar(kBarFinal), 1);
     ptx::mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0u;
@@ -376,8 +383,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       const int s = u % S, s1 = (u + 1) % S;
       const bool more = u + 1 < n_q;
       const uint64_t st_n = desc_stage_nmaj + s * kStageStep;
-      ok = __all_sync(0xffffffffu, w.wait(bar(kBarP), u & 1));
-      if (!ok) break;
+      ptx::named_barrier(kNbP, kHandOffThreads);  // P^T(u) written
       ptx::tc_fence_after();
       if (ptx::elect_one()) bwd_mma_tn<D>(t_dv, t_s, st_n + kTileStep, u > 0);  // dV += P^T dO
       __syncwarp();
@@ -391,8 +397,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         __syncwarp();
       }
-      ok = __all_sync(0xffffffffu, w.wait(bar(kBarDS), u & 1));
-      if (!ok) break;
+      ptx::named_barrier(kNbDS, kHandOffThreads);  // dS^T(u) written
       ptx::tc_fence_after();
       if (ptx::elect_one()) {
         bwd_mma_tn<D>(t_dk, t_dp, st_n, u > 0);  // dK += dS^T Q (scaled in the epilogue)
@@ -421,7 +426,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t t_s = tmem + lane_off + C::kColS + half * 64, t_dp = tmem + lane_off + C::kColDP + half * 64;
     const float c2 = p.scale_log2;
     bool ok = true;
-    int u = 0;
+    int u = 0, np = 0;  // query tiles whose dS^T (P^T) has been handed over
     for (int qt = 0; qt < p.n_qtiles && ok; ++qt) {
       if (!needed(qt)) continue;
       const int s = u % S;
@@ -444,7 +449,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(kBarP));
+      ptx::named_barrier_arrive(kNbP, kHandOffThreads);  // P^T(u) handed over
+      np = u + 1;
       ok = __all_sync(0xffffffffu, w.wait(bar(kBarDP), u & 1));
       if (!ok) break;
       ptx::tc_fence_after();
@@ -452,8 +458,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(kBarDS));
+      ptx::named_barrier_arrive(kNbDS, kHandOffThreads);  // dS^T(u) handed over
       ++u;
+    }
+    // after a failed wait: the remaining arrivals, each once the input of its step is complete
+    for (; u < n_q; ++u) {
+      if (np == u) {
+        if (!w.drain(bar(kBarS), u & 1)) break;
+        ptx::named_barrier_arrive(kNbP, kHandOffThreads);
+        ++np;
+      }
+      if (!w.drain(bar(kBarDP), u & 1)) break;
+      ptx::named_barrier_arrive(kNbDS, kHandOffThreads);
     }
     // epilogue: dV, scale*dK -> bf16 -> shared (K and V buffers, no longer read) -> TMA
     if (ok && n_q > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFinal), 0));
@@ -508,7 +524,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // barriers: 0 Q/dO, [1, 1+S) ring full, [1+S, 1+2S) ring empty, then S ready (one per
   // S buffer), dP ready, dS written, dQ final, drain
   constexpr int kBarQ = 0, kBarFull = 1, kBarEmpty = 1 + S, kBarS = 1 + 2 * S, kBarDP = kBarS + 2,
-                kBarDS = kBarDP + 1, kBarFinal = kBarDS + 1, kBarDrain = kBarFinal + 1;
+                kBarFinal = kBarDP + 1, kBarDrain = kBarFinal + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kQOffBar + C::kMaxBars * 8);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kQOffBar + C::kMaxBars * 8 + 4);
   auto bar = [&](int i) -> uint32_t { return sbase + C::kQOffBar + 8u * i; };
@@ -526,7 +542,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(bar(kBarS), 1);
     ptx::mbar_init(bar(kBarS + 1), 1);
     ptx::mbar_init(bar(kBarDP), 1);
-    ptx::mbar_init(bar(kBarDS), kBwdComputeWarps);
     ptx::mbar_init(bar(kBarFinal), 1);
     ptx::mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0u;
@@ -614,8 +629,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::tc_fence_after();
     if (ok && n_kv > 0) ok = issue_s(0) && issue_dp(0) && (n_kv < 2 || issue_s(1));
     for (int j = 0; ok && j < n_kv; ++j) {
-      ok = __all_sync(0xffffffffu, w.wait(bar(kBarDS), j & 1));
-      if (!ok) break;
+      ptx::named_barrier(kNbDS, kHandOffThreads);  // dS(j) written
       ptx::tc_fence_after();
       if (j + 1 < n_kv && !(ok = issue_dp(j + 1))) break;
       if (ptx::elect_one()) {
@@ -644,7 +658,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t t_s0 = tmem + lane_off + C::kQColS + half * 64, t_dp = tmem + lane_off + C::kQColDP + half * 64;
     const float c2 = p.scale_log2;
     bool ok = true;
-    for (int j = 0; ok && j < n_kv; ++j) {
+    int j = 0;
+    for (; ok && j < n_kv; ++j) {
       const uint32_t t_s = t_s0 + (j & 1) * 128;
       ok = __all_sync(0xffffffffu, w.wait(bar(kBarS + (j & 1)), (j >> 1) & 1));
       if (!ok) break;
@@ -675,8 +690,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
       __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(kBarDS));
+      ptx::named_barrier_arrive(kNbDS, kHandOffThreads);  // dS(j) handed over
     }
+    // after a failed wait: the remaining arrivals, each once dP of its step is complete
+    for (; j < n_kv && w.drain(bar(kBarDP), j & 1); ++j) ptx::named_barrier_arrive(kNbDS, kHandOffThreads);
     if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFinal), 0));
     if (ok && n_kv > 0) {
       ptx::tc_fence_after();

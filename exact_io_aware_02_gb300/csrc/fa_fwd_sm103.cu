@@ -21,7 +21,9 @@
 //                consumes and releases the tiles in that order);
 //   * warp 9  -- MMA issuer (one thread): S_t = Q_t K_j^T with tcgen05.mma
 //                (A and B from shared memory, fp32 accumulator in tensor memory),
-//                then O_t += P_t V_j with P_t read from tensor memory;
+//                then O_t += P_t V_j with P_t read from tensor memory; P_t is handed
+//                over through a hardware named barrier per tile (bar.arrive by the
+//                tile's softmax warps, bar.sync by this warp);
 //   * warps 0-3 / 4-7 -- softmax for tile 0 / tile 1, one row per thread:
 //                row max, exp2 with scale*log2(e) folded in, running (m, l),
 //                bf16 P written back into tensor memory over S_t, and the
@@ -42,7 +44,9 @@
 //
 // Every mbarrier wait is bounded (globaltimer); on expiry the CTA raises a
 // status bit, waits for its own copies and MMAs in flight, frees its tensor
-// memory and returns.
+// memory and returns.  The named-barrier waits of the P hand-off cannot be
+// bounded; they cannot hang either, because the softmax warps arrive once per
+// step whatever happens, and never before the S tile of that step is complete.
 #include <cuda.h>
 #include <cuda_runtime.h>
 

@@ -64,6 +64,7 @@ constexpr int kThreads = 384;  // 3 warpgroups: softmax 0, softmax 1, producer +
 constexpr uint32_t kSoftmaxRegs = 216;  // setmaxnreg split of the 384 x 168 launch budget:
 constexpr uint32_t kOtherRegs = 72;     //   2 x 128 x 216 + 128 x 72 = 384 x 168
 constexpr float kRescaleLog2Threshold = 8.0f;  // skip the O correction unless max grows > 2^8
+constexpr int kNoWithhold = -1;                 // the test hook's "load every ring tile"
 
 template <int D>
 struct Cfg {
@@ -112,7 +113,7 @@ struct Params {
   float scale;
   float scale_log2;  // scale * log2(e)
   int causal;
-  int withhold_v0;   // test hook: never load V tile 0
+  int withhold_tile;  // test hook: this ring tile (K_0 = 0, V_0 = 1, K_1 = 2, ...) is never loaded; -1: none
   unsigned long long timeout_ns;
 };
 
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tma_load_3d(sbase + C::kOffQ + C::kTileBytes + c * C::kChunkBytes, &tm_q,
                            bar(C::kBarQ), c * 64, qt1 * 128, bh);
       const int n_tiles = kDual ? 0 : 2 * nmax;
-      const int skip = p.withhold_v0 ? 1 : -1;  // test hook: tile 1 (V_0) is never loaded
+      const int skip = p.withhold_tile;  // test hook: this ring tile is never loaded (-1: none)
       int issued = 0;
       bool ok = true;
       if constexpr (kDual) {
@@ -782,7 +783,7 @@ int validate(const Problem& pr) {
 }
 
 template <int D>
-int launch(const Problem& pr, int withhold_v0, unsigned long long timeout_ns, cudaStream_t stream) {
+int launch(const Problem& pr, int withhold_tile, unsigned long long timeout_ns, cudaStream_t stream) {
   const int G = pr.Hq / pr.Hkv;
   const int groups = pr.B * pr.Hkv;
   const int R = G * pr.Nq;  // query rows per K/V head (contiguous in [B, Hq, Nq, d])
@@ -813,7 +814,7 @@ int launch(const Problem& pr, int withhold_v0, unsigned long long timeout_ns, cu
   p.scale_log2 = static_cast<float>(static_cast<double>(pr.scale) * 1.4426950408889634);
   p.causal = pr.causal ? 1 : 0;
   const bool dual = p.n_qtiles == 1 && pr.n_splits > 1;
-  p.withhold_v0 = withhold_v0;
+  p.withhold_tile = withhold_tile;
   p.timeout_ns = timeout_ns;
   const long long grid = dual ? static_cast<long long>(groups) * ((pr.n_splits + 1) / 2)
                               : static_cast<long long>(groups) * p.n_cta_q * pr.n_splits;
@@ -846,12 +847,12 @@ int launch(const Problem& pr, int withhold_v0, unsigned long long timeout_ns, cu
   return FA_OK;
 }
 
-int run(const Problem& pr, int withhold_v0, unsigned long long timeout_ns, cudaStream_t stream) {
+int run(const Problem& pr, int withhold_tile, unsigned long long timeout_ns, cudaStream_t stream) {
   int rc = validate(pr);
   if (rc != FA_OK) return rc;
   rc = prepare_device();
   if (rc != FA_OK) return rc;
-  return pr.d == 64 ? launch<64>(pr, withhold_v0, timeout_ns, stream) : launch<128>(pr, withhold_v0, timeout_ns, stream);
+  return pr.d == 64 ? launch<64>(pr, withhold_tile, timeout_ns, stream) : launch<128>(pr, withhold_tile, timeout_ns, stream);
 }
 
 Problem mha(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
@@ -955,7 +956,7 @@ int run_host(const HostBuffers& h, const Problem& pr, int groups_per_chunk, cuda
     sub.B = 1;
     sub.Hq = ng * G;
     sub.Hkv = ng;
-    rc = pr.d == 64 ? launch<64>(sub, 0, kDefaultTimeoutNs, cs) : launch<128>(sub, 0, kDefaultTimeoutNs, cs);
+    rc = pr.d == 64 ? launch<64>(sub, kNoWithhold, kDefaultTimeoutNs, cs) : launch<128>(sub, kNoWithhold, kDefaultTimeoutNs, cs);
     if (rc != FA_OK) return rc;
     if (cudaEventRecord(hp->computed[c], cs) != cudaSuccess ||
         cudaStreamWaitEvent(hp->out, hp->computed[c], 0) != cudaSuccess ||
@@ -981,14 +982,14 @@ extern "C" {
 
 int fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H, int N, int d,
            float scale, int causal, cudaStream_t stream) {
-  return fa::run(fa::mha(q, k, v, o, lse, B, H, N, d, scale, causal), 0, fa::kDefaultTimeoutNs, stream);
+  return fa::run(fa::mha(q, k, v, o, lse, B, H, N, d, scale, causal), fa::kNoWithhold, fa::kDefaultTimeoutNs, stream);
 }
 
 int fa_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq, int Hkv,
                int Nq, int Nk, int d, float scale, int causal, int n_splits, void* workspace,
                size_t workspace_bytes, cudaStream_t stream) {
   const fa::Problem pr{q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, n_splits, workspace, workspace_bytes};
-  return fa::run(pr, 0, fa::kDefaultTimeoutNs, stream);
+  return fa::run(pr, fa::kNoWithhold, fa::kDefaultTimeoutNs, stream);
 }
 
 size_t fa_fwd_gqa_workspace_bytes(int B, int Hq, int Nq, int d, int n_splits) {
@@ -1010,7 +1011,7 @@ int fa_fwd_gqa_static_workspace(const void* q, const void* k, const void* v, voi
     ws_bytes = fa::kStaticWorkspaceBytes;
   }
   const fa::Problem pr{q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, n_splits, ws, ws_bytes};
-  return fa::run(pr, 0, fa::kDefaultTimeoutNs, stream);
+  return fa::run(pr, fa::kNoWithhold, fa::kDefaultTimeoutNs, stream);
 }
 
 int fa_fwd_host(const void* q_host, const void* k_host, const void* v_host, void* o_host, float* lse_host,
@@ -1023,8 +1024,14 @@ int fa_fwd_host(const void* q_host, const void* k_host, const void* v_host, void
 int fa_fwd_withheld_tile(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
                          int N, int d, float scale, int causal, double wait_timeout_ms,
                          cudaStream_t stream) {
-  if (!(wait_timeout_ms >= 1.0 && wait_timeout_ms <= 10000.0)) return FA_ERR_ARG;
-  return fa::run(fa::mha(q, k, v, o, lse, B, H, N, d, scale, causal), 1,
+  return fa_fwd_withheld_ring_tile(q, k, v, o, lse, B, H, N, d, scale, causal, 1, wait_timeout_ms, stream);
+}
+
+int fa_fwd_withheld_ring_tile(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                              int N, int d, float scale, int causal, int ring_tile, double wait_timeout_ms,
+                              cudaStream_t stream) {
+  if (!(wait_timeout_ms >= 1.0 && wait_timeout_ms <= 10000.0) || ring_tile < 0) return FA_ERR_ARG;
+  return fa::run(fa::mha(q, k, v, o, lse, B, H, N, d, scale, causal), ring_tile,
                  static_cast<unsigned long long>(wait_timeout_ms * 1e6), stream);
 }
 

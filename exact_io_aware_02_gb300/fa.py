@@ -27,6 +27,7 @@ FA_STATUS_TIMEOUT = 0x1
 
 EXPORTED = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_gqa_workspace_bytes", "fa_fwd_gqa_static_workspace",
             "fa_fwd_host", "fa_bwd", "fa_bwd_host", "fa_fwd_fp8", "fa_fwd_fp8_host", "fa_fwd_fp8_workspace_bytes", "fa_status", "fa_fwd_withheld_tile",
+            "fa_fwd_withheld_ring_tile",
             "fa_bwd_withheld_tile", "fa_fwd_fp8_withheld_tile", "fa_strerror", "fa_version")
 
 if not os.path.exists(LIB_PATH):
@@ -47,6 +48,8 @@ lib.fa_fwd_host.argtypes = [_vp] * 10 + [_i, _i, _i, _i, _i, _i, _f, _i, _i, _vp
 lib.fa_fwd_host.restype = _i
 lib.fa_fwd_withheld_tile.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _d, _vp]
 lib.fa_fwd_withheld_tile.restype = _i
+lib.fa_fwd_withheld_ring_tile.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _d, _vp]
+lib.fa_fwd_withheld_ring_tile.restype = _i
 lib.fa_bwd.argtypes = [_vp] * 10 + [_i, _i, _i, _i, _i, _f, _i, _vp]
 lib.fa_bwd.restype = _i
 lib.fa_bwd_host.argtypes = [_vp] * 19 + [_i, _i, _i, _i, _i, _f, _i, _i, _vp]
@@ -290,6 +293,19 @@ def fa_fwd_withheld_tile(q, k, v, o=None, lse=None, scale=None, causal=False,
     return lib.fa_fwd_withheld_tile(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
                                     lse.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
                                     float(wait_timeout_ms), _stream_handle(stream, q.device))
+
+
+def fa_fwd_withheld_ring_tile(q, k, v, ring_tile, o=None, lse=None, scale=None, causal=False,
+                              wait_timeout_ms=50.0, stream=None) -> int:
+    """Test hook: run the kernel with K/V ring tile `ring_tile` (K_0 = 0, V_0 = 1, K_1 = 2, ...)
+    never loaded; returns the C return code."""
+    B, H, N, d, o, lse = _prepare(q, k, v, o, lse)
+    if scale is None:
+        scale = 1.0 / (d ** 0.5)
+    return lib.fa_fwd_withheld_ring_tile(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                         lse.data_ptr(), B, H, N, d, float(scale), int(bool(causal)),
+                                         int(ring_tile), float(wait_timeout_ms),
+                                         _stream_handle(stream, q.device))
 
 
 def fa_bwd_withheld_tile(q, k, v, o, lse, dout, wait_timeout_ms=50.0, causal=False, stream=None) -> int:

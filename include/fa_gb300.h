@@ -339,6 +339,18 @@ int fa_fwd_withheld_tile(const void* q, const void* k, const void* v, void* o, f
                          double wait_timeout_ms, cudaStream_t stream);
 
 /*
+ * fa_fwd_withheld_ring_tile -- the same test hook with the withheld tile chosen: ring_tile
+ * (>= 0) indexes the K/V tiles in the order a CTA's producer loads them, K_0 = 0, V_0 = 1,
+ * K_1 = 2, V_1 = 3, ...  (fa_fwd_withheld_tile is ring_tile = 1).  CTAs that load fewer
+ * tiles run to completion; the others give up as above, some after handing P over for the
+ * steps before the missing tile.  Returns FA_ERR_ARG for ring_tile < 0 or a timeout outside
+ * [1, 10000] ms; otherwise as fa_fwd_withheld_tile.
+ */
+int fa_fwd_withheld_ring_tile(const void* q, const void* k, const void* v, void* o, float* lse,
+                              int B, int H, int N, int d, float scale, int causal, int ring_tile,
+                              double wait_timeout_ms, cudaStream_t stream);
+
+/*
  * fa_bwd_withheld_tile, fa_fwd_fp8_withheld_tile -- the same test hook for the backward
  * and the FP8 forward.  Same arguments as fa_bwd / fa_fwd_fp8, plus wait_timeout_ms in
  * [1, 10000].  The backward's dK/dV producer never loads its first stage and its dQ

@@ -92,6 +92,14 @@ def test_withheld_tile_timeout_range(fa):
              0.088, 0, 20000.0, None) == fa.FA_ERR_ARG
 
 
+def test_withheld_ring_tile_arguments(fa):
+    f = fa.lib.fa_fwd_withheld_ring_tile
+    ptrs = (FAKE, FAKE + 2**30, FAKE + 2**31, FAKE + 3 * 2**30, FAKE + 2**32)
+    assert f(*ptrs, 1, 1, 128, 128, 0.088, 0, -1, 50.0, None) == fa.FA_ERR_ARG  # no tile named
+    assert f(*ptrs, 1, 1, 128, 128, 0.088, 0, 3, 0.5, None) == fa.FA_ERR_ARG
+    assert f(*ptrs, 1, 1, 128, 128, 0.088, 0, 3, 20000.0, None) == fa.FA_ERR_ARG
+
+
 def _bwd(fa, B=1, Hq=2, Hkv=1, N=128, d=128, scale=0.088, causal=1, **ptrs):
     names = ("q", "k", "v", "o", "lse", "dout", "dq", "dk", "dv", "delta")
     p = {n: FAKE + i * 2**30 for i, n in enumerate(names)}

@@ -30,6 +30,27 @@ def test_withheld_tile_times_out_cleanly():
     assert fa.fa_status(clear=False) == 0
 
 
+@pytest.mark.parametrize("ring_tile", [2, 5, 6])
+@pytest.mark.parametrize("causal", [False, True])
+def test_withheld_later_tile_times_out_cleanly(ring_tile, causal):
+    """A missing K or V tile after some K/V steps have completed: the softmax warps have handed
+    P over for the earlier steps (the MMA warp waited for them at the named barrier), then the
+    waits give up; with causal masking the CTAs with fewer tiles complete normally."""
+    import __graft_entry__ as entry
+    entry.build()
+    from exact_io_aware_02_gb300 import fa
+
+    dev = torch.device("cuda")
+    q, k, v = (t.to(dev) for t in make_qkv(1, 2, 1024, 128, seed=26 + ring_tile))
+    fa.fa_status(clear=True)
+    assert fa.fa_fwd_withheld_ring_tile(q, k, v, ring_tile, causal=causal, wait_timeout_ms=50.0) == fa.FA_OK
+    assert fa.fa_status(clear=True) & fa.FA_STATUS_TIMEOUT
+    o, lse = fa.fa_fwd(q, k, v, scale=1 / math.sqrt(128), causal=causal)
+    torch.cuda.synchronize()
+    assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+    assert fa.fa_status(clear=False) == 0
+
+
 def test_backward_withheld_tiles_time_out_cleanly():
     """Both backward kernels: a stage (dK/dV) and a V tile (dQ) that never arrive."""
     import __graft_entry__ as entry

@@ -113,8 +113,9 @@ struct Params {
   float scale;
   float scale_log2;  // scale * log2(e)
   int causal;
-  int withhold_tile;  // test hook: this ring tile (K_0 = 0, V_0 = 1, K_1 = 2, ...) is never loaded; -1: none
+  int withhold_v0;   // test hook: never load V tile 0 (0 in every normal launch)
   unsigned long long timeout_ns;
+  int withhold_tile;  // test hook instance only: this ring tile (K_0 = 0, V_0 = 1, ...) is never loaded
 };
 
 // Last key position (+1 in tiles) any row of query tile qt may see, causal case.
@@ -128,7 +129,7 @@ __device__ __forceinline__ int causal_tile_limit(const Params& p, int qt) {
 // kDual: one query tile per group and n_splits > 1 (decoding).  The CTA's two tile slots then
 // take the same query rows over splits 2c and 2c+1: two independent softmax/product chains
 // per SM, each with its own K/V tiles in the ring.
-template <int D, bool kDual>
+template <int D, bool kDual, bool kHook = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -220,7 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tma_load_3d(sbase + C::kOffQ + C::kTileBytes + c * C::kChunkBytes, &tm_q,
                            bar(C::kBarQ), c * 64, qt1 * 128, bh);
       const int n_tiles = kDual ? 0 : 2 * nmax;
-      const int skip = p.withhold_tile;  // test hook: this ring tile is never loaded (-1: none)
+      // test hooks: tile 1 (V_0), or in the kHook instance the ring tile named, is never loaded
+      const int skip = kHook ? p.withhold_tile : (p.withhold_v0 ? 1 : -1);
       int issued = 0;
       bool ok = true;
       if constexpr (kDual) {
@@ -726,6 +728,10 @@ int prepare_device() {
       cudaFuncSetAttribute(fa_fwd_kernel<64, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<64>::kSmemBytes) != cudaSuccess ||
       cudaFuncSetAttribute(fa_fwd_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<128>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(fa_fwd_kernel<64, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           Cfg<64>::kSmemBytes) != cudaSuccess ||
+      cudaFuncSetAttribute(fa_fwd_kernel<128, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            Cfg<128>::kSmemBytes) != cudaSuccess)
     return FA_ERR_CUDA;
   g_dev_state[dev] = 1;
@@ -814,6 +820,7 @@ int launch(const Problem& pr, int withhold_tile, unsigned long long timeout_ns, 
   p.scale_log2 = static_cast<float>(static_cast<double>(pr.scale) * 1.4426950408889634);
   p.causal = pr.causal ? 1 : 0;
   const bool dual = p.n_qtiles == 1 && pr.n_splits > 1;
+  p.withhold_v0 = 0;
   p.withhold_tile = withhold_tile;
   p.timeout_ns = timeout_ns;
   const long long grid = dual ? static_cast<long long>(groups) * ((pr.n_splits + 1) / 2)
@@ -821,6 +828,8 @@ int launch(const Problem& pr, int withhold_tile, unsigned long long timeout_ns, 
   if (grid > 2147483647LL) return FA_ERR_ARG;
   if (dual)
     fa_fwd_kernel<D, true><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(mq, mk, mv, mo, p);
+  else if (withhold_tile != kNoWithhold)
+    fa_fwd_kernel<D, false, true><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(mq, mk, mv, mo, p);
   else
     fa_fwd_kernel<D, false><<<static_cast<unsigned>(grid), kThreads, Cfg<D>::kSmemBytes, stream>>>(mq, mk, mv, mo, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;

@@ -171,39 +171,66 @@ __device__ __forceinline__ void bwd_acc_to_smem(uint32_t t_acc, uint32_t smem_ti
 // rounded to bf16 pairs, into tensor memory over the first 32 of the columns read.
 // kMasked adds the per-element test (key exists, query row exists, causal order);
 // tiles that need none take the kMasked = false instance.
+// Start a load of 32 consecutive 32-bit TMEM columns of this warp's lanes; the registers are
+// valid only after bwd_wait_ld32 on the same array (which waits for every load in flight).
+__device__ __forceinline__ void bwd_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {"
+      "%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void bwd_wait_ld32(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+        "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]),
+        "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+        "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
 template <bool kMasked>
 __device__ __forceinline__ void bwd_kv_p(uint32_t t_s, const float* vec, int col0, float c2, int key,
                                          bool key_valid, int n_rows, int pos0, int N, bool causal,
                                          float (&pr)[64]) {
-  uint32_t ra[32], rb[32];
-  ptx::tmem_ld32x2(t_s, ra, t_s + 32, rb);
+  // two 32-column halves: the first half's terms are computed and stored while the second lands
+  uint32_t r[2][32];
+  bwd_ld32_nowait(t_s, r[0]);
+  bwd_wait_ld32(r[0]);
+  bwd_ld32_nowait(t_s + 32, r[1]);
   const float2 c2v = make_float2(c2, c2);
 #pragma unroll
-  for (int i = 0; i < 64; i += 4) {
-    const float4 nl = *reinterpret_cast<const float4*>(vec + col0 + i);
-    const float nla[4] = {nl.x, nl.y, nl.z, nl.w};
-#pragma unroll
-    for (int h = 0; h < 4; h += 2) {
-      const uint32_t s0 = i + h < 32 ? ra[i + h] : rb[i + h - 32];
-      const uint32_t s1 = i + h + 1 < 32 ? ra[i + h + 1] : rb[i + h + 1 - 32];
-      const float2 x = __ffma2_rn(make_float2(__uint_as_float(s0), __uint_as_float(s1)), c2v,
-                                  make_float2(nla[h], nla[h + 1]));
-      float e[2] = {ptx::ex2_approx(x.x), ptx::ex2_approx(x.y)};
-      if constexpr (kMasked) {
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int col = col0 + i + h + t;
-          const int qpos = (pos0 + col) % N;
-          e[t] = (key_valid && col < n_rows && !(causal && qpos < key)) ? e[t] : 0.f;
-        }
-      }
-      pr[i + h] = e[0];
-      pr[i + h + 1] = e[1];
-    }
-  }
-  uint32_t pk[16];
-#pragma unroll
   for (int c = 0; c < 2; ++c) {
+    if (c == 1) bwd_wait_ld32(r[1]);
+#pragma unroll
+    for (int i = 32 * c; i < 32 * c + 32; i += 4) {
+      const float4 nl = *reinterpret_cast<const float4*>(vec + col0 + i);
+      const float nla[4] = {nl.x, nl.y, nl.z, nl.w};
+#pragma unroll
+      for (int h = 0; h < 4; h += 2) {
+        const float2 x = __ffma2_rn(make_float2(__uint_as_float(r[c][i - 32 * c + h]),
+                                                __uint_as_float(r[c][i - 32 * c + h + 1])),
+                                    c2v, make_float2(nla[h], nla[h + 1]));
+        float e[2] = {ptx::ex2_approx(x.x), ptx::ex2_approx(x.y)};
+        if constexpr (kMasked) {
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int col = col0 + i + h + t;
+            const int qpos = (pos0 + col) % N;
+            e[t] = (key_valid && col < n_rows && !(causal && qpos < key)) ? e[t] : 0.f;
+          }
+        }
+        pr[i + h] = e[0];
+        pr[i + h + 1] = e[1];
+      }
+    }
+    uint32_t pk[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(pr[32 * c + 2 * i], pr[32 * c + 2 * i + 1]);
     ptx::tmem_st16(t_s + 16 * c, pk);
@@ -216,32 +243,34 @@ __device__ __forceinline__ void bwd_kv_p(uint32_t t_s, const float* vec, int col
 template <bool kPerColumnD>
 __device__ __forceinline__ void bwd_ds(uint32_t t_dp, uint32_t t_dst, const float (&pr)[64], const float* neg_dcol,
                                        float neg_drow) {
-  uint32_t ra[32], rb[32];
-  ptx::tmem_ld32x2(t_dp, ra, t_dp + 32, rb);
-  float ds[64];
-#pragma unroll
-  for (int i = 0; i < 64; i += 4) {
-    float nd[4] = {neg_drow, neg_drow, neg_drow, neg_drow};
-    if constexpr (kPerColumnD) {
-      const float4 d4 = *reinterpret_cast<const float4*>(neg_dcol + i);
-      nd[0] = d4.x; nd[1] = d4.y; nd[2] = d4.z; nd[3] = d4.w;
-    }
-#pragma unroll
-    for (int h = 0; h < 4; h += 2) {
-      const uint32_t d0 = i + h < 32 ? ra[i + h] : rb[i + h - 32];
-      const uint32_t d1 = i + h + 1 < 32 ? ra[i + h + 1] : rb[i + h + 1 - 32];
-      const float2 t = __fadd2_rn(make_float2(__uint_as_float(d0), __uint_as_float(d1)),
-                                  make_float2(nd[h], nd[h + 1]));
-      const float2 r = __fmul2_rn(make_float2(pr[i + h], pr[i + h + 1]), t);
-      ds[i + h] = r.x;
-      ds[i + h + 1] = r.y;
-    }
-  }
-  uint32_t pk[16];
+  // two 32-column halves: the first half's dS is computed and stored while the second lands
+  uint32_t r[2][32];
+  bwd_ld32_nowait(t_dp, r[0]);
+  bwd_wait_ld32(r[0]);
+  bwd_ld32_nowait(t_dp + 32, r[1]);
 #pragma unroll
   for (int c = 0; c < 2; ++c) {
+    if (c == 1) bwd_wait_ld32(r[1]);
+    float ds[32];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(ds[32 * c + 2 * i], ds[32 * c + 2 * i + 1]);
+    for (int i = 0; i < 32; i += 4) {
+      float nd[4] = {neg_drow, neg_drow, neg_drow, neg_drow};
+      if constexpr (kPerColumnD) {
+        const float4 d4 = *reinterpret_cast<const float4*>(neg_dcol + 32 * c + i);
+        nd[0] = d4.x; nd[1] = d4.y; nd[2] = d4.z; nd[3] = d4.w;
+      }
+#pragma unroll
+      for (int h = 0; h < 4; h += 2) {
+        const float2 t = __fadd2_rn(make_float2(__uint_as_float(r[c][i + h]), __uint_as_float(r[c][i + h + 1])),
+                                    make_float2(nd[h], nd[h + 1]));
+        const float2 q = __fmul2_rn(make_float2(pr[32 * c + i + h], pr[32 * c + i + h + 1]), t);
+        ds[i + h] = q.x;
+        ds[i + h + 1] = q.y;
+      }
+    }
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = ptx::pack_bf16x2(ds[2 * i], ds[2 * i + 1]);
     ptx::tmem_st16(t_dst + 16 * c, pk);
   }
 }

@@ -120,9 +120,14 @@ def job_rate(units_per_rank: float, ms: float, world: int) -> float:
     return world * units_per_rank / (ms * 1e-3)
 
 
-def workload_config(w, l2_note):
+L2_NOTE = "GPU arm: a 256 MiB buffer is written between timed launches (L2 flushed); CUDA events per launch"
+
+
+def workload_config(w):
+    """The workload's description, the same in both arms (the L2 note says how the GPU arm
+    keeps timed launches from reusing L2; the CPU arm has no such cache to flush)."""
     cfg = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "causal": w.causal,
-           "qk_std": w.qk_std, "v_std": w.v_std, "seed": w.seed, "l2": l2_note}
+           "qk_std": w.qk_std, "v_std": w.v_std, "seed": w.seed, "l2": L2_NOTE}
     if w.Hkv is not None or w.Nk is not None:
         cfg.update({"Hkv": w.hkv, "Nk": w.nk, "n_splits": w.n_splits})
     return cfg
@@ -233,13 +238,18 @@ def gpu_selector(dev) -> str:
     return str(dev.index or 0)
 
 
-def cpu_baseline(w, budget_s=12.0, max_slices=32):
+def cpu_baseline(w, results=None, budget_s=12.0, max_slices=32):
     """The fp64 oracle as it stands, on whole (b, h) slices of the workload until
-    about ``budget_s`` seconds of CPU work; TFLOP/s counted like the GPU metric."""
+    about ``budget_s`` seconds of CPU work; TFLOP/s counted like the GPU metric.
+
+    With ``results`` (the GPU arm's outputs as CPU tensors: (O, LSE) for a forward,
+    (dQ, dK, dV) for the backward) the same oracle slices also give the raw parity
+    statistics of those outputs, returned as a second value."""
     import numpy as np
     import oracle
     import oracle.fp8 as oracle_fp8
     from exact_io_aware_02_gb300.inputs import sample_slices
+    from tests.parity import compare, grad_compare, grad_within_tolerance, merge, within_tolerance
 
     q, k, v = make_workload(w)
     do = make_workload_dout(w) if w.direction == "bwd" else None
@@ -248,25 +258,50 @@ def cpu_baseline(w, budget_s=12.0, max_slices=32):
     slices = sample_slices(w.B, w.H, max_slices, w.seed + 3)
     per_slice = units_per_step(w) / (w.B * w.H)
     done, t_total = 0, 0.0
+    stats = []
+    f64 = lambda t: t.to(torch.float64).numpy()  # noqa: E731
     for (b, h) in slices:
-        qa = q[b, h].to(torch.float64).numpy()
-        ka, va = (t[b, h // G].to(torch.float64).numpy() for t in (k, v))
+        qa = f64(q[b, h])
+        ka, va = (f64(t[b, h // G]) for t in (k, v))
         t0 = time.perf_counter()
         if do is not None:
-            oracle.attention_backward(qa, ka, va, do[b, h].to(torch.float64).numpy(), w.scale, w.causal)
+            ref = oracle.attention_backward(qa, ka, va, f64(do[b, h]), w.scale, w.causal)
         elif signs is not None:
-            oracle_fp8.fp8_attention(qa, ka, va, w.scale, w.causal, signs)
+            ref = oracle_fp8.fp8_attention(qa, ka, va, w.scale, w.causal, signs)
         else:
-            oracle.naive_attention(qa, ka, va, w.scale, w.causal, q_offset=w.nk - w.N)
+            ref = oracle.naive_attention(qa, ka, va, w.scale, w.causal, q_offset=w.nk - w.N)
         t_total += time.perf_counter() - t0
         done += 1
+        if results is not None:
+            if do is not None:  # one query head per K/V head in the backward workloads
+                stats.append([grad_compare(f64(results[i][b, h]), ref[i]) for i in range(3)])
+            else:
+                stats.append(compare(f64(results[0][b, h]), f64(results[1][b, h]), ref[0], ref[1]))
         if t_total >= budget_s:
             break
-    return {"value": done * per_slice / t_total, "unit": metric_for(w)[1],
+    base = {"value": done * per_slice / t_total, "unit": metric_for(w)[1],
             "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
             "sample": f"{done} whole (b,h) query-head slice(s) of {w.name} (N={w.N}, d={w.d}, {w.direction}), "
                       f"fp64 NumPy, "
                       f"{t_total:.1f} s; threads = NumPy BLAS default on the listed cores"}
+    if results is None:
+        return base, None
+    where = f"{done} whole (b,h) slice(s) drawn with seed {w.seed + 3}, every row"
+    if do is not None:
+        parity = {"against": "oracle.attention_backward (fp64)", "slices": where}
+        for i, name in enumerate(("dq", "dk", "dv")):
+            parity[name] = {"max_rel": max(s[i]["max_rel"] for s in stats),
+                            "mean_rel": max(s[i]["mean_rel"] for s in stats)}
+        parity["within_tolerance"] = all(grad_within_tolerance(s[i]) for s in stats for i in range(3))
+        return base, parity
+    st = merge(stats)
+    parity = {"against": ("oracle.fp8.fp8_attention (fp64, exact attention of the dequantised tensors)"
+                          if signs is not None else "oracle.naive_attention (fp64)"),
+              "slices": where, **{key: st[key] for key in ("max_abs_o", "max_abs_o_below4", "mean_abs_o",
+                                                          "max_rel_lse", "count")}}
+    if signs is None:
+        parity["within_tolerance"] = within_tolerance(st)
+    return base, parity
 
 
 def run_reference(args, w, rank, world):
@@ -323,7 +358,7 @@ def run_reference(args, w, rank, world):
     line = {"impl": "reference", "metric": metric, "value": value, "unit": unit, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(w, "n/a (CPU)"),
+            "data": "synthetic", "config": workload_config(w),
             "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle",
                              "sample": f"{args.steps} steps of one 128-row query tile of one query head "
                                        f"each ({w.direction}), fp64 NumPy"},
@@ -467,8 +502,7 @@ def run_ours(args, w, rank, world, local_rank):
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "e4m3" if w.direction == "fp8" else "bf16", "data": "synthetic",
-        "config": workload_config(w, "flushed between timed launches (256 MiB write); "
-                                     "per-launch CUDA events on the launch stream"),
+        "config": workload_config(w),
         "roofline": roofline,
         "e2e": {"value": job_rate(units, e2e_ms, world), "unit": unit,
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t, _ in inputs),
@@ -478,7 +512,10 @@ def run_ours(args, w, rank, world, local_rank):
         "kernel_ms": {"min": min(kernel_ms), "median": statistics.median(kernel_ms), "max": max(kernel_ms)},
     }
     if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w)
+        results = tuple(t.cpu() for t in (grads[:3] if w.direction == "bwd" else (o, lse)))
+        line["cpu_baseline"], parity = cpu_baseline(w, results)
+        if parity is not None:
+            line["parity"] = parity
     print(json.dumps(line), flush=True)
 
 

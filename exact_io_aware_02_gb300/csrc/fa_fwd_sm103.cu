@@ -1015,7 +1015,15 @@ int fa_fwd_gqa_static_workspace(const void* q, const void* k, const void* v, voi
     const size_t need = fa_fwd_gqa_workspace_bytes(B, Hq, Nq, d, n_splits);
     if (need == 0) return FA_ERR_ARG;  // sizes fa_fwd_gqa would reject anyway
     if (need > fa::kStaticWorkspaceBytes) return FA_ERR_WORKSPACE_TOO_LARGE;
-    const int rc = fa::static_workspace(&ws);
+    // every other argument is checked as fa_fwd_gqa checks it, then the device (so that a
+    // device of another architecture gets FA_ERR_ARCH, as from fa_fwd_gqa), and only then is
+    // the array's address looked up
+    const fa::Problem args{q, k, v, o, lse, B, Hq, Hkv, Nq, Nk, d, scale, causal, 1, nullptr, 0};
+    int rc = fa::validate(args);
+    if (rc != FA_OK) return rc;
+    rc = fa::prepare_device();
+    if (rc != FA_OK) return rc;
+    rc = fa::static_workspace(&ws);
     if (rc != FA_OK) return rc;
     ws_bytes = fa::kStaticWorkspaceBytes;
   }

@@ -155,10 +155,12 @@ def sample_slices(B: int, H: int, count: int, seed: int):
     return [(i // H, i % H) for i in sorted(idx)]
 
 
-def sample_rows(N: int, count: int, seed: int):
-    """``count`` distinct query rows of a length-N sequence, always including
-    row 0, the last row and the first/last row of the last 128-row tile."""
+def sample_rows(N: int, count: int, seed: int, leading: int = 0):
+    """``count`` distinct query rows of a length-N sequence: the first ``leading`` rows,
+    row 0, the last row and the first/last row of the last 128-row tile, and the rest
+    drawn from Generator(seed)."""
     g = torch.Generator().manual_seed(int(seed))
-    fixed = {0, N - 1, max(0, (N - 1) // 128 * 128)}
-    rest = torch.randperm(N, generator=g)[:max(0, count - len(fixed))].tolist()
+    fixed = set(range(min(leading, N))) | {0, N - 1, max(0, (N - 1) // 128 * 128)}
+    perm = torch.randperm(N, generator=g).tolist()
+    rest = [r for r in perm if r not in fixed][:max(0, count - len(fixed))]
     return sorted(fixed | set(rest))

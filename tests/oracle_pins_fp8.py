@@ -7,6 +7,8 @@ Each pin takes the module under test, so that tests/test_oracle_mutants.py can r
 the same pins against planted mistakes."""
 from __future__ import annotations
 
+import math
+
 import numpy as np
 
 import oracle.attention as exact
@@ -167,6 +169,63 @@ def pin_quantized_p_is_close(mod):
     assert np.mean(np.abs(oq - o)) < 0.01 * np.abs(v).max()
 
 
+def pin_quantized_p_worked_by_hand(mod):
+    """P rounded to E4M3 on a case worked by hand (the reading: each term p_j, taken against
+    the row max, is stored as e4m3(p_j * 64 * r_j), r_j = key j's V-tile scale over the
+    largest V-tile scale, and used as that value / (64 r_j); l and LSE use the unrounded p).
+
+    One query q = (1, 1), scale 1, no rotation, 2-row tiles.  Keys (1,1), (1,0), (0,1),
+    (-3.5,-3.5) give scores 2, 1, 1, -7, so p = (1, e^-1, e^-1, e^-9).  Every Q, K and V value
+    is exact after its tile's quantisation (codes 448, 224, 128, 0), so only P is rounded.
+    V rows (3,0), (1.5,3) | (1,0.5), (0,1): V-tile maxima 3 and 1, so r = (1, 1, 1/3, 1/3).
+      x_0 = 64                      -> 64                      p~_0 = 1
+      x_1 = 64/e     = 23.544 (step 2 in [16,32))   -> 24      p~_1 = 24/64 = 0.375
+      x_2 = 64/(3e)  = 7.8481 (step 0.5 in [4,8))   -> 8       p~_2 = 8*3/64 = 0.375
+      x_3 = 64e^-9/3 = 0.0026327 (subnormal, step 2^-9 = 0.0019531: 1.348 steps) -> 2^-9
+                                                               p~_3 = 3 * 2^-15
+    l = 1 + 2/e + e^-9 = 1.7358823; O = (3 + 0.5625 + 0.375, 1.125 + 0.1875 + 3*2^-15) / l
+      = (2.2682990, 0.7561524); LSE = 2 + ln l.
+    A power-of-two change of the gain moves no normal-range rounding (E4M3 is scale-free there)
+    but does move the subnormal x_3, and a ratio that is not sv_j / max sv changes x_3 too."""
+    q = np.array([[1.0, 1.0]])
+    k = np.array([[1.0, 1.0], [1.0, 0.0], [0.0, 1.0], [-3.5, -3.5]])
+    v = np.array([[3.0, 0.0], [1.5, 3.0], [1.0, 0.5], [0.0, 1.0]])
+    o, lse = mod.fp8_attention(q, k, v, 1.0, False, np.ones(2), rotate_qk=False, quantize_p=True,
+                               block_rows=2)
+    l = 1.0 + 2.0 * math.exp(-1.0) + math.exp(-9.0)
+    want = np.array([3.0 + 0.5625 + 0.375, 1.125 + 0.1875 + 3.0 * 2.0 ** -15]) / l
+    assert abs(l - 1.7358823) < 1e-7
+    assert np.max(np.abs(o[0] - want)) < 1e-12, (o, want)
+    assert np.max(np.abs(o[0] - np.array([2.2682990, 0.7561524]))) < 1e-7
+    assert abs(lse[0] - (2.0 + math.log(l))) < 1e-12
+    # with P exact the same inputs give the plain softmax average
+    o_exact, _ = mod.fp8_attention(q, k, v, 1.0, False, np.ones(2), rotate_qk=False, block_rows=2)
+    pe = np.exp(np.array([0.0, -1.0, -1.0, -9.0]))
+    assert np.max(np.abs(o_exact[0] - pe @ v / l)) < 1e-12
+
+
+def pin_p_rounding_within_format_bound(mod):
+    """Each rounded term of the quantize_p branch differs from p by at most half an E4M3 step:
+    2^-4 p where p * 64 * r is a normal E4M3 value, 2^-10 / (64 r) below (subnormal step
+    2^-9).  Checked term by term through one-key rows (O = v~ p~ / l with v = 1)."""
+    rng = _rng(7)
+    for t in range(200):
+        s = -rng.uniform(0.0, 14.0)           # second key's score below the first (0)
+        ratio_tile = rng.uniform(1.0, 6.0)     # first V tile's scale over the second's
+        q = np.array([[1.0, 0.0]])
+        k = np.array([[0.0, 0.0], [s, 0.0]])
+        v = np.array([[ratio_tile, 0.0], [0.0, 1.0]])   # key 1's column-1 value 1, r_1 = 1/ratio_tile
+        o, _ = mod.fp8_attention(q, k, v, 1.0, False, np.ones(2), rotate_qk=False, quantize_p=True,
+                                 block_rows=1)
+        vd = mod.fp8_inputs(q, k, v, np.ones(2), rotate_qk=False, block_rows=1)[2]
+        p1 = math.exp(float(mod.fp8_inputs(q, k, v, np.ones(2), rotate_qk=False, block_rows=1)[1][1, 0]))
+        l = 1.0 + p1
+        p1_rounded = o[0, 1] * l / vd[1, 1]
+        r1 = 1.0 / ratio_tile
+        bound = max(2.0 ** -4 * p1, 2.0 ** -10 / (64.0 * r1))
+        assert abs(p1_rounded - p1) <= bound * (1 + 1e-9), (s, ratio_tile, p1, p1_rounded, bound)
+
+
 FP8_PINS = [
     pin_e4m3_table,
     pin_e4m3_matches_torch,
@@ -177,4 +236,6 @@ FP8_PINS = [
     pin_fp8_exact_when_representable,
     pin_incoherent_processing_helps,
     pin_quantized_p_is_close,
+    pin_quantized_p_worked_by_hand,
+    pin_p_rounding_within_format_bound,
 ]

@@ -139,3 +139,38 @@ def test_bwd_host_entry_argument_errors(fa):
     assert f(*([0] + host[1:]), *dev, *tail, 0, None) == fa.FA_ERR_ARG  # null host input
     assert f(*host, *dev, *tail, -1, None) == fa.FA_ERR_ARG              # negative chunk size
 
+
+
+def _gqa_pair(fa, **kw):
+    """fa_fwd_gqa (with a fake workspace of the size it asks for) and
+    fa_fwd_gqa_static_workspace on the same arguments."""
+    a = dict(q=FAKE, k=FAKE + 2**30, v=FAKE + 2**31, o=FAKE + 3 * 2**30, lse=FAKE + 2**32,
+             B=1, Hq=4, Hkv=2, Nq=1, Nk=512, d=128, scale=0.088, causal=0, n_splits=4)
+    a.update(kw)
+    ptrs = [a[n] for n in ("q", "k", "v", "o", "lse")]
+    sizes = [a[n] for n in ("B", "Hq", "Hkv", "Nq", "Nk", "d")]
+    need = fa.lib.fa_fwd_gqa_workspace_bytes(a["B"], a["Hq"], a["Nq"], a["d"], a["n_splits"])
+    rc_gqa = fa.lib.fa_fwd_gqa(*ptrs, *sizes, a["scale"], a["causal"], a["n_splits"],
+                               FAKE + 5 * 2**30, need, None)
+    rc_static = fa.lib.fa_fwd_gqa_static_workspace(*ptrs, *sizes, a["scale"], a["causal"], a["n_splits"], None)
+    return rc_gqa, rc_static
+
+
+@pytest.mark.parametrize("kw", [
+    {"q": 0}, {"lse": 0}, {"d": 96}, {"Hkv": 3}, {"Nk": 0}, {"scale": 0.0}, {"q": FAKE + 8},
+    {"o": FAKE},            # output overlaps an input
+    {},                     # well-formed, but not device memory (fake addresses)
+])
+def test_static_workspace_entry_reports_like_fa_fwd_gqa(fa, kw):
+    """The no-allocation entry point checks its arguments as fa_fwd_gqa does, before it
+    touches the device, so both return the same code (here all are argument errors: the
+    addresses are fake)."""
+    rc_gqa, rc_static = _gqa_pair(fa, **kw)
+    assert rc_static == rc_gqa == fa.FA_ERR_ARG, (rc_gqa, rc_static)
+
+
+def test_static_workspace_entry_rejects_oversized_before_any_device_call(fa):
+    need = fa.lib.fa_fwd_gqa_workspace_bytes(1, 64, 64, 128, 16)
+    assert need > fa.FA_STATIC_WORKSPACE_BYTES
+    _, rc_static = _gqa_pair(fa, Hq=64, Hkv=8, Nq=64, n_splits=16)
+    assert rc_static == fa.FA_ERR_WORKSPACE_TOO_LARGE

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from exact_io_aware_02_gb300.inputs import WORKLOADS, make_qkv_gqa, make_workload, sample_slices
-from tests.parity import compare, within_tolerance
+from tests.parity import compare, log_stats, merge, within_tolerance
 
 pytestmark = pytest.mark.gpu
 
@@ -47,14 +47,7 @@ def check(q, k, v, o, lse, scale, causal, heads=None, rows=None):
         go = _np64(o[b, h]) if rows is None else _np64(o[b, h][rows])
         gl = _np64(lse[b, h]) if rows is None else _np64(lse[b, h][rows])
         stats.append(compare(go, gl, ro, rl))
-    return {
-        "max_abs_o_beyond_output_rounding": max(s["max_abs_o_beyond_output_rounding"] for s in stats),
-        "max_abs_o": max(s["max_abs_o"] for s in stats),
-        "mean_abs_o": float(np.average([s["mean_abs_o"] for s in stats], weights=[s["count"] for s in stats])),
-        "max_rel_lse": max(s["max_rel_lse"] for s in stats),
-        "finite": all(s["finite"] for s in stats),
-        "count": sum(s["count"] for s in stats),
-    }
+    return merge(stats)
 
 
 CASES = [  # B, Hq, Hkv, Nq, Nk, d, causal, n_splits
@@ -133,9 +126,9 @@ def test_gqa_workload_full_size_sampled(fa, name):
     q, k, v = make_workload(w)
     o, lse = run(fa, q, k, v, w.scale, w.causal, w.n_splits)
     heads = sample_slices(w.B, w.H, 8, w.seed + 1)
-    rows = None if w.N <= 2048 else sorted({0, w.N - 1, *range(0, w.N, 97)})
-    st = check(q, k, v, o, lse, w.scale, w.causal, heads=heads, rows=rows)
+    st = check(q, k, v, o, lse, w.scale, w.causal, heads=heads)   # every row of 8 query heads
     print(name, st)
+    log_stats(name, st, heads, w.N)
     assert within_tolerance(st), st
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
 

@@ -106,6 +106,18 @@ FP8_MUTANTS = [
     ("V rotated too", "for x in (qr, kr, np.asarray(v, dtype=np.float64)):",
      "for x in (qr, kr, rotate(v, signs)):", 1),
     ("only Q rotated", "kr = rotate(k, signs) if rotate_qk else", "kr = k if rotate_qk else", 1),
+    ("P gain 32 instead of 64", "p_gain: float = 64.0", "p_gain: float = 32.0", 1),
+    ("P gain 256 instead of 64", "p_gain: float = 64.0", "p_gain: float = 256.0", 1),
+    ("P gain 16 instead of 64", "p_gain: float = 64.0", "p_gain: float = 16.0", 1),
+    ("V-scale ratio inverted", "ratio = np.repeat(sv / sv.max(), block_rows)[:nk]",
+     "ratio = np.repeat(sv.max() / sv, block_rows)[:nk]", 1),
+    ("V-scale ratio against the smallest scale", "ratio = np.repeat(sv / sv.max(), block_rows)[:nk]",
+     "ratio = np.repeat(sv / sv.min(), block_rows)[:nk]", 1),
+    ("V-scale ratio dropped", "ratio = np.repeat(sv / sv.max(), block_rows)[:nk]",
+     "ratio = np.repeat(sv / sv, block_rows)[:nk]", 1),
+    ("P rounded without its gain", "pq = e4m3_round(p * p_gain * ratio[None, :]) / (p_gain * ratio[None, :])",
+     "pq = e4m3_round(p * ratio[None, :]) / (ratio[None, :])", 1),
+    ("rounded P used for l", "l = p.sum(axis=1)", "l = (e4m3_round(p * p_gain) / p_gain).sum(axis=1)", 1),
 ]
 
 

@@ -83,9 +83,15 @@ struct Cfg {
   static constexpr int kBarSFull = kBarEmpty + kSlots;  // one per query tile
   static constexpr int kBarOFinal = kBarSFull + 2;
   static constexpr int kBarDrain = kBarOFinal + 2;
-  static constexpr int kNumBars = kBarDrain + 1;
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;  // tmem base, abort flag
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + slack for 1024-B alignment
+  static constexpr int kBarConv = kBarDrain + 1;   // V_j converted to fp16: j % kSlots
+  static constexpr int kBarXchg = kBarConv + kSlots;  // the two converter warps' tile maxima
+  static constexpr int kNumBars = kBarXchg + 1;
+  // misc: tmem base (4 B), abort flag (4 B), the converters' maxima [2 buffers][2 warps] (16 B),
+  // the fp16 scale exponent of each ring slot's V tile (4 B per slot)
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kOffXmax = kOffMisc + 8;
+  static constexpr int kOffKScale = kOffMisc + 24;
+  static constexpr int kSmemBytes = kOffKScale + 4 * kSlots + 1024;  // + slack for 1024-B alignment
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;    // S_t at t*128
   static constexpr uint32_t kColO = 256;  // O_t at 256 + t*D
@@ -116,7 +122,13 @@ struct Params {
   int withhold_v0;   // test hook: never load V tile 0 (0 in every normal launch)
   unsigned long long timeout_ns;
   int withhold_tile;  // test hook instance only: this ring tile (K_0 = 0, V_0 = 1, ...) is never loaded
+  const uint16_t* v_raw;  // V [groups, Nk, D] bf16: read directly only to re-convert a tile at a new scale
 };
+
+// 2^k as a float, exactly, for k in [-126, 127]
+__device__ __forceinline__ float exp2_int(int k) { return __uint_as_float(static_cast<uint32_t>(127 + k) << 23); }
+// floor(log2 x) for x > 0 (128 for inf; -127 for subnormals, which only need a large upward scale)
+__device__ __forceinline__ int ilog2_float(float x) { return static_cast<int>((__float_as_uint(x) >> 23) & 0xffu) - 127; }
 
 // Last key position (+1 in tiles) any row of query tile qt may see, causal case.
 __device__ __forceinline__ int causal_tile_limit(const Params& p, int qt) {
@@ -135,6 +147,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const Params p) {
   using C = Cfg<D>;
+  constexpr bool kF16 = !kDual;  // P V in fp16: V tiles converted in shared memory by warps 10, 11
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -191,6 +204,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(C::kBarOFinal + t), 1);
     }
     ptx::mbar_init(bar(C::kBarDrain), 1);
+    for (int s = 0; s < C::kSlots; ++s) ptx::mbar_init(bar(C::kBarConv + s), 2);
+    ptx::mbar_init(bar(C::kBarXchg), 2);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
@@ -269,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // one elected lane issues each MMA and commit.  Descriptors are formed once: a step
     // along a tile is a constant added to the 16-byte-unit address field.
     constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 128, false);
-    constexpr uint32_t kIdescPV = ptx::idesc_bf16_f32(128, D, true);
+    constexpr uint32_t kIdescPV = kF16 ? ptx::idesc_f16_f32(128, D, true) : ptx::idesc_bf16_f32(128, D, true);
     constexpr uint64_t kSlotStep = C::kTileBytes >> 4;
     const uint64_t desc_q0 = ptx::smem_desc_sw128(sbase + C::kOffQ, 16, 1024);
     const uint64_t desc_q1 = desc_q0 + kSlotStep;
@@ -329,7 +344,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int j = 0; ok && !kDual && j <= nmax; ++j) {
       const int uk = 2 * j, uv = 2 * j - 1;  // ring tiles K_j and V_{j-1}
-      if (j >= 1) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + uv % C::kSlots), (uv / C::kSlots) & 1));
+      // V_{j-1} converted to fp16 in its ring slot (the converter waited for it to land)
+      if (j >= 1)
+        ok = __all_sync(0xffffffffu, kF16 ? w.wait(bar(C::kBarConv + (j - 1) % C::kSlots), ((j - 1) / C::kSlots) & 1)
+                                          : w.wait(bar(C::kBarFull + uv % C::kSlots), (uv / C::kSlots) & 1));
       if (!ok) break;
       bool k_ready = false;  // K_j is waited for only right before its first use
       const uint64_t dk = desc_k_ring + static_cast<uint64_t>(uk % C::kSlots) * kSlotStep;
@@ -392,6 +410,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     w.drain(bar(C::kBarDrain), 0);
     __syncwarp();
+  } else if (kF16 && warp >= 10) {
+    // ================================================================ V converters
+    // P V runs in fp16 (P rounded to 11 significant bits instead of bf16's 8), so each V tile,
+    // once landed, is rewritten in place as fp16(v * 2^-K) (same size and layout), half a tile
+    // per warp.  K is 0 for values fp16 holds exactly (|v| < 2^16, down to 2^-14 with full
+    // precision); it is set by the first tile when that tile is very small and raised whenever
+    // a later tile would overflow, which re-converts that tile from global memory.  The
+    // softmax scales O~ by 2^-(raise) in its correction step and by 2^K in the epilogue.  The
+    // MMA warp waits for both halves of a tile before its P V product.
+    const int cw = warp - 10;
+    float* xmax = reinterpret_cast<float*>(smem + C::kOffXmax);   // [j & 1][warp]
+    int* kscale = reinterpret_cast<int*>(smem + C::kOffKScale);   // [j % kSlots]
+    constexpr int kGran = C::kTileBytes / 32;  // 16-byte granules per warp (half a tile)
+    int K = 0;
+    for (int j = 0; j < nmax; ++j) {
+      const int u = 2 * j + 1, slot = u % C::kSlots;
+      if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarFull + slot), (u / C::kSlots) & 1))) break;
+      const uint32_t tile = sbase + C::kOffRing + slot * C::kTileBytes;
+      const uint32_t half = tile + cw * (C::kTileBytes / 2);
+      float mx = 0.f;  // largest |v * 2^-K| of this warp's half
+      if (K == 0) {
+#pragma unroll 4
+        for (int i = lane; i < kGran; i += 32) {
+          uint32_t x[4];
+          ptx::ld_shared_v4(half + i * 16, x[0], x[1], x[2], x[3]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = __uint_as_float(x[e] << 16), hi = __uint_as_float(x[e] & 0xffff0000u);
+            mx = ptx::fmax3(mx, fabsf(lo), fabsf(hi));
+            x[e] = ptx::pack_f16x2(lo, hi);
+          }
+          ptx::st_shared_v4(half + i * 16, x[0], x[1], x[2], x[3]);
+        }
+      } else {
+        const float mul = exp2_int(-K);
+#pragma unroll 2
+        for (int i = lane; i < kGran; i += 32) {
+          uint32_t x[4];
+          ptx::ld_shared_v4(half + i * 16, x[0], x[1], x[2], x[3]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = __uint_as_float(x[e] << 16) * mul, hi = __uint_as_float(x[e] & 0xffff0000u) * mul;
+            mx = ptx::fmax3(mx, fabsf(lo), fabsf(hi));
+            x[e] = ptx::pack_f16x2(lo, hi);
+          }
+          ptx::st_shared_v4(half + i * 16, x[0], x[1], x[2], x[3]);
+        }
+      }
+      // both warps learn the tile's largest scaled magnitude (a bounded mbarrier exchange)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0) xmax[(j & 1) * 2 + cw] = mx;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::kBarXchg));
+      if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarXchg), j & 1))) break;
+      mx = fmaxf(xmax[(j & 1) * 2], xmax[(j & 1) * 2 + 1]);
+      const bool too_big = !(mx < 65520.f);                       // rounds to inf in fp16 (or is inf)
+      const bool too_small = j == 0 && mx > 0.f && mx < 0.0625f;  // would lose bits below 2^-14
+      if (too_big || too_small) {
+        // new scale: the largest |v| lands in [2^14, 2^15); convert again from global memory
+        K = min(max(ilog2_float(mx) + K - 14, -100), 100);
+        const float mul = exp2_int(-K);
+        const size_t row_base = static_cast<size_t>(bh) * p.Nk;
+        const int kv_row0 = (lo0 + j) * 128;
+        for (int i = lane; i < kGran; i += 32) {
+          const int q = cw * kGran + i;                                        // granule in shared memory
+          const int r = (q >> 3) & 127, c = q >> 10, g = (q & 7) ^ (r & 7);   // 128-byte swizzle
+          uint4 v4 = make_uint4(0u, 0u, 0u, 0u);                               // rows past Nk are zero
+          if (kv_row0 + r < p.Nk)
+            v4 = __ldg(reinterpret_cast<const uint4*>(p.v_raw + (row_base + kv_row0 + r) * D + c * 64 + g * 8));
+          uint32_t x[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            x[e] = ptx::pack_f16x2(__uint_as_float(x[e] << 16) * mul, __uint_as_float(x[e] & 0xffff0000u) * mul);
+          ptx::st_shared_v4(tile + q * 16, x[0], x[1], x[2], x[3]);
+        }
+      }
+      if (cw == 0 && lane == 0) kscale[j % C::kSlots] = K;
+      ptx::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::kBarConv + j % C::kSlots));
+    }
   } else if (warp < 8) {
     // ================================================================ softmax warpgroups
     ptx::regs_increase<kSoftmaxRegs>();
@@ -408,7 +508,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float c2 = p.scale_log2;
     float m_run = -INFINITY;  // running max of the raw scores q.k (scale > 0)
     float l_run = 0.f;        // running sum of 2^((s - m_run) * c2)
-    float lp_run = 0.f;       // the same sum over the bf16-rounded terms
+    float lp_run = 0.f;       // bf16 P only: the same sum over the rounded terms
+    int k_cur = 0;            // fp16 P: O~ is held at the scale 2^-k_cur of the current V tile
+    const int* kscale = reinterpret_cast<const int*>(smem + C::kOffKScale);
     // d = 128: S_t is read in two halves and P written in four parts, which shortens the
     // softmax's span from S ready to P handed over.  d = 64 keeps one load and two stores:
     // its softmax is bound by instruction issue (half the tensor work per exp), and the extra
@@ -506,11 +608,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float r_fac = rescale ? ptx::ex2_approx((m_run - m_new) * c2) : 1.f;
       // a row that has seen no unmasked key yet keeps m = -inf: its terms are all 0
       const float neg = m_ref == -INFINITY ? 0.f : -m_ref * c2;
-      // P = 2^(s*c2 - m_ref*c2), rounded to bf16 pairs for the P V product and written over
-      // the first 64 columns of S_t, a part at a time while the rest is computed (four parts
-      // with the split S load, two otherwise, so the last store is short).  Two running
-      // sums: l_run over the fp32 values (for LSE) and lp_run over the rounded values the
-      // tensor core multiplies (for O = sum(P v) / sum(P), a convex combination of V rows).
+      // P = 2^(s*c2 - m_ref*c2), rounded to fp16 pairs for the P V product (bf16 in the
+      // decode instance) and written over the first 64 columns of S_t, a part at a time while
+      // the rest is computed (four parts with the split S load, two otherwise, so the last
+      // store is short).  l_run sums the fp32 values; O = O~ / l_run.  With bf16 P a second sum
+      // over the rounded values (lp_run) normalises O instead, which halves O's error when a few
+      // keys dominate; fp16 P is 8x finer and needs no second sum.
       __syncwarp();  // reconverge after the per-row mask before the warp-wide TMEM stores
       const float2 c2v = make_float2(c2, c2), negv = make_float2(neg, neg);
       float2 se[4], sp[4];
@@ -522,10 +625,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float2 x = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), c2v, negv);
         const float e0 = ptx::ex2_approx(x.x);
         const float e1 = ptx::ex2_approx(x.y);
-        pk[i] = ptx::pack_bf16x2(e0, e1);
         se[i & 3] = __fadd2_rn(se[i & 3], make_float2(e0, e1));
-        sp[i & 3] = __fadd2_rn(sp[i & 3], make_float2(__uint_as_float(pk[i] << 16),
-                                                      __uint_as_float(pk[i] & 0xffff0000u)));
+        if constexpr (kF16) {
+          pk[i] = ptx::pack_f16x2(e0, e1);
+        } else {
+          pk[i] = ptx::pack_bf16x2(e0, e1);
+          sp[i & 3] = __fadd2_rn(sp[i & 3], make_float2(__uint_as_float(pk[i] << 16),
+                                                        __uint_as_float(pk[i] & 0xffff0000u)));
+        }
         if constexpr (kSplitS) {
           if ((i & 15) == 15) {  // P_t columns [i-15, i]: keys 2(i-15) to 2i+1
             uint32_t part[16];
@@ -541,18 +648,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       const float2 se01 = __fadd2_rn(se[0], se[1]), se23 = __fadd2_rn(se[2], se[3]);
-      const float2 sp01 = __fadd2_rn(sp[0], sp[1]), sp23 = __fadd2_rn(sp[2], sp[3]);
       l_run = l_run * r_fac + ((se01.x + se01.y) + (se23.x + se23.y));
-      lp_run = lp_run * r_fac + ((sp01.x + sp01.y) + (sp23.x + sp23.y));
+      if constexpr (!kF16) {
+        const float2 sp01 = __fadd2_rn(sp[0], sp[1]), sp23 = __fadd2_rn(sp[2], sp[3]);
+        lp_run = lp_run * r_fac + ((sp01.x + sp01.y) + (sp23.x + sp23.y));
+      }
       m_run = m_ref;
-      // correction O~ *= r, before P_t(j) is handed over: PV_t(j-1) has completed (the commit
-      // behind S_t(j) covers it) and PV_t(j) waits for the arrive below
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+      // fp16 P: the scale of V_j, known once its conversion is done (nearly always by now); a
+      // raise by dk scales O~ by 2^-dk in the correction below.  A failed wait still hands this
+      // step's P over.
+      bool conv_ok = true;
+      int kj = k_cur;
+      if constexpr (kF16) {
+        conv_ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarConv + j % C::kSlots), (j / C::kSlots) & 1));
+        if (conv_ok) kj = kscale[j % C::kSlots];
+      }
+      const int dk = j > 0 ? kj - k_cur : 0;
+      k_cur = kj;
+      const float c_fac = dk > 0 ? r_fac * exp2_int(-dk) : r_fac;
+      // correction O~ *= r (and 2^-dk), before P_t(j) is handed over: PV_t(j-1) has completed
+      // (the commit behind S_t(j) covers it) and PV_t(j) waits for the arrive below
+      if (conv_ok && j > 0 && (dk > 0 || __any_sync(0xffffffffu, rescale))) {
         if constexpr (kSplitS) {  // all 128 columns of O_t in one load (S and P are dead here)
           uint32_t r[128];
           ptx::tmem_ld128(t_o, r);
 #pragma unroll
-          for (int i = 0; i < 128; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
+          for (int i = 0; i < 128; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * c_fac);
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t part[32];
@@ -566,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r[32];
             ptx::tmem_ld32(t_o + cc * 32, r);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * c_fac);
             ptx::tmem_st32(t_o + cc * 32, r);
           }
         }
@@ -575,6 +696,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       ptx::named_barrier_arrive(3 + t, 160);  // P_t(j) handed over to the MMA warp
+      if (!conv_ok) {  // this step's arrival is made; the remaining steps only arrive (below)
+        ok = false;
+        ++j;
+        break;
+      }
     }
     for (; j < nt && w.drain(bar(C::kBarSFull + t), j & 1); ++j) ptx::named_barrier_arrive(3 + t, 160);
     // ---- epilogue: O = O~ / l, LSE = m*scale + ln l; a row that saw no key gets O = 0 and
@@ -587,7 +713,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t so = sbase + C::kOffQ + t * C::kTileBytes;
     if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarOFinal + t), 0));
     const bool have = l_run > 0.f;
-    const float inv_l = have ? 1.f / lp_run : 0.f;
+    // fp16 P: O~ / l at V's scale 2^-k_cur; bf16 P: O~ / (sum of the rounded terms)
+    const float inv_l = have ? (kF16 ? exp2_int(k_cur) / l_run : 1.f / lp_run) : 0.f;
     const float lse_row = have ? m_run * p.scale + logf(l_run) : -INFINITY;
     if (ok && p.n_splits == 1) {
       ptx::tc_fence_after();
@@ -822,6 +949,7 @@ int launch(const Problem& pr, int withhold_tile, unsigned long long timeout_ns, 
   const bool dual = p.n_qtiles == 1 && pr.n_splits > 1;
   p.withhold_v0 = 0;
   p.withhold_tile = withhold_tile;
+  p.v_raw = static_cast<const uint16_t*>(pr.v);
   p.timeout_ns = timeout_ns;
   const long long grid = dual ? static_cast<long long>(groups) * ((pr.n_splits + 1) / 2)
                               : static_cast<long long>(groups) * p.n_cta_q * pr.n_splits;

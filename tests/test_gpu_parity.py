@@ -223,3 +223,42 @@ def test_stream_and_repeatability(fa):
 
 def test_status_word_clean(fa):
     assert fa.fa_status(clear=False) == 0
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("case", ["all_large", "one_tile_large", "all_tiny", "tiny_then_normal"])
+def test_v_outside_fp16_range(fa, case, d):
+    """P V runs in fp16 with V held as fp16(v * 2^-K): K is 0 for values fp16 holds exactly;
+    the first tile sets it when that tile is tiny, and a later tile that would overflow raises
+    it (that tile converted again from global memory, O~ scaled down in the correction step).
+    Each case is checked against the oracle at V's own scale lam (power-of-two scalings of
+    bf16 values are exact): |dO| / lam within the usual bounds.  Causal rows that never see a
+    large tile are checked unscaled."""
+    N = 640  # five K/V tiles; tile 3 (keys 384..511) is the 'one tile'
+    scale = 1.0 / math.sqrt(d)
+    q, k, v = make_qkv(1, 2, N, d, seed=4100 + d + len(case))
+    vf = v.float()
+    lam = 1.0
+    if case == "all_large":
+        vf, lam = vf * 2.0 ** 20, 2.0 ** 20
+    elif case == "one_tile_large":
+        vf[..., 384:512, :] *= 2.0 ** 20
+        lam = 2.0 ** 20
+    elif case == "all_tiny":
+        vf, lam = vf * 2.0 ** -30, 2.0 ** -30
+    elif case == "tiny_then_normal":
+        vf[..., :128, :] *= 2.0 ** -30
+    v2 = vf.to(torch.bfloat16)
+    assert torch.equal(v2.float(), vf)
+    for causal in (False, True):
+        o, lse = run(fa, q, k, v2, scale, causal)
+        assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+        for h in range(2):
+            ro, rl = oracle.naive_attention(_np64(q[0, h]), _np64(k[0, h]), _np64(v2[0, h]), scale, causal)
+            go, gl = _np64(o[0, h]), _np64(lse[0, h])
+            st = compare(go / lam, gl, ro / lam, rl)
+            assert within_tolerance(st), (case, causal, h, st)
+            if case == "one_tile_large" and causal:   # rows 0..383 never see tile 3
+                st0 = compare(go[:384], gl[:384], ro[:384], rl[:384])
+                assert within_tolerance(st0), (case, h, st0)
+    assert fa.fa_status(clear=False) == 0

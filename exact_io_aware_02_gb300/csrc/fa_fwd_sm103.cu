@@ -87,11 +87,11 @@ struct Cfg {
   static constexpr int kBarXchg = kBarConv + kSlots;  // the two converter warps' tile maxima
   static constexpr int kNumBars = kBarXchg + 1;
   // misc: tmem base (4 B), abort flag (4 B), the converters' maxima [2 buffers][2 warps] (16 B),
-  // the fp16 scale exponent of each ring slot's V tile (4 B per slot)
+  // the CTA's fp16 scale exponent K for V (4 B)
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffXmax = kOffMisc + 8;
   static constexpr int kOffKScale = kOffMisc + 24;
-  static constexpr int kSmemBytes = kOffKScale + 4 * kSlots + 1024;  // + slack for 1024-B alignment
+  static constexpr int kSmemBytes = kOffKScale + 16 + 1024;  // + slack for 1024-B alignment
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;    // S_t at t*128
   static constexpr uint32_t kColO = 256;  // O_t at 256 + t*D
@@ -414,14 +414,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ V converters
     // P V runs in fp16 (P rounded to 11 significant bits instead of bf16's 8), so each V tile,
     // once landed, is rewritten in place as fp16(v * 2^-K) (same size and layout), half a tile
-    // per warp.  K is 0 for values fp16 holds exactly (|v| < 2^16, down to 2^-14 with full
-    // precision); it is set by the first tile when that tile is very small and raised whenever
-    // a later tile would overflow, which re-converts that tile from global memory.  The
-    // softmax scales O~ by 2^-(raise) in its correction step and by 2^K in the epilogue.  The
-    // MMA warp waits for both halves of a tile before its P V product.
+    // per warp; the MMA warp waits for both halves before its P V product.  K is the CTA's:
+    // 0 whenever the first V tile's largest |v| lies in [2^-4, 65520) (fp16 then holds every
+    // value of that size exactly), else chosen so that it lands in [2^14, 2^15), in which case
+    // that tile is converted again from global memory; the epilogue multiplies O by 2^K.  A
+    // later tile too large for fp16 at that scale saturates at +-65504 * 2^K and sets
+    // FA_STATUS_V_RANGE (that call's O is not exact).  The two warps agree on each tile's
+    // largest magnitude through a bounded mbarrier exchange.
     const int cw = warp - 10;
     float* xmax = reinterpret_cast<float*>(smem + C::kOffXmax);   // [j & 1][warp]
-    int* kscale = reinterpret_cast<int*>(smem + C::kOffKScale);   // [j % kSlots]
+    int* kscale = reinterpret_cast<int*>(smem + C::kOffKScale);
     constexpr int kGran = C::kTileBytes / 32;  // 16-byte granules per warp (half a tile)
     int K = 0;
     for (int j = 0; j < nmax; ++j) {
@@ -431,17 +433,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t half = tile + cw * (C::kTileBytes / 2);
       float mx = 0.f;  // largest |v * 2^-K| of this warp's half
       if (K == 0) {
-#pragma unroll 4
-        for (int i = lane; i < kGran; i += 32) {
-          uint32_t x[4];
-          ptx::ld_shared_v4(half + i * 16, x[0], x[1], x[2], x[3]);
+        // eight 16-byte loads in flight, then their conversions and stores
+#pragma unroll 1
+        for (int i0 = 0; i0 < kGran; i0 += 8 * 32) {
+          uint32_t x[8][4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float lo = __uint_as_float(x[e] << 16), hi = __uint_as_float(x[e] & 0xffff0000u);
-            mx = ptx::fmax3(mx, fabsf(lo), fabsf(hi));
-            x[e] = ptx::pack_f16x2(lo, hi);
+          for (int b = 0; b < 8; ++b)
+            ptx::ld_shared_v4(half + (i0 + b * 32 + lane) * 16, x[b][0], x[b][1], x[b][2], x[b][3]);
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float lo = __uint_as_float(x[b][e] << 16), hi = __uint_as_float(x[b][e] & 0xffff0000u);
+              mx = ptx::fmax3(mx, fabsf(lo), fabsf(hi));
+              x[b][e] = ptx::pack_f16x2_sat(lo, hi);
+            }
+            ptx::st_shared_v4(half + (i0 + b * 32 + lane) * 16, x[b][0], x[b][1], x[b][2], x[b][3]);
           }
-          ptx::st_shared_v4(half + i * 16, x[0], x[1], x[2], x[3]);
         }
       } else {
         const float mul = exp2_int(-K);
@@ -453,12 +461,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < 4; ++e) {
             const float lo = __uint_as_float(x[e] << 16) * mul, hi = __uint_as_float(x[e] & 0xffff0000u) * mul;
             mx = ptx::fmax3(mx, fabsf(lo), fabsf(hi));
-            x[e] = ptx::pack_f16x2(lo, hi);
+            x[e] = ptx::pack_f16x2_sat(lo, hi);
           }
           ptx::st_shared_v4(half + i * 16, x[0], x[1], x[2], x[3]);
         }
       }
-      // both warps learn the tile's largest scaled magnitude (a bounded mbarrier exchange)
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       if (lane == 0) xmax[(j & 1) * 2 + cw] = mx;
@@ -466,14 +473,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) ptx::mbar_arrive(bar(C::kBarXchg));
       if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarXchg), j & 1))) break;
       mx = fmaxf(xmax[(j & 1) * 2], xmax[(j & 1) * 2 + 1]);
-      const bool too_big = !(mx < 65520.f);                       // rounds to inf in fp16 (or is inf)
-      const bool too_small = j == 0 && mx > 0.f && mx < 0.0625f;  // would lose bits below 2^-14
-      if (too_big || too_small) {
-        // new scale: the largest |v| lands in [2^14, 2^15); convert again from global memory
-        K = min(max(ilog2_float(mx) + K - 14, -100), 100);
+      const bool too_big = !(mx < 65520.f);  // beyond fp16 (saturated above), or inf
+      if (j == 0 && (too_big || (mx > 0.f && mx < 0.0625f))) {
+        // the CTA's scale: the first tile's largest |v| lands in [2^14, 2^15); that tile is
+        // converted again from global memory
+        K = min(max(ilog2_float(mx) - 14, -100), 100);
         const float mul = exp2_int(-K);
         const size_t row_base = static_cast<size_t>(bh) * p.Nk;
-        const int kv_row0 = (lo0 + j) * 128;
+        const int kv_row0 = lo0 * 128;
         for (int i = lane; i < kGran; i += 32) {
           const int q = cw * kGran + i;                                        // granule in shared memory
           const int r = (q >> 3) & 127, c = q >> 10, g = (q & 7) ^ (r & 7);   // 128-byte swizzle
@@ -483,11 +490,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t x[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e)
-            x[e] = ptx::pack_f16x2(__uint_as_float(x[e] << 16) * mul, __uint_as_float(x[e] & 0xffff0000u) * mul);
+            x[e] = ptx::pack_f16x2_sat(__uint_as_float(x[e] << 16) * mul, __uint_as_float(x[e] & 0xffff0000u) * mul);
           ptx::st_shared_v4(tile + q * 16, x[0], x[1], x[2], x[3]);
         }
+        if (!(mx < INFINITY) && cw == 0 && lane == 0) atomicOr(&g_status, FA_STATUS_V_RANGE);
+      } else if (too_big && cw == 0 && lane == 0) {
+        atomicOr(&g_status, FA_STATUS_V_RANGE);
       }
-      if (cw == 0 && lane == 0) kscale[j % C::kSlots] = K;
+      if (j == 0 && cw == 0 && lane == 0) *kscale = K;
       ptx::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(C::kBarConv + j % C::kSlots));
@@ -509,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m_run = -INFINITY;  // running max of the raw scores q.k (scale > 0)
     float l_run = 0.f;        // running sum of 2^((s - m_run) * c2)
     float lp_run = 0.f;       // bf16 P only: the same sum over the rounded terms
-    int k_cur = 0;            // fp16 P: O~ is held at the scale 2^-k_cur of the current V tile
+    int k_cur = 0;            // fp16 P: O~ is held at V's scale 2^-k_cur
     const int* kscale = reinterpret_cast<const int*>(smem + C::kOffKScale);
     // d = 128: S_t is read in two halves and P written in four parts, which shortens the
     // softmax's span from S ready to P handed over.  d = 64 keeps one load and two stores:
@@ -654,26 +664,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         lp_run = lp_run * r_fac + ((sp01.x + sp01.y) + (sp23.x + sp23.y));
       }
       m_run = m_ref;
-      // fp16 P: the scale of V_j, known once its conversion is done (nearly always by now); a
-      // raise by dk scales O~ by 2^-dk in the correction below.  A failed wait still hands this
-      // step's P over.
-      bool conv_ok = true;
-      int kj = k_cur;
-      if constexpr (kF16) {
-        conv_ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarConv + j % C::kSlots), (j / C::kSlots) & 1));
-        if (conv_ok) kj = kscale[j % C::kSlots];
-      }
-      const int dk = j > 0 ? kj - k_cur : 0;
-      k_cur = kj;
-      const float c_fac = dk > 0 ? r_fac * exp2_int(-dk) : r_fac;
-      // correction O~ *= r (and 2^-dk), before P_t(j) is handed over: PV_t(j-1) has completed
-      // (the commit behind S_t(j) covers it) and PV_t(j) waits for the arrive below
-      if (conv_ok && j > 0 && (dk > 0 || __any_sync(0xffffffffu, rescale))) {
+      // correction O~ *= r, before P_t(j) is handed over: PV_t(j-1) has completed (the commit
+      // behind S_t(j) covers it) and PV_t(j) waits for the arrive below
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
         if constexpr (kSplitS) {  // all 128 columns of O_t in one load (S and P are dead here)
           uint32_t r[128];
           ptx::tmem_ld128(t_o, r);
 #pragma unroll
-          for (int i = 0; i < 128; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * c_fac);
+          for (int i = 0; i < 128; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
 #pragma unroll
           for (int cc = 0; cc < 4; ++cc) {
             uint32_t part[32];
@@ -687,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t r[32];
             ptx::tmem_ld32(t_o + cc * 32, r);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * c_fac);
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
             ptx::tmem_st32(t_o + cc * 32, r);
           }
         }
@@ -696,11 +694,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       ptx::named_barrier_arrive(3 + t, 160);  // P_t(j) handed over to the MMA warp
-      if (!conv_ok) {  // this step's arrival is made; the remaining steps only arrive (below)
-        ok = false;
-        ++j;
-        break;
-      }
     }
     for (; j < nt && w.drain(bar(C::kBarSFull + t), j & 1); ++j) ptx::named_barrier_arrive(3 + t, 160);
     // ---- epilogue: O = O~ / l, LSE = m*scale + ln l; a row that saw no key gets O = 0 and
@@ -712,6 +705,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_valid = qrow < p.R;
     const uint32_t so = sbase + C::kOffQ + t * C::kTileBytes;
     if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarOFinal + t), 0));
+    // fp16 P: O~ is held at V's scale 2^-K, fixed by the CTA's first V tile.  The wait is for
+    // this tile's last conversion (which follows the first); that barrier phase cannot have
+    // been reused yet, as the converters are at most one V tile ahead of this tile's last.
+    if (kF16 && ok && nt > 0) {
+      ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarConv + (nt - 1) % C::kSlots), ((nt - 1) / C::kSlots) & 1));
+      if (ok) k_cur = *kscale;
+    }
     const bool have = l_run > 0.f;
     // fp16 P: O~ / l at V's scale 2^-k_cur; bf16 P: O~ / (sum of the rounded terms)
     const float inv_l = have ? (kF16 ? exp2_int(k_cur) / l_run : 1.f / lp_run) : 0.f;

@@ -24,6 +24,7 @@ FA_ERR_CUDA = -5
 FA_ERR_WORKSPACE_TOO_LARGE = -6
 FA_STATIC_WORKSPACE_BYTES = 16 << 20
 FA_STATUS_TIMEOUT = 0x1
+FA_STATUS_V_RANGE = 0x2
 
 EXPORTED = ("fa_fwd", "fa_fwd_gqa", "fa_fwd_gqa_workspace_bytes", "fa_fwd_gqa_static_workspace",
             "fa_fwd_host", "fa_bwd", "fa_bwd_host", "fa_fwd_fp8", "fa_fwd_fp8_host", "fa_fwd_fp8_workspace_bytes", "fa_status", "fa_fwd_withheld_tile",

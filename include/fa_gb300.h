@@ -47,6 +47,9 @@ extern "C" {
 
 /* Bits of the device status word (fa_status). */
 #define FA_STATUS_TIMEOUT 0x1u  /* some CTA's bounded mbarrier wait expired and it bailed out */
+#define FA_STATUS_V_RANGE 0x2u  /* fa_fwd / fa_fwd_gqa: a V tile outside the range the fp16 P V
+                                   product can hold at the scale the call had reached (see
+                                   fa_fwd); that call's O is not exact */
 
 /*
  * fa_fwd -- exact attention forward, O and LSE.
@@ -70,6 +73,13 @@ extern "C" {
  * error return nothing was written.  A device-side wait that gives up (never
  * expected in correct operation) does not surface here: it sets
  * FA_STATUS_TIMEOUT in the status word, which fa_status() reads.
+ *
+ * Precision: S, O and the row sums accumulate in fp32; P is rounded to fp16 for
+ * the P V product, with V converted to fp16 in shared memory at a power-of-two
+ * scale that each CTA fixes from the first V tile it reads (1 unless that tile's
+ * largest |v| is below 2^-4 or at least 65520).  A later V tile that fp16 cannot
+ * hold at that scale (with the scale 1: any |v| >= 65520) is saturated and sets
+ * FA_STATUS_V_RANGE; that call's O is then not exact.
  *
  * Returns FA_OK, FA_ERR_ARG, FA_ERR_ARCH or FA_ERR_LAUNCH.
  */

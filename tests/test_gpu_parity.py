@@ -226,39 +226,58 @@ def test_status_word_clean(fa):
 
 
 @pytest.mark.parametrize("d", [64, 128])
-@pytest.mark.parametrize("case", ["all_large", "one_tile_large", "all_tiny", "tiny_then_normal"])
+@pytest.mark.parametrize("case", ["all_large", "large_first_tile", "all_tiny", "tiny_later_tile"])
 def test_v_outside_fp16_range(fa, case, d):
-    """P V runs in fp16 with V held as fp16(v * 2^-K): K is 0 for values fp16 holds exactly;
-    the first tile sets it when that tile is tiny, and a later tile that would overflow raises
-    it (that tile converted again from global memory, O~ scaled down in the correction step).
-    Each case is checked against the oracle at V's own scale lam (power-of-two scalings of
-    bf16 values are exact): |dO| / lam within the usual bounds.  Causal rows that never see a
-    large tile are checked unscaled."""
-    N = 640  # five K/V tiles; tile 3 (keys 384..511) is the 'one tile'
+    """P V runs in fp16 with V held as fp16(v * 2^-K), K fixed per CTA by its first V tile:
+    0 when that tile's largest |v| is in [2^-4, 65520), else chosen to bring it into
+    [2^14, 2^15).  Uniformly large or tiny V, a large first tile before ordinary ones, and a
+    tiny tile after ordinary ones are all exact.  Each case is checked against the oracle at
+    V's own scale lam (power-of-two scalings of bf16 values are exact): |dO| / lam within the
+    usual bounds, with the status word clean."""
+    N = 640  # five K/V tiles
     scale = 1.0 / math.sqrt(d)
     q, k, v = make_qkv(1, 2, N, d, seed=4100 + d + len(case))
     vf = v.float()
     lam = 1.0
     if case == "all_large":
         vf, lam = vf * 2.0 ** 20, 2.0 ** 20
-    elif case == "one_tile_large":
-        vf[..., 384:512, :] *= 2.0 ** 20
+    elif case == "large_first_tile":
+        vf[..., :128, :] *= 2.0 ** 20
         lam = 2.0 ** 20
     elif case == "all_tiny":
         vf, lam = vf * 2.0 ** -30, 2.0 ** -30
-    elif case == "tiny_then_normal":
-        vf[..., :128, :] *= 2.0 ** -30
+    elif case == "tiny_later_tile":
+        vf[..., 384:512, :] *= 2.0 ** -30
     v2 = vf.to(torch.bfloat16)
     assert torch.equal(v2.float(), vf)
+    fa.fa_status(clear=True)
     for causal in (False, True):
         o, lse = run(fa, q, k, v2, scale, causal)
         assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
         for h in range(2):
             ro, rl = oracle.naive_attention(_np64(q[0, h]), _np64(k[0, h]), _np64(v2[0, h]), scale, causal)
-            go, gl = _np64(o[0, h]), _np64(lse[0, h])
-            st = compare(go / lam, gl, ro / lam, rl)
+            st = compare(_np64(o[0, h]) / lam, _np64(lse[0, h]), ro / lam, rl)
             assert within_tolerance(st), (case, causal, h, st)
-            if case == "one_tile_large" and causal:   # rows 0..383 never see tile 3
-                st0 = compare(go[:384], gl[:384], ro[:384], rl[:384])
-                assert within_tolerance(st0), (case, h, st0)
+    assert fa.fa_status(clear=False) == 0
+
+
+@pytest.mark.parametrize("case", ["large_later_tile", "tiny_first_tile"])
+def test_v_tile_beyond_fp16_at_the_cta_scale_is_flagged(fa, case):
+    """A V tile that fp16 cannot hold at the scale the CTA's first V tile fixed (a tile of
+    values >= 65520 after ordinary ones; ordinary tiles after a tiny first tile) saturates,
+    and the status word says so (FA_STATUS_V_RANGE); nothing faults, and the next call is
+    clean."""
+    N, d = 384, 128
+    q, k, v = make_qkv(1, 1, N, d, seed=4202)
+    vf = v.float()
+    if case == "large_later_tile":
+        vf[..., 256:384, :] *= 2.0 ** 20
+    else:
+        vf[..., :128, :] *= 2.0 ** -30
+    fa.fa_status(clear=True)
+    o, lse = run(fa, q, k, vf.to(torch.bfloat16), 1.0 / math.sqrt(d), False)
+    assert torch.isfinite(lse).all()
+    assert fa.fa_status(clear=True) & fa.FA_STATUS_V_RANGE
+    q, k, v = make_qkv(1, 1, N, d, seed=4203)
+    o, lse = run(fa, q, k, v, 1.0 / math.sqrt(d), False)
     assert fa.fa_status(clear=False) == 0

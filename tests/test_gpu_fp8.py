@@ -8,10 +8,17 @@ Two stages are checked.
   every code must equal the oracle's or sit one E4M3 step from it, and nearly all must be
   equal.  Scales agree to fp32 rounding.
 * The attention.  The oracle's reference is the exact attention of its dequantised Q', K'
-  and V; the kernel also rounds P to E4M3 before the product with V.  The size of that one
-  rounding is measured on the same inputs with the oracle's P-rounded variant (m_P), and the
-  kernel must stay within mean|dO| <= 1.5 mean(m_P) + 1e-3 and max|dO| <= 2 max(m_P) + 2e-2.
-  LSE does not see the P rounding: |dLSE| <= 1e-3 max(1, |LSE|).
+  and V (fp8_attention); the kernel's one further rounding is P's, to E4M3 before the
+  product with V.  The bounds come from the format alone: a term stored as an E4M3 value
+  moves by at most half a step, 2^-4 of itself in the normal range and 2^-10 of the encoding
+  scale below it, so the attention weight a_ij = p_ij / l_i moves by at most
+  h_ij = max(2^-4 a_ij, 2^-10 / (sigma_j l_i)), sigma_j = 64 r_j the encoding scale of P's
+  column j (the per-tile V scale over the largest one, reading R22).  Then, element by
+  element, |dO| <= sum_j h_ij |v'_j| + half a bf16 ulp of O (the output's rounding); and,
+  treating each rounding as uniform within its half step, the mean |dO| is held to 1.25 times
+  the root-mean-square that model predicts.  LSE does not see P's rounding:
+  |dLSE| <= 1e-3 max(1, |LSE|).  The oracle's own P-rounded variant (quantize_p=True, one
+  plausible placement) is printed as a diagnostic only.
 """
 import math
 
@@ -23,6 +30,8 @@ import oracle.attention as exact
 import oracle.fp8 as f8
 from exact_io_aware_02_gb300.inputs import (WORKLOADS, make_qkv, make_signs, make_workload, make_workload_signs,
                                             sample_rows, sample_slices)
+
+from tests.parity import log_stats
 
 pytestmark = pytest.mark.gpu
 D = 128
@@ -115,33 +124,55 @@ def test_fp8_quantisation_matches_oracle(fa, case):
             assert not np.any(got[bh, N:n_pad])  # padding rows hold zero codes
 
 
+def bf16_half_ulp(x):
+    ax = np.abs(np.asarray(x, dtype=np.float64))
+    _, e = np.frexp(np.maximum(ax, 2.0 ** -126))
+    return np.ldexp(1.0, e - 9)
+
+
+def p_rounding_bounds(qa, ka, va, s, scale, causal, rows=None):
+    """The oracle's reference for one (b, h) slice and the format's bounds on P's rounding:
+    (O_ref, LSE_ref, envelope, variance), envelope = H |V'|, variance = (H^2 / 3) V'^2."""
+    qd, kd, vd = f8.fp8_inputs(qa, ka, va, s)
+    ro, rl = exact.naive_attention(qd, kd, vd, scale, causal, rows=rows)
+    nk = kd.shape[0]
+    r = np.arange(qd.shape[0]) if rows is None else np.asarray(rows)
+    sc = scale * (qd[r] @ kd.T)
+    if causal:
+        sc = np.where(np.arange(nk)[None, :] > r[:, None], -np.inf, sc)
+    p = np.exp(sc - sc.max(axis=1, keepdims=True))
+    l = p.sum(axis=1, keepdims=True)
+    _, sv = f8.quantize_blocks(np.asarray(va, dtype=np.float64))
+    sigma = 64.0 * np.repeat(sv / sv.max(), f8.BLOCK_ROWS)[:nk]
+    h = np.where(p > 0.0, np.maximum(2.0 ** -4 * p / l, 2.0 ** -10 / (sigma[None, :] * l)), 0.0)
+    return ro, rl, h @ np.abs(vd), (h * h / 3.0) @ (vd * vd)
+
+
 def fp8_stats(o, lse, q, k, v, signs, causal, scale, heads, rows=None):
     s = signs.numpy().astype(np.float64)
-    out = {"d_mean": [], "d_max": 0.0, "m_mean": [], "m_max": 0.0, "lse": 0.0, "n": []}
+    over, d_sum, d_max, n, var_sum, lse_err, m_max = -np.inf, 0.0, 0.0, 0, 0.0, 0.0, 0.0
     for b, h in heads:
         qa, ka, va = _np(q[b, h]), _np(k[b, h]), _np(v[b, h])
-        ro, rl = f8.fp8_attention(qa, ka, va, scale, causal, s, rows=rows)
-        mo, _ = f8.fp8_attention(qa, ka, va, scale, causal, s, rows=rows, quantize_p=True)
+        ro, rl, env, var = p_rounding_bounds(qa, ka, va, s, scale, causal, rows)
         go = _np(o[b, h]) if rows is None else _np(o[b, h])[rows]
         gl = _np(lse[b, h]) if rows is None else _np(lse[b, h])[rows]
-        d = np.abs(go - ro)
-        m = np.abs(mo - ro)
-        out["d_mean"].append(d.mean())
-        out["m_mean"].append(m.mean())
-        out["n"].append(d.size)
-        out["d_max"] = max(out["d_max"], float(d.max()))
-        out["m_max"] = max(out["m_max"], float(m.max()))
-        out["lse"] = max(out["lse"], float(np.max(np.abs(gl - rl) / np.maximum(1.0, np.abs(rl)))))
         assert np.all(np.isfinite(go)) and np.all(np.isfinite(gl))
-    w = np.array(out["n"], dtype=np.float64)
-    out["d_mean"] = float(np.average(out["d_mean"], weights=w))
-    out["m_mean"] = float(np.average(out["m_mean"], weights=w))
-    return out
+        d = np.abs(go - ro)
+        half = bf16_half_ulp(ro)
+        over = max(over, float(np.max(d - (env + half + 1e-4))))
+        d_sum += float(d.sum())
+        d_max = max(d_max, float(d.max()))
+        n += d.size
+        var_sum += float((var + half * half / 3.0).sum())
+        lse_err = max(lse_err, float(np.max(np.abs(gl - rl) / np.maximum(1.0, np.abs(rl)))))
+        mo, _ = f8.fp8_attention(qa, ka, va, scale, causal, s, rows=rows, quantize_p=True)
+        m_max = max(m_max, float(np.abs(mo - ro).max()))
+    return {"over_envelope": over, "d_mean": d_sum / n, "d_max": d_max, "rms_model": float(np.sqrt(var_sum / n)),
+            "lse": lse_err, "replay_max_diagnostic": m_max}
 
 
 def within(st):
-    return (st["d_mean"] <= 1.5 * st["m_mean"] + 1e-3 and st["d_max"] <= 2 * st["m_max"] + 2e-2
-            and st["lse"] <= 1e-3)
+    return st["over_envelope"] <= 0.0 and st["d_mean"] <= 1.25 * st["rms_model"] and st["lse"] <= 1e-3
 
 
 @pytest.mark.parametrize("case", CASES, ids=IDS)
@@ -153,12 +184,15 @@ def test_fp8_attention_parity(fa, case):
     o, lse, _ = run(fa, q, k, v, signs, causal)
     st = fp8_stats(o, lse, q, k, v, signs, causal, scale, [(b, h) for b in range(B) for h in range(H)])
     print(case, st)
+    log_stats("fp8_" + "_".join(str(x) for x in case), st, [(b, h) for b in range(B) for h in range(H)], N)
     assert within(st), st
 
 
 def test_fp8_close_to_exact_attention(fa):
-    """The FP8 result is as close to exact (bf16-input) attention as the method's own
-    model: RMSE within 1.25x of the oracle's P-rounded FP8 attention."""
+    """Against exact (bf16-input) attention: the kernel's RMSE is at most the FP8 reference's own
+    (the error of quantising Q', K' and V, which the oracle measures directly) plus the
+    root-mean-square the format predicts for P's rounding and the bf16 output (the triangle
+    inequality).  The oracle's P-rounded variant is printed for comparison only."""
     B, H, N = 1, 2, 1024
     q, k, v = make_qkv(B, H, N, D, seed=8301)
     signs = make_signs(D, 8302)
@@ -167,11 +201,15 @@ def test_fp8_close_to_exact_attention(fa):
     for h in range(H):
         qa, ka, va = _np(q[0, h]), _np(k[0, h]), _np(v[0, h])
         oe, _ = exact.naive_attention(qa, ka, va, 1 / math.sqrt(D), True)
+        ro, _, _, var = p_rounding_bounds(qa, ka, va, s, 1 / math.sqrt(D), True)
         om, _ = f8.fp8_attention(qa, ka, va, 1 / math.sqrt(D), True, s, quantize_p=True)
         rmse_k = float(np.sqrt(np.mean((_np(o[0, h]) - oe) ** 2)))
-        rmse_m = float(np.sqrt(np.mean((om - oe) ** 2)))
-        print("rmse kernel", rmse_k, "model", rmse_m)
-        assert rmse_k <= 1.25 * rmse_m + 1e-4
+        rmse_ref = float(np.sqrt(np.mean((ro - oe) ** 2)))
+        half = bf16_half_ulp(ro)
+        rms_p = float(np.sqrt(np.mean(var + half * half / 3.0)))
+        print("rmse kernel", rmse_k, "reference", rmse_ref, "P model", rms_p,
+              "replay (diagnostic)", float(np.sqrt(np.mean((om - oe) ** 2))))
+        assert rmse_k <= rmse_ref + 1.25 * rms_p
 
 
 FP8_WORKLOADS = [n for n, w in WORKLOADS.items() if w.direction == "fp8"]
@@ -187,6 +225,7 @@ def test_fp8_workload_full_size_sampled(fa, name):
     rows = sample_rows(w.N, 256, w.seed + 2)
     st = fp8_stats(o, lse, q, k, v, signs, w.causal, w.scale, heads, rows)
     print(name, st)
+    log_stats(name, st, heads, len(rows))
     assert within(st), st
     assert torch.isfinite(o.to(torch.float32)).all() and torch.isfinite(lse).all()
     assert fa.fa_status(clear=False) == 0

@@ -86,8 +86,8 @@ struct Cfg {
   static constexpr int kBarConv = kBarDrain + 1;   // V_j converted to fp16: j % kSlots
   static constexpr int kBarXchg = kBarConv + kSlots;  // the two converter warps' tile maxima
   static constexpr int kNumBars = kBarXchg + 1;
-  // misc: tmem base (4 B), abort flag (4 B), the converters' maxima [2 buffers][2 warps] (16 B),
-  // the CTA's fp16 scale exponent K for V (4 B)
+  // misc: tmem base (4 B), abort flag (4 B), the two converters' maxima of the first V tile
+  // (8 B, 16 reserved), the CTA's fp16 scale exponent K for V (4 B)
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kOffXmax = kOffMisc + 8;
   static constexpr int kOffKScale = kOffMisc + 24;
@@ -129,6 +129,33 @@ struct Params {
 __device__ __forceinline__ float exp2_int(int k) { return __uint_as_float(static_cast<uint32_t>(127 + k) << 23); }
 // floor(log2 x) for x > 0 (128 for inf; -127 for subnormals, which only need a large upward scale)
 __device__ __forceinline__ int ilog2_float(float x) { return static_cast<int>((__float_as_uint(x) >> 23) & 0xffu) - 127; }
+
+// Rewrites granules base + lane + 32 i (i < N) of a 16-byte-granule tile in shared memory in
+// place from bf16 to fp16, kBatch loads in flight at a time; with kMeasure also returns the
+// largest magnitude seen by this lane.
+template <int N, int kBatch, bool kMeasure>
+__device__ __forceinline__ float convert_granules(const uint32_t tile, const int base, const int lane) {
+  static_assert(N % kBatch == 0, "whole batches");
+  float mx = 0.f;
+#pragma unroll 1
+  for (int i0 = 0; i0 < N; i0 += kBatch) {
+    uint32_t x[kBatch][4];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b)
+      ptx::ld_shared_v4(tile + (base + lane + 32 * (i0 + b)) * 16, x[b][0], x[b][1], x[b][2], x[b][3]);
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float lo = __uint_as_float(x[b][e] << 16), hi = __uint_as_float(x[b][e] & 0xffff0000u);
+        if (kMeasure) mx = ptx::fmax3(mx, fabsf(lo), fabsf(hi));
+        x[b][e] = ptx::pack_f16x2(lo, hi);
+      }
+      ptx::st_shared_v4(tile + (base + lane + 32 * (i0 + b)) * 16, x[b][0], x[b][1], x[b][2], x[b][3]);
+    }
+  }
+  return mx;
+}
 
 // Last key position (+1 in tiles) any row of query tile qt may see, causal case.
 __device__ __forceinline__ int causal_tile_limit(const Params& p, int qt) {
@@ -204,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::mbar_init(bar(C::kBarOFinal + t), 1);
     }
     ptx::mbar_init(bar(C::kBarDrain), 1);
-    for (int s = 0; s < C::kSlots; ++s) ptx::mbar_init(bar(C::kBarConv + s), 2);
+    for (int s = 0; s < C::kSlots; ++s) ptx::mbar_init(bar(C::kBarConv + s), 3);
     ptx::mbar_init(bar(C::kBarXchg), 2);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
@@ -219,9 +246,100 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Waiter w{abort_flag, p.timeout_ns};
 
+  // ---- V conversion for the fp16 P V product.  Each landed V tile is rewritten in place as
+  // fp16(v * 2^-K), same size and layout; the MMA warp waits for the tile's conversion barrier,
+  // which counts three arrivals.  The first tile is converted by warps 10 and 11 in halves
+  // (the producer arrives without work); every later tile by three warps on three SM
+  // sub-partitions: the producer (warp 8) a quarter, converting V_{j-1} right after it has
+  // issued V_j's copy, warps 10 and 11 three eighths each.  K is the CTA's: 0 whenever the first
+  // V tile's largest |v| lies in [2^-4, 65520) (fp16 then holds every value of that size
+  // exactly), else chosen so that it lands in [2^14, 2^15), that tile then converted again from
+  // global memory; the epilogue multiplies O by 2^K.  Only the first tile is measured.  A later
+  // tile too large for fp16 at that scale turns into infinities, which reach every row of the
+  // CTA's O (p * inf, or 0 * inf for a masked key); the epilogue then sets FA_STATUS_V_RANGE:
+  // flagged, never silent.
+  constexpr int kGranT = C::kTileBytes / 16;  // 16-byte granules per tile
+  int v_scale = 0;                            // K, as each converter knows it
+  // the first V tile: warps 10 and 11 (parts 1, 2), a half each, measured
+  auto convert_first = [&](const int part) -> bool {
+    if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarFull + 1 % C::kSlots), 0))) return false;
+    const uint32_t tile = sbase + C::kOffRing + (1 % C::kSlots) * C::kTileBytes;
+    {
+      const int g0 = (part - 1) * (kGranT / 2);
+      float mx = convert_granules<kGranT / 64, 8, true>(tile, g0, lane);
+      float* xmax = reinterpret_cast<float*>(smem + C::kOffXmax);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      if (lane == 0) xmax[part - 1] = mx;
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(C::kBarXchg));
+      if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarXchg), 0))) return false;
+      mx = fmaxf(xmax[0], xmax[1]);
+      if (!(mx < 65520.f) || (mx > 0.f && mx < 0.0625f)) {
+        v_scale = min(max(ilog2_float(mx) - 14, -100), 100);
+        const float mul = exp2_int(-v_scale);
+        const size_t row_base = static_cast<size_t>(bh) * p.Nk;
+        const int kv_row0 = lo0 * 128;
+        for (int q = g0 + lane; q < g0 + kGranT / 2; q += 32) {
+          const int r = (q >> 3) & 127, c = q >> 10, g = (q & 7) ^ (r & 7);   // 128-byte swizzle
+          uint4 v4 = make_uint4(0u, 0u, 0u, 0u);                               // rows past Nk are zero
+          if (kv_row0 + r < p.Nk)
+            v4 = __ldg(reinterpret_cast<const uint4*>(p.v_raw + (row_base + kv_row0 + r) * D + c * 64 + g * 8));
+          uint32_t y[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            y[e] = ptx::pack_f16x2(__uint_as_float(y[e] << 16) * mul, __uint_as_float(y[e] & 0xffff0000u) * mul);
+          ptx::st_shared_v4(tile + q * 16, y[0], y[1], y[2], y[3]);
+        }
+      }
+      if (part == 1 && lane == 0) *reinterpret_cast<int*>(smem + C::kOffKScale) = v_scale;
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar(C::kBarConv));
+    return true;
+  };
+  // a later V tile j: the producer (part 0) a quarter, warps 10 and 11 three eighths each
+  auto convert_share = [&](const int j, const int part) -> bool {
+    const int u = 2 * j + 1, slot = u % C::kSlots;
+    if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarFull + slot), (u / C::kSlots) & 1))) return false;
+    const uint32_t tile = sbase + C::kOffRing + slot * C::kTileBytes;
+    {
+      const int g0 = part == 0 ? 0 : part == 1 ? kGranT / 4 : 5 * kGranT / 8;  // granules [g0, g1)
+      const int g1 = part == 0 ? kGranT / 4 : part == 1 ? 5 * kGranT / 8 : kGranT;
+      if (v_scale != 0) {  // a scaled CTA (rare): each value times 2^-K on the way
+        const float mul = exp2_int(-v_scale);
+        for (int q = g0 + lane; q < g1; q += 32) {
+          uint32_t x[4];
+          ptx::ld_shared_v4(tile + q * 16, x[0], x[1], x[2], x[3]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            x[e] = ptx::pack_f16x2(__uint_as_float(x[e] << 16) * mul, __uint_as_float(x[e] & 0xffff0000u) * mul);
+          ptx::st_shared_v4(tile + q * 16, x[0], x[1], x[2], x[3]);
+        }
+      } else if (part == 0) {
+        convert_granules<kGranT / 128, 8, false>(tile, g0, lane);
+      } else {
+        convert_granules<3 * kGranT / 256, (3 * kGranT / 256) % 8 ? 4 : 8, false>(tile, g0, lane);
+      }
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar(C::kBarConv + j % C::kSlots));
+    return true;
+  };
+  // the producer's scale: known once the first tile's conversion is done (before its first part)
+  auto producer_scale = [&]() -> bool {
+    if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarConv), 0))) return false;
+    v_scale = *reinterpret_cast<const int*>(smem + C::kOffKScale);
+    return true;
+  };
+
   if (warp >= 8) ptx::regs_decrease<kOtherRegs>();
   if (warp == 8) {
     // ================================================================ TMA producer
+    // Lane 0 issues the copies; the whole warp runs the ring loop, because with fp16 P V it
+    // also converts a third of each V tile (V_{j-1} right after V_j's copy is issued).
     if (lane == 0) {
       ptx::prefetch_tensormap(&tm_q);
       ptx::prefetch_tensormap(&tm_k);
@@ -235,12 +353,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < C::kChunks; ++c)
           ptx::tma_load_3d(sbase + C::kOffQ + C::kTileBytes + c * C::kChunkBytes, &tm_q,
                            bar(C::kBarQ), c * 64, qt1 * 128, bh);
-      const int n_tiles = kDual ? 0 : 2 * nmax;
-      // test hooks: tile 1 (V_0), or in the kHook instance the ring tile named, is never loaded
-      const int skip = kHook ? p.withhold_tile : (p.withhold_v0 ? 1 : -1);
-      int issued = 0;
-      bool ok = true;
-      if constexpr (kDual) {
+    }
+    const int n_tiles = kDual ? 0 : 2 * nmax;
+    if (kF16 && nmax >= 1 && lane == 0) ptx::mbar_arrive(bar(C::kBarConv));  // its part of V_0: none
+    // test hooks: tile 1 (V_0), or in the kHook instance the ring tile named, is never loaded
+    const int skip = kHook ? p.withhold_tile : (p.withhold_v0 ? 1 : -1);
+    int issued = 0;
+    bool ok = true;
+    if constexpr (kDual) {
+      if (lane == 0) {
         // ring order = the MMA warp's order: per step j and slot t, V_t(j-1) then K_t(j)
         auto load = [&](int kv_tile, bool is_v) -> bool {
           const int u = issued, slot = u % C::kSlots, use = u / C::kSlots;
@@ -259,23 +380,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (ok && j < nt) ok = load(lo + j, false);
           }
       }
-      for (int u = 0; u < n_tiles; ++u) {
-        const int slot = u % C::kSlots, use = u / C::kSlots;
-        if (use > 0 && !w.wait(bar(C::kBarEmpty + slot), (use - 1) & 1)) { ok = false; break; }
-        if (u != skip) {
-          ptx::mbar_arrive_expect_tx(bar(C::kBarFull + slot), C::kTileBytes);
-          const CUtensorMap* m = (u & 1) ? &tm_v : &tm_k;
-          for (int c = 0; c < C::kChunks; ++c)
-            ptx::tma_load_3d(sbase + C::kOffRing + slot * C::kTileBytes + c * C::kChunkBytes, m,
-                             bar(C::kBarFull + slot), c * 64, (lo0 + (u >> 1)) * 128, bh);
-        }
-        issued = u + 1;
+    }
+    for (int u = 0; u < n_tiles; ++u) {
+      const int slot = u % C::kSlots, use = u / C::kSlots;
+      if (use > 0 && !__all_sync(0xffffffffu, w.wait(bar(C::kBarEmpty + slot), (use - 1) & 1))) { ok = false; break; }
+      if (lane == 0 && u != skip) {
+        ptx::mbar_arrive_expect_tx(bar(C::kBarFull + slot), C::kTileBytes);
+        const CUtensorMap* m = (u & 1) ? &tm_v : &tm_k;
+        for (int c = 0; c < C::kChunks; ++c)
+          ptx::tma_load_3d(sbase + C::kOffRing + slot * C::kTileBytes + c * C::kChunkBytes, m,
+                           bar(C::kBarFull + slot), c * 64, (lo0 + (u >> 1)) * 128, bh);
       }
-      if (!ok) {  // let every copy already issued land before the CTA's memory is released
-        w.drain(bar(C::kBarQ), 0);
-        for (int u = issued - C::kSlots > 0 ? issued - C::kSlots : 0; u < issued; ++u)
-          if (u != skip) w.drain(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1);
+      __syncwarp();
+      issued = u + 1;
+      // its quarter of V_{j-1}, right after issuing V_j (j >= 2: V_{j-1} has long landed)
+      if (kF16 && (u & 1) && u >= 5) {
+        if (u == 5 && !producer_scale()) { ok = false; break; }
+        if (!convert_share((u >> 1) - 1, 0)) { ok = false; break; }
       }
+    }
+    if (kF16 && ok && nmax >= 2) {
+      if (nmax == 2) ok = producer_scale();
+      if (ok) ok = convert_share(nmax - 1, 0);
+    }
+    if (!ok && lane == 0) {  // let every copy already issued land before the CTA's memory is released
+      w.drain(bar(C::kBarQ), 0);
+      for (int u = issued - C::kSlots > 0 ? issued - C::kSlots : 0; u < issued; ++u)
+        if (u != skip) w.drain(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1);
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -411,97 +542,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     w.drain(bar(C::kBarDrain), 0);
     __syncwarp();
   } else if (kF16 && warp >= 10) {
-    // ================================================================ V converters
-    // P V runs in fp16 (P rounded to 11 significant bits instead of bf16's 8), so each V tile,
-    // once landed, is rewritten in place as fp16(v * 2^-K) (same size and layout), half a tile
-    // per warp; the MMA warp waits for both halves before its P V product.  K is the CTA's:
-    // 0 whenever the first V tile's largest |v| lies in [2^-4, 65520) (fp16 then holds every
-    // value of that size exactly), else chosen so that it lands in [2^14, 2^15), in which case
-    // that tile is converted again from global memory; the epilogue multiplies O by 2^K.  A
-    // later tile too large for fp16 at that scale saturates at +-65504 * 2^K and sets
-    // FA_STATUS_V_RANGE (that call's O is not exact).  The two warps agree on each tile's
-    // largest magnitude through a bounded mbarrier exchange.
-    const int cw = warp - 10;
-    float* xmax = reinterpret_cast<float*>(smem + C::kOffXmax);   // [j & 1][warp]
-    int* kscale = reinterpret_cast<int*>(smem + C::kOffKScale);
-    constexpr int kGran = C::kTileBytes / 32;  // 16-byte granules per warp (half a tile)
-    int K = 0;
-    for (int j = 0; j < nmax; ++j) {
-      const int u = 2 * j + 1, slot = u % C::kSlots;
-      if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarFull + slot), (u / C::kSlots) & 1))) break;
-      const uint32_t tile = sbase + C::kOffRing + slot * C::kTileBytes;
-      const uint32_t half = tile + cw * (C::kTileBytes / 2);
-      float mx = 0.f;  // largest |v * 2^-K| of this warp's half
-      if (K == 0) {
-        // eight 16-byte loads in flight, then their conversions and stores
-#pragma unroll 1
-        for (int i0 = 0; i0 < kGran; i0 += 8 * 32) {
-          uint32_t x[8][4];
-#pragma unroll
-          for (int b = 0; b < 8; ++b)
-            ptx::ld_shared_v4(half + (i0 + b * 32 + lane) * 16, x[b][0], x[b][1], x[b][2], x[b][3]);
-#pragma unroll
-          for (int b = 0; b < 8; ++b) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float lo = __uint_as_float(x[b][e] << 16), hi = __uint_as_float(x[b][e] & 0xffff0000u);
-              mx = ptx::fmax3(mx, fabsf(lo), fabsf(hi));
-              x[b][e] = ptx::pack_f16x2_sat(lo, hi);
-            }
-            ptx::st_shared_v4(half + (i0 + b * 32 + lane) * 16, x[b][0], x[b][1], x[b][2], x[b][3]);
-          }
-        }
-      } else {
-        const float mul = exp2_int(-K);
-#pragma unroll 2
-        for (int i = lane; i < kGran; i += 32) {
-          uint32_t x[4];
-          ptx::ld_shared_v4(half + i * 16, x[0], x[1], x[2], x[3]);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float lo = __uint_as_float(x[e] << 16) * mul, hi = __uint_as_float(x[e] & 0xffff0000u) * mul;
-            mx = ptx::fmax3(mx, fabsf(lo), fabsf(hi));
-            x[e] = ptx::pack_f16x2_sat(lo, hi);
-          }
-          ptx::st_shared_v4(half + i * 16, x[0], x[1], x[2], x[3]);
-        }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-      if (lane == 0) xmax[(j & 1) * 2 + cw] = mx;
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(C::kBarXchg));
-      if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarXchg), j & 1))) break;
-      mx = fmaxf(xmax[(j & 1) * 2], xmax[(j & 1) * 2 + 1]);
-      const bool too_big = !(mx < 65520.f);  // beyond fp16 (saturated above), or inf
-      if (j == 0 && (too_big || (mx > 0.f && mx < 0.0625f))) {
-        // the CTA's scale: the first tile's largest |v| lands in [2^14, 2^15); that tile is
-        // converted again from global memory
-        K = min(max(ilog2_float(mx) - 14, -100), 100);
-        const float mul = exp2_int(-K);
-        const size_t row_base = static_cast<size_t>(bh) * p.Nk;
-        const int kv_row0 = lo0 * 128;
-        for (int i = lane; i < kGran; i += 32) {
-          const int q = cw * kGran + i;                                        // granule in shared memory
-          const int r = (q >> 3) & 127, c = q >> 10, g = (q & 7) ^ (r & 7);   // 128-byte swizzle
-          uint4 v4 = make_uint4(0u, 0u, 0u, 0u);                               // rows past Nk are zero
-          if (kv_row0 + r < p.Nk)
-            v4 = __ldg(reinterpret_cast<const uint4*>(p.v_raw + (row_base + kv_row0 + r) * D + c * 64 + g * 8));
-          uint32_t x[4] = {v4.x, v4.y, v4.z, v4.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            x[e] = ptx::pack_f16x2_sat(__uint_as_float(x[e] << 16) * mul, __uint_as_float(x[e] & 0xffff0000u) * mul);
-          ptx::st_shared_v4(tile + q * 16, x[0], x[1], x[2], x[3]);
-        }
-        if (!(mx < INFINITY) && cw == 0 && lane == 0) atomicOr(&g_status, FA_STATUS_V_RANGE);
-      } else if (too_big && cw == 0 && lane == 0) {
-        atomicOr(&g_status, FA_STATUS_V_RANGE);
-      }
-      if (j == 0 && cw == 0 && lane == 0) *kscale = K;
-      ptx::fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(C::kBarConv + j % C::kSlots));
-    }
+    // ================================================================ V converters (two of three)
+    if (nmax >= 1 && convert_first(warp - 9))
+      for (int j = 1; j < nmax; ++j)
+        if (!convert_share(j, warp - 9)) break;
   } else if (warp < 8) {
     // ================================================================ softmax warpgroups
     ptx::regs_increase<kSoftmaxRegs>();
@@ -719,13 +763,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (ok && p.n_splits == 1) {
       ptx::tc_fence_after();
 #pragma unroll 1
+      float2 nonfinite = make_float2(0.f, 0.f);  // fp16 P V: stays 0 unless some O~ value is inf or NaN
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t r[32];
         ptx::tmem_ld32(t_o + cc * 32, r);
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * inv_l, __uint_as_float(r[2 * i + 1]) * inv_l);
+        for (int i = 0; i < 16; ++i) {
+          const float2 x = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
+          if constexpr (kF16) nonfinite = __ffma2_rn(x, make_float2(0.f, 0.f), nonfinite);
+          pk[i] = ptx::pack_bf16x2(x.x * inv_l, x.y * inv_l);
+        }
         const uint32_t chunk_base = so + (cc >> 1) * C::kChunkBytes + row * 128;
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
@@ -735,6 +783,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (row_valid) p.lse[grow] = lse_row;
+      if (kF16 && __any_sync(0xffffffffu, row_valid && have && l_run < INFINITY &&
+                                               !(nonfinite.x == 0.f && nonfinite.y == 0.f)) && lane == 0)
+        atomicOr(&g_status, FA_STATUS_V_RANGE);  // a V tile fp16 could not hold at the CTA's scale
       ptx::fence_proxy_async_smem();
     } else if (ok && p.n_splits > 1) {
       ptx::tc_fence_after();

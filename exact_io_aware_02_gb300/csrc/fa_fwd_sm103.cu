@@ -790,10 +790,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (ok && p.n_splits > 1) {
       ptx::tc_fence_after();
       float4* dst = reinterpret_cast<float4*>(p.o_part + (static_cast<size_t>(my_split) * p.groups * p.R + grow) * D);
+      float2 nonfinite = make_float2(0.f, 0.f);  // fp16 P V: stays 0 unless some O~ value is inf or NaN
 #pragma unroll 1
       for (int cc = 0; cc < D / 32; ++cc) {
         uint32_t r[32];
         ptx::tmem_ld32(t_o + cc * 32, r);
+        if constexpr (kF16) {
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            nonfinite = __ffma2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                                   make_float2(0.f, 0.f), nonfinite);
+        }
         if (row_valid) {
 #pragma unroll
           for (int i = 0; i < 8; ++i)
@@ -802,6 +809,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (row_valid) p.lse_part[static_cast<size_t>(my_split) * p.groups * p.R + grow] = lse_row;
+      if (kF16 && __any_sync(0xffffffffu, row_valid && have && l_run < INFINITY &&
+                                               !(nonfinite.x == 0.f && nonfinite.y == 0.f)) && lane == 0)
+        atomicOr(&g_status, FA_STATUS_V_RANGE);  // a V tile fp16 could not hold at the CTA's scale
     } else if (tile_exists && nt == 0 && row_valid) {
       // no K/V tile of this split is visible to the tile: the empty result
       if (p.n_splits == 1) {

@@ -135,3 +135,20 @@ def test_gqa_workload_full_size_sampled(fa, name):
 
 def test_status_word_clean_after_gqa(fa):
     assert fa.fa_status(clear=False) == 0
+
+
+def test_split_kv_v_beyond_fp16_is_flagged(fa):
+    """Split-K/V with several query tiles runs the fp16 P V instance and writes fp32 partials:
+    a V tile fp16 cannot hold at the CTA's scale is flagged there too (FA_STATUS_V_RANGE), and
+    ordinary V on the same shape is exact and clean."""
+    q, k, v = make_qkv_gqa(1, 4, 2, 300, 1024, 128, seed=3301)
+    scale = 1.0 / math.sqrt(128)
+    fa.fa_status(clear=True)
+    o, lse = run(fa, q, k, v, scale, False, 3)
+    assert within_tolerance(check(q, k, v, o, lse, scale, False))
+    assert fa.fa_status(clear=True) == 0
+    vf = v.float()
+    vf[:, :, 640:768, :] *= 2.0 ** 20          # a K/V tile of the second split
+    o, lse = run(fa, q, k, vf.to(torch.bfloat16), scale, False, 3)
+    assert torch.isfinite(lse).all()
+    assert fa.fa_status(clear=True) & fa.FA_STATUS_V_RANGE

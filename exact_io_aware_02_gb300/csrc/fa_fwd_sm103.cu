@@ -12,30 +12,38 @@
 // shared memory while the math warps consume it, and softmax work overlaps
 // the tensor-core work.
 //
-// GB300 design (one CTA per SM, 384 threads in three warpgroups):
-//   * two 128-row query tiles per CTA (Q_0, Q_1) share every K/V tile that is
-//     loaded, halving K/V traffic per flop;
-//   * warps 8-11 give registers to warps 0-7 (setmaxnreg); warps 10, 11 idle;
-//   * warp 8  -- TMA producer: Q_0, Q_1 once, then K_0, V_0, K_1, V_1, ... into one
-//                shared-memory ring gated by full/empty mbarriers (the MMA warp
-//                consumes and releases the tiles in that order);
+// GB300 design (one persistent CTA per SM, 384 threads in three warpgroups):
+//   * a work item is a pair of 128-row query tiles (Q_0, Q_1) of one group over one
+//     K/V split; both tiles share every K/V tile that is loaded, halving K/V traffic
+//     per flop.  The grid holds one CTA per item; a running CTA takes over CTAs that
+//     have not started yet (cluster launch control) and does their items itself, so the
+//     SMs pick items up in order as they free, and an item's start and end overlap its
+//     neighbours' work instead of costing a CTA launch, set-up and drain each;
+//   * warps 8-11 give registers to warps 0-7 (setmaxnreg);
+//   * warp 8  -- TMA producer and scheduler: per item Q_0, Q_1 (each once the previous
+//                item's last S product of that slot has read its buffer), then K_0, V_0,
+//                K_1, V_1, ... into one shared-memory ring gated by landed/released
+//                mbarriers, continued from item to item; it asks for the next item a few
+//                steps before the end of the current one and publishes it to the others;
 //   * warp 9  -- MMA issuer (one thread): S_t = Q_t K_j^T with tcgen05.mma
 //                (A and B from shared memory, fp32 accumulator in tensor memory),
 //                then O_t += P_t V_j with P_t read from tensor memory; P_t is handed
 //                over through a hardware named barrier per tile (bar.arrive by the
-//                tile's softmax warps, bar.sync by this warp);
+//                tile's softmax warps, bar.sync by this warp).  The next item's S
+//                products start right after the current item's last P V products;
+//   * warps 8, 10, 11 -- convert each landed V tile to fp16 in place for the P V product;
 //   * warps 0-3 / 4-7 -- softmax for tile 0 / tile 1, one row per thread:
 //                row max, exp2 with scale*log2(e) folded in, running (m, l),
-//                bf16 P written back into tensor memory over S_t, and the
+//                fp16 P written back into tensor memory over S_t, and the
 //                correction O_t *= r, which only runs when some row's max grew
 //                by more than 2^8 (the rescale is exact for any reference m,
-//                because l and O~ share it); epilogue O = O~/l -> bf16 ->
-//                shared memory -> TMA store, LSE = m*scale + ln l.
+//                because l and O~ share it); epilogue O = O~/l -> bf16 -> a ring
+//                slot -> TMA store, LSE = m*scale + ln l.
 //   * causal: query tile i visits K/V tiles 0..i only; the mask is applied on
-//     the diagonal tile (and on a ragged last tile) only; CTAs are scheduled
+//     the diagonal tile (and on a ragged last tile) only; items are numbered
 //     longest first.
 // Tensor memory (512 columns): S_0 [0,128), S_1 [128,256), O_0 and O_1 after
-// that (d columns each).  P_t overwrites the first 64 columns of S_t (bf16 pairs).
+// that (d columns each).  P_t overwrites the first 64 columns of S_t (16-bit pairs).
 //
 // Also here: split-K/V (FlashDecoding) with fa_combine_kernel, launched as a programmatic
 // dependent of the split kernel; the decode instance fa_fwd_kernel<D, true>, whose CTA runs
@@ -71,32 +79,53 @@ struct Cfg {
   static constexpr int kChunks = D / 64;           // 128-byte swizzle atoms along d
   static constexpr int kChunkBytes = 128 * 128;    // 128 rows x 64 bf16
   static constexpr int kTileBytes = 128 * D * 2;   // one 128-row tile of Q, K, V or O
-  // One ring of K/V tiles in the order the MMA warp consumes and releases them:
-  // K_0, V_0, K_1, V_1, ...  (tile u is K_{u/2} for even u, V_{u/2} for odd u)
+  // One ring of tiles, continued from one work item to the next: an item's K_0, V_0, K_1, V_1,
+  // ... in the order the MMA warp consumes and releases them (its tile u is K_{u/2} for even u,
+  // V_{u/2} for odd u), then, with one split, a staging slot for the epilogue of each of its
+  // query tiles that has K/V tiles to visit (O is written there and stored by TMA; the epilogue
+  // releases the slot).  A
+  // CTA's ring tile g (counted over all its items) sits in slot g % kSlots.  V tiles are
+  // numbered J over all items for their conversion barriers.
   static constexpr int kSlots = D == 128 ? 5 : 12;
-  static constexpr int kOffQ = 0;                  // Q_0, Q_1 (reused for the O staging)
+  static constexpr int kOffQ = 0;                  // Q_0, Q_1
   static constexpr int kOffRing = 2 * kTileBytes;
   static constexpr int kOffBar = kOffRing + kSlots * kTileBytes;
-  static constexpr int kBarQ = 0;
-  static constexpr int kBarFull = 1;
-  static constexpr int kBarEmpty = kBarFull + kSlots;
-  static constexpr int kBarSFull = kBarEmpty + kSlots;  // one per query tile
+  static constexpr int kBarQFull = 0;                   // one per query tile slot
+  static constexpr int kBarQEmpty = 2;                  // one per slot: its item's last S is complete
+  // Landed tiles: with one query tile per slot, K tile i (counted over the CTA's items) on
+  // kBarFull + i % kSlots and V tile i on kBarVFull + i % kSlots, so that each barrier's phases
+  // are waited for in order by the warps that use them; the decode instance's ring on kBarFull
+  // by ring position.
+  static constexpr int kBarFull = 4;
+  static constexpr int kBarEmpty = kBarFull + kSlots;   // per ring slot: its tile released
+  static constexpr int kBarVFull = kBarEmpty + kSlots;
+  static constexpr int kBarSFull = kBarVFull + kSlots;  // one per query tile slot
   static constexpr int kBarOFinal = kBarSFull + 2;
-  static constexpr int kBarDrain = kBarOFinal + 2;
-  static constexpr int kBarConv = kBarDrain + 1;   // V_j converted to fp16: j % kSlots
-  static constexpr int kBarXchg = kBarConv + kSlots;  // the two converter warps' tile maxima
-  static constexpr int kNumBars = kBarXchg + 1;
-  // misc: tmem base (4 B), abort flag (4 B), the two converters' maxima of the first V tile
-  // (8 B, 16 reserved), the CTA's fp16 scale exponent K for V (4 B)
-  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kOffXmax = kOffMisc + 8;
-  static constexpr int kOffKScale = kOffMisc + 24;
-  static constexpr int kSmemBytes = kOffKScale + 16 + 1024;  // + slack for 1024-B alignment
+  static constexpr int kBarOEmpty = kBarOFinal + 2;     // one per slot: its four softmax warps have read O out
+  static constexpr int kBarDrain = kBarOEmpty + 2;
+  static constexpr int kBarConv = kBarDrain + 1;        // V tile J converted to fp16: J % kSlots
+  static constexpr int kBarXchg = kBarConv + kSlots;    // the two converter warps' tile maxima
+  static constexpr int kBarItemFull = kBarXchg + 1;     // the next work item published: 2 entries
+  static constexpr int kBarItemEmpty = kBarItemFull + 2;
+  static constexpr int kBarClc = kBarItemEmpty + 2;     // a take-over request answered
+  static constexpr int kNumBars = kBarClc + 1;
+  // misc, 16-byte aligned: tmem base (4 B), abort flag (4 B), two published work items (8 B),
+  // the 16-byte take-over response, the converters' first-tile maxima (two items x two warps),
+  // the fp16 scale exponent K of V per conversion slot
+  static constexpr int kOffMisc = (kOffBar + kNumBars * 8 + 15) / 16 * 16;
+  static constexpr int kOffItems = kOffMisc + 8;
+  static constexpr int kOffClc = kOffMisc + 16;
+  static constexpr int kOffXmax = kOffMisc + 32;
+  static constexpr int kOffKScale = kOffMisc + 48;
+  // each softmax warp's per-item bookkeeping, parked here during the K/V steps (8 x 8 ints)
+  static constexpr int kOffPark = (kOffKScale + 4 * kSlots + 15) / 16 * 16;
+  static constexpr int kSmemBytes = kOffPark + 256 + 1024;  // + slack for 1024-B alignment
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS = 0;    // S_t at t*128
   static constexpr uint32_t kColO = 256;  // O_t at 256 + t*D
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
+
 
 // A "group" is the set of query rows that share one K/V head: the G = Hq / Hkv query
 // heads of that K/V head, Nq rows each, contiguous in [B, Hq, Nq, d] (R = G * Nq rows).
@@ -119,7 +148,6 @@ struct Params {
   float scale;
   float scale_log2;  // scale * log2(e)
   int causal;
-  int withhold_v0;   // test hook: never load V tile 0 (0 in every normal launch)
   unsigned long long timeout_ns;
   int withhold_tile;  // test hook instance only: this ring tile (K_0 = 0, V_0 = 1, ...) is never loaded
   const uint16_t* v_raw;  // V [groups, Nk, D] bf16: read directly only to re-convert a tile at a new scale
@@ -165,22 +193,93 @@ __device__ __forceinline__ int causal_tile_limit(const Params& p, int qt) {
   return max_pos < 0 ? 0 : max_pos / 128 + 1;
 }
 
-// kDual: one query tile per group and n_splits > 1 (decoding).  The CTA's two tile slots then
+// K/V tiles [lo, lo + n) a query tile visits in the split starting at tile lo; causal tiles end
+// at the last key any of its rows may see.
+__device__ __forceinline__ int tiles_visible(const Params& p, int qt, int lo) {
+  const int hi0 = min(lo + p.split_tiles, p.n_kv_tiles);
+  const int hi = p.causal ? min(hi0, causal_tile_limit(p, qt)) : hi0;
+  return hi > lo ? hi - lo : 0;
+}
+
+// One work item: a group's pair of query tiles over one K/V split (the CTA's tile slots 0 and
+// 1).  kDual: one query tile per group and n_splits > 1 (decoding); the two tile slots then
 // take the same query rows over splits 2c and 2c+1: two independent softmax/product chains
 // per SM, each with its own K/V tiles in the ring.
+struct Item {
+  int bh;              // group (batch x K/V head)
+  int qt0, qt1;        // query tile of each slot
+  int split, split1;   // K/V split of each slot
+  int lo0, lo1;        // first K/V tile of each slot's split
+  int n0, n1;          // K/V tiles each slot visits
+  int nmax;
+  bool has1;           // slot 1 holds a query tile
+};
+
+// Items are numbered longest first for causal attention with one split (the last query tiles
+// see the most K/V tiles), otherwise group-major (the items of one K/V head run together and
+// share its K and V in L2).  CTA b starts with item b and takes further items over from CTAs
+// not yet started, so the SMs pick items up in this order as they free, as the hardware's own
+// CTA scheduler would.
+template <bool kDual>
+__device__ __forceinline__ Item decode_item(const Params& p, int bid) {
+  Item it;
+  int split = 0, split1 = 0;
+  if constexpr (kDual) {
+    const int pairs = (p.n_splits + 1) / 2;
+    split = 2 * (bid % pairs);
+    split1 = split + 1;
+    it.bh = bid / pairs;
+    it.qt0 = it.qt1 = 0;
+    it.has1 = split1 < p.n_splits;
+  } else {
+    int cta_q;
+    if (p.n_splits == 1 && p.causal) {
+      cta_q = p.n_cta_q - 1 - bid / p.groups;
+      it.bh = bid % p.groups;
+    } else {
+      split = bid % p.n_splits;
+      const int b = bid / p.n_splits;
+      it.bh = b / p.n_cta_q;
+      cta_q = b % p.n_cta_q;
+    }
+    split1 = split;
+    it.qt0 = 2 * cta_q;
+    it.qt1 = it.qt0 + 1;
+    it.has1 = it.qt1 < p.n_qtiles;
+  }
+  it.split = split;
+  it.split1 = split1;
+  it.lo0 = split * p.split_tiles;
+  it.lo1 = split1 * p.split_tiles;
+  it.n0 = tiles_visible(p, it.qt0, it.lo0);
+  it.n1 = it.has1 ? tiles_visible(p, it.qt1, it.lo1) : 0;
+  it.nmax = max(it.n0, it.n1);
+  return it;
+}
+
+// A persistent CTA per SM: the grid holds one CTA per work item, and each running CTA takes
+// over not-yet-started CTAs (cluster launch control) and does their items itself.  Across
+// items every role keeps its place in the shared pipelines: the producer loads the next item's
+// Q tiles as soon as the current item's last S products have read them and carries the K/V
+// ring on, and the MMA warp starts the next item's S products right after the current item's
+// last P V products, while the softmax warps are still in the epilogue.  The next item's first
+// P V product (which overwrites O) waits until all eight softmax warps have read O out.
 template <int D, bool kDual, bool kHook = false>
 __global__ void __launch_bounds__(kThreads, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                   const Params p) {
   using C = Cfg<D>;
-  constexpr bool kF16 = !kDual;  // P V in fp16: V tiles converted in shared memory by warps 10, 11
+  constexpr bool kF16 = !kDual;  // P V in fp16: V tiles converted in shared memory
+  constexpr int kReaders = kF16 ? 11 : 9;  // warps that read each published item: MMA, softmax, converters
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = ptx::smem_addr(smem);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
+  volatile int* items = reinterpret_cast<volatile int*>(smem + C::kOffItems);
+  volatile int* kscale = reinterpret_cast<volatile int*>(smem + C::kOffKScale);  // per conversion slot
   auto bar = [&](int i) -> uint32_t { return sbase + C::kOffBar + 8u * i; };
 
   const int warp = threadIdx.x >> 5;
@@ -188,51 +287,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the split combine (if any) may be scheduled now; it waits for this grid to complete
   ptx::griddep_launch_dependents();
 
-  // ---- which (group, query-tile pair, K/V split) this CTA owns
-  int bid = blockIdx.x;
-  int bh, cta_q, split = 0;
-  if constexpr (kDual) {
-    const int pairs = (p.n_splits + 1) / 2;
-    split = 2 * (bid % pairs);
-    bh = bid / pairs;
-    cta_q = 0;
-  } else if (p.n_splits == 1 && p.causal) {  // longest first: the last query tiles have the most K/V tiles
-    cta_q = p.n_cta_q - 1 - bid / p.groups;
-    bh = bid % p.groups;
-  } else {  // group-major: CTAs of one K/V head run together and share K/V in L2
-    split = bid % p.n_splits;
-    bid /= p.n_splits;
-    bh = bid / p.n_cta_q;
-    cta_q = bid % p.n_cta_q;
-  }
-  const int qt0 = kDual ? 0 : 2 * cta_q;
-  const int qt1 = kDual ? 0 : qt0 + 1;
-  const bool has1 = kDual ? split + 1 < p.n_splits : qt1 < p.n_qtiles;
-  // K/V tiles [lo_t, hi_t) of tile slot t's split; causal tiles end at the last visible key
-  const int split1 = kDual ? split + 1 : split;
-  const int lo0 = split * p.split_tiles, lo1 = split1 * p.split_tiles;
-  auto tiles_for = [&](int qt, int lo) {
-    const int hi0 = min(lo + p.split_tiles, p.n_kv_tiles);
-    const int hi = p.causal ? min(hi0, causal_tile_limit(p, qt)) : hi0;
-    return hi > lo ? hi - lo : 0;
-  };
-  const int n0 = tiles_for(qt0, lo0);  // K/V tiles visited by tile slot 0
-  const int n1 = has1 ? tiles_for(qt1, lo1) : 0;
-  const int nmax = n0 > n1 ? n0 : n1;
-
   if (warp == 8 && lane == 0) {
-    ptx::mbar_init(bar(C::kBarQ), 1);
-    for (int s = 0; s < C::kSlots; ++s) {
-      ptx::mbar_init(bar(C::kBarFull + s), 1);
-      ptx::mbar_init(bar(C::kBarEmpty + s), 1);
-    }
     for (int t = 0; t < 2; ++t) {
+      ptx::mbar_init(bar(C::kBarQFull + t), 1);
+      ptx::mbar_init(bar(C::kBarQEmpty + t), 1);
       ptx::mbar_init(bar(C::kBarSFull + t), 1);
       ptx::mbar_init(bar(C::kBarOFinal + t), 1);
+      ptx::mbar_init(bar(C::kBarItemFull + t), 1);
+      ptx::mbar_init(bar(C::kBarItemEmpty + t), kReaders);
+      ptx::mbar_init(bar(C::kBarOEmpty + t), 4);
+    }
+    for (int s = 0; s < C::kSlots; ++s) {
+      ptx::mbar_init(bar(C::kBarFull + s), 1);
+      ptx::mbar_init(bar(C::kBarVFull + s), 1);
+      ptx::mbar_init(bar(C::kBarEmpty + s), 1);
+      ptx::mbar_init(bar(C::kBarConv + s), 3);
     }
     ptx::mbar_init(bar(C::kBarDrain), 1);
-    for (int s = 0; s < C::kSlots; ++s) ptx::mbar_init(bar(C::kBarConv + s), 3);
     ptx::mbar_init(bar(C::kBarXchg), 2);
+    ptx::mbar_init(bar(C::kBarClc), 1);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
   }
@@ -246,40 +319,61 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const Waiter w{abort_flag, p.timeout_ns};
 
+  // The item after this CTA's item k, as the producer published it: its number, -1 when there
+  // is none, -2 when the wait failed.
+  auto next_item = [&](const int k) -> int {
+    if constexpr (kDual) return -1;
+    const int e = k & 1;
+    if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarItemFull + e), (k >> 1) & 1))) return -2;
+    const int v = items[e];
+    __syncwarp();
+    if (lane == 0) ptx::mbar_arrive(bar(C::kBarItemEmpty + e));
+    return v;
+  };
+
   // ---- V conversion for the fp16 P V product.  Each landed V tile is rewritten in place as
   // fp16(v * 2^-K), same size and layout; the MMA warp waits for the tile's conversion barrier,
-  // which counts three arrivals.  The first tile is converted by warps 10 and 11 in halves
-  // (the producer arrives without work); every later tile by three warps on three SM
+  // which counts three arrivals.  An item's first V tile is converted by warps 10 and 11 in
+  // halves (the producer arrives without work); every later tile by three warps on three SM
   // sub-partitions: the producer (warp 8) a quarter, converting V_{j-1} right after it has
-  // issued V_j's copy, warps 10 and 11 three eighths each.  K is the CTA's: 0 whenever the first
-  // V tile's largest |v| lies in [2^-4, 65520) (fp16 then holds every value of that size
+  // issued V_j's copy, warps 10 and 11 three eighths each.  K is the item's: 0 whenever its
+  // first V tile's largest |v| lies in [2^-4, 65520) (fp16 then holds every value of that size
   // exactly), else chosen so that it lands in [2^14, 2^15), that tile then converted again from
   // global memory; the epilogue multiplies O by 2^K.  Only the first tile is measured.  A later
   // tile too large for fp16 at that scale turns into infinities, which reach every row of the
-  // CTA's O (p * inf, or 0 * inf for a masked key); the epilogue then sets FA_STATUS_V_RANGE:
-  // flagged, never silent.
+  // item's O (p * inf, or 0 * inf for a masked key); the epilogue then sets FA_STATUS_V_RANGE:
+  // flagged, never silent.  Each converted tile's K is also left in its conversion slot, where
+  // the epilogue reads it after waiting for the item's last tile.
   constexpr int kGranT = C::kTileBytes / 16;  // 16-byte granules per tile
-  int v_scale = 0;                            // K, as each converter knows it
-  // the first V tile: warps 10 and 11 (parts 1, 2), a half each, measured
-  auto convert_first = [&](const int part) -> bool {
-    if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarFull + 1 % C::kSlots), 0))) return false;
-    const uint32_t tile = sbase + C::kOffRing + (1 % C::kSlots) * C::kTileBytes;
+  int v_scale = 0;                            // K of the current item, as each converter knows it
+  // an item's first V tile (the CTA's V tile J0, ring tile g): warps 10 and 11 (parts 1, 2), a
+  // half each, measured; xk counts the items measured before (maxima exchange phase and buffer)
+  // V tile J (counted over the CTA's items) has landed: its barrier's earlier phases were each
+  // waited for by these warps (or, for the producer, passed before the tile was issued)
+  auto wait_v = [&](const int J) -> bool {
+    return __all_sync(0xffffffffu, w.wait(bar(C::kBarVFull + J % C::kSlots), (J / C::kSlots) & 1));
+  };
+  auto convert_first = [&](const int J0, const int g, const int part, const int xk, const int bh,
+                           const int kv_row0) -> bool {
+    const int slot = g % C::kSlots;
+    if (!wait_v(J0)) return false;
+    const uint32_t tile = sbase + C::kOffRing + slot * C::kTileBytes;
     {
       const int g0 = (part - 1) * (kGranT / 2);
       float mx = convert_granules<kGranT / 64, 8, true>(tile, g0, lane);
-      float* xmax = reinterpret_cast<float*>(smem + C::kOffXmax);
+      volatile float* xmax = reinterpret_cast<volatile float*>(smem + C::kOffXmax) + 2 * (xk & 1);
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       if (lane == 0) xmax[part - 1] = mx;
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(C::kBarXchg));
-      if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarXchg), 0))) return false;
+      if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarXchg), xk & 1))) return false;
       mx = fmaxf(xmax[0], xmax[1]);
+      v_scale = 0;
       if (!(mx < 65520.f) || (mx > 0.f && mx < 0.0625f)) {
         v_scale = min(max(ilog2_float(mx) - 14, -100), 100);
         const float mul = exp2_int(-v_scale);
         const size_t row_base = static_cast<size_t>(bh) * p.Nk;
-        const int kv_row0 = lo0 * 128;
         for (int q = g0 + lane; q < g0 + kGranT / 2; q += 32) {
           const int r = (q >> 3) & 127, c = q >> 10, g = (q & 7) ^ (r & 7);   // 128-byte swizzle
           uint4 v4 = make_uint4(0u, 0u, 0u, 0u);                               // rows past Nk are zero
@@ -292,22 +386,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::st_shared_v4(tile + q * 16, y[0], y[1], y[2], y[3]);
         }
       }
-      if (part == 1 && lane == 0) *reinterpret_cast<int*>(smem + C::kOffKScale) = v_scale;
+      if (part == 1 && lane == 0) kscale[J0 % C::kSlots] = v_scale;
     }
     ptx::fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(bar(C::kBarConv));
+    if (lane == 0) ptx::mbar_arrive(bar(C::kBarConv + J0 % C::kSlots));
     return true;
   };
-  // a later V tile j: the producer (part 0) a quarter, warps 10 and 11 three eighths each
-  auto convert_share = [&](const int j, const int part) -> bool {
-    const int u = 2 * j + 1, slot = u % C::kSlots;
-    if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarFull + slot), (u / C::kSlots) & 1))) return false;
+  // a later V tile J (ring tile g): the producer (part 0) a quarter, warps 10 and 11 three
+  // eighths each
+  auto convert_share = [&](const int J, const int g, const int part) -> bool {
+    const int slot = g % C::kSlots;
+    if (!wait_v(J)) return false;
     const uint32_t tile = sbase + C::kOffRing + slot * C::kTileBytes;
     {
       const int g0 = part == 0 ? 0 : part == 1 ? kGranT / 4 : 5 * kGranT / 8;  // granules [g0, g1)
       const int g1 = part == 0 ? kGranT / 4 : part == 1 ? 5 * kGranT / 8 : kGranT;
-      if (v_scale != 0) {  // a scaled CTA (rare): each value times 2^-K on the way
+      if (v_scale != 0) {  // a scaled item (rare): each value times 2^-K on the way
         const float mul = exp2_int(-v_scale);
         for (int q = g0 + lane; q < g1; q += 32) {
           uint32_t x[4];
@@ -322,91 +417,194 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         convert_granules<3 * kGranT / 256, (3 * kGranT / 256) % 8 ? 4 : 8, false>(tile, g0, lane);
       }
+      if (part == 1 && lane == 0) kscale[J % C::kSlots] = v_scale;
     }
     ptx::fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) ptx::mbar_arrive(bar(C::kBarConv + j % C::kSlots));
+    if (lane == 0) ptx::mbar_arrive(bar(C::kBarConv + J % C::kSlots));
     return true;
   };
-  // the producer's scale: known once the first tile's conversion is done (before its first part)
-  auto producer_scale = [&]() -> bool {
-    if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarConv), 0))) return false;
-    v_scale = *reinterpret_cast<const int*>(smem + C::kOffKScale);
+  // the producer's K for the item whose first V tile is J0: known once that tile is converted
+  auto producer_scale = [&](const int J0) -> bool {
+    if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarConv + J0 % C::kSlots), (J0 / C::kSlots) & 1))) return false;
+    v_scale = kscale[J0 % C::kSlots];
     return true;
   };
 
   if (warp >= 8) ptx::regs_decrease<kOtherRegs>();
   if (warp == 8) {
-    // ================================================================ TMA producer
-    // Lane 0 issues the copies; the whole warp runs the ring loop, because with fp16 P V it
-    // also converts a third of each V tile (V_{j-1} right after V_j's copy is issued).
+    // ================================================================ TMA producer and scheduler
+    // Lane 0 issues the copies; the whole warp runs the loops, because with fp16 P V it also
+    // converts a quarter of each later V tile (V_{j-1} right after V_j's copy is issued).  Per
+    // item: the Q tiles (each after the previous item's last S product of that slot has read
+    // its buffer), then the item's ring tiles; a few steps before the end of the ring tiles it
+    // asks to take over a CTA not yet started, and after them it publishes that CTA's item
+    // (or the end) to the other warps.
     if (lane == 0) {
       ptx::prefetch_tensormap(&tm_q);
       ptx::prefetch_tensormap(&tm_k);
       ptx::prefetch_tensormap(&tm_v);
       ptx::prefetch_tensormap(&tm_o);
-      ptx::mbar_arrive_expect_tx(bar(C::kBarQ), (has1 ? 2 : 1) * C::kTileBytes);
-      for (int c = 0; c < C::kChunks; ++c)
-        ptx::tma_load_3d(sbase + C::kOffQ + c * C::kChunkBytes, &tm_q, bar(C::kBarQ), c * 64,
-                         qt0 * 128, bh);
-      if (has1)
-        for (int c = 0; c < C::kChunks; ++c)
-          ptx::tma_load_3d(sbase + C::kOffQ + C::kTileBytes + c * C::kChunkBytes, &tm_q,
-                           bar(C::kBarQ), c * 64, qt1 * 128, bh);
     }
-    const int n_tiles = kDual ? 0 : 2 * nmax;
-    if (kF16 && nmax >= 1 && lane == 0) ptx::mbar_arrive(bar(C::kBarConv));  // its part of V_0: none
-    // test hooks: tile 1 (V_0), or in the kHook instance the ring tile named, is never loaded
-    const int skip = kHook ? p.withhold_tile : (p.withhold_v0 ? 1 : -1);
-    int issued = 0;
+    const uint32_t clc_resp = sbase + C::kOffClc;
+    int idx = blockIdx.x;
+    int U = 0;                // ring tiles issued before the current item
+    int Vc = 0;               // V tiles of the items before the current one
+    const bool staged = !kDual && p.n_splits == 1;  // each item ends with two O staging slots
+    int qn[2] = {0, 0};       // Q tiles loaded per slot
+    int n_req = 0;            // take-over requests issued (one phase of kBarClc each)
+    bool more = !kDual;       // a request may still find a CTA not yet started
+    bool req_open = false;    // a request whose answer has not been read
+    int issued = 0;           // ring tiles issued (the decode instance's ring positions)
+    int n_k = 0, n_v = 0;     // K and V tiles issued
+    int withheld = -1;        // test hook: the first item's ring tile left out
     bool ok = true;
-    if constexpr (kDual) {
+    auto request = [&]() {
       if (lane == 0) {
-        // ring order = the MMA warp's order: per step j and slot t, V_t(j-1) then K_t(j)
-        auto load = [&](int kv_tile, bool is_v) -> bool {
-          const int u = issued, slot = u % C::kSlots, use = u / C::kSlots;
-          if (use > 0 && !w.wait(bar(C::kBarEmpty + slot), (use - 1) & 1)) return false;
-          ptx::mbar_arrive_expect_tx(bar(C::kBarFull + slot), C::kTileBytes);
-          for (int c = 0; c < C::kChunks; ++c)
-            ptx::tma_load_3d(sbase + C::kOffRing + slot * C::kTileBytes + c * C::kChunkBytes, is_v ? &tm_v : &tm_k,
-                             bar(C::kBarFull + slot), c * 64, kv_tile * 128, bh);
-          issued = u + 1;
-          return true;
-        };
-        for (int j = 0; ok && j <= nmax; ++j)
-          for (int t = 0; ok && t < 2; ++t) {
-            const int nt = t ? n1 : n0, lo = t ? lo1 : lo0;
-            if (j >= 1 && j - 1 < nt) ok = load(lo + j - 1, true);
-            if (ok && j < nt) ok = load(lo + j, false);
-          }
-      }
-    }
-    for (int u = 0; u < n_tiles; ++u) {
-      const int slot = u % C::kSlots, use = u / C::kSlots;
-      if (use > 0 && !__all_sync(0xffffffffu, w.wait(bar(C::kBarEmpty + slot), (use - 1) & 1))) { ok = false; break; }
-      if (lane == 0 && u != skip) {
-        ptx::mbar_arrive_expect_tx(bar(C::kBarFull + slot), C::kTileBytes);
-        const CUtensorMap* m = (u & 1) ? &tm_v : &tm_k;
-        for (int c = 0; c < C::kChunks; ++c)
-          ptx::tma_load_3d(sbase + C::kOffRing + slot * C::kTileBytes + c * C::kChunkBytes, m,
-                           bar(C::kBarFull + slot), c * 64, (lo0 + (u >> 1)) * 128, bh);
+        ptx::fence_proxy_async_smem();  // the previous answer has been read through the generic proxy
+        ptx::mbar_arrive_expect_tx(bar(C::kBarClc), 16);
+        ptx::clc_try_cancel(clc_resp, bar(C::kBarClc));
       }
       __syncwarp();
-      issued = u + 1;
-      // its quarter of V_{j-1}, right after issuing V_j (j >= 2: V_{j-1} has long landed)
-      if (kF16 && (u & 1) && u >= 5) {
-        if (u == 5 && !producer_scale()) { ok = false; break; }
-        if (!convert_share((u >> 1) - 1, 0)) { ok = false; break; }
+      ++n_req;
+      req_open = true;
+    };
+    for (int k = 0;; ++k) {
+      const Item it = decode_item<kDual>(p, idx);
+      const int n_tiles = kDual ? 0 : 2 * it.nmax;
+      const int u_req = n_tiles > 8 ? n_tiles - 8 : 0;  // ring tile before which to ask for the next item
+      if (more && n_tiles == 0) request();
+      if (it.nmax >= 1) {
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (!ok || (t ? it.n1 : it.n0) == 0) continue;
+          if (qn[t] > 0 && !__all_sync(0xffffffffu, w.wait(bar(C::kBarQEmpty + t), (qn[t] - 1) & 1))) {
+            ok = false;
+            continue;
+          }
+          if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bar(C::kBarQFull + t), C::kTileBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+              ptx::tma_load_3d(sbase + C::kOffQ + t * C::kTileBytes + c * C::kChunkBytes, &tm_q,
+                               bar(C::kBarQFull + t), c * 64, (t ? it.qt1 : it.qt0) * 128, it.bh);
+          }
+          __syncwarp();
+          ++qn[t];
+        }
+        if (!ok) break;
+        if constexpr (kDual) {
+          if (lane == 0) {
+            // ring order = the MMA warp's order: per step j and slot t, V_t(j-1) then K_t(j)
+            auto load = [&](int kv_tile, bool is_v) -> bool {
+              const int u = issued, slot = u % C::kSlots, use = u / C::kSlots;
+              if (use > 0 && !w.wait(bar(C::kBarEmpty + slot), (use - 1) & 1)) return false;
+              ptx::mbar_arrive_expect_tx(bar(C::kBarFull + slot), C::kTileBytes);
+              for (int c = 0; c < C::kChunks; ++c)
+                ptx::tma_load_3d(sbase + C::kOffRing + slot * C::kTileBytes + c * C::kChunkBytes,
+                                 is_v ? &tm_v : &tm_k, bar(C::kBarFull + slot), c * 64, kv_tile * 128, it.bh);
+              issued = u + 1;
+              return true;
+            };
+            for (int j = 0; ok && j <= it.nmax; ++j)
+              for (int t = 0; ok && t < 2; ++t) {
+                const int nt = t ? it.n1 : it.n0, lo = t ? it.lo1 : it.lo0;
+                if (j >= 1 && j - 1 < nt) ok = load(lo + j - 1, true);
+                if (ok && j < nt) ok = load(lo + j, false);
+              }
+          }
+          ok = __all_sync(0xffffffffu, ok);
+          issued = __shfl_sync(0xffffffffu, issued, 0);
+          if (!ok) break;
+        }
+        const int J0 = Vc;  // the item's first V tile
+        for (int u = 0; u < n_tiles; ++u) {
+          if (more && u == u_req) request();
+          const int g = U + u, slot = g % C::kSlots, use = g / C::kSlots;
+          if (use > 0 && !__all_sync(0xffffffffu, w.wait(bar(C::kBarEmpty + slot), (use - 1) & 1))) {
+            ok = false;
+            break;
+          }
+          const bool withhold = kHook && k == 0 && u == p.withhold_tile;
+          const int ti = Vc + (u >> 1);  // the CTA's K (even u) or V (odd u) tile number
+          const uint32_t full = bar(((u & 1) ? C::kBarVFull : C::kBarFull) + ti % C::kSlots);
+          if (lane == 0 && !withhold) {
+            ptx::mbar_arrive_expect_tx(full, C::kTileBytes);
+            const CUtensorMap* m = (u & 1) ? &tm_v : &tm_k;
+            for (int c = 0; c < C::kChunks; ++c)
+              ptx::tma_load_3d(sbase + C::kOffRing + slot * C::kTileBytes + c * C::kChunkBytes, m, full, c * 64,
+                               (it.lo0 + (u >> 1)) * 128, it.bh);
+          }
+          if (withhold) withheld = u;  // (first item: K or V tile u / 2)
+          __syncwarp();
+          issued = g + 1;
+          if (u & 1) n_v = ti + 1;
+          else n_k = ti + 1;
+          // its part of the item's first V tile: none.  Arriving only now, after this slot's
+          // previous tile was released, keeps the arrival out of the conversion barrier's
+          // previous phase (V tile J0 - kSlots, converted before that release).
+          if (kF16 && u == 1 && lane == 0) ptx::mbar_arrive(bar(C::kBarConv + J0 % C::kSlots));
+          // its quarter of V_{j-1}, right after issuing V_j (j >= 2: V_{j-1} has long landed)
+          if (kF16 && (u & 1) && u >= 5) {
+            if (u == 5 && !producer_scale(J0)) {
+              ok = false;
+              break;
+            }
+            if (!convert_share(J0 + (u >> 1) - 1, U + u - 2, 0)) {
+              ok = false;
+              break;
+            }
+          }
+        }
+        if (kF16 && ok && it.nmax >= 2) {
+          if (it.nmax == 2) ok = producer_scale(J0);
+          if (ok) ok = convert_share(J0 + it.nmax - 1, U + n_tiles - 1, 0);
+        }
+        // the staging slots: nothing to load; each epilogue waits for its slot's previous tile
+        // to be released, and releases the slot itself
+        const int n_stage = staged ? (it.n0 > 0) + (it.n1 > 0) : 0;
+        if (!ok) break;
+        U += n_tiles + n_stage;
+        Vc += it.nmax;
       }
-    }
-    if (kF16 && ok && nmax >= 2) {
-      if (nmax == 2) ok = producer_scale();
-      if (ok) ok = convert_share(nmax - 1, 0);
+      if (kDual) break;
+      // the item after this one: the CTA this item's request took over, if any
+      int next = -1;
+      if (req_open) {
+        if (!__all_sync(0xffffffffu, w.wait(bar(C::kBarClc), (n_req - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        req_open = false;
+        more = ptx::clc_query(clc_resp, &next);
+        if (!more) next = -1;
+      }
+      // publish it in entry k & 1, once every reader has taken that entry's previous item
+      if (k >= 2 && !__all_sync(0xffffffffu, w.wait(bar(C::kBarItemEmpty + (k & 1)), ((k >> 1) - 1) & 1))) {
+        ok = false;
+        break;
+      }
+      if (lane == 0) {
+        items[k & 1] = next;
+        ptx::mbar_arrive(bar(C::kBarItemFull + (k & 1)));
+      }
+      __syncwarp();
+      if (next < 0) break;
+      idx = next;
     }
     if (!ok && lane == 0) {  // let every copy already issued land before the CTA's memory is released
-      w.drain(bar(C::kBarQ), 0);
-      for (int u = issued - C::kSlots > 0 ? issued - C::kSlots : 0; u < issued; ++u)
-        if (u != skip) w.drain(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+        if (qn[t] > 0) w.drain(bar(C::kBarQFull + t), (qn[t] - 1) & 1);
+      if constexpr (kDual) {
+        for (int g = issued - C::kSlots > 0 ? issued - C::kSlots : 0; g < issued; ++g)
+          w.drain(bar(C::kBarFull + g % C::kSlots), (g / C::kSlots) & 1);
+      } else {
+        for (int i = n_k - C::kSlots > 0 ? n_k - C::kSlots : 0; i < n_k; ++i)
+          if (withheld != 2 * i) w.drain(bar(C::kBarFull + i % C::kSlots), (i / C::kSlots) & 1);
+        for (int i = n_v - C::kSlots > 0 ? n_v - C::kSlots : 0; i < n_v; ++i)
+          if (withheld != 2 * i + 1) w.drain(bar(C::kBarVFull + i % C::kSlots), (i / C::kSlots) & 1);
+      }
+      if (req_open) w.drain(bar(C::kBarClc), (n_req - 1) & 1);
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -416,125 +614,189 @@ __global__ void __launch_bounds__(kThreads, 1)
     // along a tile is a constant added to the 16-byte-unit address field.
     constexpr uint32_t kIdescQK = ptx::idesc_bf16_f32(128, 128, false);
     constexpr uint32_t kIdescPV = kF16 ? ptx::idesc_f16_f32(128, D, true) : ptx::idesc_bf16_f32(128, D, true);
-    constexpr uint64_t kSlotStep = C::kTileBytes >> 4;
-    const uint64_t desc_q0 = ptx::smem_desc_sw128(sbase + C::kOffQ, 16, 1024);
-    const uint64_t desc_q1 = desc_q0 + kSlotStep;
-    const uint64_t desc_k_ring = ptx::smem_desc_sw128(sbase + C::kOffRing, 16, 1024);
+    // Descriptors are kept as their low 32 bits (address and leading offset); the high half is
+    // the same constant for Q, K and V (stride 1024 B, 128-byte swizzle) and joins at the MMA.
+    constexpr uint32_t kSlotStep = C::kTileBytes >> 4;
+    constexpr uint32_t kDescHi32 = ptx::desc_sw128_hi(1024);
+    constexpr uint64_t kDescHi = static_cast<uint64_t>(kDescHi32) << 32;
+    const uint32_t desc_q0 = ptx::desc_sw128_lo(sbase + C::kOffQ, 16);
+    const uint32_t desc_q1 = desc_q0 + kSlotStep;
+    const uint32_t desc_k_ring = ptx::desc_sw128_lo(sbase + C::kOffRing, 16);
     // V: N-contiguous; next 64 d-columns at +16 KB (LBO), next 8 keys at +1 KB (SBO)
-    const uint64_t desc_v_ring = ptx::smem_desc_sw128(sbase + C::kOffRing, C::kChunkBytes, 1024);
-    bool ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarQ), 0));
-    ptx::tc_fence_after();
-    if constexpr (kDual) {
-      // each tile slot has K/V tiles of its own, consumed (and released) in ring order
-      int u = 0;
-      for (int j = 0; ok && j <= nmax; ++j) {
+    const uint32_t desc_v_ring = ptx::desc_sw128_lo(sbase + C::kOffRing, C::kChunkBytes);
+    int idx = blockIdx.x;
+    int U = 0;            // ring tiles of the items before the current one
+    int Vc = 0;           // V tiles of the items before the current one
+    const bool staged = !kDual && p.n_splits == 1;
+    // barrier parities and flags, one bit each: bit t the next Q-full phase of slot t, bit 2 + t
+    // the next O-empty phase of slot t, bit 4 + t set while slot t's O of an earlier item has
+    // not been waited for (every earlier epilogue ends before the next item's first P V product)
+    uint32_t ph = 0;
+    bool ok = true;
+    for (int k = 0;; ++k) {
+      const Item it = decode_item<kDual>(p, idx);
+      if (it.nmax >= 1) {
+        if constexpr (kDual) {
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          const int nt = t ? n1 : n0;
-          if (j >= 1 && j - 1 < nt) {
-            ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1));
-            if (!ok) break;
-            ptx::named_barrier(3 + t, 160);  // P_t(j-1) handed over (see the non-dual loop)
-            ptx::tc_fence_after();
-            const uint64_t dv = desc_v_ring + static_cast<uint64_t>(u % C::kSlots) * kSlotStep;
-            const uint32_t t_o = tmem + C::kColO + t * D;
-            const uint32_t t_p = tmem + C::kColS + t * 128;
-            if (ptx::elect_one()) {
-              if (j > 1) ptx::mma_ts_i<1>(t_o, t_p, dv, kIdescPV);
-              else ptx::mma_ts_i<0>(t_o, t_p, dv, kIdescPV);
-#pragma unroll
-              for (int kk = 1; kk < 8; ++kk) ptx::mma_ts_i<1>(t_o, t_p + kk * 8, dv + kk * 128, kIdescPV);
-              if (j - 1 == nt - 1) ptx::tc_commit(bar(C::kBarOFinal + t));
-              ptx::tc_commit(bar(C::kBarEmpty + u % C::kSlots));
-            }
-            __syncwarp();
-            ++u;
-          }
-          if (j < nt) {
-            ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1));
-            if (!ok) break;
-            ptx::tc_fence_after();
-            const uint64_t dk = desc_k_ring + static_cast<uint64_t>(u % C::kSlots) * kSlotStep;
-            const uint32_t t_s = tmem + C::kColS + t * 128;
-            const uint64_t dq = t ? desc_q1 : desc_q0;
-            if (ptx::elect_one()) {
-              ptx::mma_ss_i<0>(t_s, dq, dk, kIdescQK);
-#pragma unroll
-              for (int kk = 1; kk < D / 16; ++kk) {
-                const uint64_t o = (kk >> 2) * (C::kChunkBytes >> 4) + (kk & 3) * 2;
-                ptx::mma_ss_i<1>(t_s, dq + o, dk + o, kIdescQK);
-              }
-              ptx::tc_commit(bar(C::kBarSFull + t));
-              ptx::tc_commit(bar(C::kBarEmpty + u % C::kSlots));
-            }
-            __syncwarp();
-            ++u;
-          }
-        }
-      }
-    }
-    for (int j = 0; ok && !kDual && j <= nmax; ++j) {
-      const int uk = 2 * j, uv = 2 * j - 1;  // ring tiles K_j and V_{j-1}
-      // V_{j-1} converted to fp16 in its ring slot (the converter waited for it to land)
-      if (j >= 1)
-        ok = __all_sync(0xffffffffu, kF16 ? w.wait(bar(C::kBarConv + (j - 1) % C::kSlots), ((j - 1) / C::kSlots) & 1)
-                                          : w.wait(bar(C::kBarFull + uv % C::kSlots), (uv / C::kSlots) & 1));
-      if (!ok) break;
-      bool k_ready = false;  // K_j is waited for only right before its first use
-      const uint64_t dk = desc_k_ring + static_cast<uint64_t>(uk % C::kSlots) * kSlotStep;
-      const uint64_t dv = desc_v_ring + static_cast<uint64_t>((uv + C::kSlots) % C::kSlots) * kSlotStep;
-#pragma unroll
-      for (int t = 0; t < 2; ++t) {
-        const int nt = t ? n1 : n0;
-        if (j >= 1 && j - 1 < nt) {
-          // O_t += P_t V_{j-1}: P from tensor memory (8 columns per 16 keys), V from the ring.
-          // The hand-off is a hardware named barrier (tile t's four softmax warps arrive,
-          // this warp waits), which wakes far sooner than an mbarrier wait.  It has no
-          // timeout, so the softmax warps arrive once per K/V step whatever happens, and never
-          // for step j before S_t(j) is complete (issued after this warp's wait for step j-1).
-          ptx::named_barrier(3 + t, 160);
+          for (int t = 0; t < 2; ++t)
+            if (ok && (t ? it.n1 : it.n0) > 0) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarQFull + t), 0));
           ptx::tc_fence_after();
-          const uint32_t t_o = tmem + C::kColO + t * D;
-          const uint32_t t_p = tmem + C::kColS + t * 128;
-          if (ptx::elect_one()) {
-            if (j > 1) ptx::mma_ts_i<1>(t_o, t_p, dv, kIdescPV);
-            else ptx::mma_ts_i<0>(t_o, t_p, dv, kIdescPV);
+          // each tile slot has K/V tiles of its own, consumed (and released) in ring order
+          int u = 0;
+          for (int j = 0; ok && j <= it.nmax; ++j) {
 #pragma unroll
-            for (int kk = 1; kk < 8; ++kk) ptx::mma_ts_i<1>(t_o, t_p + kk * 8, dv + kk * 128, kIdescPV);
-            if (j - 1 == nt - 1) ptx::tc_commit(bar(C::kBarOFinal + t));
-          }
-          __syncwarp();
-        }
-        if (j < nt) {
-          if (!k_ready) {
-            ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + uk % C::kSlots), (uk / C::kSlots) & 1));
-            if (!ok) break;
-            ptx::tc_fence_after();
-            k_ready = true;
-          }
-          // S_t = Q_t K_j^T, both K-major: 16 d-columns per step, +32 B inside a 128-byte
-          // swizzle atom, next atom (d >= 64) at +16 KB
-          const uint32_t t_s = tmem + C::kColS + t * 128;
-          const uint64_t dq = t ? desc_q1 : desc_q0;
-          if (ptx::elect_one()) {
-            ptx::mma_ss_i<0>(t_s, dq, dk, kIdescQK);
+            for (int t = 0; t < 2; ++t) {
+              const int nt = t ? it.n1 : it.n0;
+              if (j >= 1 && j - 1 < nt) {
+                ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1));
+                if (!ok) break;
+                ptx::named_barrier(3 + t, 160);  // P_t(j-1) handed over (see the non-dual loop)
+                ptx::tc_fence_after();
+                const uint32_t dv = desc_v_ring + (u % C::kSlots) * kSlotStep;
+                const uint32_t t_o = tmem + C::kColO + t * D;
+                const uint32_t t_p = tmem + C::kColS + t * 128;
+                if (ptx::elect_one()) {
+                  if (j > 1) ptx::mma_ts_i<1>(t_o, t_p, kDescHi | dv, kIdescPV);
+                  else ptx::mma_ts_i<0>(t_o, t_p, kDescHi | dv, kIdescPV);
 #pragma unroll
-            for (int kk = 1; kk < D / 16; ++kk) {
-              const uint64_t o = (kk >> 2) * (C::kChunkBytes >> 4) + (kk & 3) * 2;
-              ptx::mma_ss_i<1>(t_s, dq + o, dk + o, kIdescQK);
+                  for (int kk = 1; kk < 8; ++kk) ptx::mma_ts_i<1>(t_o, t_p + kk * 8, kDescHi | (dv + kk * 128), kIdescPV);
+                  if (j - 1 == nt - 1) ptx::tc_commit(bar(C::kBarOFinal + t));
+                  ptx::tc_commit(bar(C::kBarEmpty + u % C::kSlots));
+                }
+                __syncwarp();
+                ++u;
+              }
+              if (j < nt) {
+                ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1));
+                if (!ok) break;
+                ptx::tc_fence_after();
+                const uint32_t dk = desc_k_ring + (u % C::kSlots) * kSlotStep;
+                const uint32_t t_s = tmem + C::kColS + t * 128;
+                const uint32_t dq = t ? desc_q1 : desc_q0;
+                if (ptx::elect_one()) {
+                  ptx::mma_ss_i<0>(t_s, kDescHi | dq, kDescHi | dk, kIdescQK);
+#pragma unroll
+                  for (int kk = 1; kk < D / 16; ++kk) {
+                    const uint32_t o = (kk >> 2) * (C::kChunkBytes >> 4) + (kk & 3) * 2;
+                    ptx::mma_ss_i<1>(t_s, kDescHi | (dq + o), kDescHi | (dk + o), kIdescQK);
+                  }
+                  ptx::tc_commit(bar(C::kBarSFull + t));
+                  ptx::tc_commit(bar(C::kBarEmpty + u % C::kSlots));
+                }
+                __syncwarp();
+                ++u;
+              }
             }
-            ptx::tc_commit(bar(C::kBarSFull + t));
           }
+        } else {
+          // Step 0: S_t = Q_t K_0^T for each tile slot with K/V tiles, then K_0's release.  The
+          // steady steps below carry no per-item checks and advance their slot and barrier
+          // indices by increments: this warp feeds the tensor pipe, and its loop has to stay short.
+          const int n0 = it.n0, n1 = it.n1, nmax = it.nmax;
+          const uint32_t s_k0 = U % C::kSlots;
+          ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + Vc % C::kSlots), (Vc / C::kSlots) & 1));
+          if (ok) ptx::tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const int nt = t ? n1 : n0;
+            if (!ok || nt == 0) continue;
+            ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarQFull + t), (ph >> t) & 1u));  // Q_t of this item
+            if (!ok) break;
+            ph ^= 1u << t;
+            ptx::tc_fence_after();
+            const uint32_t t_s = tmem + C::kColS + t * 128;
+            const uint32_t dq = t ? desc_q1 : desc_q0, dk = desc_k_ring + s_k0 * kSlotStep;
+            if (ptx::elect_one()) {
+              ptx::mma_qk_run<kDescHi32>(t_s, dq, dk, kIdescQK, std::make_integer_sequence<int, D / 16>{});
+              ptx::tc_commit(bar(C::kBarSFull + t));
+              if (nt == 1) ptx::tc_commit(bar(C::kBarQEmpty + t));  // Q_t's buffer free for the next item
+            }
+            __syncwarp();
+          }
+          if (ptx::elect_one()) ptx::tc_commit(bar(C::kBarEmpty + s_k0));
           __syncwarp();
+          // the item's first P V products overwrite O: every earlier epilogue has read its O out
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (ok && (ph & (16u << t))) {
+              ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarOEmpty + t), (ph >> (2 + t)) & 1u));
+              ph ^= (4u << t) | (16u << t);
+            }
+          // steps j = 1 .. nmax: O_t += P_t V_{j-1}, then S_t = Q_t K_j^T
+          // V_{j-1}'s ring slot, and its number (J, counted over the CTA's items) modulo 2 kSlots:
+          // barrier J % kSlots, phase parity J / kSlots; K_j is ring slot and number one further
+          uint32_t s_v = (U + 1) % C::kSlots, n_v = Vc % (2 * C::kSlots);
+          for (int j = 1; ok && j <= nmax; ++j) {
+            const uint32_t s_k = s_v + 1 == C::kSlots ? 0 : s_v + 1;
+            const uint32_t n_k = n_v + 1 == 2 * C::kSlots ? 0 : n_v + 1;
+            // V_{j-1} converted to fp16 in its ring slot (the converters waited for it to land)
+            ok = __all_sync(0xffffffffu, w.wait(bar((kF16 ? C::kBarConv : C::kBarVFull) + (n_v % C::kSlots)), n_v >= C::kSlots));
+            if (!ok) break;
+            bool k_ready = false;  // K_j is waited for only right before its first use
+            const uint32_t dk = desc_k_ring + s_k * kSlotStep, dv = desc_v_ring + s_v * kSlotStep;
+#pragma unroll
+            for (int t = 0; t < 2; ++t) {
+              const int nt = t ? n1 : n0;
+              if (j - 1 < nt) {
+                // O_t += P_t V_{j-1}: P from tensor memory (8 columns per 16 keys), V from the ring.
+                // The hand-off is a hardware named barrier (tile t's four softmax warps arrive,
+                // this warp waits), which wakes far sooner than an mbarrier wait.  It has no
+                // timeout, so the softmax warps arrive once per K/V step whatever happens, and
+                // never for a step before its S_t is complete (issued after this warp's wait for
+                // the step before).  Across items the same holds: the first wait of an item
+                // follows the O-empty waits, which the softmax warps pass only by finishing the
+                // previous item.
+                ptx::named_barrier(3 + t, 160);
+                ptx::tc_fence_after();
+                const uint32_t t_o = tmem + C::kColO + t * D;
+                const uint32_t t_p = tmem + C::kColS + t * 128;
+                if (ptx::elect_one()) {
+                  if (j > 1) ptx::mma_ts_lo<1, kDescHi32, 0, 0>(t_o, t_p, dv, kIdescPV);
+                  else ptx::mma_ts_lo<0, kDescHi32, 0, 0>(t_o, t_p, dv, kIdescPV);
+                  ptx::mma_pv_rest<kDescHi32>(t_o, t_p, dv, kIdescPV, std::make_integer_sequence<int, 7>{});
+                  if (j == nt) ptx::tc_commit(bar(C::kBarOFinal + t));
+                }
+                __syncwarp();
+              }
+              if (j < nt) {
+                if (!k_ready) {
+                  ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + (n_k % C::kSlots)), n_k >= C::kSlots));
+                  if (!ok) break;
+                  ptx::tc_fence_after();
+                  k_ready = true;
+                }
+                // S_t = Q_t K_j^T, both K-major: 16 d-columns per step, +32 B inside a 128-byte
+                // swizzle atom, next atom (d >= 64) at +16 KB
+                const uint32_t t_s = tmem + C::kColS + t * 128;
+                const uint32_t dq = t ? desc_q1 : desc_q0;
+                if (ptx::elect_one()) {
+                  ptx::mma_qk_run<kDescHi32>(t_s, dq, dk, kIdescQK, std::make_integer_sequence<int, D / 16>{});
+                  ptx::tc_commit(bar(C::kBarSFull + t));
+                  if (j == nt - 1) ptx::tc_commit(bar(C::kBarQEmpty + t));  // Q_t's buffer free for the next item
+                }
+                __syncwarp();
+              }
+            }
+            if (!ok) break;
+            // release in ring order: V_{j-1}, then K_j
+            if (ptx::elect_one()) {
+              ptx::tc_commit(bar(C::kBarEmpty + s_v));
+              if (j < nmax) ptx::tc_commit(bar(C::kBarEmpty + s_k));
+            }
+            __syncwarp();
+            s_v = s_k + 1 == C::kSlots ? 0 : s_k + 1;
+            n_v = n_k;
+          }
+          U += 2 * it.nmax + (staged ? (it.n0 > 0) + (it.n1 > 0) : 0);
+          Vc += it.nmax;
         }
+        ph |= (it.n0 > 0 ? 16u : 0u) | (it.n1 > 0 ? 32u : 0u);
       }
       if (!ok) break;
-      // release in ring order: V_{j-1} (tile 2j-1), then K_j (tile 2j)
-      if (ptx::elect_one()) {
-        if (j >= 1) ptx::tc_commit(bar(C::kBarEmpty + uv % C::kSlots));
-        if (j < nmax) ptx::tc_commit(bar(C::kBarEmpty + uk % C::kSlots));
-      }
-      __syncwarp();
+      const int nx = next_item(k);
+      if (nx == -2) ok = false;
+      if (nx < 0) break;
+      idx = nx;
     }
     // every MMA issued by this warp completes before tensor memory is freed
     if (ptx::elect_one()) ptx::tc_commit(bar(C::kBarDrain));
@@ -543,295 +805,382 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (kF16 && warp >= 10) {
     // ================================================================ V converters (two of three)
-    if (nmax >= 1 && convert_first(warp - 9))
-      for (int j = 1; j < nmax; ++j)
-        if (!convert_share(j, warp - 9)) break;
+    int idx = blockIdx.x;
+    int U = 0, Vc = 0, xk = 0;  // ring tiles and V tiles of the items before, items measured
+    const bool staged = p.n_splits == 1;
+    for (int k = 0;; ++k) {
+      const Item it = decode_item<kDual>(p, idx);
+      if (it.nmax >= 1) {
+        if (!convert_first(Vc, U + 1, warp - 9, xk, it.bh, it.lo0 * 128)) break;
+        ++xk;
+        bool good = true;
+        for (int j = 1; good && j < it.nmax; ++j) good = convert_share(Vc + j, U + 2 * j + 1, warp - 9);
+        if (!good) break;
+        U += 2 * it.nmax + (staged ? (it.n0 > 0) + (it.n1 > 0) : 0);
+        Vc += it.nmax;
+      }
+      const int nx = next_item(k);
+      if (nx < 0) break;
+      idx = nx;
+    }
   } else if (warp < 8) {
     // ================================================================ softmax warpgroups
     ptx::regs_increase<kSoftmaxRegs>();
     const int t = warp >> 2;
     const int quarter = warp & 3;
-    const int nt = t ? n1 : n0;
-    const int qt = t ? qt1 : qt0;
     const int row = quarter * 32 + lane;
-    const int qrow = qt * 128 + row;              // row within the group
-    const int qpos = p.q_offset + qrow % p.Nq;    // its sequence position (causal mask)
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s = tmem + lane_off + C::kColS + t * 128;
     const uint32_t t_o = tmem + lane_off + C::kColO + t * D;
     const float c2 = p.scale_log2;
-    float m_run = -INFINITY;  // running max of the raw scores q.k (scale > 0)
-    float l_run = 0.f;        // running sum of 2^((s - m_run) * c2)
-    float lp_run = 0.f;       // bf16 P only: the same sum over the rounded terms
-    int k_cur = 0;            // fp16 P: O~ is held at V's scale 2^-k_cur
-    const int* kscale = reinterpret_cast<const int*>(smem + C::kOffKScale);
     // d = 128: S_t is read in two halves and P written in four parts, which shortens the
     // softmax's span from S ready to P handed over.  d = 64 keeps one load and two stores:
     // its softmax is bound by instruction issue (half the tensor work per exp), and the extra
     // instructions cost it more than the shorter span wins.
     constexpr bool kSplitS = D == 128;
-    // One arrive at the P hand-off barrier per K/V step, whatever happens: the MMA warp waits
-    // there without a timeout.  After a failed wait the remaining steps only arrive (the loop
-    // after this one), each once S_t of its step is complete, so that no arrival runs ahead
-    // into a later step's barrier phase: S_t(j) is issued after the MMA warp's wait for step
-    // j-1, and the MMA warp cannot wait for step j before issuing it.  That wait ignores the
-    // abort flag; once the MMA warp has left its loop it ends at the deadline, and the
-    // arrivals stop.
-    bool ok = nt > 0;
-    int j = 0;
-    for (; j < nt; ++j) {
-      ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarSFull + t), j & 1));
-      if (!ok) break;
-      ptx::tc_fence_after();
-      // mask: keys past the end of the sequence, and keys after the query when causal
-      const int col0 = ((t ? lo1 : lo0) + j) * 128;
-      int lim = p.Nk - col0;
-      if (p.causal && qpos - col0 + 1 < lim) lim = qpos - col0 + 1;
-      float s[128];
-      float mx0, mx1, mx2, mx3;
-      if constexpr (kSplitS) {
-        // S_t in two 64-column halves: the row max of the first runs while the second lands
-        uint32_t rb[64];
-        {
-          uint32_t ra[64];
-          ptx::tmem_ld64_nowait(t_s, ra);
-          ptx::tmem_wait_ld64(ra);
-          ptx::tmem_ld64_nowait(t_s + 64, rb);
-#pragma unroll
-          for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(ra[i]);
-        }
-        if (lim < 64) {
-#pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (c >= lim) s[c] = -INFINITY;
-        }
-        mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-        for (int c = 4; c < 60; c += 8) {
-          mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
-          mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
-          mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
-          mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
-        }
-        mx0 = ptx::fmax3(mx0, s[60], s[61]);
-        mx1 = ptx::fmax3(mx1, s[62], s[63]);
-        ptx::tmem_wait_ld64(rb);
-#pragma unroll
-        for (int i = 0; i < 64; ++i) s[64 + i] = __uint_as_float(rb[i]);
-        if (lim < 128) {
-#pragma unroll
-          for (int c = 64; c < 128; ++c)
-            if (c >= lim) s[c] = -INFINITY;
-        }
-#pragma unroll
-        for (int c = 64; c < 128; c += 8) {
-          mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
-          mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
-          mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
-          mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
-        }
+    int idx = blockIdx.x;
+    int U = 0;      // ring tiles of the items before the current one
+    int Vc = 0;     // V tiles of the items before the current one
+    const bool staged = p.n_splits == 1;  // O leaves through the item's staging slot for this tile
+    int n_s = 0;    // S_t tiles taken (phases of S-full)
+    int n_o = 0;    // final O_t waited for (phases of O-final)
+    // The epilogue's row addresses are derived from the item number again after the K/V steps
+    // rather than kept live through them: the steps need every register they can get.
+    struct Rows {
+      size_t grow;      // row in [B*Hq*Nq]
+      int my_split;     // the partials this tile slot writes (n_splits > 1)
+      bool row_valid;
+      int bh, row0;     // the tile's group and first row within it (the TMA store's coordinates)
+    };
+    auto rows_of = [&](const int item) -> Rows {
+      const Item e = decode_item<kDual>(p, item);
+      const int row0 = (t ? e.qt1 : e.qt0) * 128, qrow = row0 + row;
+      return Rows{static_cast<size_t>(e.bh) * p.R + qrow, t ? e.split1 : e.split, (t == 0 || e.has1) && qrow < p.R,
+                  e.bh, row0};
+    };
+    // no K/V tile of this split is visible to the tile: the empty result (O = 0, LSE = -inf)
+    auto write_empty = [&](const Rows& w_) {
+      if (!w_.row_valid) return;
+      if (p.n_splits == 1) {
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.o_bf16) + w_.grow * D * 2);
+        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+        p.lse[w_.grow] = -INFINITY;
       } else {
-        {
-          uint32_t r[128];
-          ptx::tmem_ld128(t_s, r);
-#pragma unroll
-          for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
-        }
-        if (lim < 128) {
-#pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c >= lim) s[c] = -INFINITY;
-        }
-        mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
-#pragma unroll
-        for (int c = 4; c < 124; c += 8) {
-          mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
-          mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
-          mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
-          mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
-        }
-        mx0 = ptx::fmax3(mx0, s[124], s[125]);
-        mx1 = ptx::fmax3(mx1, s[126], s[127]);
+        float4* dst = reinterpret_cast<float4*>(p.o_part + (static_cast<size_t>(w_.my_split) * p.groups * p.R + w_.grow) * D);
+        for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        p.lse_part[static_cast<size_t>(w_.my_split) * p.groups * p.R + w_.grow] = -INFINITY;
       }
-      const float tile_max = fmaxf(ptx::fmax3(mx0, mx1, mx2), mx3);
-      const float m_new = fmaxf(m_run, tile_max);
-      // Keep the old reference unless the max grew by more than 2^8: l and O~ share the
-      // reference, so O = O~/l is unchanged; only the size of the terms is bounded.
-      const bool rescale = (m_new - m_run) * c2 > kRescaleLog2Threshold;
-      const float m_ref = rescale ? m_new : m_run;
-      const float r_fac = rescale ? ptx::ex2_approx((m_run - m_new) * c2) : 1.f;
-      // a row that has seen no unmasked key yet keeps m = -inf: its terms are all 0
-      const float neg = m_ref == -INFINITY ? 0.f : -m_ref * c2;
-      // P = 2^(s*c2 - m_ref*c2), rounded to fp16 pairs for the P V product (bf16 in the
-      // decode instance) and written over the first 64 columns of S_t, a part at a time while
-      // the rest is computed (four parts with the split S load, two otherwise, so the last
-      // store is short).  l_run sums the fp32 values; O = O~ / l_run.  With bf16 P a second sum
-      // over the rounded values (lp_run) normalises O instead, which halves O's error when a few
-      // keys dominate; fp16 P is 8x finer and needs no second sum.
-      __syncwarp();  // reconverge after the per-row mask before the warp-wide TMEM stores
-      const float2 c2v = make_float2(c2, c2), negv = make_float2(neg, neg);
-      float2 se[4], sp[4];
+    };
+    for (int k = 0;; ++k) {
+      const Item it = decode_item<kDual>(p, idx);
+      const int nt = t ? it.n1 : it.n0;
+      const int qpos = p.q_offset + ((t ? it.qt1 : it.qt0) * 128 + row) % p.Nq;  // sequence position (causal mask)
+      if (it.nmax == 0) {  // an item with no K/V tile at all takes no part in the pipelines
+        write_empty(rows_of(idx));
+      } else {
+        // the ring position after this item; this tile's staging slot (if it has K/V tiles) is
+        // the last before it, or the one before that for slot 0 when slot 1 has one too
+        const int U_next = U + 2 * it.nmax + (staged ? (it.n0 > 0) + (it.n1 > 0) : 0);
+        const int stage_g = U_next - 1 - (t == 0 && it.n1 > 0 ? 1 : 0);
+        // The K/V steps hold the whole S row, its exponentials and P in registers, right at the
+        // warpgroup's budget: the item's bookkeeping waits in shared memory meanwhile (volatile,
+        // so that it is read back rather than kept live).
+        volatile int* park = reinterpret_cast<volatile int*>(smem + C::kOffPark) + warp * 8;
+        park[0] = idx;
+        park[1] = k;
+        park[2] = U_next;
+        park[3] = Vc;
+        park[4] = n_o;
+        park[5] = stage_g;
+        park[6] = it.nmax;
+        float m_run = -INFINITY;  // running max of the raw scores q.k (scale > 0)
+        float l_run = 0.f;        // running sum of 2^((s - m_run) * c2)
+        float lp_run = 0.f;       // bf16 P only: the same sum over the rounded terms
+        // One arrive at the P hand-off barrier per K/V step, whatever happens: the MMA warp waits
+        // there without a timeout.  After a failed wait the remaining steps of the item only
+        // arrive (the loop after this one), each once S_t of its step is complete, so that no
+        // arrival runs ahead into a later step's barrier phase: S_t(j) is issued after the MMA
+        // warp's wait for step j-1, and the MMA warp cannot wait for step j before issuing it.
+        // That wait ignores the abort flag; once the MMA warp has left its loop it ends at the
+        // deadline, and the arrivals stop.  The warp then leaves without reading O out, so the
+        // MMA warp's wait for that (before the next item's first P V product) fails too.
+        bool ok = true;
+        int j = 0;
+        for (; j < nt; ++j) {
+          ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarSFull + t), n_s & 1));
+          if (!ok) break;
+          ++n_s;
+          ptx::tc_fence_after();
+          // mask: keys past the end of the sequence, and keys after the query when causal
+          const int col0 = ((t ? it.lo1 : it.lo0) + j) * 128;
+          int lim = p.Nk - col0;
+          if (p.causal && qpos - col0 + 1 < lim) lim = qpos - col0 + 1;
+          float s[128];
+          float mx0, mx1, mx2, mx3;
+          if constexpr (kSplitS) {
+            // S_t in two 64-column halves: the row max of the first runs while the second lands
+            uint32_t rb[64];
+            {
+              uint32_t ra[64];
+              ptx::tmem_ld64_nowait(t_s, ra);
+              ptx::tmem_wait_ld64(ra);
+              ptx::tmem_ld64_nowait(t_s + 64, rb);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) se[i] = sp[i] = make_float2(0.f, 0.f);
-      uint32_t pk[64];
+              for (int i = 0; i < 64; ++i) s[i] = __uint_as_float(ra[i]);
+            }
+            if (lim < 64) {
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const float2 x = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), c2v, negv);
-        const float e0 = ptx::ex2_approx(x.x);
-        const float e1 = ptx::ex2_approx(x.y);
-        se[i & 3] = __fadd2_rn(se[i & 3], make_float2(e0, e1));
-        if constexpr (kF16) {
-          pk[i] = ptx::pack_f16x2(e0, e1);
-        } else {
-          pk[i] = ptx::pack_bf16x2(e0, e1);
-          sp[i & 3] = __fadd2_rn(sp[i & 3], make_float2(__uint_as_float(pk[i] << 16),
-                                                        __uint_as_float(pk[i] & 0xffff0000u)));
-        }
-        if constexpr (kSplitS) {
-          if ((i & 15) == 15) {  // P_t columns [i-15, i]: keys 2(i-15) to 2i+1
-            uint32_t part[16];
+              for (int c = 0; c < 64; ++c)
+                if (c >= lim) s[c] = -INFINITY;
+            }
+            mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) part[k] = pk[i - 15 + k];
-            ptx::tmem_st16(t_s + (i - 15), part);
+            for (int c = 4; c < 60; c += 8) {
+              mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
+              mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
+              mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
+              mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
+            }
+            mx0 = ptx::fmax3(mx0, s[60], s[61]);
+            mx1 = ptx::fmax3(mx1, s[62], s[63]);
+            ptx::tmem_wait_ld64(rb);
+#pragma unroll
+            for (int i = 0; i < 64; ++i) s[64 + i] = __uint_as_float(rb[i]);
+            if (lim < 128) {
+#pragma unroll
+              for (int c = 64; c < 128; ++c)
+                if (c >= lim) s[c] = -INFINITY;
+            }
+#pragma unroll
+            for (int c = 64; c < 128; c += 8) {
+              mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
+              mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
+              mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
+              mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
+            }
+          } else {
+            {
+              uint32_t r[128];
+              ptx::tmem_ld128(t_s, r);
+#pragma unroll
+              for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(r[i]);
+            }
+            if (lim < 128) {
+#pragma unroll
+              for (int c = 0; c < 128; ++c)
+                if (c >= lim) s[c] = -INFINITY;
+            }
+            mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+            for (int c = 4; c < 124; c += 8) {
+              mx0 = ptx::fmax3(mx0, s[c], s[c + 1]);
+              mx1 = ptx::fmax3(mx1, s[c + 2], s[c + 3]);
+              mx2 = ptx::fmax3(mx2, s[c + 4], s[c + 5]);
+              mx3 = ptx::fmax3(mx3, s[c + 6], s[c + 7]);
+            }
+            mx0 = ptx::fmax3(mx0, s[124], s[125]);
+            mx1 = ptx::fmax3(mx1, s[126], s[127]);
           }
-        } else if (i == 31 || i == 63) {  // P_t columns [0,32) (keys 0-63), then [32,64)
-          uint32_t half[32];
+          const float tile_max = fmaxf(ptx::fmax3(mx0, mx1, mx2), mx3);
+          const float m_new = fmaxf(m_run, tile_max);
+          // Keep the old reference unless the max grew by more than 2^8: l and O~ share the
+          // reference, so O = O~/l is unchanged; only the size of the terms is bounded.
+          const bool rescale = (m_new - m_run) * c2 > kRescaleLog2Threshold;
+          const float m_ref = rescale ? m_new : m_run;
+          const float r_fac = rescale ? ptx::ex2_approx((m_run - m_new) * c2) : 1.f;
+          // a row that has seen no unmasked key yet keeps m = -inf: its terms are all 0
+          const float neg = m_ref == -INFINITY ? 0.f : -m_ref * c2;
+          // P = 2^(s*c2 - m_ref*c2), rounded to fp16 pairs for the P V product (bf16 in the
+          // decode instance) and written over the first 64 columns of S_t, a part at a time while
+          // the rest is computed (four parts with the split S load, two otherwise, so the last
+          // store is short).  l_run sums the fp32 values; O = O~ / l_run.  With bf16 P a second sum
+          // over the rounded values (lp_run) normalises O instead, which halves O's error when a few
+          // keys dominate; fp16 P is 8x finer and needs no second sum.
+          __syncwarp();  // reconverge after the per-row mask before the warp-wide TMEM stores
+          const float2 c2v = make_float2(c2, c2), negv = make_float2(neg, neg);
+          float2 se[4], sp[4];
 #pragma unroll
-          for (int k = 0; k < 32; ++k) half[k] = pk[i - 31 + k];
-          ptx::tmem_st32(t_s + (i - 31), half);
-        }
-      }
-      const float2 se01 = __fadd2_rn(se[0], se[1]), se23 = __fadd2_rn(se[2], se[3]);
-      l_run = l_run * r_fac + ((se01.x + se01.y) + (se23.x + se23.y));
-      if constexpr (!kF16) {
-        const float2 sp01 = __fadd2_rn(sp[0], sp[1]), sp23 = __fadd2_rn(sp[2], sp[3]);
-        lp_run = lp_run * r_fac + ((sp01.x + sp01.y) + (sp23.x + sp23.y));
-      }
-      m_run = m_ref;
-      // correction O~ *= r, before P_t(j) is handed over: PV_t(j-1) has completed (the commit
-      // behind S_t(j) covers it) and PV_t(j) waits for the arrive below
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        if constexpr (kSplitS) {  // all 128 columns of O_t in one load (S and P are dead here)
-          uint32_t r[128];
-          ptx::tmem_ld128(t_o, r);
+          for (int i = 0; i < 4; ++i) se[i] = sp[i] = make_float2(0.f, 0.f);
+          uint32_t pk[64];
 #pragma unroll
-          for (int i = 0; i < 128; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
+          for (int i = 0; i < 64; ++i) {
+            const float2 x = __ffma2_rn(make_float2(s[2 * i], s[2 * i + 1]), c2v, negv);
+            const float e0 = ptx::ex2_approx(x.x);
+            const float e1 = ptx::ex2_approx(x.y);
+            se[i & 3] = __fadd2_rn(se[i & 3], make_float2(e0, e1));
+            if constexpr (kF16) {
+              pk[i] = ptx::pack_f16x2(e0, e1);
+            } else {
+              pk[i] = ptx::pack_bf16x2(e0, e1);
+              sp[i & 3] = __fadd2_rn(sp[i & 3], make_float2(__uint_as_float(pk[i] << 16),
+                                                            __uint_as_float(pk[i] & 0xffff0000u)));
+            }
+            if constexpr (kSplitS) {
+              if ((i & 15) == 15) {  // P_t columns [i-15, i]: keys 2(i-15) to 2i+1
+                uint32_t part[16];
 #pragma unroll
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t part[32];
+                for (int k = 0; k < 16; ++k) part[k] = pk[i - 15 + k];
+                ptx::tmem_st16(t_s + (i - 15), part);
+              }
+            } else if (i == 31 || i == 63) {  // P_t columns [0,32) (keys 0-63), then [32,64)
+              uint32_t half[32];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) part[i] = r[cc * 32 + i];
-            ptx::tmem_st32(t_o + cc * 32, part);
+              for (int k = 0; k < 32; ++k) half[k] = pk[i - 31 + k];
+              ptx::tmem_st32(t_s + (i - 31), half);
+            }
           }
+          const float2 se01 = __fadd2_rn(se[0], se[1]), se23 = __fadd2_rn(se[2], se[3]);
+          l_run = l_run * r_fac + ((se01.x + se01.y) + (se23.x + se23.y));
+          if constexpr (!kF16) {
+            const float2 sp01 = __fadd2_rn(sp[0], sp[1]), sp23 = __fadd2_rn(sp[2], sp[3]);
+            lp_run = lp_run * r_fac + ((sp01.x + sp01.y) + (sp23.x + sp23.y));
+          }
+          m_run = m_ref;
+          // correction O~ *= r, before P_t(j) is handed over: PV_t(j-1) has completed (the commit
+          // behind S_t(j) covers it) and PV_t(j) waits for the arrive below
+          if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+            if constexpr (kSplitS) {  // all 128 columns of O_t in one load (S and P are dead here)
+              uint32_t r[128];
+              ptx::tmem_ld128(t_o, r);
+#pragma unroll
+              for (int i = 0; i < 128; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
+#pragma unroll
+              for (int cc = 0; cc < 4; ++cc) {
+                uint32_t part[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) part[i] = r[cc * 32 + i];
+                ptx::tmem_st32(t_o + cc * 32, part);
+              }
+            } else {
+#pragma unroll 1
+              for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t r[32];
+                ptx::tmem_ld32(t_o + cc * 32, r);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
+                ptx::tmem_st32(t_o + cc * 32, r);
+              }
+            }
+          }
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          __syncwarp();
+          ptx::named_barrier_arrive(3 + t, 160);  // P_t(j) handed over to the MMA warp
+        }
+        if (!ok) {
+          for (; j < nt && w.drain(bar(C::kBarSFull + t), n_s & 1); ++j, ++n_s) ptx::named_barrier_arrive(3 + t, 160);
+          break;
+        }
+        idx = park[0];
+        k = park[1];
+        const int U_after = park[2];
+        Vc = park[3];
+        n_o = park[4];
+        const int stage_at = park[5];
+        const int nmax_item = park[6];
+        // ---- epilogue: O = O~ / l, LSE = m*scale + ln l; a row that saw no key gets O = 0 and
+        // LSE = -inf.  O~ is read out of tensor memory whole, the O-empty barrier arrived at, and
+        // the row written from registers: one split, bf16 O straight to its row; several splits,
+        // fp32 partial O and partial LSE to the workspace for the combine.
+        const uint32_t stage_slot = stage_at % C::kSlots;
+        if (nt == 0) {  // no K/V tile for this tile slot: no O, no staging slot, no barrier
+          write_empty(rows_of(idx));
         } else {
+          ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarOFinal + t), n_o & 1));
+          if (!ok) break;
+          ++n_o;
+          int k_cur = 0;  // fp16 P: O~ is held at V's scale 2^-k_cur, fixed by the item's first V tile
+          if constexpr (kF16) {
+            // the wait is for this tile's last conversion, which follows the first; that barrier
+            // phase cannot have been reused yet: the next item's P V products wait for this
+            // epilogue, so the converters are at most a few V tiles ahead of this tile's last
+            const int J = Vc + nt - 1;
+            ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarConv + J % C::kSlots), (J / C::kSlots) & 1));
+            if (!ok) break;
+            k_cur = kscale[J % C::kSlots];
+          }
+          if (staged) {  // the staging slot (long free: it is waited for here, before O is read out)
+            // the slot's previous tile has been released (its release is the latest phase the
+            // barrier can have completed: the next is this epilogue's own)
+            if (stage_at >= C::kSlots)
+              ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarEmpty + stage_slot), ((stage_at / C::kSlots) - 1) & 1));
+            if (!ok) break;
+          }
+          ptx::tc_fence_after();
+          // O~ leaves in 32-column chunks (a rolled loop: this runs once per item, and the code
+          // of the K/V steps is what must stay in the instruction cache)
+          const Rows rw = rows_of(idx);
+          const bool have = l_run > 0.f;
+          // fp16 P: O~ / l at V's scale 2^-k_cur; bf16 P: O~ / (sum of the rounded terms)
+          const float inv_l = have ? (kF16 ? exp2_int(k_cur) / l_run : 1.f / lp_run) : 0.f;
+          const float lse_row = have ? m_run * p.scale + logf(l_run) : -INFINITY;
+          float2 nonfinite = make_float2(0.f, 0.f);  // fp16 P V: stays 0 unless some O~ value is inf or NaN
+          // one split: bf16 O through the item's staging slot for this tile (the tile's 128 rows in
+          // 64-column chunks, 128-byte swizzle, the layout a K or V tile has there) and TMA
+          // stores (rows past the group's end are clipped).  Each thread owns one row, so direct
+          // stores would put 32 rows' partial lines into every store instruction and hold the
+          // SM's load/store pipe (and with it every warp's shared-memory and barrier operations)
+          // for microseconds.  Several splits: fp32 partial O straight to the workspace.
+          const uint32_t stage = sbase + C::kOffRing + stage_slot * C::kTileBytes;
+          float4* part = reinterpret_cast<float4*>(p.o_part + (static_cast<size_t>(rw.my_split) * p.groups * p.R + rw.grow) * D);
 #pragma unroll 1
           for (int cc = 0; cc < D / 32; ++cc) {
             uint32_t r[32];
             ptx::tmem_ld32(t_o + cc * 32, r);
+            if constexpr (kF16) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
-            ptx::tmem_st32(t_o + cc * 32, r);
+              for (int i = 0; i < 16; ++i)
+                nonfinite = __ffma2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
+                                       make_float2(0.f, 0.f), nonfinite);
+            }
+            if (staged) {
+              const uint32_t chunk_base = stage + (cc >> 1) * C::kChunkBytes + row * 128;
+#pragma unroll
+              for (int g = 0; g < 4; ++g) {
+                const int gran = (cc & 1) * 4 + g;  // 16-byte granule within the 128-byte row
+                ptx::st_shared_v4(chunk_base + ((gran ^ (row & 7)) << 4),
+                                  ptx::pack_bf16x2(__uint_as_float(r[8 * g]) * inv_l, __uint_as_float(r[8 * g + 1]) * inv_l),
+                                  ptx::pack_bf16x2(__uint_as_float(r[8 * g + 2]) * inv_l, __uint_as_float(r[8 * g + 3]) * inv_l),
+                                  ptx::pack_bf16x2(__uint_as_float(r[8 * g + 4]) * inv_l, __uint_as_float(r[8 * g + 5]) * inv_l),
+                                  ptx::pack_bf16x2(__uint_as_float(r[8 * g + 6]) * inv_l, __uint_as_float(r[8 * g + 7]) * inv_l));
+              }
+            } else if (rw.row_valid) {
+#pragma unroll
+              for (int i = 0; i < 8; ++i)
+                part[cc * 8 + i] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
+                                               __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
+            }
           }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(bar(C::kBarOEmpty + t));  // O_t may be overwritten now
+          if (staged) {
+            ptx::fence_proxy_async_smem();
+            ptx::named_barrier(1 + t, 128);  // all 128 rows written
+            if (row == 0) {  // the stores, and the slot's release once they have read it
+              for (int c = 0; c < D / 64; ++c) ptx::tma_store_3d(&tm_o, stage + c * C::kChunkBytes, c * 64, rw.row0, rw.bh);
+              ptx::bulk_commit();
+              ptx::bulk_wait_read<0>();
+              ptx::mbar_arrive(bar(C::kBarEmpty + stage_slot));
+            }
+            if (rw.row_valid) p.lse[rw.grow] = lse_row;
+          } else if (rw.row_valid) {
+            p.lse_part[static_cast<size_t>(rw.my_split) * p.groups * p.R + rw.grow] = lse_row;
+          }
+          if (kF16 && __any_sync(0xffffffffu, rw.row_valid && have && l_run < INFINITY &&
+                                                   !(nonfinite.x == 0.f && nonfinite.y == 0.f)) && lane == 0)
+            atomicOr(&g_status, FA_STATUS_V_RANGE);  // a V tile fp16 could not hold at the item's scale
         }
+        U = U_after;
+        Vc += nmax_item;
       }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      __syncwarp();
-      ptx::named_barrier_arrive(3 + t, 160);  // P_t(j) handed over to the MMA warp
-    }
-    for (; j < nt && w.drain(bar(C::kBarSFull + t), j & 1); ++j) ptx::named_barrier_arrive(3 + t, 160);
-    // ---- epilogue: O = O~ / l, LSE = m*scale + ln l; a row that saw no key gets O = 0 and
-    // LSE = -inf.  One split: O -> bf16 -> shared (Q_t's buffer) -> TMA store.  Several
-    // splits: fp32 partial O and partial LSE straight to the workspace for the combine.
-    const bool tile_exists = t == 0 || has1;
-    const int my_split = t ? split1 : split;  // the partials this tile slot writes (n_splits > 1)
-    const size_t grow = static_cast<size_t>(bh) * p.R + qrow;  // row in [B*Hq*Nq]
-    const bool row_valid = qrow < p.R;
-    const uint32_t so = sbase + C::kOffQ + t * C::kTileBytes;
-    if (ok) ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarOFinal + t), 0));
-    // fp16 P: O~ is held at V's scale 2^-K, fixed by the CTA's first V tile.  The wait is for
-    // this tile's last conversion (which follows the first); that barrier phase cannot have
-    // been reused yet, as the converters are at most one V tile ahead of this tile's last.
-    if (kF16 && ok && nt > 0) {
-      ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarConv + (nt - 1) % C::kSlots), ((nt - 1) / C::kSlots) & 1));
-      if (ok) k_cur = *kscale;
-    }
-    const bool have = l_run > 0.f;
-    // fp16 P: O~ / l at V's scale 2^-k_cur; bf16 P: O~ / (sum of the rounded terms)
-    const float inv_l = have ? (kF16 ? exp2_int(k_cur) / l_run : 1.f / lp_run) : 0.f;
-    const float lse_row = have ? m_run * p.scale + logf(l_run) : -INFINITY;
-    if (ok && p.n_splits == 1) {
-      ptx::tc_fence_after();
-#pragma unroll 1
-      float2 nonfinite = make_float2(0.f, 0.f);  // fp16 P V: stays 0 unless some O~ value is inf or NaN
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        ptx::tmem_ld32(t_o + cc * 32, r);
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 x = make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1]));
-          if constexpr (kF16) nonfinite = __ffma2_rn(x, make_float2(0.f, 0.f), nonfinite);
-          pk[i] = ptx::pack_bf16x2(x.x * inv_l, x.y * inv_l);
-        }
-        const uint32_t chunk_base = so + (cc >> 1) * C::kChunkBytes + row * 128;
-#pragma unroll
-        for (int g = 0; g < 4; ++g) {
-          const int gran = (cc & 1) * 4 + g;  // 16-byte granule within the 128-byte row
-          ptx::st_shared_v4(chunk_base + ((gran ^ (row & 7)) << 4), pk[4 * g], pk[4 * g + 1],
-                            pk[4 * g + 2], pk[4 * g + 3]);
-        }
-      }
-      if (row_valid) p.lse[grow] = lse_row;
-      if (kF16 && __any_sync(0xffffffffu, row_valid && have && l_run < INFINITY &&
-                                               !(nonfinite.x == 0.f && nonfinite.y == 0.f)) && lane == 0)
-        atomicOr(&g_status, FA_STATUS_V_RANGE);  // a V tile fp16 could not hold at the CTA's scale
-      ptx::fence_proxy_async_smem();
-    } else if (ok && p.n_splits > 1) {
-      ptx::tc_fence_after();
-      float4* dst = reinterpret_cast<float4*>(p.o_part + (static_cast<size_t>(my_split) * p.groups * p.R + grow) * D);
-      float2 nonfinite = make_float2(0.f, 0.f);  // fp16 P V: stays 0 unless some O~ value is inf or NaN
-#pragma unroll 1
-      for (int cc = 0; cc < D / 32; ++cc) {
-        uint32_t r[32];
-        ptx::tmem_ld32(t_o + cc * 32, r);
-        if constexpr (kF16) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i)
-            nonfinite = __ffma2_rn(make_float2(__uint_as_float(r[2 * i]), __uint_as_float(r[2 * i + 1])),
-                                   make_float2(0.f, 0.f), nonfinite);
-        }
-        if (row_valid) {
-#pragma unroll
-          for (int i = 0; i < 8; ++i)
-            dst[cc * 8 + i] = make_float4(__uint_as_float(r[4 * i]) * inv_l, __uint_as_float(r[4 * i + 1]) * inv_l,
-                                          __uint_as_float(r[4 * i + 2]) * inv_l, __uint_as_float(r[4 * i + 3]) * inv_l);
-        }
-      }
-      if (row_valid) p.lse_part[static_cast<size_t>(my_split) * p.groups * p.R + grow] = lse_row;
-      if (kF16 && __any_sync(0xffffffffu, row_valid && have && l_run < INFINITY &&
-                                               !(nonfinite.x == 0.f && nonfinite.y == 0.f)) && lane == 0)
-        atomicOr(&g_status, FA_STATUS_V_RANGE);  // a V tile fp16 could not hold at the CTA's scale
-    } else if (tile_exists && nt == 0 && row_valid) {
-      // no K/V tile of this split is visible to the tile: the empty result
-      if (p.n_splits == 1) {
-        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.o_bf16) + grow * D * 2);
-        for (int i = 0; i < D / 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
-        p.lse[grow] = -INFINITY;
-      } else {
-        float4* dst = reinterpret_cast<float4*>(p.o_part + (static_cast<size_t>(my_split) * p.groups * p.R + grow) * D);
-        for (int i = 0; i < D / 4; ++i) dst[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        p.lse_part[static_cast<size_t>(my_split) * p.groups * p.R + grow] = -INFINITY;
-      }
-    }
-    ptx::named_barrier(1 + t, 128);
-    if (ok && p.n_splits == 1 && row == 0) {
-      for (int c = 0; c < C::kChunks; ++c) ptx::tma_store_3d(&tm_o, so + c * C::kChunkBytes, c * 64, qt * 128, bh);
-      ptx::bulk_commit();
-      ptx::bulk_wait_all();
+      const int nx = next_item(k);
+      if (nx < 0) break;
+      idx = nx;
     }
   }
 
+  if (warp < 8 && (threadIdx.x & 127) == 0) ptx::bulk_wait_all();  // the O stores this thread issued
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 9) {
@@ -1008,7 +1357,6 @@ int launch(const Problem& pr, int withhold_tile, unsigned long long timeout_ns, 
   p.scale_log2 = static_cast<float>(static_cast<double>(pr.scale) * 1.4426950408889634);
   p.causal = pr.causal ? 1 : 0;
   const bool dual = p.n_qtiles == 1 && pr.n_splits > 1;
-  p.withhold_v0 = 0;
   p.withhold_tile = withhold_tile;
   p.v_raw = static_cast<const uint16_t*>(pr.v);
   p.timeout_ns = timeout_ns;

@@ -8,6 +8,8 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include <utility>
+
 namespace fa {
 namespace ptx {
 
@@ -46,6 +48,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+// ---------------------------------------------------------------- cluster launch control
+// Ask to take over a CTA of this grid that has not started yet (its cluster of one is
+// cancelled and this CTA does its work).  The 16-byte response lands at `resp` and is counted
+// on `bar` as 16 transaction bytes; read it with clc_query once that phase completes.  A CTA
+// issues no further request after one has failed.
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+  asm volatile("clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 [%0], [%1];" ::"r"(
+                   resp),
+               "r"(bar)
+               : "memory");
+}
+// true when the request took a CTA over; then *x is that CTA's blockIdx.x
+__device__ __forceinline__ bool clc_query(uint32_t resp, int* x) {
+  uint32_t took, cx;
+  asm volatile(
+      "{\n\t.reg .b128 h;\n\t.reg .pred p;\n\t"
+      "ld.shared.b128 h, [%2];\n\t"
+      "clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t"
+      "clusterlaunchcontrol.query_cancel.get_first_ctaid::x.b32.b128 %1, h;\n\t}\n"
+      : "=r"(took), "=r"(cx)
+      : "r"(resp)
+      : "memory");
+  *x = static_cast<int>(cx);
+  return took != 0;
 }
 
 // ---------------------------------------------------------------- TMA
@@ -293,15 +322,17 @@ __device__ __forceinline__ void tmem_wait_st() {
 // ---------------------------------------------------------------- tcgen05.mma
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
 // stride byte offsets (16-byte units), version 1 at bit 46, 128-byte swizzle.
+// The two 32-bit halves: the low one holds the start address and the leading byte offset,
+// the high one the stride byte offset, the version and the swizzle mode (a constant per layout).
+__host__ __device__ constexpr uint32_t desc_sw128_lo(uint32_t saddr, uint32_t lbo_bytes) {
+  return ((saddr & 0x3FFFFu) >> 4) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
+}
+__host__ __device__ constexpr uint32_t desc_sw128_hi(uint32_t sbo_bytes) {
+  return ((sbo_bytes >> 4) & 0x3FFFu) | (1u << 14) | (2u << 29);
+}
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
                                                     uint32_t sbo_bytes) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
-  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
-  return d;
+  return (static_cast<uint64_t>(desc_sw128_hi(sbo_bytes)) << 32) | desc_sw128_lo(saddr, lbo_bytes);
 }
 
 // Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, dense.
@@ -393,6 +424,53 @@ __device__ __forceinline__ void mma_ts_f8_i(uint32_t d_tmem, uint32_t a_tmem, ui
       "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "n"(kAccumulate)
       : "memory");
+}
+
+// The same two MMA forms with each shared-memory descriptor given as its low half (address and
+// leading offset) plus a constant step; the high half (stride, version, swizzle), shared by A and
+// B, is an immediate.  Forming the 64-bit descriptors inside the instruction's own block keeps a
+// long unrolled run of MMAs from holding one register pair per descriptor.
+template <int kAccumulate, uint32_t kHi, uint32_t kStep>
+__device__ __forceinline__ void mma_ss_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 la, lb, hh;\n\t.reg .b64 da, db;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "add.u32 la, %1, %5;\n\t"
+      "add.u32 lb, %2, %5;\n\t"
+      "mov.b32 hh, %6;\n\t"
+      "mov.b64 da, {la, hh};\n\t"
+      "mov.b64 db, {lb, hh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_lo), "r"(b_lo), "r"(idesc), "n"(kAccumulate), "n"(kStep), "n"(kHi)
+      : "memory");
+}
+// A from tensor memory (its address plus kTStep columns), B from shared memory (low half plus kBStep)
+template <int kAccumulate, uint32_t kHi, uint32_t kTStep, uint32_t kBStep>
+__device__ __forceinline__ void mma_ts_lo(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t.reg .b32 ta, lb, hh;\n\t.reg .b64 db;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "add.u32 ta, %1, %5;\n\t"
+      "add.u32 lb, %2, %6;\n\t"
+      "mov.b32 hh, %7;\n\t"
+      "mov.b64 db, {lb, hh};\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "r"(b_lo), "r"(idesc), "n"(kAccumulate), "n"(kTStep), "n"(kBStep), "n"(kHi)
+      : "memory");
+}
+// S = Q K^T over d = 16 * (sizeof...(KK)) columns: one MMA per 16 columns, K-major 128-byte
+// swizzle atoms of 64 columns (+32 B inside an atom, the next atom 16 KB on)
+template <uint32_t kHi, int... KK>
+__device__ __forceinline__ void mma_qk_run(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                           std::integer_sequence<int, KK...>) {
+  (mma_ss_lo<(KK > 0), kHi, static_cast<uint32_t>((KK >> 2) * 1024 + (KK & 3) * 2)>(d_tmem, a_lo, b_lo, idesc), ...);
+}
+// O += P V over 128 keys, P's first 16 keys already issued: one MMA per further 16 keys (8 P
+// columns of packed pairs, V 8 rows of 128 bytes on)
+template <uint32_t kHi, int... KK>
+__device__ __forceinline__ void mma_pv_rest(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo, uint32_t idesc,
+                                            std::integer_sequence<int, KK...>) {
+  (mma_ts_lo<1, kHi, static_cast<uint32_t>((KK + 1) * 8), static_cast<uint32_t>((KK + 1) * 128)>(d_tmem, p_tmem, v_lo, idesc), ...);
 }
 
 // true in exactly one lane of the (fully converged) warp

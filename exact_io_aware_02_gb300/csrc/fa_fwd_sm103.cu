@@ -28,9 +28,11 @@
 //   * warp 9  -- MMA issuer (one thread): S_t = Q_t K_j^T with tcgen05.mma
 //                (A and B from shared memory, fp32 accumulator in tensor memory),
 //                then O_t += P_t V_j with P_t read from tensor memory; P_t is handed
-//                over through a hardware named barrier per tile (bar.arrive by the
-//                tile's softmax warps, bar.sync by this warp).  The next item's S
-//                products start right after the current item's last P V products;
+//                over in two halves (keys 0-63, 64-127) through hardware named
+//                barriers (bar.arrive by the tile's softmax warps, bar.sync by this
+//                warp), so that the first half's products run while the softmax
+//                computes the second.  The next item's S products start right after
+//                the current item's last P V products;
 //   * warps 8, 10, 11 -- convert each landed V tile to fp16 in place for the P V product;
 //   * warps 0-3 / 4-7 -- softmax for tile 0 / tile 1, one row per thread:
 //                row max, exp2 with scale*log2(e) folded in, running (m, l),
@@ -650,7 +652,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (j >= 1 && j - 1 < nt) {
                 ok = __all_sync(0xffffffffu, w.wait(bar(C::kBarFull + u % C::kSlots), (u / C::kSlots) & 1));
                 if (!ok) break;
-                ptx::named_barrier(3 + t, 160);  // P_t(j-1) handed over (see the non-dual loop)
+                ptx::named_barrier(3 + t, 160);  // P_t(j-1) handed over in two halves (see the non-dual loop)
+                ptx::named_barrier(5 + t, 160);
                 ptx::tc_fence_after();
                 const uint32_t dv = desc_v_ring + (u % C::kSlots) * kSlotStep;
                 const uint32_t t_o = tmem + C::kColO + t * D;
@@ -746,14 +749,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // the step before).  Across items the same holds: the first wait of an item
                 // follows the O-empty waits, which the softmax warps pass only by finishing the
                 // previous item.
-                ptx::named_barrier(3 + t, 160);
-                ptx::tc_fence_after();
+                // P arrives in two halves, keys 0-63 then 64-127 (barriers 3 + t, 5 + t): the first
+                // half's products run while the softmax warps compute the second half.
                 const uint32_t t_o = tmem + C::kColO + t * D;
                 const uint32_t t_p = tmem + C::kColS + t * 128;
+                ptx::named_barrier(3 + t, 160);
+                ptx::tc_fence_after();
                 if (ptx::elect_one()) {
                   if (j > 1) ptx::mma_ts_lo<1, kDescHi32, 0, 0>(t_o, t_p, dv, kIdescPV);
                   else ptx::mma_ts_lo<0, kDescHi32, 0, 0>(t_o, t_p, dv, kIdescPV);
-                  ptx::mma_pv_rest<kDescHi32>(t_o, t_p, dv, kIdescPV, std::make_integer_sequence<int, 7>{});
+                  ptx::mma_pv_run<kDescHi32, 1>(t_o, t_p, dv, kIdescPV, std::make_integer_sequence<int, 3>{});
+                }
+                __syncwarp();
+                ptx::named_barrier(5 + t, 160);
+                ptx::tc_fence_after();
+                if (ptx::elect_one()) {
+                  ptx::mma_pv_run<kDescHi32, 4>(t_o, t_p, dv, kIdescPV, std::make_integer_sequence<int, 4>{});
                   if (j == nt) ptx::tc_commit(bar(C::kBarOFinal + t));
                 }
                 __syncwarp();
@@ -1028,6 +1039,25 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int k = 0; k < 32; ++k) half[k] = pk[i - 31 + k];
               ptx::tmem_st32(t_s + (i - 31), half);
             }
+            if (i == 31) {
+              // keys 0-63 of P_t(j) are stored: hand them over, after the correction O~ *= r
+              // (PV_t(j-1) has completed: the commit behind S_t(j) covers it; PV_t(j) waits for
+              // this arrive), so that their products run while the second half is computed
+              if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                  uint32_t r[32];
+                  ptx::tmem_ld32(t_o + cc * 32, r);
+#pragma unroll
+                  for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) * r_fac);
+                  ptx::tmem_st32(t_o + cc * 32, r);
+                }
+              }
+              ptx::tmem_wait_st();
+              ptx::tc_fence_before();
+              __syncwarp();
+              ptx::named_barrier_arrive(3 + t, 160);
+            }
           }
           const float2 se01 = __fadd2_rn(se[0], se[1]), se23 = __fadd2_rn(se[2], se[3]);
           l_run = l_run * r_fac + ((se01.x + se01.y) + (se23.x + se23.y));
@@ -1036,39 +1066,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             lp_run = lp_run * r_fac + ((sp01.x + sp01.y) + (sp23.x + sp23.y));
           }
           m_run = m_ref;
-          // correction O~ *= r, before P_t(j) is handed over: PV_t(j-1) has completed (the commit
-          // behind S_t(j) covers it) and PV_t(j) waits for the arrive below
-          if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-            if constexpr (kSplitS) {  // all 128 columns of O_t in one load (S and P are dead here)
-              uint32_t r[128];
-              ptx::tmem_ld128(t_o, r);
-#pragma unroll
-              for (int i = 0; i < 128; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
-#pragma unroll
-              for (int cc = 0; cc < 4; ++cc) {
-                uint32_t part[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) part[i] = r[cc * 32 + i];
-                ptx::tmem_st32(t_o + cc * 32, part);
-              }
-            } else {
-#pragma unroll 1
-              for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t r[32];
-                ptx::tmem_ld32(t_o + cc * 32, r);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * r_fac);
-                ptx::tmem_st32(t_o + cc * 32, r);
-              }
-            }
-          }
           ptx::tmem_wait_st();
           ptx::tc_fence_before();
           __syncwarp();
-          ptx::named_barrier_arrive(3 + t, 160);  // P_t(j) handed over to the MMA warp
+          ptx::named_barrier_arrive(5 + t, 160);  // keys 64-127 of P_t(j) handed over to the MMA warp
         }
         if (!ok) {
-          for (; j < nt && w.drain(bar(C::kBarSFull + t), n_s & 1); ++j, ++n_s) ptx::named_barrier_arrive(3 + t, 160);
+          for (; j < nt && w.drain(bar(C::kBarSFull + t), n_s & 1); ++j, ++n_s) {
+            ptx::named_barrier_arrive(3 + t, 160);
+            ptx::named_barrier_arrive(5 + t, 160);
+          }
           break;
         }
         idx = park[0];

@@ -465,12 +465,14 @@ __device__ __forceinline__ void mma_qk_run(uint32_t d_tmem, uint32_t a_lo, uint3
                                            std::integer_sequence<int, KK...>) {
   (mma_ss_lo<(KK > 0), kHi, static_cast<uint32_t>((KK >> 2) * 1024 + (KK & 3) * 2)>(d_tmem, a_lo, b_lo, idesc), ...);
 }
-// O += P V over 128 keys, P's first 16 keys already issued: one MMA per further 16 keys (8 P
-// columns of packed pairs, V 8 rows of 128 bytes on)
-template <uint32_t kHi, int... KK>
-__device__ __forceinline__ void mma_pv_rest(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo, uint32_t idesc,
-                                            std::integer_sequence<int, KK...>) {
-  (mma_ts_lo<1, kHi, static_cast<uint32_t>((KK + 1) * 8), static_cast<uint32_t>((KK + 1) * 128)>(d_tmem, p_tmem, v_lo, idesc), ...);
+// O += P V over keys 16 (kFirst + KK) .. +15 for each KK: one MMA per 16 keys (8 P columns of
+// packed pairs, V 8 rows of 128 bytes on), accumulating
+template <uint32_t kHi, int kFirst, int... KK>
+__device__ __forceinline__ void mma_pv_run(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_lo, uint32_t idesc,
+                                           std::integer_sequence<int, KK...>) {
+  (mma_ts_lo<1, kHi, static_cast<uint32_t>((kFirst + KK) * 8), static_cast<uint32_t>((kFirst + KK) * 128)>(
+       d_tmem, p_tmem, v_lo, idesc),
+   ...);
 }
 
 // true in exactly one lane of the (fully converged) warp

@@ -76,8 +76,9 @@ extern "C" {
  *
  * Precision: S, O and the row sums accumulate in fp32; P is rounded to fp16 for
  * the P V product, with V converted to fp16 in shared memory at a power-of-two
- * scale that each CTA fixes from the first V tile it reads (1 unless that tile's
- * largest |v| is below 2^-4 or at least 65520).  A later V tile that fp16 cannot
+ * scale fixed per work item (a pair of 128-row query tiles over one key range) from
+ * the first V tile it reads (1 unless that tile's largest |v| is below 2^-4 or at
+ * least 65520).  A later V tile that fp16 cannot
  * hold at that scale (with the scale 1: any |v| >= 65520) is saturated and sets
  * FA_STATUS_V_RANGE; that call's O is then not exact.
  *
@@ -350,10 +351,11 @@ int fa_fwd_withheld_tile(const void* q, const void* k, const void* v, void* o, f
 
 /*
  * fa_fwd_withheld_ring_tile -- the same test hook with the withheld tile chosen: ring_tile
- * (>= 0) indexes the K/V tiles in the order a CTA's producer loads them, K_0 = 0, V_0 = 1,
- * K_1 = 2, V_1 = 3, ...  (fa_fwd_withheld_tile is ring_tile = 1).  CTAs that load fewer
- * tiles run to completion; the others give up as above, some after handing P over for the
- * steps before the missing tile.  Returns FA_ERR_ARG for ring_tile < 0 or a timeout outside
+ * (>= 0) indexes the K/V tiles of a CTA's first work item in the order its producer loads
+ * them, K_0 = 0, V_0 = 1, K_1 = 2, V_1 = 3, ...  (fa_fwd_withheld_tile is ring_tile = 1).
+ * CTAs whose first item loads fewer tiles run to completion; the others give up as above,
+ * some after handing P over for the steps before the missing tile, and take on no further
+ * item.  Returns FA_ERR_ARG for ring_tile < 0 or a timeout outside
  * [1, 10000] ms; otherwise as fa_fwd_withheld_tile.
  */
 int fa_fwd_withheld_ring_tile(const void* q, const void* k, const void* v, void* o, float* lse,

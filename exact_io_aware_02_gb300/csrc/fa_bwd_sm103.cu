@@ -94,6 +94,24 @@ __device__ __forceinline__ int bwd_tile_max_pos(const BwdParams& p, int qt) {
   return (r1 / p.N != r0 / p.N) ? p.N - 1 : r1 % p.N;
 }
 
+// The query tiles of a group in order, with the sequence position of each tile's first row
+// (its row mod N) carried from tile to tile, so that testing whether a tile reaches a key tile
+// costs a few additions and no division (a loop over every tile with divisions took a key
+// tile's CTA several microseconds before its first load).
+struct QTileWalk {
+  int qt = 0, pos0 = 0;
+  // the highest position of the tile's rows (a tile straddling heads reaches N - 1)
+  __device__ __forceinline__ int max_pos(const BwdParams& p) const {
+    const int last = pos0 + min(128, p.R - qt * 128) - 1;
+    return last >= p.N ? p.N - 1 : last;
+  }
+  __device__ __forceinline__ void next(const BwdParams& p) {
+    ++qt;
+    pos0 += 128;
+    while (pos0 >= p.N) pos0 -= p.N;
+  }
+};
+
 template <int D>
 struct BwdCfg {
   static constexpr int kChunks = D / 64;
@@ -301,10 +319,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x % p.groups;
   const int kt = blockIdx.x / p.groups;  // causal: the first key tiles have the most work, so go first
-  // query tiles that see this key tile: causal needs some position >= kt*128
-  auto needed = [&](int qt) { return !p.causal || bwd_tile_max_pos(p, qt) >= kt * 128; };
-  int n_q = 0;
-  for (int qt = 0; qt < p.n_qtiles; ++qt) n_q += needed(qt) ? 1 : 0;
+  // query tiles that see this key tile: causal needs some position >= kt*128 (counted once,
+  // by the thread that initialises the barriers, and shared)
+  auto needed = [&](const QTileWalk& q) { return !p.causal || q.max_pos(p) >= kt * 128; };
+  volatile int* n_q_slot = reinterpret_cast<volatile int*>(smem + C::kKVOffBar + C::kMaxBars * 8 + 8);
 
   if (warp == kBwdComputeWarps && lane == 0) {
     ptx::mbar_init(bar(kBarKV), 1);
@@ -317,6 +335,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(bar(kBarFinal), 1);
     ptx::mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0u;
+    int count = 0;
+    for (QTileWalk q; q.qt < p.n_qtiles; q.next(p)) count += needed(q) ? 1 : 0;
+    *n_q_slot = count;
     ptx::fence_mbar_init();
   }
   if (warp == kBwdComputeWarps + 1) {
@@ -327,6 +348,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  const int n_q = *n_q_slot;
   const Waiter w{abort_flag, p.timeout_ns};
   constexpr float kLog2e = 1.4426950408889634f;
 
@@ -341,8 +363,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     int u = 0, issued = 0;
     bool ok = true;
-    for (int qt = 0; qt < p.n_qtiles && ok; ++qt) {
-      if (!needed(qt)) continue;
+    for (QTileWalk qw; qw.qt < p.n_qtiles && ok; qw.next(p)) {
+      if (!needed(qw)) continue;
+      const int qt = qw.qt;
       const int s = u % S, use = u / S;
       // -LSE*log2(e) and -D of the tile's rows (padding rows: 0): eight independent,
       // bounds-checked loads per lane, issued before the wait so their latency hides there
@@ -456,14 +479,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float c2 = p.scale_log2;
     bool ok = true;
     int u = 0, np = 0;  // query tiles whose dS^T (P^T) has been handed over
-    for (int qt = 0; qt < p.n_qtiles && ok; ++qt) {
-      if (!needed(qt)) continue;
+    for (QTileWalk qw; qw.qt < p.n_qtiles && ok; qw.next(p)) {
+      if (!needed(qw)) continue;
+      const int qt = qw.qt;
       const int s = u % S;
       // the tile needs no mask when all 128 rows exist, all keys exist and (causal) its
       // lowest position is at or after the key tile's last key
       const int r0 = qt * 128;
       const int n_rows = min(128, p.R - r0);
-      const int pos0 = r0 % p.N;
+      const int pos0 = qw.pos0;
       const bool one_head = pos0 + 128 <= p.N;
       const bool no_mask = n_rows == 128 && key_tile_full && (!p.causal || (one_head && pos0 >= kt * 128 + 127));
       ok = __all_sync(0xffffffffu, w.wait(bar(kBarS), u & 1));

@@ -94,10 +94,11 @@ __device__ __forceinline__ int bwd_tile_max_pos(const BwdParams& p, int qt) {
   return (r1 / p.N != r0 / p.N) ? p.N - 1 : r1 % p.N;
 }
 
-// The query tiles of a group in order, with the sequence position of each tile's first row
-// (its row mod N) carried from tile to tile, so that testing whether a tile reaches a key tile
-// costs a few additions and no division (a loop over every tile with divisions took a key
-// tile's CTA several microseconds before its first load).
+// The query tiles of a group that reach key tile kt, in order, with the sequence position of
+// each tile's first row (its row mod N) carried along.  With causal masking the tiles of a head
+// that end before position kt*128 are jumped over in one step (one division per head), not
+// tested one by one: a loop over every tile with divisions took a key tile's CTA several
+// microseconds before its first load.
 struct QTileWalk {
   int qt = 0, pos0 = 0;
   // the highest position of the tile's rows (a tile straddling heads reaches N - 1)
@@ -105,10 +106,22 @@ struct QTileWalk {
     const int last = pos0 + min(128, p.R - qt * 128) - 1;
     return last >= p.N ? p.N - 1 : last;
   }
-  __device__ __forceinline__ void next(const BwdParams& p) {
+  // from the current tile to the first that reaches key tile kt: a tile that does not lies in
+  // one head, below position kt*128, and the tile holding that position of the same head does
+  __device__ __forceinline__ void seek(const BwdParams& p, int kt) {
+    if (!p.causal) return;
+    while (qt < p.n_qtiles && max_pos(p) < kt * 128) {
+      const int head_row0 = qt * 128 - pos0;
+      const int to = (head_row0 + kt * 128) / 128;
+      pos0 += (to - qt) * 128;
+      qt = to;
+    }
+  }
+  __device__ __forceinline__ void next(const BwdParams& p, int kt) {
     ++qt;
     pos0 += 128;
     while (pos0 >= p.N) pos0 -= p.N;
+    seek(p, kt);
   }
 };
 
@@ -319,9 +332,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int bh = blockIdx.x % p.groups;
   const int kt = blockIdx.x / p.groups;  // causal: the first key tiles have the most work, so go first
-  // query tiles that see this key tile: causal needs some position >= kt*128 (counted once,
-  // by the thread that initialises the barriers, and shared)
-  auto needed = [&](const QTileWalk& q) { return !p.causal || q.max_pos(p) >= kt * 128; };
+  // the query tiles that see this key tile (causal: some position >= kt*128), counted once by
+  // the thread that initialises the barriers and shared
   volatile int* n_q_slot = reinterpret_cast<volatile int*>(smem + C::kKVOffBar + C::kMaxBars * 8 + 8);
 
   if (warp == kBwdComputeWarps && lane == 0) {
@@ -336,7 +348,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0u;
     int count = 0;
-    for (QTileWalk q; q.qt < p.n_qtiles; q.next(p)) count += needed(q) ? 1 : 0;
+    QTileWalk q;
+    for (q.seek(p, kt); q.qt < p.n_qtiles; q.next(p, kt)) ++count;
     *n_q_slot = count;
     ptx::fence_mbar_init();
   }
@@ -363,8 +376,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     int u = 0, issued = 0;
     bool ok = true;
-    for (QTileWalk qw; qw.qt < p.n_qtiles && ok; qw.next(p)) {
-      if (!needed(qw)) continue;
+    QTileWalk qw;
+    for (qw.seek(p, kt); qw.qt < p.n_qtiles && ok; qw.next(p, kt)) {
       const int qt = qw.qt;
       const int s = u % S, use = u / S;
       // -LSE*log2(e) and -D of the tile's rows (padding rows: 0): eight independent,
@@ -479,8 +492,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float c2 = p.scale_log2;
     bool ok = true;
     int u = 0, np = 0;  // query tiles whose dS^T (P^T) has been handed over
-    for (QTileWalk qw; qw.qt < p.n_qtiles && ok; qw.next(p)) {
-      if (!needed(qw)) continue;
+    QTileWalk qw;
+    for (qw.seek(p, kt); qw.qt < p.n_qtiles && ok; qw.next(p, kt)) {
       const int qt = qw.qt;
       const int s = u % S;
       // the tile needs no mask when all 128 rows exist, all keys exist and (causal) its

@@ -333,25 +333,28 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int bh = blockIdx.x % p.groups;
   const int kt = blockIdx.x / p.groups;  // causal: the first key tiles have the most work, so go first
   // the query tiles that see this key tile (causal: some position >= kt*128), counted once by
-  // the thread that initialises the barriers and shared
+  // the producer warp and shared
   volatile int* n_q_slot = reinterpret_cast<volatile int*>(smem + C::kKVOffBar + C::kMaxBars * 8 + 8);
 
-  if (warp == kBwdComputeWarps && lane == 0) {
-    ptx::mbar_init(bar(kBarKV), 1);
-    for (int s = 0; s < S; ++s) {
-      ptx::mbar_init(bar(kBarFull + s), 2);  // TMA bytes + the producer's LSE/D stores
-      ptx::mbar_init(bar(kBarEmpty + s), 1);
-    }
-    ptx::mbar_init(bar(kBarS), 1);
-    ptx::mbar_init(bar(kBarDP), 1);
-    ptx::mbar_init(bar(kBarFinal), 1);
-    ptx::mbar_init(bar(kBarDrain), 1);
-    *abort_flag = 0u;
+  if (warp == kBwdComputeWarps) {
+    // the count, a tile per lane at a time
     int count = 0;
-    QTileWalk q;
-    for (q.seek(p, kt); q.qt < p.n_qtiles; q.next(p, kt)) ++count;
-    *n_q_slot = count;
-    ptx::fence_mbar_init();
+    for (int qt = lane; qt < p.n_qtiles; qt += 32) count += (!p.causal || bwd_tile_max_pos(p, qt) >= kt * 128) ? 1 : 0;
+    count = __reduce_add_sync(0xffffffffu, count);
+    if (lane == 0) {
+      ptx::mbar_init(bar(kBarKV), 1);
+      for (int s = 0; s < S; ++s) {
+        ptx::mbar_init(bar(kBarFull + s), 2);  // TMA bytes + the producer's LSE/D stores
+        ptx::mbar_init(bar(kBarEmpty + s), 1);
+      }
+      ptx::mbar_init(bar(kBarS), 1);
+      ptx::mbar_init(bar(kBarDP), 1);
+      ptx::mbar_init(bar(kBarFinal), 1);
+      ptx::mbar_init(bar(kBarDrain), 1);
+      *abort_flag = 0u;
+      *n_q_slot = count;
+      ptx::fence_mbar_init();
+    }
   }
   if (warp == kBwdComputeWarps + 1) {
     ptx::tmem_alloc(ptx::smem_addr(tmem_slot), 512);

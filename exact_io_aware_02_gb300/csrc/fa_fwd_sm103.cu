@@ -882,7 +882,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.lse_part[static_cast<size_t>(w_.my_split) * p.groups * p.R + w_.grow] = -INFINITY;
       }
     };
+    // row 0's staging slot + 1 whose store has not yet been waited for (kept in this warp's park
+    // entry 7, not in a register through the K/V steps)
+    volatile int* pend = reinterpret_cast<volatile int*>(smem + C::kOffPark) + warp * 8 + 7;
+    if (row == 0) *pend = 0;
     for (int k = 0;; ++k) {
+      // the previous item's O store: its staging slot is released once the store has read it,
+      // here rather than in the epilogue, before any wait of this item (the producer may need
+      // the slot before this tile's next S)
+      if (row == 0) {
+        const int ps = *pend;
+        if (ps) {
+          ptx::bulk_wait_read<0>();
+          ptx::mbar_arrive(bar(C::kBarEmpty + ps - 1));
+          *pend = 0;
+        }
+      }
       const Item it = decode_item<kDual>(p, idx);
       const int nt = t ? it.n1 : it.n0;
       const int qpos = p.q_offset + ((t ? it.qt1 : it.qt0) * 128 + row) % p.Nq;  // sequence position (causal mask)
@@ -1167,8 +1182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row == 0) {  // the stores, and the slot's release once they have read it
               for (int c = 0; c < D / 64; ++c) ptx::tma_store_3d(&tm_o, stage + c * C::kChunkBytes, c * 64, rw.row0, rw.bh);
               ptx::bulk_commit();
-              ptx::bulk_wait_read<0>();
-              ptx::mbar_arrive(bar(C::kBarEmpty + stage_slot));
+              *pend = static_cast<int>(stage_slot) + 1;  // released at the next item's top
             }
             if (rw.row_valid) p.lse[rw.grow] = lse_row;
           } else if (rw.row_valid) {

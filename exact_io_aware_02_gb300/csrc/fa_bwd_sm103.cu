@@ -41,34 +41,65 @@ constexpr uint32_t kNbP = 2, kNbDS = 3;
 constexpr uint32_t kHandOffThreads = 32 * (kBwdComputeWarps + 1);
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
+// Memory-bound: each lane reads 16-byte pieces (8 elements) of a row of O and of dO, a row
+// spans D/8 lanes, and every lane has kPrepLoads pieces of each tensor in flight.  The sum is
+// formed in one fixed order: sequential fused multiply-adds over runs of D/32 elements, then a
+// pairwise tree over the D/32-element runs (the partner at the largest distance first), so D is
+// the same bits whatever the load width.
+constexpr int kPrepThreads = 256, kPrepLoads = 4;
 template <int D>
-__global__ void __launch_bounds__(256)
+__host__ __device__ constexpr int prep_rows_per_warp() { return (32 / (D / 8)) * kPrepLoads; }
+
+template <int D>
+__global__ void __launch_bounds__(kPrepThreads)
     fa_bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                        float* __restrict__ dvec, int rows) {
-  constexpr int E = D / 32;
-  const int row = static_cast<int>((static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  constexpr int kLanesPerRow = D / 8, kRowsPerLoad = 32 / kLanesPerRow;
+  constexpr int kRun = D / 32;          // elements per sequential run
+  constexpr int kRuns = 8 / kRun;       // runs per 16-byte piece
+  constexpr int kWordsPerRun = kRun / 2;
   const int lane = threadIdx.x & 31;
-  if (row >= rows) return;
-  const size_t base = static_cast<size_t>(row) * D + lane * E;
-  float acc = 0.f;
-  if constexpr (E == 4) {
-    const uint2 a = *reinterpret_cast<const uint2*>(o + base);
-    const uint2 b = *reinterpret_cast<const uint2*>(dout + base);
-    const uint32_t av[2] = {a.x, a.y}, bv[2] = {b.x, b.y};
+  const long long warp_id = static_cast<long long>(blockIdx.x) * (kPrepThreads / 32) + (threadIdx.x >> 5);
+  const long long row0 = warp_id * prep_rows_per_warp<D>() + lane / kLanesPerRow;
+  const int piece = lane % kLanesPerRow;
+  uint4 a[kPrepLoads], b[kPrepLoads];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      acc += __uint_as_float(av[i] << 16) * __uint_as_float(bv[i] << 16);
-      acc += __uint_as_float(av[i] & 0xffff0000u) * __uint_as_float(bv[i] & 0xffff0000u);
+  for (int i = 0; i < kPrepLoads; ++i) {
+    const long long row = row0 + i * kRowsPerLoad;
+    a[i] = b[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (row < rows) {
+      const size_t off = static_cast<size_t>(row) * D + piece * 8;
+      a[i] = __ldg(reinterpret_cast<const uint4*>(o + off));
+      b[i] = __ldg(reinterpret_cast<const uint4*>(dout + off));
     }
-  } else {
-    const uint32_t a = *reinterpret_cast<const uint32_t*>(o + base);
-    const uint32_t b = *reinterpret_cast<const uint32_t*>(dout + base);
-    acc += __uint_as_float(a << 16) * __uint_as_float(b << 16);
-    acc += __uint_as_float(a & 0xffff0000u) * __uint_as_float(b & 0xffff0000u);
   }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-  if (lane == 0) dvec[row] = acc;
+  for (int i = 0; i < kPrepLoads; ++i) {
+    const uint32_t av[4] = {a[i].x, a[i].y, a[i].z, a[i].w}, bv[4] = {b[i].x, b[i].y, b[i].z, b[i].w};
+    float part[kRuns];
+#pragma unroll
+    for (int r = 0; r < kRuns; ++r) {
+      float acc = 0.f;
+#pragma unroll
+      for (int w = r * kWordsPerRun; w < (r + 1) * kWordsPerRun; ++w) {
+        acc += __uint_as_float(av[w] << 16) * __uint_as_float(bv[w] << 16);
+        acc += __uint_as_float(av[w] & 0xffff0000u) * __uint_as_float(bv[w] & 0xffff0000u);
+      }
+      part[r] = acc;
+    }
+    // the tree over the row's runs: first across lanes (run distances kRuns * off), then
+    // within the lane
+#pragma unroll
+    for (int off = kLanesPerRow / 2; off > 0; off >>= 1)
+#pragma unroll
+      for (int r = 0; r < kRuns; ++r) part[r] += __shfl_xor_sync(0xffffffffu, part[r], off);
+#pragma unroll
+    for (int step = kRuns / 2; step > 0; step >>= 1)
+#pragma unroll
+      for (int r = 0; r < step; ++r) part[r] = part[r] + part[r + step];
+    const long long row = row0 + i * kRowsPerLoad;
+    if (piece == 0 && row < rows) dvec[row] = part[0];
+  }
 }
 
 struct BwdParams {
@@ -176,27 +207,6 @@ __device__ __forceinline__ void bwd_mma_tn(uint32_t c, uint32_t a_tmem, uint64_t
     ptx::mma_ts_i<1>(c, a_tmem + (kk >> 2) * 64 + (kk & 3) * 8, db + kk * 128, idesc);
 }
 
-// Convert columns [c0, c0 + D/2) of a 128-row fp32 accumulator (this thread's row) to
-// bf16, times `mul`, into a 128B-swizzled shared tile (the TMA layout).
-template <int D>
-__device__ __forceinline__ void bwd_acc_to_smem(uint32_t t_acc, uint32_t smem_tile, int row, int c0, float mul) {
-#pragma unroll 1
-  for (int cc = c0 / 32; cc < (c0 + D / 2) / 32; ++cc) {
-    uint32_t r[32];
-    ptx::tmem_ld32(t_acc + cc * 32, r);
-    uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      pk[i] = ptx::pack_bf16x2(__uint_as_float(r[2 * i]) * mul, __uint_as_float(r[2 * i + 1]) * mul);
-    const uint32_t base = smem_tile + (cc >> 1) * BwdCfg<D>::kChunkBytes + row * 128;
-#pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      const int gran = (cc & 1) * 4 + g;
-      ptx::st_shared_v4(base + ((gran ^ (row & 7)) << 4), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
-    }
-  }
-}
-
 // The dK/dV kernel's first elementwise step for this thread's key row, over this warp's
 // 64 query columns: P^T = exp2(S^T * scale*log2(e) - LSE*log2(e)) into pr[] (fp32) and,
 // rounded to bf16 pairs, into tensor memory over the first 32 of the columns read.
@@ -224,6 +234,38 @@ __device__ __forceinline__ void bwd_wait_ld32(uint32_t (&r)[32]) {
         "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
                :
                : "memory");
+}
+
+// Convert columns [c0, c0 + D/2) of kN 128-row fp32 accumulators (this thread's row), each
+// times its own factor, to bf16 in 128B-swizzled shared tiles (the TMA layout).  Every
+// tensor-memory load is issued before the first is waited for: one round trip in all, not one
+// per 32 columns.
+template <int D, int kN>
+__device__ __forceinline__ void bwd_accs_to_smem(const uint32_t (&t_acc)[kN], const uint32_t (&smem_tile)[kN],
+                                                 const float (&mul)[kN], int row, int c0) {
+  constexpr int kC = D / 64;  // 32-column chunks per accumulator in this thread's half
+  uint32_t r[kN][kC][32];
+#pragma unroll
+  for (int n = 0; n < kN; ++n)
+#pragma unroll
+    for (int cc = 0; cc < kC; ++cc) bwd_ld32_nowait(t_acc[n] + c0 + 32 * cc, r[n][cc]);
+#pragma unroll
+  for (int n = 0; n < kN; ++n)
+#pragma unroll
+    for (int cc = 0; cc < kC; ++cc) {
+      bwd_wait_ld32(r[n][cc]);  // the first waits for every load; the others only order the registers
+      const int chunk = c0 / 32 + cc;  // 32-column chunk of the row
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        pk[i] = ptx::pack_bf16x2(__uint_as_float(r[n][cc][2 * i]) * mul[n], __uint_as_float(r[n][cc][2 * i + 1]) * mul[n]);
+      const uint32_t base = smem_tile[n] + (chunk >> 1) * BwdCfg<D>::kChunkBytes + row * 128;
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const int gran = (chunk & 1) * 4 + g;
+        ptx::st_shared_v4(base + ((gran ^ (row & 7)) << 4), pk[4 * g], pk[4 * g + 1], pk[4 * g + 2], pk[4 * g + 3]);
+      }
+    }
 }
 
 template <bool kMasked>
@@ -335,8 +377,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   // the query tiles that see this key tile (causal: some position >= kt*128), counted once by
   // the producer warp and shared
   volatile int* n_q_slot = reinterpret_cast<volatile int*>(smem + C::kKVOffBar + C::kMaxBars * 8 + 8);
+  // the dQ kernel, which reads nothing this grid writes, may take the SMs this grid leaves idle
+  ptx::griddep_launch_dependents();
 
+  // Producer state, carried across the set-up barrier: the walk over the query tiles and the
+  // LSE and D of the next tile's rows (loaded one tile ahead, so their latency hides behind the
+  // set-up and then behind each stage's wait)
+  QTileWalk qw;
+  float lse_next[4], d_next[4];
+  auto load_vec = [&](int qt) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int r = qt * 128 + lane + 32 * j;
+      const size_t g = static_cast<size_t>(bh) * p.R + (r < p.R ? r : 0);
+      lse_next[j] = r < p.R ? __ldg(p.lse + g) : 0.f;
+      d_next[j] = r < p.R ? __ldg(p.dvec + g) : 0.f;
+    }
+  };
   if (warp == kBwdComputeWarps) {
+    qw.seek(p, kt);
+    load_vec(qw.qt);
     // the count, a tile per lane at a time
     int count = 0;
     for (int qt = lane; qt < p.n_qtiles; qt += 32) count += (!p.causal || bwd_tile_max_pos(p, qt) >= kt * 128) ? 1 : 0;
@@ -354,6 +414,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       *abort_flag = 0u;
       *n_q_slot = count;
       ptx::fence_mbar_init();
+      // K, V and the first query tile's Q, dO start loading before the set-up barrier
+      ptx::mbar_arrive_expect_tx(bar(kBarKV), 2 * C::kTileBytes);
+      for (int c = 0; c < C::kChunks; ++c) {
+        ptx::tma_load_3d(sbase + c * C::kChunkBytes, &tm_k, bar(kBarKV), c * 64, kt * 128, bh);
+        ptx::tma_load_3d(sbase + C::kTileBytes + c * C::kChunkBytes, &tm_v, bar(kBarKV), c * 64, kt * 128, bh);
+      }
+      if (count > 0 && !p.withhold) {
+        ptx::mbar_arrive_expect_tx(bar(kBarFull), 2 * C::kTileBytes);
+        for (int c = 0; c < C::kChunks; ++c) {
+          ptx::tma_load_3d(stage_addr(0) + c * C::kChunkBytes, &tm_q, bar(kBarFull), c * 64, qw.qt * 128, bh);
+          ptx::tma_load_3d(stage_addr(0) + C::kTileBytes + c * C::kChunkBytes, &tm_do, bar(kBarFull), c * 64,
+                           qw.qt * 128, bh);
+        }
+      }
     }
   }
   if (warp == kBwdComputeWarps + 1) {
@@ -369,50 +443,39 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   constexpr float kLog2e = 1.4426950408889634f;
 
   if (warp == kBwdComputeWarps) {
-    // ------------------------------------------------ producer: K, V once; stages of Q, dO, LSE, D
-    if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(bar(kBarKV), 2 * C::kTileBytes);
-      for (int c = 0; c < C::kChunks; ++c) {
-        ptx::tma_load_3d(sbase + c * C::kChunkBytes, &tm_k, bar(kBarKV), c * 64, kt * 128, bh);
-        ptx::tma_load_3d(sbase + C::kTileBytes + c * C::kChunkBytes, &tm_v, bar(kBarKV), c * 64, kt * 128, bh);
-      }
-    }
+    // ------------------------------------------------ producer: stages of Q, dO, -LSE log2 e, -D
+    // (K, V and stage 0's Q, dO were issued before the set-up barrier)
     int u = 0, issued = 0;
     bool ok = true;
-    QTileWalk qw;
-    for (qw.seek(p, kt); qw.qt < p.n_qtiles && ok; qw.next(p, kt)) {
+    while (qw.qt < p.n_qtiles) {
       const int qt = qw.qt;
       const int s = u % S, use = u / S;
-      // -LSE*log2(e) and -D of the tile's rows (padding rows: 0): eight independent,
-      // bounds-checked loads per lane, issued before the wait so their latency hides there
-      float nl[4], dd[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int r = qt * 128 + lane + 32 * j;
-        const size_t g = static_cast<size_t>(bh) * p.R + (r < p.R ? r : 0);
-        nl[j] = r < p.R ? -__ldg(p.lse + g) * kLog2e : 0.f;
-        dd[j] = r < p.R ? -__ldg(p.dvec + g) : 0.f;
-      }
       if (use > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarEmpty + s), (use - 1) & 1));
       if (!ok) break;
       const uint32_t st = stage_addr(s);
-      if (lane == 0 && !(p.withhold && u == 0)) {
+      if (lane == 0 && u > 0) {
         ptx::mbar_arrive_expect_tx(bar(kBarFull + s), 2 * C::kTileBytes);
         for (int c = 0; c < C::kChunks; ++c) {
           ptx::tma_load_3d(st + c * C::kChunkBytes, &tm_q, bar(kBarFull + s), c * 64, qt * 128, bh);
           ptx::tma_load_3d(st + C::kTileBytes + c * C::kChunkBytes, &tm_do, bar(kBarFull + s), c * 64, qt * 128, bh);
         }
       }
+      // the loaded LSE and D are first used here, after the tile's loads are on their way
+      asm volatile("" : "+f"(lse_next[0]), "+f"(lse_next[1]), "+f"(lse_next[2]), "+f"(lse_next[3]),
+                   "+f"(d_next[0]), "+f"(d_next[1]), "+f"(d_next[2]), "+f"(d_next[3]));
       float* vec = reinterpret_cast<float*>(smem + C::kKVOffStage + s * C::kStageBytes + 2 * C::kTileBytes);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        vec[lane + 32 * j] = nl[j];
-        vec[128 + lane + 32 * j] = dd[j];
+        const bool row_exists = qt * 128 + lane + 32 * j < p.R;  // padding rows: 0
+        vec[lane + 32 * j] = row_exists ? -lse_next[j] * kLog2e : 0.f;
+        vec[128 + lane + 32 * j] = row_exists ? -d_next[j] : 0.f;
       }
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(bar(kBarFull + s));
       ++u;
       issued = u;
+      qw.next(p, kt);
+      if (qw.qt < p.n_qtiles) load_vec(qw.qt);
     }
     if (!ok && lane == 0) {
       w.drain(bar(kBarKV), 0);
@@ -495,15 +558,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const float c2 = p.scale_log2;
     bool ok = true;
     int u = 0, np = 0;  // query tiles whose dS^T (P^T) has been handed over
-    QTileWalk qw;
-    for (qw.seek(p, kt); qw.qt < p.n_qtiles && ok; qw.next(p, kt)) {
-      const int qt = qw.qt;
+    QTileWalk walk;
+    for (walk.seek(p, kt); walk.qt < p.n_qtiles && ok; walk.next(p, kt)) {
+      const int qt = walk.qt;
       const int s = u % S;
       // the tile needs no mask when all 128 rows exist, all keys exist and (causal) its
       // lowest position is at or after the key tile's last key
       const int r0 = qt * 128;
       const int n_rows = min(128, p.R - r0);
-      const int pos0 = qw.pos0;
+      const int pos0 = walk.pos0;
       const bool one_head = pos0 + 128 <= p.N;
       const bool no_mask = n_rows == 128 && key_tile_full && (!p.causal || (one_head && pos0 >= kt * 128 + 127));
       ok = __all_sync(0xffffffffu, w.wait(bar(kBarS), u & 1));
@@ -544,8 +607,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok && n_q > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFinal), 0));
     if (ok && n_q > 0) {
       ptx::tc_fence_after();
-      bwd_acc_to_smem<D>(tmem + lane_off + C::kColAcc0, sbase + C::kTileBytes, row, half * (D / 2), 1.f);
-      bwd_acc_to_smem<D>(tmem + lane_off + C::kColAcc1, sbase, row, half * (D / 2), p.scale);
+      const uint32_t t_acc[2] = {tmem + lane_off + C::kColAcc0, tmem + lane_off + C::kColAcc1};  // dV, dK
+      const uint32_t dst[2] = {sbase + C::kTileBytes, sbase};
+      const float mul[2] = {1.f, p.scale};
+      bwd_accs_to_smem<D, 2>(t_acc, dst, mul, row, half * (D / 2));
       ptx::fence_proxy_async_smem();
     } else if (n_q == 0 && ok) {
       // no query sees this key tile: zero gradients (the K/V tiles may still be landing)
@@ -601,6 +666,29 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const int bh = blockIdx.x % p.groups;
   const int qt = p.n_qtiles - 1 - blockIdx.x / p.groups;  // causal: the last query tiles have most work
   const int n_kv = p.causal ? min(p.n_ktiles, bwd_tile_max_pos(p, qt) / 128 + 1) : p.n_ktiles;
+  // compute threads: the LSE and D of this thread's query row, loaded before the set-up barrier
+  const int qrow = qt * 128 + (warp & 3) * 32 + lane;
+  const bool row_valid = qrow < p.R;
+  float lse_row = 0.f, d_row = 0.f;
+  if (warp < kBwdComputeWarps && row_valid) {
+    const size_t g = static_cast<size_t>(bh) * p.R + qrow;
+    lse_row = __ldg(p.lse + g);
+    d_row = __ldg(p.dvec + g);
+  }
+  // producer (warp 8, lane 0): ring tiles issued so far, carried across the set-up barrier
+  int issued = 0;
+  auto prefetch = [&](int u) {
+    if (u < 2 * n_kv)
+      for (int c = 0; c < C::kChunks; ++c)
+        ptx::tma_prefetch_3d((u & 1) ? &tm_v : &tm_k, c * 64, (u >> 1) * 128, bh);
+  };
+  auto load_ring = [&](int u) {  // K_{u/2} (u even) or V_{u/2} (u odd) into slot u % S
+    const int s = u % S;
+    ptx::mbar_arrive_expect_tx(bar(kBarFull + s), C::kTileBytes);
+    for (int c = 0; c < C::kChunks; ++c)
+      ptx::tma_load_3d(sbase + C::kQOffRing + s * C::kTileBytes + c * C::kChunkBytes, (u & 1) ? &tm_v : &tm_k,
+                       bar(kBarFull + s), c * 64, (u >> 1) * 128, bh);
+  };
 
   if (warp == kBwdComputeWarps && lane == 0) {
     ptx::mbar_init(bar(kBarQ), 1);
@@ -615,6 +703,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::mbar_init(bar(kBarDrain), 1);
     *abort_flag = 0u;
     ptx::fence_mbar_init();
+    // Q, dO and the ring's first tiles (no slot to wait for yet) start loading before the
+    // set-up barrier
+    ptx::mbar_arrive_expect_tx(bar(kBarQ), 2 * C::kTileBytes);
+    for (int c = 0; c < C::kChunks; ++c) {
+      ptx::tma_load_3d(sbase + c * C::kChunkBytes, &tm_q, bar(kBarQ), c * 64, qt * 128, bh);
+      ptx::tma_load_3d(sbase + C::kTileBytes + c * C::kChunkBytes, &tm_do, bar(kBarQ), c * 64, qt * 128, bh);
+    }
+    for (int u = 0; u < C::kPrefetchAhead; ++u) prefetch(u);
+    for (int u = 0; u < S && u < 2 * n_kv; ++u) {
+      prefetch(u + C::kPrefetchAhead);
+      issued = u + 1;
+      if (p.withhold && u == 1) continue;  // test hook: V_0 is never loaded
+      load_ring(u);
+    }
   }
   if (warp == kBwdComputeWarps + 1) {
     ptx::tmem_alloc(ptx::smem_addr(tmem_slot), 512);
@@ -628,30 +730,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
   if (warp == kBwdComputeWarps) {
     // ------------------------------------------------ producer: Q, dO once; K_0, V_0, K_1, ...
+    // (Q, dO and the first S ring tiles were issued before the set-up barrier)
     if (lane == 0) {
-      ptx::mbar_arrive_expect_tx(bar(kBarQ), 2 * C::kTileBytes);
-      for (int c = 0; c < C::kChunks; ++c) {
-        ptx::tma_load_3d(sbase + c * C::kChunkBytes, &tm_q, bar(kBarQ), c * 64, qt * 128, bh);
-        ptx::tma_load_3d(sbase + C::kTileBytes + c * C::kChunkBytes, &tm_do, bar(kBarQ), c * 64, qt * 128, bh);
-      }
-      int issued = 0;
       bool ok = true;
-      auto prefetch = [&](int u) {
-        if (u < 2 * n_kv)
-          for (int c = 0; c < C::kChunks; ++c)
-            ptx::tma_prefetch_3d((u & 1) ? &tm_v : &tm_k, c * 64, (u >> 1) * 128, bh);
-      };
-      for (int u = 0; u < C::kPrefetchAhead; ++u) prefetch(u);
-      for (int u = 0; u < 2 * n_kv; ++u) {
+      for (int u = issued; u < 2 * n_kv; ++u) {
         const int s = u % S, use = u / S;
         prefetch(u + C::kPrefetchAhead);
         if (use > 0 && !w.wait(bar(kBarEmpty + s), (use - 1) & 1)) { ok = false; break; }
         issued = u + 1;
         if (p.withhold && u == 1) continue;  // test hook: V_0 is never loaded
-        ptx::mbar_arrive_expect_tx(bar(kBarFull + s), C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          ptx::tma_load_3d(sbase + C::kQOffRing + s * C::kTileBytes + c * C::kChunkBytes, (u & 1) ? &tm_v : &tm_k,
-                           bar(kBarFull + s), c * 64, (u >> 1) * 128, bh);
+        load_ring(u);
       }
       if (!ok) {
         w.drain(bar(kBarQ), 0);
@@ -717,12 +805,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // ------------------------------------------------ compute: thread = query row, warp = column half
     const int quarter = warp & 3, half = warp >> 2;
     const int row = quarter * 32 + lane;
-    const int qrow = qt * 128 + row;
-    const bool row_valid = qrow < p.R;
     const int qpos = qrow % p.N;
-    const size_t g = static_cast<size_t>(bh) * p.R + (row_valid ? qrow : 0);
-    const float neg = row_valid ? -p.lse[g] * 1.4426950408889634f : 0.f;  // -LSE in log2 units
-    const float neg_drow = row_valid ? -p.dvec[g] : 0.f;
+    const float neg = row_valid ? -lse_row * 1.4426950408889634f : 0.f;  // -LSE in log2 units
+    const float neg_drow = row_valid ? -d_row : 0.f;
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
     const uint32_t t_s0 = tmem + lane_off + C::kQColS + half * 64, t_dp = tmem + lane_off + C::kQColDP + half * 64;
     const float c2 = p.scale_log2;
@@ -766,7 +851,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, w.wait(bar(kBarFinal), 0));
     if (ok && n_kv > 0) {
       ptx::tc_fence_after();
-      bwd_acc_to_smem<D>(tmem + lane_off + C::kQColDQ, sbase, row, half * (D / 2), p.scale);  // into Q's buffer
+      const uint32_t t_acc[1] = {tmem + lane_off + C::kQColDQ};
+      const uint32_t dst[1] = {sbase};  // Q's buffer
+      const float mul[1] = {p.scale};
+      bwd_accs_to_smem<D, 1>(t_acc, dst, mul, row, half * (D / 2));
       ptx::fence_proxy_async_smem();
     }
     ptx::named_barrier(1, 32 * kBwdComputeWarps);
@@ -782,6 +870,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, 512);
   }
+  // Launched as a dependent of the dK/dV grid, this grid may start before that one ends; a CTA
+  // leaves only once it has completed, so the end of this grid is the end of the backward
+  // for whatever the stream runs next.
+  if (threadIdx.x == 0) ptx::griddep_wait();
 }
 
 // ==================================================================== host side
@@ -886,19 +978,32 @@ int launch_bwd(const BwdProblem& pr, int withhold, unsigned long long timeout_ns
   p.withhold = withhold;
   p.timeout_ns = timeout_ns;
   const long long rows = static_cast<long long>(groups) * R;
-  const long long prep_blocks = (rows * 32 + 255) / 256;
+  constexpr long long kRowsPerBlock = static_cast<long long>(kPrepThreads / 32) * prep_rows_per_warp<D>();
+  const long long prep_blocks = (rows + kRowsPerBlock - 1) / kRowsPerBlock;
   const long long grid_kv = static_cast<long long>(groups) * p.n_ktiles;
   const long long grid_q = static_cast<long long>(groups) * p.n_qtiles;
   if (prep_blocks > 2147483647LL || grid_kv > 2147483647LL || grid_q > 2147483647LL) return FA_ERR_ARG;
-  fa_bwd_prep_kernel<D><<<static_cast<unsigned>(prep_blocks), 256, 0, stream>>>(
+  fa_bwd_prep_kernel<D><<<static_cast<unsigned>(prep_blocks), kPrepThreads, 0, stream>>>(
       static_cast<const uint16_t*>(pr.o), static_cast<const uint16_t*>(pr.dout), pr.delta, static_cast<int>(rows));
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
   fa_bwd_dkdv_kernel<D><<<static_cast<unsigned>(grid_kv), kBwdThreads, BwdCfg<D>::kSmemKV, stream>>>(
       mq, mk, mv, mdo, mdk, mdv, p);
   if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
-  fa_bwd_dq_kernel<D><<<static_cast<unsigned>(grid_q), kBwdThreads, BwdCfg<D>::kSmemQ, stream>>>(
-      mq, mk, mv, mdo, mdq, p);
-  if (cudaGetLastError() != cudaSuccess) return FA_ERR_LAUNCH;
+  // programmatic dependent launch: the dQ CTAs, which read nothing the dK/dV kernel writes,
+  // take the SMs the dK/dV grid leaves idle in its last wave
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid_q));
+  cfg.blockDim = dim3(kBwdThreads);
+  cfg.dynamicSmemBytes = BwdCfg<D>::kSmemQ;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, fa_bwd_dq_kernel<D>, mq, mk, mv, mdo, mdq, p) != cudaSuccess ||
+      cudaGetLastError() != cudaSuccess)
+    return FA_ERR_LAUNCH;
   return FA_OK;
 }
 

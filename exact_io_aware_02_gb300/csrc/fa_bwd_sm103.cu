@@ -8,12 +8,16 @@
 //     dQ = scale * dS K,   dK = scale * dS^T Q.
 //
 // Three kernels, all on one stream:
-//   fa_bwd_prep_kernel  -- D = rowsum(dO * O) (memory-bound, one warp per row);
+//   fa_bwd_prep_kernel  -- D = rowsum(dO * O) (memory-bound, 16-byte loads, a row per D/8
+//                          lanes);
 //   fa_bwd_dkdv_kernel  -- one CTA per 128-key tile: loops over the query tiles that see
 //                          it, recomputes S^T = K Q^T and dP^T = V dO^T, and accumulates
 //                          dV += P^T dO and dK += dS^T Q in tensor memory;
 //   fa_bwd_dq_kernel    -- one CTA per 128-query tile: loops over its key tiles,
 //                          recomputes S = Q K^T and dP = dO V^T, accumulates dQ += dS K.
+//                          It reads nothing the dK/dV kernel writes and is launched as its
+//                          programmatic dependent, so it fills the SMs that kernel's last wave
+//                          leaves idle; each of its CTAs waits for the dK/dV grid before exiting.
 // Splitting dQ from dK/dV costs two extra products per tile pair (7 instead of 5) but
 // needs no atomics and keeps every accumulator in tensor memory.
 //

@@ -168,6 +168,29 @@ def test_bwd_repeatable_and_status_clean(fa):
     assert fa.fa_status(clear=False) == 0
 
 
+def test_bwd_next_work_on_the_stream_sees_complete_gradients(fa):
+    """The dQ kernel is launched as a programmatic dependent of the dK/dV kernel and may start
+    before that kernel ends; whatever the stream runs next must still see dQ, dK and dV complete.
+    The outputs are filled with NaN, the backward runs, and the next kernels on the same stream
+    (copies, with no synchronisation in between) must read exactly a synchronised run's
+    gradients."""
+    dev = torch.device("cuda")
+    q, k, v = (t.to(dev) for t in make_qkv_gqa(2, 16, 16, 4096, 4096, 128, seed=4801))
+    do = make_dout(q.shape, seed=4802).to(dev)
+    o, lse = fa.fa_fwd_gqa(q, k, v, causal=True)
+    ref = fa.fa_bwd(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    ref = [t.clone() for t in ref[:3]]
+    for _ in range(3):
+        outs = [torch.full_like(t, float("nan")) for t in ref]
+        fa.fa_bwd(q, k, v, o, lse, do, dq=outs[0], dk=outs[1], dv=outs[2], causal=True)
+        snap = [t.clone() for t in outs]  # the stream's next kernels
+        torch.cuda.synchronize()
+        for got, want in zip(snap, ref):
+            assert torch.equal(got, want)
+    assert fa.fa_status(clear=False) == 0
+
+
 def test_bwd_argument_errors_on_device(fa):
     dev = torch.device("cuda")
     q, k, v = (t.to(dev) for t in make_qkv_gqa(1, 2, 2, 128, 128, 64, seed=4701))

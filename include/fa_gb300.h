@@ -288,8 +288,12 @@ size_t fa_fwd_fp8_workspace_bytes(int B, int H, int N, int d);
  * B, Hq, Hkv, N >= 1 with Hq % Hkv == 0 (queries and keys have the same length N);
  * d is 64 or 128; scale finite and > 0; causal: nonzero = query i sees keys 0..i.
  * B*Hq*N <= 2^31 - 1.  Three kernels are enqueued on `stream` (D, then dK/dV, then
- * dQ); the call returns once they are enqueued.  On an error return nothing was
- * enqueued.  A device-side wait that gives up sets FA_STATUS_TIMEOUT (fa_status).
+ * dQ); the call returns once they are enqueued.  The dQ kernel, which reads nothing the
+ * dK/dV kernel writes, is launched as its programmatic dependent and may start before it
+ * ends, but it completes only after it, so whatever the stream runs after this call sees
+ * dQ, dK and dV complete.  On FA_ERR_ARG or FA_ERR_ARCH nothing was enqueued; on
+ * FA_ERR_LAUNCH the kernels before the failing launch may have been.  A device-side wait
+ * that gives up sets FA_STATUS_TIMEOUT (fa_status).
  *
  * Returns FA_OK, FA_ERR_ARG, FA_ERR_ARCH or FA_ERR_LAUNCH.
  */
